@@ -1,0 +1,432 @@
+#!/usr/bin/env python3
+"""Throughput of the fused row softmax on one GB300 (or N, as replicas).
+
+One step = one softmax_rows call (the whole hot path: plan, persistent
+schedule, row load, max, exp-sum, normalise-and-store) over the workload's
+M x N matrix, inputs resident in HBM. The headline workload is the FP32
+4096 x 4096 matrix with extreme rows (seed 1).
+
+Cold-L2 lane (default): before every step a 512 MiB (>= 4x L2) buffer is READ
+outside the event pair, evicting the L2 without leaving dirty lines that the
+timed kernel would have to write back. Each step is timed with CUDA events
+on the stream the kernel is launched on; value = algorithmic bytes
+(2*M*N*elem_bytes per step, one read and one write of every element) over the
+summed step time.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all]
+                  [--lane cold|warm] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain FP64 C implementation) on the
+host cores, on the same workload and metric. Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+NOMINAL_HBM_GBS = 8000.0  # the bar's denominator: ~8 TB/s HBM3e
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=synth.HEADLINE,
+                    help="one of %s, or 'all'" % ", ".join(synth.WORKLOADS))
+    ap.add_argument("--lane", choices=("cold", "warm"), default="cold")
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--plan", type=int, default=0, help="forced plan (0 = automatic)")
+    ap.add_argument("--cpu-budget", type=float, default=6.0,
+                    help="seconds of oracle time for the CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--burst", type=float, default=1.0, help="seconds of load before timing")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def recorded_traffic(workload: str, source_hash: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on this build."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        rec = d.get(workload)
+        if rec and rec.get("source_hash") == source_hash:
+            return rec.get("dram_bytes_per_launch"), rec
+    except (OSError, ValueError):
+        pass
+    return None, None
+
+
+# ---- clocks --------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi sampled every 100 ms in the background while the GPU is loaded."""
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return self
+
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append(line.strip())
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], [], set()
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(REASON_NAMES, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---- CPU oracle leg (cpu_baseline and the reference arm) -------------------------
+
+def oracle_pass(w, x, nthreads):
+    import oracle
+    t0 = time.perf_counter()
+    y = oracle.softmax_rows(x.reshape(-1), w.M, w.N, w.ld_in, w.ld_out, w.dtype,
+                            nthreads=nthreads)
+    return time.perf_counter() - t0, y
+
+
+def cpu_baseline(w, x, budget_s: float):
+    """The oracle as it stands, on all host cores, repeated for about budget_s."""
+    nthreads = synth.host_threads()
+    times, y = [], None
+    t_start = time.perf_counter()
+    while True:
+        dt, y = oracle_pass(w, x, nthreads)
+        times.append(dt)
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    gbs = w.fused_bytes * len(times) / sum(times) / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
+            "sample": "whole %s matrix (%d x %d), %d pass(es) of the FP64 C oracle, %d threads"
+                      % (w.name, w.M, w.N, len(times), nthreads),
+            "rows_per_s": round(w.M * len(times) / sum(times), 1)}, y
+
+
+# ---- GPU leg ----------------------------------------------------------------------
+
+def gpu_uuid(device_index: int):
+    import torch
+    try:
+        u = torch.cuda.get_device_properties(device_index).uuid
+        s = str(u)
+        return s if s.startswith("GPU-") else "GPU-" + s
+    except Exception:
+        return None
+
+
+def run_ours(args, w, rank, local_rank, world):
+    import torch
+
+    import memory_bound_row_rows_gb300 as sr
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = sr.load()
+    x = w.generate()
+    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[w.dtype]
+
+    def host_tensor(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t if w.dtype == synth.F32 else t.view(torch.int16).view(tdt)
+
+    x_dev = host_tensor(x).to(dev)
+    y_dev = torch.empty((w.M, w.ld_out), dtype=tdt, device=dev)
+    flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    plan_used = sr.softmax_rows_plan(x_dev, y_dev, w.M, w.N, w.ld_in, w.ld_out, w.dtype) \
+        if args.plan == 0 else args.plan
+
+    def step():
+        st = lib.softmax_rows_ex(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
+                                 w.ld_out, w.dtype, args.plan, sh)
+        if st != 0:
+            raise RuntimeError("softmax_rows failed: %s" % sr.softmax_rows_strerror(st))
+
+    def flush_l2():
+        if args.lane == "cold":
+            torch.sum(flush)  # reads 512 MiB: L2 now holds clean lines only
+
+    for _ in range(max(3, args.warmup)):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+
+    clk = ClockSampler(gpu_uuid(local_rank) if rank == 0 else None)
+    with clk:
+        t_end = time.perf_counter() + args.burst
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                flush_l2()
+                step()
+            torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush_l2()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, x, dev, lib, host_tensor, tdt)
+    return {"ms": ms, "clocks": clk.summary(), "plan": sr.PLAN_NAMES.get(plan_used, str(plan_used)),
+            "y_dev": y_dev, "e2e": e2e, "x": x}
+
+
+def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
+    """Same metric through the C ABI with host buffers: pinned H2D, softmax, D2H."""
+    import torch
+    x_pin = host_tensor(x).pin_memory()
+    y_pin = torch.empty((w.M, w.ld_out), dtype=tdt).pin_memory()
+    x_dev = torch.empty((w.M, w.ld_in), dtype=tdt, device=dev)
+    y_dev = torch.empty((w.M, w.ld_out), dtype=tdt, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        x_dev.copy_(x_pin, non_blocking=True)
+        st = lib.softmax_rows(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in, w.ld_out,
+                              w.dtype, stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError("softmax_rows failed")
+        y_pin.copy_(y_dev, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    k = max(3, min(args.steps, 20))
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(k):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    sec = t0.elapsed_time(t1) / 1e3 / k
+    eb = w.elem_bytes
+    return {"value": round(w.fused_bytes / sec / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": w.M * w.ld_in * eb, "d2h_bytes_per_step": w.M * w.ld_out * eb,
+            "ms_per_step": round(sec * 1e3, 4), "steps": k}
+
+
+def parity_vs_oracle(w, y_dev, y_ref):
+    """Compare the GPU output with the CPU-baseline leg's oracle output (every row)."""
+    import torch
+    y = y_dev.detach().cpu()
+    if w.dtype != synth.F32:
+        y = y.view(torch.int16)
+    y = y.numpy()
+    if w.dtype != synth.F32:
+        y = y.view(np.uint16)
+    g = synth.storage_to_float64(y[:, :w.N], w.dtype)
+    r = synth.storage_to_float64(y_ref[:, :w.N], w.dtype)
+    atol = 1e-6 if w.dtype == synth.F32 else 4e-3
+    bad = ~(np.abs(g - r) <= atol + atol * np.abs(r))
+    bad &= ~(np.isnan(g) & np.isnan(r))
+    return {"rows": w.M, "elements": int(g.size), "outside_tolerance": int(bad.sum()),
+            "atol": atol, "rtol": atol, "max_abs_err": float(np.nanmax(np.abs(g - r)))}
+
+
+def bench_ours(args, w):
+    import torch
+    rank, local_rank, world = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl")
+    from memory_bound_row_rows_gb300 import _build
+    res = run_ours(args, w, rank, local_rank, world)
+    ms = res["ms"]
+    total_s = sum(ms) / 1e3
+    if world > 1:
+        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_s = float(t.item())
+    if rank != 0:
+        return None
+    steps = len(ms)
+    mean_s = total_s / steps
+    value = world * w.fused_bytes * steps / total_s / 1e9
+    peaks = measured_peaks()
+    src_hash = _build.source_hash()
+    traffic, rec = recorded_traffic(w.name, src_hash)
+    achieved = w.fused_bytes / (sum(ms) / 1e3 / steps) / 1e9
+    line = {
+        "metric": "cold-L2 softmax GB/s (2*M*N*bytes/time)" if args.lane == "cold"
+        else "warm-L2 softmax GB/s (2*M*N*bytes/time)",
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_s * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": synth.DTYPE_NAMES[w.dtype],
+        "data": "synthetic: seeded SplitMix64/Box-Muller (seed %d), generated on the host" % w.seed,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "ld_in": w.ld_in, "ld_out": w.ld_out,
+                   "plan": res["plan"], "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": ("flushed: a 512 MiB device buffer is read before every step, outside "
+                          "the event pair") if args.lane == "cold" else "warm (no flush)",
+                   "inputs_resident_in_hbm": True},
+        "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "rows_per_s": round(world * w.M * steps / total_s, 1),
+        "median_step_us": round(statistics.median(ms) * 1e3, 3),
+        "p10_p90_step_us": [round(float(np.percentile(ms, 10)) * 1e3, 3),
+                            round(float(np.percentile(ms, 90)) * 1e3, 3)],
+        "gpu_launches": steps,
+        "clocks": res["clocks"],
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic,
+                     "traffic_note": (rec or {}).get("note") if traffic else
+                     "null: no ncu capture recorded for this build of the kernels"},
+        "source_hash": src_hash,
+    }
+    if res["e2e"] is not None:
+        line["e2e"] = res["e2e"]
+    if world == 1:
+        cpu, y_ref = cpu_baseline(w, res["x"], args.cpu_budget)
+        line["cpu_baseline"] = cpu
+        line["parity"] = parity_vs_oracle(w, res["y_dev"], y_ref)
+    return line
+
+
+def bench_reference(args, w):
+    """The CPU oracle as the reference arm: each step is one oracle pass over the workload."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    x = w.generate()
+    nthreads = synth.host_threads()
+    for _ in range(max(0, args.warmup)):
+        oracle_pass(w, x, nthreads)
+    times = []
+    for _ in range(args.steps):
+        dt, _y = oracle_pass(w, x, nthreads)
+        times.append(dt)
+    total = sum(times)
+    value = w.fused_bytes * len(times) / total / 1e9
+    return {
+        "impl": "reference",
+        "metric": "cold-L2 softmax GB/s (2*M*N*bytes/time)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": synth.DTYPE_NAMES[w.dtype],
+        "data": "synthetic: seeded SplitMix64/Box-Muller (seed %d)" % w.seed,
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "ld_in": w.ld_in, "ld_out": w.ld_out},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
+                         "kind": "oracle",
+                         "sample": "whole %s matrix per step, FP64 C oracle, %d threads"
+                                   % (w.name, nthreads)},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    names = list(synth.WORKLOADS) if args.workload == "all" else [args.workload]
+    for name in names:
+        w = synth.WORKLOADS[name]
+        line = bench_reference(args, w) if args.impl == "reference" else bench_ours(args, w)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    if args.impl == "ours":
+        import torch
+        if torch.distributed.is_initialized():
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

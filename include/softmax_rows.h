@@ -1,0 +1,156 @@
+/*
+ * softmax_rows: fused, numerically stable row-wise softmax on one GB300 GPU.
+ *
+ * For every row i of an M x N row-major matrix x (leading dimension ld_in
+ * elements), the library writes
+ *
+ *     y[i,j] = exp(x[i,j] - m_i) / sum_k exp(x[i,k] - m_i),  m_i = max_k x[i,k],
+ *
+ * to an M x N row-major matrix y (leading dimension ld_out). This is the
+ * fused softmax of "Triton: Writing GPU Kernels in Python, Measured" (Step 2:
+ * subtract the row maximum, exponentiate, divide by the sum, one pass over
+ * the row held on chip), with the row-stride interface of "Fused Softmax on
+ * GPU: From Naive PyTorch to Persistent Triton Kernels" (Triton, one block
+ * per row: input and output row strides), and the numeric contract of the
+ * "Warpline" README (Providers): reduction state in FP32 and a single cast
+ * back to the input dtype. Wide rows use the online max/sum merge of
+ * "Measured optimization case studies" (Wide rows), including its guard for
+ * all -inf chunks.
+ *
+ * Conventions shared by every entry point:
+ *   - in, out: DEVICE pointers owned by the caller; the library never frees,
+ *     keeps or allocates them. The input and output dtype are the same.
+ *   - M >= 0 rows, N >= 1 columns; ld_in >= N, ld_out >= N count elements.
+ *     Element (i, j) is in[i*ld_in + j] / out[i*ld_out + j]. Columns
+ *     [N, ld) are never read and never written.
+ *   - M == 0 is a no-op returning SR_OK.
+ *   - in == out with ld_in == ld_out (in place) is allowed; any other
+ *     overlap is undefined.
+ *   - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) on the current device. Nothing blocks the
+ *     host and nothing is allocated per call. The first call on a device
+ *     queries and caches its properties.
+ *   - Arguments are checked before anything is launched; a rejected call
+ *     launches nothing and leaves `out` untouched.
+ *   - Misaligned pointers or pitches are not an error: they select plans
+ *     that use narrower memory accesses.
+ *   - Results follow the definition exactly in the special cases: a row that
+ *     is all -inf is NaN; a NaN or +inf anywhere in a row makes the row NaN;
+ *     -inf entries of an otherwise finite row give exact zeros.
+ */
+#ifndef SOFTMAX_ROWS_H
+#define SOFTMAX_ROWS_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SR_API __attribute__((visibility("default")))
+#else
+#define SR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t. */
+typedef struct CUstream_st* sr_stream_t;
+
+/* Element types: IEEE binary32, bfloat16 (upper half of binary32), IEEE binary16. */
+enum sr_dtype { SR_F32 = 0, SR_BF16 = 1, SR_F16 = 2 };
+
+enum sr_status {
+    SR_OK = 0,
+    SR_EINVAL = 1,          /* bad size, pitch or null pointer */
+    SR_EDTYPE = 2,          /* unknown dtype */
+    SR_ECUDA = 3,           /* a CUDA runtime call or launch failed */
+    SR_EDEVICE_TIMEOUT = 4, /* a kernel's bounded wait expired (see softmax_rows_last_device_error) */
+    SR_EPLAN = 5            /* the forced plan cannot handle this shape or alignment */
+};
+
+/*
+ * Kernel plans. AUTO picks by row width, dtype and alignment:
+ *   WARP    one warp per row, the row resident in registers; rows up to 2048 elements.
+ *   CTA     one thread block per row, the row staged in shared memory by
+ *           bulk asynchronous copies; aligned rows up to 32 KiB.
+ *   CLUSTER one thread-block cluster per row, each block holding a slice in
+ *           shared memory and the per-slice (max, sum) merged across the
+ *           cluster; aligned rows up to 512 KiB. One HBM read per element.
+ *   ONLINE  one thread block per row, an online (max, sum) pass over the
+ *           row followed by a normalise-and-write pass; any width, any alignment.
+ * All plans run a persistent grid sized to the device's SM count.
+ */
+enum sr_plan {
+    SR_PLAN_AUTO = 0,
+    SR_PLAN_WARP = 1,
+    SR_PLAN_CTA = 2,
+    SR_PLAN_CLUSTER = 3,
+    SR_PLAN_ONLINE = 4
+};
+
+/*
+ * The fused row softmax (definition above; "Triton: Writing GPU Kernels in
+ * Python, Measured", Step 2, and "Fused Softmax on GPU", Triton one block per
+ * row). in: M x N input at pitch ld_in; out: M x N output at pitch ld_out;
+ * dtype: an sr_dtype; stream: the CUDA stream to enqueue on.
+ * Returns SR_OK, or SR_EINVAL / SR_EDTYPE (nothing launched) or SR_ECUDA.
+ */
+SR_API int softmax_rows(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                 int64_t ld_out, int dtype, sr_stream_t stream);
+
+/*
+ * softmax_rows with a forced plan (an sr_plan; SR_PLAN_AUTO behaves like
+ * softmax_rows). Same arguments and results; returns SR_EPLAN, launching
+ * nothing, when the plan cannot handle the shape or alignment. For tests and
+ * plan sweeps ("Measured optimization case studies", Wide rows and Choosing
+ * the plans from a grid: every plan forced on the same shape).
+ */
+SR_API int softmax_rows_ex(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                    int64_t ld_out, int dtype, int plan, sr_stream_t stream);
+
+/*
+ * The plan softmax_rows would run for these arguments (an sr_plan > 0), or a
+ * negative sr_status when they would be rejected. Pure host logic: launches
+ * nothing and needs no device. The pointers are read only for alignment.
+ */
+SR_API int softmax_rows_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t ld_in,
+                      int64_t ld_out, int dtype);
+
+/*
+ * Host planning of a forced plan: `plan` if it can run these arguments,
+ * otherwise -SR_EPLAN (or another negative status for rejected arguments).
+ */
+SR_API int softmax_rows_plan_check(const void* in, const void* out, int64_t M, int64_t N,
+                            int64_t ld_in, int64_t ld_out, int dtype, int plan);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word, which a kernel sets when one of its bounded waits (for a bulk copy
+ * into shared memory) expires. Returns SR_OK, SR_EDEVICE_TIMEOUT, or SR_ECUDA.
+ * A kernel whose wait expired skips the rest of its rows and returns, so the
+ * CUDA context stays usable; the output of that call is then incomplete.
+ */
+SR_API int softmax_rows_last_device_error(sr_stream_t stream);
+
+/*
+ * Test hook for the bounded-wait path: runs `plan` (CTA or CLUSTER) on the
+ * given arguments with its bulk copies switched off, so every wait for a copy
+ * expires after `timeout_ns` nanoseconds; the kernel then records
+ * SR_EDEVICE_TIMEOUT and returns without writing `out`. Nothing hangs and
+ * nothing faults. Returns like softmax_rows_ex.
+ */
+SR_API int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                             int64_t ld_out, int dtype, int plan, uint64_t timeout_ns,
+                             sr_stream_t stream);
+
+/* A static, human-readable name for an sr_status value. */
+SR_API const char* softmax_rows_strerror(int status);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SR_API int softmax_rows_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SOFTMAX_ROWS_H */

@@ -1,0 +1,169 @@
+"""Python binding of the softmax_rows C ABI (include/softmax_rows.h).
+
+Argument marshalling only: every step of the softmax runs in the CUDA kernels
+of ``lib/libsoftmax_rows.so``. The functions keep the C names and arguments;
+pointers may be given as integers or as tensors (their ``data_ptr()``), and a
+stream as a ``torch.cuda.Stream``, a raw handle, or None for torch's current
+stream. There is no CPU fallback: if the library is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = [
+    "SR_F32", "SR_BF16", "SR_F16", "SR_OK", "SR_EINVAL", "SR_EDTYPE", "SR_ECUDA",
+    "SR_EDEVICE_TIMEOUT", "SR_EPLAN", "SR_PLAN_AUTO", "SR_PLAN_WARP", "SR_PLAN_CTA",
+    "SR_PLAN_CLUSTER", "SR_PLAN_ONLINE", "PLAN_NAMES", "SoftmaxRowsError", "load", "lib_path",
+    "softmax_rows", "softmax_rows_ex", "softmax_rows_plan", "softmax_rows_plan_check",
+    "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
+    "softmax_rows_version", "softmax", "dtype_code",
+]
+
+SR_F32, SR_BF16, SR_F16 = 0, 1, 2
+SR_OK, SR_EINVAL, SR_EDTYPE, SR_ECUDA, SR_EDEVICE_TIMEOUT, SR_EPLAN = 0, 1, 2, 3, 4, 5
+SR_PLAN_AUTO, SR_PLAN_WARP, SR_PLAN_CTA, SR_PLAN_CLUSTER, SR_PLAN_ONLINE = 0, 1, 2, 3, 4
+PLAN_NAMES = {SR_PLAN_AUTO: "auto", SR_PLAN_WARP: "warp", SR_PLAN_CTA: "cta",
+              SR_PLAN_CLUSTER: "cluster", SR_PLAN_ONLINE: "online"}
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "lib", "libsoftmax_rows.so")
+_lib = None
+
+
+class SoftmaxRowsError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, softmax_rows_strerror(status), status))
+
+
+def lib_path() -> str:
+    return os.environ.get("SOFTMAX_ROWS_LIB", _LIB_PATH)
+
+
+def load():
+    """The loaded CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "softmax_rows CUDA library not found at %s; build it with "
+            "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
+    lib = ctypes.CDLL(path)
+    vp, i64, c_int, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+    sig = {
+        "softmax_rows": [vp, vp, i64, i64, i64, i64, c_int, vp],
+        "softmax_rows_ex": [vp, vp, i64, i64, i64, i64, c_int, c_int, vp],
+        "softmax_rows_plan": [vp, vp, i64, i64, i64, i64, c_int],
+        "softmax_rows_plan_check": [vp, vp, i64, i64, i64, i64, c_int, c_int],
+        "softmax_rows_last_device_error": [vp],
+        "softmax_rows_test_expiry": [vp, vp, i64, i64, i64, i64, c_int, c_int, u64, vp],
+        "softmax_rows_strerror": [c_int],
+        "softmax_rows_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "softmax_rows_strerror" else c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return int(x.data_ptr())
+    raise TypeError("expected a pointer (int) or a tensor, got %r" % type(x))
+
+
+def _stream(s) -> int:
+    if s is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) if torch.cuda.is_available() else 0
+    if isinstance(s, int):
+        return s
+    if hasattr(s, "cuda_stream"):
+        return int(s.cuda_stream)
+    raise TypeError("expected a CUDA stream, a handle or None, got %r" % type(s))
+
+
+def _check(status: int, where: str) -> int:
+    if status != SR_OK:
+        raise SoftmaxRowsError(status, where)
+    return status
+
+
+def softmax_rows(in_, out, M, N, ld_in, ld_out, dtype, stream=None) -> int:
+    return _check(load().softmax_rows(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
+                                      _stream(stream)), "softmax_rows")
+
+
+def softmax_rows_ex(in_, out, M, N, ld_in, ld_out, dtype, plan, stream=None) -> int:
+    return _check(load().softmax_rows_ex(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype, plan,
+                                         _stream(stream)), "softmax_rows_ex")
+
+
+def softmax_rows_plan(in_, out, M, N, ld_in, ld_out, dtype) -> int:
+    """The plan softmax_rows would run (> 0), or a negative status."""
+    return int(load().softmax_rows_plan(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype))
+
+
+def softmax_rows_plan_check(in_, out, M, N, ld_in, ld_out, dtype, plan) -> int:
+    return int(load().softmax_rows_plan_check(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
+                                              plan))
+
+
+def softmax_rows_last_device_error(stream=None) -> int:
+    """Status of the device error word (SR_OK or SR_EDEVICE_TIMEOUT); clears it."""
+    return int(load().softmax_rows_last_device_error(_stream(stream)))
+
+
+def softmax_rows_test_expiry(in_, out, M, N, ld_in, ld_out, dtype, plan, timeout_ns,
+                             stream=None) -> int:
+    return _check(load().softmax_rows_test_expiry(_ptr(in_), _ptr(out), M, N, ld_in, ld_out,
+                                                  dtype, plan, timeout_ns, _stream(stream)),
+                  "softmax_rows_test_expiry")
+
+
+def softmax_rows_strerror(status: int) -> str:
+    try:
+        return load().softmax_rows_strerror(status).decode()
+    except RuntimeError:
+        return "status %d" % status
+
+
+def softmax_rows_version() -> int:
+    return int(load().softmax_rows_version())
+
+
+def dtype_code(torch_dtype) -> int:
+    import torch
+    codes = {torch.float32: SR_F32, torch.bfloat16: SR_BF16, torch.float16: SR_F16}
+    if torch_dtype not in codes:
+        raise TypeError("softmax_rows supports float32, bfloat16 and float16, not %s" % torch_dtype)
+    return codes[torch_dtype]
+
+
+def softmax(x, out=None, plan: int = SR_PLAN_AUTO, stream=None):
+    """Row softmax of a 2-D CUDA tensor with unit column stride (any row stride).
+
+    ``out`` (optional) is a CUDA tensor of the same shape and dtype with unit
+    column stride; a new contiguous tensor is returned otherwise.
+    """
+    import torch
+    if x.dim() != 2 or x.stride(1) != 1 or not x.is_cuda:
+        raise ValueError("expected a 2-D CUDA tensor with unit column stride")
+    M, N = x.shape
+    if out is None:
+        out = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if out.shape != x.shape or out.dtype != x.dtype or out.stride(1) != 1:
+        raise ValueError("out must match x in shape and dtype, with unit column stride")
+    ld_in = x.stride(0) if M > 1 else N
+    ld_out = out.stride(0) if M > 1 else N
+    softmax_rows_ex(x, out, M, N, ld_in, ld_out, dtype_code(x.dtype), plan, stream)
+    return out

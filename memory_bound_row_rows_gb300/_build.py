@@ -1,0 +1,91 @@
+"""Build the CUDA library in-tree: nvcc, sm_103a only, translation units in parallel.
+
+Produces ``memory_bound_row_rows_gb300/lib/libsoftmax_rows.so`` (statically
+linked CUDA runtime, C ABI declared in ``include/softmax_rows.h``). A stamp of
+the sources and flags skips the rebuild when nothing changed.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import hashlib
+import os
+import shutil
+import subprocess
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+LIBDIR = os.path.join(PKG, "lib")
+LIB = os.path.join(LIBDIR, "libsoftmax_rows.so")
+HEADER = os.path.join(ROOT, "include", "softmax_rows.h")
+
+UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+              "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build softmax_rows")
+
+
+def _stamp(extra_flags) -> str:
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    with open(HEADER, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS + list(extra_flags)).encode())
+    return h.hexdigest()
+
+
+def source_hash() -> str:
+    """Hash of the kernel sources (used to tie profiler counters to a build)."""
+    return _stamp([])[:16]
+
+
+def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: bool = False) -> str:
+    out = out or LIB
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    stamp_path = out + ".stamp"
+    stamp = _stamp(extra_flags)
+    if not force and os.path.exists(out) and os.path.exists(stamp_path):
+        with open(stamp_path) as f:
+            if f.read().strip() == stamp:
+                return out
+    objdir = out + ".obj"
+    os.makedirs(objdir, exist_ok=True)
+    cc = nvcc()
+
+    def compile_unit(unit):
+        obj = os.path.join(objdir, unit + ".o")
+        cmd = [cc, *ARCH, *NVCC_FLAGS, *extra_flags, "-I", os.path.join(ROOT, "include"),
+               "-c", os.path.join(CSRC, unit), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed on %s:\n%s\n%s" % (unit, r.stdout, r.stderr))
+        with open(obj + ".ptxas.log", "w") as f:
+            f.write(r.stderr)
+        return obj
+
+    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+        objs = list(ex.map(compile_unit, UNITS))
+    tmp = out + ".tmp%d" % os.getpid()
+    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError("nvcc link failed:\n%s\n%s" % (r.stdout, r.stderr))
+    os.replace(tmp, out)
+    with open(stamp_path, "w") as f:
+        f.write(stamp)
+    if verbose:
+        print("built", out)
+    return out
+
+
+if __name__ == "__main__":
+    build(force=True, verbose=True)

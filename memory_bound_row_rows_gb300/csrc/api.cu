@@ -1,0 +1,281 @@
+// C ABI of the row-softmax library: argument checks, plan choice, the
+// per-device cache (SM count, shared-memory limits, occupancy, the device
+// error word) and the launch. See include/softmax_rows.h for the contract.
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/softmax_rows.h"
+#include "internal.h"
+
+namespace sr {
+
+// Set (bit 0) by a kernel whose bounded wait for a bulk copy expired. One
+// word per device (each device holds its own copy of this module's globals).
+__device__ unsigned int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+// Default limit for one bounded wait: far above any copy's real latency.
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+
+struct OccKey {
+    int dev;
+    const void* func;
+    int threads;
+    size_t smem;
+    int cluster;
+    bool operator==(const OccKey& o) const {
+        return dev == o.dev && func == o.func && threads == o.threads && smem == o.smem &&
+               cluster == o.cluster;
+    }
+};
+struct OccHash {
+    size_t operator()(const OccKey& k) const {
+        size_t h = std::hash<const void*>()(k.func);
+        h ^= (size_t)k.dev * 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h ^= (size_t)k.threads * 0xBF58476D1CE4E5B9ull + (h << 6) + (h >> 2);
+        h ^= (size_t)k.smem * 0x94D049BB133111EBull + (h << 6) + (h >> 2);
+        h ^= (size_t)k.cluster + (h << 6) + (h >> 2);
+        return h;
+    }
+};
+std::unordered_map<OccKey, int, OccHash> g_occ;
+std::unordered_map<OccKey, size_t, OccHash> g_smem_set;
+
+int current_device() {
+    int d = -1;
+    if (cudaGetDevice(&d) != cudaSuccess) return -1;
+    return d;
+}
+
+// Per-device properties, queried once per device.
+const DeviceInfo* device_info(cudaError_t* err) {
+    const int d = current_device();
+    if (d < 0 || d >= kMaxDevices) {
+        *err = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_dev_ready[d]) {
+        DeviceInfo info;
+        info.id = d;
+        cudaError_t e;
+        if ((e = cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, d)) ||
+            (e = cudaDeviceGetAttribute(&info.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        d)) ||
+            (e = cudaDeviceGetAttribute(&info.smem_per_sm,
+                                        cudaDevAttrMaxSharedMemoryPerMultiprocessor, d)) ||
+            (e = cudaDeviceGetAttribute(&info.l2_bytes, cudaDevAttrL2CacheSize, d)) ||
+            (e = cudaGetSymbolAddress(reinterpret_cast<void**>(&info.err), g_error_word))) {
+            *err = e;
+            return nullptr;
+        }
+        g_dev[d] = info;
+        g_dev_ready[d] = true;
+    }
+    *err = cudaSuccess;
+    return &g_dev[d];
+}
+
+}  // namespace
+
+int blocks_per_sm(const void* func, int threads, size_t smem) {
+    const OccKey key{current_device(), func, threads, smem, 0};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, func, threads, smem) != cudaSuccess)
+        return -1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ[key] = n;
+    return n;
+}
+
+int max_active_clusters(const void* func, int threads, size_t smem, int cluster) {
+    const OccKey key{current_device(), func, threads, smem, cluster};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_occ.find(key);
+        if (it != g_occ.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, func, &cfg) != cudaSuccess) return -1;
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_occ[key] = n;
+    return n;
+}
+
+cudaError_t ensure_smem_limit(const void* func, size_t smem, bool nonportable_cluster) {
+    const OccKey key{current_device(), func, 0, 0, nonportable_cluster ? 1 : 0};
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_smem_set.find(key);
+        if (it != g_smem_set.end() && it->second >= smem) return cudaSuccess;
+    }
+    cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    if (nonportable_cluster) {
+        e = cudaFuncSetAttribute(func, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_smem_set[key] = smem;
+    return cudaSuccess;
+}
+
+namespace {
+
+// Argument check shared by every entry point: 0 or a positive sr_status.
+int check_args(const void* in, const void* out, int64_t M, int64_t N, int64_t ld_in,
+               int64_t ld_out, int dtype) {
+    if (dtype != SR_F32 && dtype != SR_BF16 && dtype != SR_F16) return SR_EDTYPE;
+    if (M < 0 || N < 1 || ld_in < N || ld_out < N) return SR_EINVAL;
+    if (M > 0 && (in == nullptr || out == nullptr)) return SR_EINVAL;
+    // Index arithmetic stays in int64: the last byte addressed must fit.
+    if (M > 0) {
+        const __int128 ld = ld_in > ld_out ? ld_in : ld_out;
+        const __int128 last = ((__int128)(M - 1) * ld + N) * elem_bytes(dtype);
+        if (last > (__int128)INT64_MAX) return SR_EINVAL;
+    }
+    return 0;
+}
+
+// Whether a plan can run the arguments (host logic only).
+bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_in,
+               int64_t ld_out, int dtype) {
+    const bool vec = rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
+    const int64_t row_bytes = N * elem_bytes(dtype);
+    switch (plan) {
+        case SR_PLAN_WARP: return N <= kWarpMaxN;
+        case SR_PLAN_CTA: return vec && row_bytes <= kSliceMaxBytes;
+        case SR_PLAN_CLUSTER: return vec && cluster_size_for(N, dtype, 2) > 0;
+        case SR_PLAN_ONLINE: return true;
+    }
+    return false;
+}
+
+// Automatic plan: registers for short rows, one block with a shared-memory
+// ring for rows up to 32 KiB, a cluster for rows up to 512 KiB, else the
+// two-pass online fallback.
+int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
+                int dtype) {
+    if (N <= kWarpMaxN) return SR_PLAN_WARP;
+    if (plan_fits(SR_PLAN_CTA, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CTA;
+    if (plan_fits(SR_PLAN_CLUSTER, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CLUSTER;
+    return SR_PLAN_ONLINE;
+}
+
+int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
+        int dtype, int plan, cudaStream_t stream, unsigned long long timeout_ns, int flags) {
+    const int bad = check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return bad;
+    if (plan == SR_PLAN_AUTO) {
+        plan = choose_plan(in, out, N, ld_in, ld_out, dtype);
+    } else if (!plan_fits(plan, in, out, N, ld_in, ld_out, dtype)) {
+        return SR_EPLAN;
+    }
+    if (M == 0) return SR_OK;
+    cudaError_t e;
+    const DeviceInfo* dev = device_info(&e);
+    if (!dev) return SR_ECUDA;
+    Problem p{in, out, M, N, ld_in, ld_out, dtype, stream, dev, timeout_ns, flags};
+    switch (plan) {
+        case SR_PLAN_WARP: e = launch_warp(p); break;
+        case SR_PLAN_CTA: e = launch_tma(p, 1); break;
+        case SR_PLAN_CLUSTER: e = launch_tma(p, cluster_size_for(N, dtype, 2)); break;
+        case SR_PLAN_ONLINE: e = launch_online(p); break;
+        default: return SR_EPLAN;
+    }
+    return e == cudaSuccess ? SR_OK : SR_ECUDA;
+}
+
+}  // namespace
+}  // namespace sr
+
+extern "C" {
+
+int softmax_rows(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
+                 int dtype, sr_stream_t stream) {
+    return sr::run(in, out, M, N, ld_in, ld_out, dtype, SR_PLAN_AUTO, (cudaStream_t)stream,
+                   sr::kDefaultTimeoutNs, 0);
+}
+
+int softmax_rows_ex(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                    int64_t ld_out, int dtype, int plan, sr_stream_t stream) {
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ONLINE) return SR_EPLAN;
+    return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
+                   sr::kDefaultTimeoutNs, 0);
+}
+
+int softmax_rows_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t ld_in,
+                      int64_t ld_out, int dtype) {
+    const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return -bad;
+    return sr::choose_plan(in, out, N, ld_in, ld_out, dtype);
+}
+
+int softmax_rows_plan_check(const void* in, const void* out, int64_t M, int64_t N,
+                            int64_t ld_in, int64_t ld_out, int dtype, int plan) {
+    const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return -bad;
+    if (plan == SR_PLAN_AUTO) return sr::choose_plan(in, out, N, ld_in, ld_out, dtype);
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ONLINE) return -SR_EPLAN;
+    return sr::plan_fits(plan, in, out, N, ld_in, ld_out, dtype) ? plan : -SR_EPLAN;
+}
+
+int softmax_rows_last_device_error(sr_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return SR_ECUDA;
+    unsigned int word = 0;
+    if (cudaMemcpyFromSymbol(&word, sr::g_error_word, sizeof(word)) != cudaSuccess) return SR_ECUDA;
+    if (word != 0) {
+        const unsigned int zero = 0;
+        if (cudaMemcpyToSymbol(sr::g_error_word, &zero, sizeof(zero)) != cudaSuccess)
+            return SR_ECUDA;
+        return SR_EDEVICE_TIMEOUT;
+    }
+    return SR_OK;
+}
+
+int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                             int64_t ld_out, int dtype, int plan, uint64_t timeout_ns,
+                             sr_stream_t stream) {
+    if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER) return SR_EPLAN;
+    return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
+                   (unsigned long long)timeout_ns, sr::kFlagNoCopy);
+}
+
+const char* softmax_rows_strerror(int status) {
+    switch (status) {
+        case SR_OK: return "success";
+        case SR_EINVAL: return "invalid size, pitch or pointer";
+        case SR_EDTYPE: return "unknown dtype";
+        case SR_ECUDA: return "CUDA runtime error";
+        case SR_EDEVICE_TIMEOUT: return "a bounded device wait expired";
+        case SR_EPLAN: return "plan cannot handle this shape or alignment";
+    }
+    return "unknown status";
+}
+
+int softmax_rows_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,290 @@
+// Device-side building blocks for the row-softmax kernels (sm_103a).
+//
+// Inline PTX for the Blackwell data-movement path: mbarrier transaction
+// barriers, 1-D bulk asynchronous copies global -> shared
+// (cp.async.bulk ... mbarrier::complete_tx), cluster ranks, distributed
+// shared memory (mapa / st.shared::cluster) and cluster barriers; plus
+// 16-byte streaming loads and stores, and the element packing for
+// f32 / bf16 / f16.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sr {
+
+constexpr float kLog2e = 1.4426950408889634074f;
+
+__device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
+
+// ---------------------------------------------------------------------------
+// Element packing. A 16-byte vector holds kVec elements of storage type T.
+// unpack() widens to float exactly; pack() rounds to nearest even once.
+// ---------------------------------------------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+    static constexpr int kVec = 4;
+    static constexpr bool kAccurateExp = true;
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        f[0] = __uint_as_float(u.x);
+        f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z);
+        f[3] = __uint_as_float(u.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* f) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+    __device__ __forceinline__ static float load1(const float* p) { return __ldg(p); }
+    __device__ __forceinline__ static void store1(float* p, float v) { __stcs(p, v); }
+};
+
+template <>
+struct Elem<__nv_bfloat16> {
+    static constexpr int kVec = 8;
+    static constexpr bool kAccurateExp = false;
+    __device__ __forceinline__ static void unpack2(uint32_t w, float* f) {
+        f[0] = __uint_as_float(w << 16);
+        f[1] = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        unpack2(u.x, f + 0);
+        unpack2(u.y, f + 2);
+        unpack2(u.z, f + 4);
+        unpack2(u.w, f + 6);
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* f) {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                          pack2(f[6], f[7]));
+    }
+    __device__ __forceinline__ static float load1(const __nv_bfloat16* p) {
+        unsigned short s = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return __uint_as_float(((uint32_t)s) << 16);
+    }
+    __device__ __forceinline__ static void store1(__nv_bfloat16* p, float v) {
+        *p = __float2bfloat16_rn(v);
+    }
+};
+
+template <>
+struct Elem<__half> {
+    static constexpr int kVec = 8;
+    static constexpr bool kAccurateExp = false;
+    __device__ __forceinline__ static void unpack2(uint32_t w, float* f) {
+        __half2 h = *reinterpret_cast<__half2*>(&w);
+        float2 v = __half22float2(h);
+        f[0] = v.x;
+        f[1] = v.y;
+    }
+    __device__ __forceinline__ static void unpack(const uint4& u, float* f) {
+        unpack2(u.x, f + 0);
+        unpack2(u.y, f + 2);
+        unpack2(u.z, f + 4);
+        unpack2(u.w, f + 6);
+    }
+    __device__ __forceinline__ static uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __device__ __forceinline__ static uint4 pack(const float* f) {
+        return make_uint4(pack2(f[0], f[1]), pack2(f[2], f[3]), pack2(f[4], f[5]),
+                          pack2(f[6], f[7]));
+    }
+    __device__ __forceinline__ static float load1(const __half* p) {
+        unsigned short s = __ldg(reinterpret_cast<const unsigned short*>(p));
+        return __half2float(*reinterpret_cast<__half*>(&s));
+    }
+    __device__ __forceinline__ static void store1(__half* p, float v) { *p = __float2half_rn(v); }
+};
+
+// ---------------------------------------------------------------------------
+// Exponential of (x - shift). FP32 data uses the accurate library expf on the
+// exact difference (its outputs are compared at 1e-6). 16-bit data uses one
+// FMA and the hardware base-2 exponential: x*log2(e) - shift*log2(e), whose
+// relative error (~1e-6) is far below one bf16/f16 unit in the last place.
+// `shift_l2` is shift*log2(e), precomputed per row.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T>
+__device__ __forceinline__ float exp_shifted(float x, float shift, float shift_l2) {
+    if constexpr (Elem<T>::kAccurateExp) {
+        return expf(x - shift);
+    } else {
+        return ex2_approx(fmaf(x, kLog2e, -shift_l2));
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Warp reductions (butterfly, every lane ends with the result).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Scale factor exp(m - mref) of a partial (max m, sum s) being merged into a
+// result whose max is mref, with the all -inf guard of the online merge: a
+// part whose max is -inf contributes 0 (exp(-inf - (-inf)) is never formed).
+// Multiplying a NaN partial sum by it still gives NaN, so NaN propagates.
+__device__ __forceinline__ float merge_scale(float m, float mref) {
+    return (m == neg_inf()) ? 0.0f : expf(m - mref);
+}
+
+// Online (max, sum) merge: (m, s) <- (m, s) combined with (m2, s2).
+__device__ __forceinline__ void merge_ms(float& m, float& s, float m2, float s2) {
+    const float mn = fmaxf(m, m2);
+    s = s * merge_scale(m, mn) + s2 * merge_scale(m2, mn);
+    m = mn;
+}
+
+// 1/S for the final normalisation, NaN when the whole row was -inf (0/0 by
+// the definition) so that every output of such a row is NaN.
+__device__ __forceinline__ float final_rcp(float M, float S) {
+    return (M == neg_inf()) ? __int_as_float(0x7fc00000) : __frcp_rn(S);
+}
+
+// ---------------------------------------------------------------------------
+// Global memory: 16-byte streaming load (read-only path, no L1 allocation)
+// and streaming store.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void stg_stream(void* p, const uint4& v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Shared memory, mbarriers and bulk copies.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// 1-D bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned)
+// from global memory into this CTA's shared memory; completion is signalled
+// on the mbarrier as transaction bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of the mbarrier to complete, for at most
+// `timeout_ns` nanoseconds of wall time. Returns false on expiry.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t timeout_ns) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+#pragma unroll 1
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Thread-block clusters and distributed shared memory.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t local_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::
+                     : "memory");
+}
+
+}  // namespace sr

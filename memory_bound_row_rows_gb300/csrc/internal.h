@@ -1,0 +1,76 @@
+// Host-side interface between the C ABI (api.cu) and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sr {
+
+enum : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
+
+// Debug flag for the bounded-wait test hook: issue no bulk copies.
+constexpr int kFlagNoCopy = 1;
+
+// Rows up to this many elements run one warp per row (64 values per lane).
+constexpr int64_t kWarpMaxN = 2048;
+// Largest row slice a thread block stages in shared memory.
+constexpr int64_t kSliceMaxBytes = 32 * 1024;
+// Largest cluster (non-portable size 16 needs an opt-in attribute).
+constexpr int kMaxCluster = 16;
+
+struct DeviceInfo {
+    int id = -1;
+    int sm_count = 0;
+    int smem_optin = 0;    // max dynamic shared memory per block (opt-in)
+    int smem_per_sm = 0;
+    int l2_bytes = 0;
+    unsigned int* err = nullptr;  // device address of the error word
+};
+
+struct Problem {
+    const void* in;
+    void* out;
+    int64_t M, N, ld_in, ld_out;
+    int dtype;
+    cudaStream_t stream;
+    const DeviceInfo* dev;
+    unsigned long long timeout_ns;
+    int flags;
+};
+
+inline int elem_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }
+
+// True when every row start of `in` and `out` is 16-byte aligned and a row is
+// a whole number of 16-byte vectors.
+inline bool rows_vector_aligned(const void* in, const void* out, int64_t N, int64_t ld_in,
+                                int64_t ld_out, int dtype) {
+    const int64_t es = elem_bytes(dtype);
+    return (reinterpret_cast<uintptr_t>(in) % 16 == 0) &&
+           (reinterpret_cast<uintptr_t>(out) % 16 == 0) && ((ld_in * es) % 16 == 0) &&
+           ((ld_out * es) % 16 == 0) && ((N * es) % 16 == 0);
+}
+
+// Cluster size for a row: the smallest power of two whose slices fit
+// kSliceMaxBytes, at least `min_cluster`; 0 when the row is too wide.
+inline int cluster_size_for(int64_t N, int dtype, int min_cluster) {
+    const int64_t row_bytes = N * elem_bytes(dtype);
+    for (int c = min_cluster; c <= kMaxCluster; c *= 2) {
+        const int64_t nvec = row_bytes / 16;
+        const int64_t per = (nvec + c - 1) / c;
+        if (per * 16 <= kSliceMaxBytes && nvec >= c) return c;
+    }
+    return 0;
+}
+
+// Resident blocks per SM for a kernel (cached per device).
+int blocks_per_sm(const void* func, int threads, size_t smem);
+// Resident clusters on the device for a cluster launch (cached per device).
+int max_active_clusters(const void* func, int threads, size_t smem, int cluster);
+// Raise a kernel's dynamic shared memory limit once per device.
+cudaError_t ensure_smem_limit(const void* func, size_t smem, bool nonportable_cluster);
+
+cudaError_t launch_warp(const Problem& p);
+cudaError_t launch_tma(const Problem& p, int cluster);
+cudaError_t launch_online(const Problem& p);
+
+}  // namespace sr

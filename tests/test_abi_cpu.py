@@ -1,0 +1,121 @@
+"""The C-ABI library without a GPU: it loads, exports every declared entry
+point, and its host-side argument checks and plan choice behave as declared."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import memory_bound_row_rows_gb300 as sr
+import synth
+from memory_bound_row_rows_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sr.load()
+
+
+def declared_functions():
+    names = set()
+    for path in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(path).read()
+        names |= set(re.findall(r"SR_API\s+[\w\s\*]+?\b(\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    for must in ("softmax_rows", "softmax_rows_ex", "softmax_rows_plan",
+                 "softmax_rows_last_device_error", "softmax_rows_strerror"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    raw = ctypes.CDLL(sr.lib_path())
+    missing = [n for n in declared_functions() if not hasattr(raw, n)]
+    assert not missing, missing
+
+
+def test_version_and_strerror(lib):
+    assert sr.softmax_rows_version() >= 100
+    for st in range(6):
+        assert sr.softmax_rows_strerror(st)
+    assert sr.softmax_rows_strerror(99) == "unknown status"
+
+
+ALIGNED_IN, ALIGNED_OUT = 0x7F0000000000, 0x7F0100000000
+
+
+def test_rejected_arguments_touch_no_device(lib):
+    L = lib
+    # No device exists here: each of these must return before any CUDA call.
+    assert L.softmax_rows(None, None, 0, 8, 8, 8, 0, None) == sr.SR_OK  # empty
+    assert L.softmax_rows(ALIGNED_IN, ALIGNED_OUT, 4, 0, 8, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows(ALIGNED_IN, ALIGNED_OUT, -1, 8, 8, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows(ALIGNED_IN, ALIGNED_OUT, 4, 8, 7, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 7, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows(None, ALIGNED_OUT, 4, 8, 8, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows(ALIGNED_IN, None, 4, 8, 8, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 3, None) == sr.SR_EDTYPE
+    assert L.softmax_rows(ALIGNED_IN, ALIGNED_OUT, 2**40, 2**30, 2**30, 2**30, 0,
+                          None) == sr.SR_EINVAL  # index arithmetic would overflow
+    assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 4096, 4096, 4096, 0, sr.SR_PLAN_WARP,
+                             None) == sr.SR_EPLAN
+    assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, 9, None) == sr.SR_EPLAN
+    assert L.softmax_rows_test_expiry(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, sr.SR_PLAN_WARP,
+                                      1000, None) == sr.SR_EPLAN
+
+
+EXPECTED_PLANS = {
+    "f32_1024x256": sr.SR_PLAN_WARP,
+    "f32_4096x4096": sr.SR_PLAN_CTA,
+    "bf16_16384x1000_ld1024": sr.SR_PLAN_WARP,
+    "bf16_1024x131072": sr.SR_PLAN_CLUSTER,
+    "f16_causal_524288x2048": sr.SR_PLAN_WARP,
+}
+
+
+@pytest.mark.parametrize("name", sorted(EXPECTED_PLANS))
+def test_plan_for_each_workload(lib, name):
+    w = synth.WORKLOADS[name]
+    got = sr.softmax_rows_plan(ALIGNED_IN, ALIGNED_OUT, w.M, w.N, w.ld_in, w.ld_out, w.dtype)
+    assert got == EXPECTED_PLANS[name]
+
+
+def test_plan_depends_on_alignment_and_width(lib):
+    P = sr.softmax_rows_plan
+    A, B = ALIGNED_IN, ALIGNED_OUT
+    assert P(A, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_CTA
+    assert P(A + 4, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_ONLINE   # misaligned input
+    assert P(A, B, 10, 4096, 4097, 4096, 0) == sr.SR_PLAN_ONLINE       # odd pitch
+    assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_CTA          # 32 KiB rows
+    assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_CLUSTER      # just over 32 KiB
+    assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_CLUSTER  # 512 KiB bf16
+    assert P(A, B, 10, 262152, 262152, 262152, 1) == sr.SR_PLAN_ONLINE  # wider than a cluster
+    assert P(A, B, 10, 2048, 2048, 2048, 2) == sr.SR_PLAN_WARP
+    assert P(A + 2, B, 10, 2048, 2048, 2048, 2) == sr.SR_PLAN_WARP     # scalar warp variant
+    assert P(A, B, 10, 0, 8, 8, 0) == -sr.SR_EINVAL
+    assert P(A, B, 10, 8, 8, 8, 5) == -sr.SR_EDTYPE
+
+
+def test_forced_plan_checks(lib):
+    C = sr.softmax_rows_plan_check
+    A, B = ALIGNED_IN, ALIGNED_OUT
+    assert C(A, B, 5, 4096, 4096, 4096, 0, sr.SR_PLAN_CLUSTER) == sr.SR_PLAN_CLUSTER
+    assert C(A, B, 5, 4096, 4096, 4096, 0, sr.SR_PLAN_WARP) == -sr.SR_EPLAN
+    assert C(A, B, 5, 131072, 131072, 131072, 1, sr.SR_PLAN_CTA) == -sr.SR_EPLAN
+    assert C(A + 2, B, 5, 1000, 1000, 1000, 1, sr.SR_PLAN_CTA) == -sr.SR_EPLAN
+    assert C(A + 2, B, 5, 1000, 1000, 1000, 1, sr.SR_PLAN_ONLINE) == sr.SR_PLAN_ONLINE
+    assert C(A, B, 5, 8, 8, 8, 1, sr.SR_PLAN_CLUSTER) == -sr.SR_EPLAN  # one vector per row
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setenv("SOFTMAX_ROWS_LIB", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(sr, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        sr.softmax_rows(1, 2, 1, 8, 8, 8, 0, 0)

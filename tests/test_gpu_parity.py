@@ -1,0 +1,286 @@
+"""CUDA path against the CPU oracle, element by element (GPU required).
+
+Every call goes through the C ABI (the ctypes binding). Inputs come from the
+seeded generator; outputs are pre-filled with NaN so a kernel that skips an
+element cannot pass on stale values.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import memory_bound_row_rows_gb300 as sr
+import oracle
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+PLANS = [sr.SR_PLAN_AUTO, sr.SR_PLAN_WARP, sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_ONLINE]
+
+
+def nan_filled(M, ld, dtype):
+    return torch.full((M, ld), float("nan"), dtype=gu.torch_dtype(dtype), device="cuda")
+
+
+def run_plan(x_dev, M, N, ld_in, ld_out, dtype, plan, out=None):
+    y = nan_filled(M, ld_out, dtype) if out is None else out
+    st = sr.load().softmax_rows_ex(x_dev.data_ptr(), y.data_ptr(), M, N, ld_in, ld_out, dtype,
+                                   plan, torch.cuda.current_stream().cuda_stream)
+    return st, y
+
+
+def plan_applies(x_dev, y_dev, M, N, ld_in, ld_out, dtype, plan):
+    return sr.softmax_rows_plan_check(x_dev, y_dev, M, N, ld_in, ld_out, dtype, plan) > 0
+
+
+# ---- every workload's value law at oracle-friendly row counts, every plan ----
+
+SMALL_CASES = [
+    ("f32_1024x256", 0, 300),
+    ("f32_4096x4096", 0, 70),
+    ("bf16_16384x1000_ld1024", 0, 300),
+    ("bf16_1024x131072", 0, 10),
+    ("f16_causal_524288x2048", 0, 300),
+    ("f16_causal_524288x2048", 1900, 300),  # crosses the causal period
+]
+
+
+@pytest.mark.parametrize("name,row0,rows", SMALL_CASES, ids=lambda v: str(v))
+@pytest.mark.parametrize("plan", PLANS, ids=lambda p: sr.PLAN_NAMES[p])
+def test_small_parity(name, row0, rows, plan):
+    w = synth.WORKLOADS[name]
+    x = w.rows(row0, rows)
+    xd = gu.to_device(x, w.dtype)
+    y = nan_filled(rows, w.ld_out, w.dtype)
+    if not plan_applies(xd, y, rows, w.N, w.ld_in, w.ld_out, w.dtype, plan):
+        st, _ = run_plan(xd, rows, w.N, w.ld_in, w.ld_out, w.dtype, plan, out=y)
+        assert st == sr.SR_EPLAN
+        assert torch.isnan(y).all(), "a rejected plan wrote to the output"
+        return
+    st, y = run_plan(xd, rows, w.N, w.ld_in, w.ld_out, w.dtype, plan, out=y)
+    assert st == sr.SR_OK, sr.softmax_rows_strerror(st)
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, w.dtype), x, w.N, w.ld_in, w.dtype,
+                  "%s[%d:+%d] plan %s" % (name, row0, rows, sr.PLAN_NAMES[plan]))
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
+# ---- full sizes, automatic plan (the benchmark's launch), sampled rows ----
+
+FULL = ["f32_1024x256", "f32_4096x4096", "bf16_16384x1000_ld1024", "bf16_1024x131072",
+        "f16_causal_524288x2048"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w = synth.WORKLOADS[name]
+    x = w.generate()
+    xd = gu.to_device(x, w.dtype)
+    y = nan_filled(w.M, w.ld_out, w.dtype)
+    st = sr.softmax_rows(xd, y, w.M, w.N, w.ld_in, w.ld_out, w.dtype)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(1234)
+    sample = np.unique(np.concatenate([np.arange(min(64, w.M)), np.arange(max(0, w.M - 64), w.M),
+                                       rng.integers(0, w.M, 128)]))
+    ys = gu.to_host(y[torch.from_numpy(sample).to("cuda")], w.dtype)
+    gu.check_rows(ys, x[sample], w.N, w.ld_in, w.dtype, "%s sampled" % name)
+    # Properties of every row: finite, in [0, 1], sums to 1 within rounding,
+    # exact zeros where the input is -inf.
+    bound = {synth.F32: 2.0 ** -24, synth.BF16: 2.0 ** -9, synth.F16: 2.0 ** -11}[w.dtype]
+    chunk = max(1, (1 << 26) // w.N)
+    for r0 in range(0, w.M, chunk):
+        yc = y[r0:r0 + chunk, :w.N].double()
+        assert torch.isfinite(yc).all(), "%s: non-finite output near row %d" % (name, r0)
+        assert (yc >= 0).all() and (yc <= 1).all()
+        err = (yc.sum(dim=1) - 1).abs().max().item()
+        assert err <= bound + 2.0 ** -20, "%s: row sum off by %g near row %d" % (name, err, r0)
+        if w.causal_period:
+            xc = xd[r0:r0 + chunk, :w.N]
+            assert (y[r0:r0 + chunk, :w.N][torch.isneginf(xc)] == 0).all()
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
+# ---- edge shapes: widths around every plan boundary, odd row counts ----
+
+EDGE_N = [1, 2, 3, 7, 31, 33, 127, 255, 1000, 2047, 2048, 2049, 4095, 4104, 8192, 8193, 16384,
+          32769, 65536]
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N", EDGE_N)
+def test_edge_shapes(dtype, N):
+    for M in (1, 3, 157):
+        if M * N > 4_000_000:
+            continue
+        x = synth.generate(M, N, dtype=dtype, seed=N * 7 + M, p1=3.0)
+        xd = gu.to_device(x, dtype)
+        for plan in PLANS:
+            y = nan_filled(M, N, dtype)
+            if not plan_applies(xd, y, M, N, N, N, dtype, plan):
+                continue
+            st, y = run_plan(xd, M, N, N, N, dtype, plan, out=y)
+            assert st == sr.SR_OK
+            torch.cuda.synchronize()
+            gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype,
+                          "edge M=%d N=%d plan %s" % (M, N, sr.PLAN_NAMES[plan]))
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N", [100, 1000, 2048, 5000, 40000])
+def test_misaligned_rows(dtype, N):
+    """Rows not 16-byte aligned (one-element offsets, odd pitches) take the scalar plans."""
+    M = 37
+    ld_in, ld_out = N + 1, N + 3
+    x = synth.generate(M, N, ld=ld_in, dtype=dtype, seed=N + 3, p1=2.0)
+    base_in = gu.to_device(np.concatenate([x.reshape(-1)[:1], x.reshape(-1)]), dtype)
+    xd = base_in[1:]  # one element past a 16-byte boundary
+    yb = torch.full((M * ld_out + 1,), float("nan"), dtype=gu.torch_dtype(dtype), device="cuda")
+    yd = yb[1:]
+    for plan in PLANS:
+        if not plan_applies(xd, yd, M, N, ld_in, ld_out, dtype, plan):
+            assert plan in (sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_WARP)
+            continue
+        yb.fill_(float("nan"))
+        st = sr.load().softmax_rows_ex(xd.data_ptr(), yd.data_ptr(), M, N, ld_in, ld_out, dtype,
+                                       plan, torch.cuda.current_stream().cuda_stream)
+        assert st == sr.SR_OK
+        torch.cuda.synchronize()
+        out = gu.to_host(yd, dtype).reshape(M, ld_out)
+        gu.check_rows(out, x, N, ld_in, dtype, "misaligned N=%d plan %s" % (N, sr.PLAN_NAMES[plan]))
+        assert torch.isnan(yd.view(M, ld_out)[:, N:]).all(), "pad columns written"
+        assert torch.isnan(yb[:1]).all()
+
+
+# ---- rows whose answer is fixed by the definition ----
+
+def special_rows(N, dtype):
+    rows = []
+    rows.append(np.full(N, -math.inf))                       # all -inf -> NaN
+    r = np.linspace(-2, 2, N); r[N // 3] = math.nan; rows.append(r)   # NaN -> NaN row
+    r = np.linspace(-2, 2, N); r[N // 2] = math.inf; rows.append(r)   # +inf -> NaN row
+    rows.append(np.zeros(N))                                 # uniform -> 1/N
+    r = np.full(N, -math.inf); r[[0, N // 2, N - 1]] = 3.0; rows.append(r)  # 3 tied maxima
+    r = np.full(N, -math.inf); r[: max(1, N // 5)] = np.linspace(-1, 1, max(1, N // 5))
+    rows.append(r)                                           # masked suffix (causal row)
+    r = np.full(N, -math.inf); r[-1] = -7.0; rows.append(r)  # single finite entry -> 1
+    r = np.linspace(-100, 100, N); rows.append(r)            # extreme logits
+    from tests import pins
+    return pins.to_grid(np.array(rows), dtype)
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N", [5, 1000, 4096, 40000])
+def test_special_rows(dtype, N):
+    from tests import pins
+    vals = special_rows(N, dtype)
+    M = vals.shape[0]
+    x = pins.encode_exact(vals, dtype)
+    xd = gu.to_device(x, dtype)
+    for plan in PLANS:
+        y = nan_filled(M, N, dtype)
+        if not plan_applies(xd, y, M, N, N, N, dtype, plan):
+            continue
+        st, y = run_plan(xd, M, N, N, N, dtype, plan, out=y)
+        assert st == sr.SR_OK
+        torch.cuda.synchronize()
+        out = gu.to_host(y, dtype)
+        ref = gu.check_rows(out, x, N, N, dtype, "special N=%d plan %s" % (N, sr.PLAN_NAMES[plan]))
+        g = synth.storage_to_float64(out, dtype)
+        assert np.isnan(g[0]).all() and np.isnan(g[1]).all() and np.isnan(g[2]).all()
+        # Uniform row: the FP32 reciprocal of N rounded once to the dtype; for
+        # bf16/f16 that is the oracle's value unless rounding 1/N to binary32
+        # first lands on a tie of the 16-bit format.
+        want = {pins.to_grid([np.float32(1.0) / np.float32(N)], dtype)[0],
+                synth.storage_to_float64(ref[3:4, :1], dtype)[0, 0]}
+        assert set(np.unique(g[3])) <= want, (plan, np.unique(g[3]), want)
+        assert np.all(g[4][vals[4] == -math.inf] == 0.0)
+        assert np.all(g[5][vals[5] == -math.inf] == 0.0)
+        assert g[6][-1] == 1.0 and np.all(g[6][:-1] == 0.0)
+
+
+# ---- in place, canaries, streams, empty and rejected calls ----
+
+@pytest.mark.parametrize("name", ["f32_4096x4096", "bf16_16384x1000_ld1024", "bf16_1024x131072",
+                                  "f16_causal_524288x2048"])
+def test_in_place(name):
+    w = synth.WORKLOADS[name].with_rows(24)
+    x = w.generate()
+    for plan in PLANS:
+        buf = gu.to_device(x, w.dtype)
+        if not plan_applies(buf, buf, w.M, w.N, w.ld_in, w.ld_in, w.dtype, plan):
+            continue
+        st = sr.load().softmax_rows_ex(buf.data_ptr(), buf.data_ptr(), w.M, w.N, w.ld_in, w.ld_in,
+                                       w.dtype, plan, torch.cuda.current_stream().cuda_stream)
+        assert st == sr.SR_OK
+        torch.cuda.synchronize()
+        gu.check_rows(gu.to_host(buf, w.dtype), x, w.N, w.ld_in, w.dtype,
+                      "in place %s plan %s" % (name, sr.PLAN_NAMES[plan]))
+
+
+def test_guard_regions_untouched():
+    """Bytes before and after the output and its pad columns stay bit-identical."""
+    for name in FULL[:4]:
+        w = synth.WORKLOADS[name].with_rows(33)
+        x = w.generate()
+        xd = gu.to_device(x, w.dtype)
+        ld_out = w.N + 64
+        guard = 4096
+        total = guard + w.M * ld_out + guard
+        big = torch.full((total,), 0.125, dtype=gu.torch_dtype(w.dtype), device="cuda")
+        yd = big[guard:guard + w.M * ld_out]
+        for plan in PLANS:
+            if not plan_applies(xd, yd, w.M, w.N, w.ld_in, ld_out, w.dtype, plan):
+                continue
+            big.fill_(0.125)
+            st = sr.load().softmax_rows_ex(xd.data_ptr(), yd.data_ptr(), w.M, w.N, w.ld_in, ld_out,
+                                           w.dtype, plan, torch.cuda.current_stream().cuda_stream)
+            assert st == sr.SR_OK
+            torch.cuda.synchronize()
+            assert (big[:guard] == 0.125).all() and (big[-guard:] == 0.125).all()
+            assert (yd.view(w.M, ld_out)[:, w.N:] == 0.125).all()
+            gu.check_rows(gu.to_host(yd, w.dtype).reshape(w.M, ld_out), x, w.N, w.ld_in, w.dtype,
+                          "guard %s plan %s" % (name, sr.PLAN_NAMES[plan]))
+
+
+def test_side_stream_and_empty_calls():
+    w = synth.WORKLOADS["f32_4096x4096"].with_rows(50)
+    x = w.generate()
+    xd = gu.to_device(x, w.dtype)
+    y = nan_filled(w.M, w.N, w.dtype)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        st = sr.load().softmax_rows(xd.data_ptr(), y.data_ptr(), w.M, w.N, w.N, w.N, w.dtype,
+                                    s.cuda_stream)
+    assert st == sr.SR_OK
+    s.synchronize()
+    gu.check_rows(gu.to_host(y, w.dtype), x, w.N, w.N, w.dtype, "side stream")
+    y2 = nan_filled(4, 8, synth.F32)
+    assert sr.load().softmax_rows(xd.data_ptr(), y2.data_ptr(), 0, 8, 8, 8, 0, None) == sr.SR_OK
+    assert sr.load().softmax_rows(xd.data_ptr(), y2.data_ptr(), 4, 8, 4, 8, 0, None) == sr.SR_EINVAL
+    assert sr.load().softmax_rows(xd.data_ptr(), y2.data_ptr(), 4, 8, 8, 8, 7, None) == sr.SR_EDTYPE
+    torch.cuda.synchronize()
+    assert torch.isnan(y2).all()
+
+
+# ---- the bounded wait: an expiring wait reports an error, the context survives ----
+
+@pytest.mark.parametrize("name,plan", [("f32_4096x4096", sr.SR_PLAN_CTA),
+                                       ("bf16_1024x131072", sr.SR_PLAN_CLUSTER)])
+def test_bounded_wait_expiry(name, plan):
+    w = synth.WORKLOADS[name].with_rows(5)
+    x = w.generate()
+    xd = gu.to_device(x, w.dtype)
+    y = nan_filled(w.M, w.N, w.dtype)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    sr.softmax_rows_test_expiry(xd, y, w.M, w.N, w.ld_in, w.ld_out, w.dtype, plan, 2_000_000)
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert torch.isnan(y).all(), "an expired kernel wrote output"
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK  # the word was cleared
+    sr.softmax_rows_ex(xd, y, w.M, w.N, w.ld_in, w.ld_out, w.dtype, plan)
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, w.dtype), x, w.N, w.ld_in, w.dtype, "after expiry")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
