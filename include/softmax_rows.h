@@ -78,6 +78,9 @@ enum sr_status {
  *           cluster; aligned rows up to 512 KiB. One HBM read per element.
  *   ONLINE  one thread block per row, an online (max, sum) pass over the
  *           row followed by a normalise-and-write pass; any width, any alignment.
+ *   SMEM    one warp per row, each warp streaming its rows through its own
+ *           ring of shared-memory slots filled by bulk asynchronous copies;
+ *           no block barrier at all; aligned rows up to 32 KiB.
  * All plans run a persistent grid sized to the device's SM count.
  */
 enum sr_plan {
@@ -85,7 +88,8 @@ enum sr_plan {
     SR_PLAN_WARP = 1,
     SR_PLAN_CTA = 2,
     SR_PLAN_CLUSTER = 3,
-    SR_PLAN_ONLINE = 4
+    SR_PLAN_ONLINE = 4,
+    SR_PLAN_SMEM = 5
 };
 
 /*
@@ -133,7 +137,7 @@ SR_API int softmax_rows_plan_check(const void* in, const void* out, int64_t M, i
 SR_API int softmax_rows_last_device_error(sr_stream_t stream);
 
 /*
- * Test hook for the bounded-wait path: runs `plan` (CTA or CLUSTER) on the
+ * Test hook for the bounded-wait path: runs `plan` (CTA, CLUSTER or SMEM) on the
  * given arguments with its bulk copies switched off, so every wait for a copy
  * expires after `timeout_ns` nanoseconds; the kernel then records
  * SR_EDEVICE_TIMEOUT and returns without writing `out`. Nothing hangs and

@@ -170,17 +170,18 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
         case SR_PLAN_CTA: return vec && row_bytes <= kSliceMaxBytes;
         case SR_PLAN_CLUSTER: return vec && cluster_size_for(N, dtype, 2) > 0;
         case SR_PLAN_ONLINE: return true;
+        case SR_PLAN_SMEM: return vec && row_bytes <= kSmemMaxRowBytes;
     }
     return false;
 }
 
-// Automatic plan: registers for short rows, one block with a shared-memory
-// ring for rows up to 32 KiB, a cluster for rows up to 512 KiB, else the
-// two-pass online fallback.
+// Automatic plan: registers for short rows, a warp with its own shared-memory
+// ring for aligned rows up to 32 KiB, a cluster for rows up to 512 KiB, else
+// the two-pass online fallback.
 int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype) {
     if (N <= kWarpMaxN) return SR_PLAN_WARP;
-    if (plan_fits(SR_PLAN_CTA, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CTA;
+    if (plan_fits(SR_PLAN_SMEM, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_SMEM;
     if (plan_fits(SR_PLAN_CLUSTER, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CLUSTER;
     return SR_PLAN_ONLINE;
 }
@@ -204,6 +205,7 @@ int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t 
         case SR_PLAN_CTA: e = launch_tma(p, 1); break;
         case SR_PLAN_CLUSTER: e = launch_tma(p, cluster_size_for(N, dtype, 2)); break;
         case SR_PLAN_ONLINE: e = launch_online(p); break;
+        case SR_PLAN_SMEM: e = launch_smem(p); break;
         default: return SR_EPLAN;
     }
     return e == cudaSuccess ? SR_OK : SR_ECUDA;
@@ -222,7 +224,7 @@ int softmax_rows(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
 
 int softmax_rows_ex(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                     int64_t ld_out, int dtype, int plan, sr_stream_t stream) {
-    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ONLINE) return SR_EPLAN;
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_SMEM) return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    sr::kDefaultTimeoutNs, 0);
 }
@@ -239,7 +241,7 @@ int softmax_rows_plan_check(const void* in, const void* out, int64_t M, int64_t 
     const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
     if (bad) return -bad;
     if (plan == SR_PLAN_AUTO) return sr::choose_plan(in, out, N, ld_in, ld_out, dtype);
-    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ONLINE) return -SR_EPLAN;
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_SMEM) return -SR_EPLAN;
     return sr::plan_fits(plan, in, out, N, ld_in, ld_out, dtype) ? plan : -SR_EPLAN;
 }
 
@@ -259,7 +261,7 @@ int softmax_rows_last_device_error(sr_stream_t stream) {
 int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                              int64_t ld_out, int dtype, int plan, uint64_t timeout_ns,
                              sr_stream_t stream) {
-    if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER) return SR_EPLAN;
+    if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER && plan != SR_PLAN_SMEM) return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    (unsigned long long)timeout_ns, sr::kFlagNoCopy);
 }

@@ -281,6 +281,17 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float4 v) {
                  : "memory");
 }
 
+// Asynchronous 16-byte store into (possibly another block's) shared memory,
+// completing 16 transaction bytes on the mbarrier at `remote_bar` (both are
+// shared::cluster addresses of the same destination block).
+__device__ __forceinline__ void st_async_f4(uint32_t remote_addr, float4 v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+            "r"(remote_addr),
+        "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::

@@ -13,8 +13,15 @@ constexpr int kFlagNoCopy = 1;
 
 // Rows up to this many elements run one warp per row (64 values per lane).
 constexpr int64_t kWarpMaxN = 2048;
-// Largest row slice a thread block stages in shared memory.
+// Largest row slice a thread block stages in shared memory (CTA plan rows,
+// CLUSTER slices), and largest row a warp stages in its own ring (SMEM plan).
 constexpr int64_t kSliceMaxBytes = 32 * 1024;
+constexpr int64_t kSmemMaxRowBytes = 32 * 1024;
+// Preferred CLUSTER slice: smaller slices mean fewer registers per thread and
+// more blocks per SM; clusters grow up to kMaxCluster before slices grow.
+#ifndef SR_CLUSTER_SLICE_BYTES
+#define SR_CLUSTER_SLICE_BYTES (16 * 1024)
+#endif
 // Largest cluster (non-portable size 16 needs an opt-in attribute).
 constexpr int kMaxCluster = 16;
 
@@ -50,14 +57,16 @@ inline bool rows_vector_aligned(const void* in, const void* out, int64_t N, int6
            ((ld_out * es) % 16 == 0) && ((N * es) % 16 == 0);
 }
 
-// Cluster size for a row: the smallest power of two whose slices fit
-// kSliceMaxBytes, at least `min_cluster`; 0 when the row is too wide.
+// Cluster size for a row: the smallest power of two (at least `min_cluster`)
+// whose slices fit SR_CLUSTER_SLICE_BYTES, else the smallest whose slices fit
+// kSliceMaxBytes; 0 when the row is too wide (or too short to split).
 inline int cluster_size_for(int64_t N, int dtype, int min_cluster) {
-    const int64_t row_bytes = N * elem_bytes(dtype);
-    for (int c = min_cluster; c <= kMaxCluster; c *= 2) {
-        const int64_t nvec = row_bytes / 16;
-        const int64_t per = (nvec + c - 1) / c;
-        if (per * 16 <= kSliceMaxBytes && nvec >= c) return c;
+    const int64_t nvec = N * elem_bytes(dtype) / 16;
+    for (int64_t limit : {(int64_t)SR_CLUSTER_SLICE_BYTES, kSliceMaxBytes}) {
+        for (int c = min_cluster; c <= kMaxCluster; c *= 2) {
+            const int64_t per = (nvec + c - 1) / c;
+            if (per * 16 <= limit && nvec >= c) return c;
+        }
     }
     return 0;
 }
@@ -72,5 +81,6 @@ cudaError_t ensure_smem_limit(const void* func, size_t smem, bool nonportable_cl
 cudaError_t launch_warp(const Problem& p);
 cudaError_t launch_tma(const Problem& p, int cluster);
 cudaError_t launch_online(const Problem& p);
+cudaError_t launch_smem(const Problem& p);
 
 }  // namespace sr

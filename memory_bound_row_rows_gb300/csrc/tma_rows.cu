@@ -11,20 +11,22 @@
 // CLUSTER plan (the split plan of "Measured optimization case studies",
 // Wide rows, kept on chip): a cluster of `csize` blocks owns a row; block k
 // stages slice k. Each block reduces its slice to an online (max, sum) pair
-// with the all -inf guard of the same section, pushes the pair into every
-// peer's shared memory (distributed shared memory), and after one cluster
-// barrier every block merges the csize pairs and writes its slice. Every input
-// element is read from HBM once and written once, and exponentiated once.
+// with the all -inf guard of the same section and stores the pair into every
+// peer's shared memory with st.async, which completes on the peer's exchange
+// mbarrier; each block waits (bounded) for the csize pairs, merges them and
+// writes its slice. No cluster-wide barrier (and so no cluster-scope fence)
+// sits in the row loop. Every input element is read from HBM once, written
+// once and exponentiated once.
 //
 // Per row (both plans): each warp reduces its values to (m_w, s_w) with
-// e = exp(x - m_w); warp 0 merges the warps' pairs; the exchange barrier
-// (block or cluster) publishes the merged pair(s); each warp rescales its e by
-// exp(m_w - M) / S and stores.
+// e = exp(x - m_w); warp 0 merges the warps' pairs and publishes the block's
+// pair (block barrier, or st.async to the cluster); each warp rescales its e
+// by exp(m_w - M) / S and stores.
 //
-// Every wait for a bulk copy is bounded (wall clock, `timeout_ns`); on expiry
-// the kernel records the failure in the error word, all blocks of the
-// cluster stop at the same row, in-flight copies are drained (again bounded)
-// and the kernel returns.
+// Every wait (bulk copy, exchange) is bounded (wall clock, `timeout_ns`); on
+// expiry the block records the failure in the error word, stops at its next
+// block barrier, drains its in-flight copies (again bounded) and returns; its
+// peers' exchange waits then expire too.
 #include "device.cuh"
 #include "internal.h"
 
@@ -43,8 +45,10 @@ constexpr int kTmaThreads = 256;
 struct SmemLayout {
     uint32_t stage_bytes;
     int stages;
+    // [stages x stage_bytes] rows | 8 stage mbarriers + 2 exchange mbarriers |
+    // 32 warp partials (float4) | 2 x kMaxCluster exchange slots (float4)
     __host__ __device__ uint32_t bar_off() const { return stage_bytes * stages; }
-    __host__ __device__ uint32_t red_off() const { return bar_off() + 8u * 8u; }
+    __host__ __device__ uint32_t red_off() const { return bar_off() + 16u * 8u; }
     __host__ __device__ uint32_t xch_off() const { return red_off() + 32u * 16u; }
     __host__ __device__ uint32_t total() const { return xch_off() + 2u * kMaxCluster * 16u; }
 };
@@ -58,7 +62,8 @@ __global__ void __launch_bounds__(NT)
     constexpr int NW = NT / 32;
     extern __shared__ __align__(128) unsigned char smem[];
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t bar0 = sbase + L.bar_off();
+    const uint32_t bar0 = sbase + L.bar_off();   // stage barriers
+    const uint32_t xbar0 = bar0 + 8u * 8u;      // exchange barriers (cluster plan)
     float4* red = reinterpret_cast<float4*>(smem + L.red_off());
     float4* xch = reinterpret_cast<float4*>(smem + L.xch_off());
 
@@ -77,6 +82,8 @@ __global__ void __launch_bounds__(NT)
 
     if (tid == 0) {
         for (int s = 0; s < L.stages; ++s) mbar_init(bar0 + 8u * s, 1);
+        mbar_init(xbar0, 1);
+        mbar_init(xbar0 + 8u, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -94,16 +101,17 @@ __global__ void __launch_bounds__(NT)
         for (int s = 0; s < L.stages && unit + (int64_t)s * nunits < M; ++s) issue(issued++);
     }
 
+    bool local_fail = false;
     for (int64_t it = 0;; ++it) {
         const int64_t r = unit + it * nunits;
-        if (r >= M) break;
+        if (r >= M) break;  // uniform: every block of a cluster walks the same rows
         const int s = (int)(it % L.stages);
-        const uint32_t parity = (uint32_t)((it / L.stages) & 1);
 
-        bool ok = true;
-        if (cnt > 0) {
-            ok = mbar_wait_bounded(bar0 + 8u * s, parity, timeout_ns);
+        bool ok = !local_fail;
+        if (ok && cnt > 0) {
+            ok = mbar_wait_bounded(bar0 + 8u * s, (uint32_t)((it / L.stages) & 1), timeout_ns);
             if (tid == 0 && ok) confirmed = it + 1;
+            local_fail = !ok;
         }
 
         // Slice values into registers (vectors tid, tid+NT, ...).
@@ -120,7 +128,7 @@ __global__ void __launch_bounds__(NT)
             }
         }
 
-        // Warp partial: m_w, then e = exp(x - shift) and s_w.
+        // Warp partial: m_w, then e = exp(x - shift) and s_w (all -inf guard).
         float mx = v[0][0];
 #pragma unroll
         for (int k = 0; k < KV; ++k)
@@ -144,49 +152,55 @@ __global__ void __launch_bounds__(NT)
 #pragma unroll
             for (int e = 0; e < w; ++e) sv[e] += sv[e + w];
         const float s_w = warp_sum(sv[0]);
-        const bool warp_failed = __any_sync(0xffffffffu, !ok);
-        if (lane == 0) red[warp] = make_float4(m_w, s_w, warp_failed ? 1.0f : 0.0f, 0.0f);
-        __syncthreads();  // the stage is consumed; warp partials are visible
+        if (lane == 0) red[warp] = make_float4(m_w, s_w, 0.0f, 0.0f);
+        // The stage is consumed and the warp partials are visible; a failure
+        // anywhere in the block stops every thread here, together.
+        if (__syncthreads_or(local_fail)) {
+            local_fail = true;
+            break;
+        }
 
         if (warp == 0) {
             const float4 pw = lane < NW ? red[lane] : make_float4(neg_inf(), 0.0f, 0.0f, 0.0f);
             const float mk = warp_max(pw.x);
             const float sk = warp_sum(pw.y * merge_scale(pw.x, mk));
-            const bool fk = __any_sync(0xffffffffu, pw.z != 0.0f);
-            const float4 pk = make_float4(mk, sk, fk ? 1.0f : 0.0f, 0.0f);
             // Refill the consumed stage with the row `stages` iterations ahead.
-            if (tid == 0 && copies && !fk && issued == it + L.stages &&
-                unit + (it + L.stages) * nunits < M) {
-                fence_proxy_async_smem();
+            if (tid == 0 && copies && issued == it + L.stages &&
+                unit + (it + L.stages) * nunits < M)
                 issue(issued++);
-            }
             if constexpr (CLUSTER) {
-                const int slot = (int)(it & 1) * kMaxCluster + rank;
-                if (lane < csize) st_cluster_f4(map_to_rank(smem_addr(xch + slot), lane), pk);
+                // Publish (mk, sk) into slot [it&1][rank] of every block of the
+                // cluster; each store completes 16 bytes on the receiver's
+                // exchange barrier for this parity.
+                const int p = (int)(it & 1);
+                if (tid == 0) mbar_expect_tx(xbar0 + 8u * p, (uint32_t)csize * 16u);
+                if (lane < csize) {
+                    const uint32_t slot = smem_addr(xch + p * kMaxCluster + rank);
+                    st_async_f4(map_to_rank(slot, lane), make_float4(mk, sk, 0.0f, 0.0f),
+                                map_to_rank(xbar0 + 8u * p, lane));
+                }
             } else {
-                if (lane == 0) xch[0] = pk;
+                if (lane == 0) xch[0] = make_float4(mk, sk, 0.0f, 0.0f);
             }
         }
-        if constexpr (CLUSTER) cluster_sync_all(); else __syncthreads();
 
         // Row (M, S) from the published pair(s).
         float Mr, Sr;
-        bool failed;
         if constexpr (CLUSTER) {
-            const int base = (int)(it & 1) * kMaxCluster;
-            const float4 pk = lane < csize ? xch[base + lane] : make_float4(neg_inf(), 0.0f, 0.0f, 0.0f);
+            const int p = (int)(it & 1);
+            if (!mbar_wait_bounded(xbar0 + 8u * p, (uint32_t)((it >> 1) & 1), timeout_ns)) {
+                local_fail = true;  // a peer stopped; the next block barrier stops us
+                continue;
+            }
+            const float4 pk = lane < csize ? xch[p * kMaxCluster + lane]
+                                           : make_float4(neg_inf(), 0.0f, 0.0f, 0.0f);
             Mr = warp_max(pk.x);
             Sr = warp_sum(pk.y * merge_scale(pk.x, Mr));
-            failed = __any_sync(0xffffffffu, pk.z != 0.0f);
         } else {
+            __syncthreads();
             const float4 pk = xch[0];
             Mr = pk.x;
             Sr = pk.y;
-            failed = pk.z != 0.0f;
-        }
-        if (failed) {
-            if (tid == 0) atomicOr(err, 1u);
-            break;  // uniform across the cluster: every block read the same flags
         }
 
         const float f = merge_scale(m_w, Mr) * final_rcp(Mr, Sr);
@@ -203,12 +217,14 @@ __global__ void __launch_bounds__(NT)
         }
     }
 
-    // Drain copies still in flight (only after a failure), bounded.
     if (tid == 0) {
+        if (local_fail) atomicOr(err, 1u);
+        // Drain copies still in flight (only after a failure), bounded.
         for (int64_t j = confirmed; j < issued; ++j)
             mbar_wait_bounded(bar0 + 8u * (uint32_t)(j % L.stages), (uint32_t)((j / L.stages) & 1),
                               timeout_ns);
     }
+    // No block of the cluster leaves while a peer may still store into it.
     if constexpr (CLUSTER) cluster_sync_all();
 }
 

@@ -67,13 +67,14 @@ def test_rejected_arguments_touch_no_device(lib):
     assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 4096, 4096, 4096, 0, sr.SR_PLAN_WARP,
                              None) == sr.SR_EPLAN
     assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, 9, None) == sr.SR_EPLAN
+    assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, 6, None) == sr.SR_EPLAN
     assert L.softmax_rows_test_expiry(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, sr.SR_PLAN_WARP,
                                       1000, None) == sr.SR_EPLAN
 
 
 EXPECTED_PLANS = {
     "f32_1024x256": sr.SR_PLAN_WARP,
-    "f32_4096x4096": sr.SR_PLAN_CTA,
+    "f32_4096x4096": sr.SR_PLAN_SMEM,
     "bf16_16384x1000_ld1024": sr.SR_PLAN_WARP,
     "bf16_1024x131072": sr.SR_PLAN_CLUSTER,
     "f16_causal_524288x2048": sr.SR_PLAN_WARP,
@@ -90,10 +91,10 @@ def test_plan_for_each_workload(lib, name):
 def test_plan_depends_on_alignment_and_width(lib):
     P = sr.softmax_rows_plan
     A, B = ALIGNED_IN, ALIGNED_OUT
-    assert P(A, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_CTA
+    assert P(A, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_SMEM
     assert P(A + 4, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_ONLINE   # misaligned input
     assert P(A, B, 10, 4096, 4097, 4096, 0) == sr.SR_PLAN_ONLINE       # odd pitch
-    assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_CTA          # 32 KiB rows
+    assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_SMEM         # 32 KiB rows
     assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_CLUSTER      # just over 32 KiB
     assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_CLUSTER  # 512 KiB bf16
     assert P(A, B, 10, 262152, 262152, 262152, 1) == sr.SR_PLAN_ONLINE  # wider than a cluster
@@ -112,6 +113,10 @@ def test_forced_plan_checks(lib):
     assert C(A + 2, B, 5, 1000, 1000, 1000, 1, sr.SR_PLAN_CTA) == -sr.SR_EPLAN
     assert C(A + 2, B, 5, 1000, 1000, 1000, 1, sr.SR_PLAN_ONLINE) == sr.SR_PLAN_ONLINE
     assert C(A, B, 5, 8, 8, 8, 1, sr.SR_PLAN_CLUSTER) == -sr.SR_EPLAN  # one vector per row
+    assert C(A, B, 5, 8, 8, 8, 1, sr.SR_PLAN_SMEM) == sr.SR_PLAN_SMEM
+    assert C(A, B, 5, 16384, 16384, 16384, 1, sr.SR_PLAN_SMEM) == sr.SR_PLAN_SMEM
+    assert C(A, B, 5, 16392, 16392, 16392, 1, sr.SR_PLAN_SMEM) == -sr.SR_EPLAN  # > 32 KiB
+    assert C(A, B, 5, 8, 8, 8, 1, 6) == -sr.SR_EPLAN
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

@@ -18,7 +18,8 @@ pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
-PLANS = [sr.SR_PLAN_AUTO, sr.SR_PLAN_WARP, sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_ONLINE]
+PLANS = [sr.SR_PLAN_AUTO, sr.SR_PLAN_WARP, sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_ONLINE,
+         sr.SR_PLAN_SMEM]
 
 
 def nan_filled(M, ld, dtype):
@@ -142,7 +143,7 @@ def test_misaligned_rows(dtype, N):
     yd = yb[1:]
     for plan in PLANS:
         if not plan_applies(xd, yd, M, N, ld_in, ld_out, dtype, plan):
-            assert plan in (sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_WARP)
+            assert plan in (sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_WARP, sr.SR_PLAN_SMEM)
             continue
         yb.fill_(float("nan"))
         st = sr.load().softmax_rows_ex(xd.data_ptr(), yd.data_ptr(), M, N, ld_in, ld_out, dtype,
@@ -269,7 +270,9 @@ def test_side_stream_and_empty_calls():
 # ---- the bounded wait: an expiring wait reports an error, the context survives ----
 
 @pytest.mark.parametrize("name,plan", [("f32_4096x4096", sr.SR_PLAN_CTA),
-                                       ("bf16_1024x131072", sr.SR_PLAN_CLUSTER)])
+                                       ("bf16_1024x131072", sr.SR_PLAN_CLUSTER),
+                                       ("f32_4096x4096", sr.SR_PLAN_SMEM),
+                                       ("f16_causal_524288x2048", sr.SR_PLAN_SMEM)])
 def test_bounded_wait_expiry(name, plan):
     w = synth.WORKLOADS[name].with_rows(5)
     x = w.generate()
