@@ -69,7 +69,10 @@ enum sr_status {
 };
 
 /*
- * Kernel plans. AUTO picks by row width, dtype and alignment:
+ * Kernel plans. AUTO picks by row width, dtype and alignment: ROW for
+ * aligned rows of 4 KiB to 32 KiB, WARP for shorter rows, CLUSTER for aligned
+ * rows up to 512 KiB, ONLINE otherwise. Every plan computes the same
+ * function; forcing one (softmax_rows_ex) only changes the schedule:
  *   WARP    one warp per row, the row resident in registers; rows up to 2048 elements.
  *   CTA     one thread block per row, the row staged in shared memory by
  *           bulk asynchronous copies; aligned rows up to 32 KiB.
@@ -81,7 +84,9 @@ enum sr_status {
  *   SMEM    one warp per row, each warp streaming its rows through its own
  *           ring of shared-memory slots filled by bulk asynchronous copies;
  *           no block barrier at all; aligned rows up to 32 KiB.
- * All plans run a persistent grid sized to the device's SM count.
+ *   ROW     one thread block per row loaded straight into registers, one
+ *           block per row in the grid; aligned rows up to 2048 vectors.
+ * All plans but ROW run a persistent grid sized to the device's SM count.
  */
 enum sr_plan {
     SR_PLAN_AUTO = 0,
@@ -89,7 +94,8 @@ enum sr_plan {
     SR_PLAN_CTA = 2,
     SR_PLAN_CLUSTER = 3,
     SR_PLAN_ONLINE = 4,
-    SR_PLAN_SMEM = 5
+    SR_PLAN_SMEM = 5,
+    SR_PLAN_ROW = 6
 };
 
 /*

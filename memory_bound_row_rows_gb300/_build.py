@@ -19,7 +19,8 @@ LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libsoftmax_rows.so")
 HEADER = os.path.join(ROOT, "include", "softmax_rows.h")
 
-UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu", "smem_rows.cu"]
+UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu", "smem_rows.cu",
+         "block_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]

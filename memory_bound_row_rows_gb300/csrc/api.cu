@@ -171,17 +171,22 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
         case SR_PLAN_CLUSTER: return vec && cluster_size_for(N, dtype, 2) > 0;
         case SR_PLAN_ONLINE: return true;
         case SR_PLAN_SMEM: return vec && row_bytes <= kSmemMaxRowBytes;
+        case SR_PLAN_ROW: return vec && row_plan_fits(N, dtype);
     }
     return false;
 }
 
-// Automatic plan: registers for short rows, a warp with its own shared-memory
-// ring for aligned rows up to 32 KiB, a cluster for rows up to 512 KiB, else
-// the two-pass online fallback.
+// Automatic plan (from plan sweeps on GB300, cold L2):
+//  - aligned rows of 256..2048 16-byte vectors: ROW (one block per row);
+//  - shorter rows (or unaligned rows up to 2048 elements): WARP;
+//  - aligned rows up to 512 KiB: CLUSTER;
+//  - anything else: ONLINE.
 int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype) {
+    const bool vec = rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
+    const int64_t nvec = N * elem_bytes(dtype) / 16;
+    if (vec && nvec >= kRowMinVectors && row_plan_fits(N, dtype)) return SR_PLAN_ROW;
     if (N <= kWarpMaxN) return SR_PLAN_WARP;
-    if (plan_fits(SR_PLAN_SMEM, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_SMEM;
     if (plan_fits(SR_PLAN_CLUSTER, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CLUSTER;
     return SR_PLAN_ONLINE;
 }
@@ -206,6 +211,7 @@ int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t 
         case SR_PLAN_CLUSTER: e = launch_tma(p, cluster_size_for(N, dtype, 2)); break;
         case SR_PLAN_ONLINE: e = launch_online(p); break;
         case SR_PLAN_SMEM: e = launch_smem(p); break;
+        case SR_PLAN_ROW: e = launch_row(p); break;
         default: return SR_EPLAN;
     }
     return e == cudaSuccess ? SR_OK : SR_ECUDA;
@@ -224,7 +230,7 @@ int softmax_rows(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
 
 int softmax_rows_ex(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                     int64_t ld_out, int dtype, int plan, sr_stream_t stream) {
-    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_SMEM) return SR_EPLAN;
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    sr::kDefaultTimeoutNs, 0);
 }
@@ -241,7 +247,7 @@ int softmax_rows_plan_check(const void* in, const void* out, int64_t M, int64_t 
     const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
     if (bad) return -bad;
     if (plan == SR_PLAN_AUTO) return sr::choose_plan(in, out, N, ld_in, ld_out, dtype);
-    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_SMEM) return -SR_EPLAN;
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return -SR_EPLAN;
     return sr::plan_fits(plan, in, out, N, ld_in, ld_out, dtype) ? plan : -SR_EPLAN;
 }
 

@@ -1,0 +1,161 @@
+// ROW plan: one thread block per row, the row loaded straight into registers.
+//
+// The one-program-per-row fused softmax of "Fused Softmax on GPU" (Triton,
+// one block per row) and of "Triton: Writing GPU Kernels in Python,
+// Measured" (Step 2), written for sm_103a: every thread issues all of its
+// 16-byte loads at once, the block reduces the max and the sum through
+// shuffles and one shared-memory step each, and stores with 16-byte
+// streaming stores. The grid has one block per row (not persistent): the
+// hardware block scheduler hands rows to SMs as blocks retire, so a row that
+// finishes late never holds back a whole statically assigned share, which is
+// what sets the tail of a short kernel.
+#include "device.cuh"
+#include "internal.h"
+
+// Threads per row: the power of two that gives each thread about
+// SR_ROW_TARGET_KV 16-byte vectors, within [SR_ROW_MIN_THREADS, SR_ROW_MAX_THREADS].
+#ifndef SR_ROW_TARGET_KV
+#define SR_ROW_TARGET_KV 4
+#endif
+#ifndef SR_ROW_MIN_THREADS
+#define SR_ROW_MIN_THREADS 64
+#endif
+#ifndef SR_ROW_MAX_THREADS
+#define SR_ROW_MAX_THREADS 256
+#endif
+constexpr int kRowMaxKV = 8;
+
+namespace sr {
+namespace {
+
+template <typename T, int NT, int KV>
+__global__ void __launch_bounds__(NT)
+    block_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                      int64_t ld_in, int64_t ld_out) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int NW = NT / 32;
+    __shared__ float red_m[NW], red_s[NW];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nvec = (int)(N / VEC);
+
+    for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
+        const T* rin = in + r * ld_in;
+        float v[KV][VEC];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + NT * k;
+            if (idx < nvec) {
+                Elem<T>::unpack(ldg_stream(rin + (int64_t)idx * VEC), v[k]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) v[k][e] = neg_inf();
+            }
+        }
+        float mx = v[0][0];
+#pragma unroll
+        for (int k = 0; k < KV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, v[k][e]);
+        mx = warp_max(mx);
+        if (lane == 0) red_m[warp] = mx;
+        __syncthreads();
+        float m = red_m[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) m = fmaxf(m, red_m[w]);
+        const float m_l2 = m * kLog2e;
+
+        float sv[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) sv[e] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k)
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                v[k][e] = exp_shifted<T>(v[k][e], m, m_l2);
+                sv[e] += v[k][e];
+            }
+#pragma unroll
+        for (int w = VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+            for (int e = 0; e < w; ++e) sv[e] += sv[e + w];
+        const float sw = warp_sum(sv[0]);
+        if (lane == 0) red_s[warp] = sw;
+        __syncthreads();
+        float s = red_s[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) s += red_s[w];
+        const float rs = __frcp_rn(s);
+
+        T* rout = out + r * ld_out;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + NT * k;
+            if (idx < nvec) {
+                float y[VEC];
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) y[e] = v[k][e] * rs;
+                stg_stream(rout + (int64_t)idx * VEC, Elem<T>::pack(y));
+            }
+        }
+    }
+}
+
+template <typename T, int NT, int KV>
+cudaError_t launch_nt_kv(const Problem& p) {
+    auto kern = block_rows_kernel<T, NT, KV>;
+    // One block per row, capped at the largest grid dimension; rows beyond it
+    // are walked with a grid stride.
+    const int64_t cap = 0x7fffffff;
+    const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
+    kern<<<grid, NT, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
+                                    p.N, p.ld_in, p.ld_out);
+    return cudaGetLastError();
+}
+
+template <typename T, int NT>
+cudaError_t launch_nt(const Problem& p, int64_t nvec) {
+    const int64_t kv = (nvec + NT - 1) / NT;
+    if (kv <= 1) return launch_nt_kv<T, NT, 1>(p);
+    if (kv <= 2) return launch_nt_kv<T, NT, 2>(p);
+    if (kv <= 4) return launch_nt_kv<T, NT, 4>(p);
+    if (kv <= kRowMaxKV) return launch_nt_kv<T, NT, kRowMaxKV>(p);
+    return cudaErrorInvalidValue;
+}
+
+inline int row_threads(int64_t nvec) {
+    int nt = SR_ROW_MIN_THREADS;
+    while (nt < SR_ROW_MAX_THREADS && (int64_t)nt * SR_ROW_TARGET_KV < nvec) nt *= 2;
+    return nt;
+}
+
+template <typename T>
+cudaError_t launch_typed(const Problem& p) {
+    constexpr int VEC = Elem<T>::kVec;
+    const int64_t nvec = p.N / VEC;
+    const int nt = row_threads(nvec);
+    if constexpr (SR_ROW_MIN_THREADS <= 32) if (nt == 32) return launch_nt<T, 32>(p, nvec);
+    if constexpr (SR_ROW_MIN_THREADS <= 64) if (nt == 64) return launch_nt<T, 64>(p, nvec);
+    if (nt == 128) return launch_nt<T, 128>(p, nvec);
+    if constexpr (SR_ROW_MAX_THREADS >= 256) if (nt == 256) return launch_nt<T, 256>(p, nvec);
+    if constexpr (SR_ROW_MAX_THREADS >= 512) if (nt == 512) return launch_nt<T, 512>(p, nvec);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+// Rows the ROW plan takes (aligned ones): at most kRowMaxKV vectors per thread.
+bool row_plan_fits(int64_t N, int dtype) {
+    const int64_t nvec = N / (16 / elem_bytes(dtype));
+    return nvec <= (int64_t)kRowMaxKV * row_threads(nvec);
+}
+
+cudaError_t launch_row(const Problem& p) {
+    switch (p.dtype) {
+        case kF32: return launch_typed<float>(p);
+        case kBF16: return launch_typed<__nv_bfloat16>(p);
+        case kF16: return launch_typed<__half>(p);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sr

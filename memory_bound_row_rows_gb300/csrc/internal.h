@@ -13,6 +13,8 @@ constexpr int kFlagNoCopy = 1;
 
 // Rows up to this many elements run one warp per row (64 values per lane).
 constexpr int64_t kWarpMaxN = 2048;
+// Aligned rows of at least this many 16-byte vectors run one block per row.
+constexpr int64_t kRowMinVectors = 256;
 // Largest row slice a thread block stages in shared memory (CTA plan rows,
 // CLUSTER slices), and largest row a warp stages in its own ring (SMEM plan).
 constexpr int64_t kSliceMaxBytes = 32 * 1024;
@@ -20,7 +22,7 @@ constexpr int64_t kSmemMaxRowBytes = 32 * 1024;
 // Preferred CLUSTER slice: smaller slices mean fewer registers per thread and
 // more blocks per SM; clusters grow up to kMaxCluster before slices grow.
 #ifndef SR_CLUSTER_SLICE_BYTES
-#define SR_CLUSTER_SLICE_BYTES (16 * 1024)
+#define SR_CLUSTER_SLICE_BYTES (32 * 1024)
 #endif
 // Largest cluster (non-portable size 16 needs an opt-in attribute).
 constexpr int kMaxCluster = 16;
@@ -82,5 +84,7 @@ cudaError_t launch_warp(const Problem& p);
 cudaError_t launch_tma(const Problem& p, int cluster);
 cudaError_t launch_online(const Problem& p);
 cudaError_t launch_smem(const Problem& p);
+cudaError_t launch_row(const Problem& p);
+bool row_plan_fits(int64_t N, int dtype);
 
 }  // namespace sr

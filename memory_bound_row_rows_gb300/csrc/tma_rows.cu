@@ -36,6 +36,15 @@
 #ifndef SR_TMA_MAX_STAGES
 #define SR_TMA_MAX_STAGES 4
 #endif
+// CLUSTER plan: stage budget per block, and the resident blocks per SM the
+// widest slices are compiled for (the register file holds every block's
+// FP32 slice values, so it is what bounds the blocks per SM).
+#ifndef SR_CLUSTER_STAGE_BUDGET
+#define SR_CLUSTER_STAGE_BUDGET (96 * 1024)
+#endif
+#ifndef SR_CLUSTER_MIN_BLOCKS
+#define SR_CLUSTER_MIN_BLOCKS 2
+#endif
 
 namespace sr {
 namespace {
@@ -54,7 +63,7 @@ struct SmemLayout {
 };
 
 template <typename T, int NT, int KV, bool CLUSTER>
-__global__ void __launch_bounds__(NT)
+__global__ void __launch_bounds__(NT, (CLUSTER && KV * Elem<T>::kVec >= 64) ? SR_CLUSTER_MIN_BLOCKS : 1)
     tma_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                     int64_t ld_in, int64_t ld_out, int csize, SmemLayout L, unsigned int* err,
                     unsigned long long timeout_ns, int flags) {
@@ -275,7 +284,7 @@ cudaError_t launch_typed(const Problem& p, int csize) {
     const int64_t per = (nvec + csize - 1) / csize;  // vectors per block
     SmemLayout L;
     L.stage_bytes = (uint32_t)(((per * 16) + 127) / 128 * 128);
-    int stages = (int)(SR_TMA_STAGE_BUDGET / L.stage_bytes);
+    int stages = (int)((CLUSTER ? SR_CLUSTER_STAGE_BUDGET : SR_TMA_STAGE_BUDGET) / L.stage_bytes);
     stages = stages < 2 ? 2 : (stages > SR_TMA_MAX_STAGES ? SR_TMA_MAX_STAGES : stages);
     L.stages = stages;
     if ((int64_t)L.total() > p.dev->smem_optin) return cudaErrorInvalidValue;

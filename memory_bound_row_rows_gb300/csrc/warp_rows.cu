@@ -20,6 +20,11 @@ namespace sr {
 namespace {
 
 constexpr int kWarpBlock = 256;  // 8 warps per block
+// 1: persistent grid (resident blocks x SMs, grid-stride over rows);
+// 0: one warp per row, the hardware scheduler hands out the rows.
+#ifndef SR_WARP_PERSISTENT
+#define SR_WARP_PERSISTENT 1
+#endif
 
 template <typename T, int VEC, int KV>
 __global__ void __launch_bounds__(kWarpBlock)
@@ -105,11 +110,14 @@ __global__ void __launch_bounds__(kWarpBlock)
 template <typename T, int VEC, int KV>
 cudaError_t launch_one(const Problem& p) {
     auto kern = warp_rows_kernel<T, VEC, KV>;
-    const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(kern), kWarpBlock, 0);
-    if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     const int64_t warps_per_block = kWarpBlock / 32;
     const int64_t need = (p.M + warps_per_block - 1) / warps_per_block;
-    const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
+    int64_t cap = 0x7fffffff;
+    if (SR_WARP_PERSISTENT) {
+        const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(kern), kWarpBlock, 0);
+        if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+        cap = (int64_t)per_sm * p.dev->sm_count;
+    }
     const unsigned grid = (unsigned)(need < cap ? need : cap);
     kern<<<grid, kWarpBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
                                             p.M, (int)p.N, p.ld_in, p.ld_out);

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 PLANS = [sr.SR_PLAN_AUTO, sr.SR_PLAN_WARP, sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_ONLINE,
-         sr.SR_PLAN_SMEM]
+         sr.SR_PLAN_SMEM, sr.SR_PLAN_ROW]
 
 
 def nan_filled(M, ld, dtype):
@@ -143,7 +143,8 @@ def test_misaligned_rows(dtype, N):
     yd = yb[1:]
     for plan in PLANS:
         if not plan_applies(xd, yd, M, N, ld_in, ld_out, dtype, plan):
-            assert plan in (sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_WARP, sr.SR_PLAN_SMEM)
+            assert plan in (sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_WARP, sr.SR_PLAN_SMEM,
+                            sr.SR_PLAN_ROW)
             continue
         yb.fill_(float("nan"))
         st = sr.load().softmax_rows_ex(xd.data_ptr(), yd.data_ptr(), M, N, ld_in, ld_out, dtype,
