@@ -81,16 +81,20 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
-def recorded_traffic(workload: str, source_hash: str):
-    """DRAM bytes per launch from the committed ncu summary, if taken on this build."""
+def recorded_traffic(workload: str, plan: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current sources of the kernel this plan runs (else None)."""
+    from memory_bound_row_rows_gb300 import _build
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         rec = d.get(workload)
-        if rec and rec.get("source_hash") == source_hash:
+        files = _build.PLAN_SOURCES.get(plan)
+        if rec and files and rec.get("plan") == plan and \
+                rec.get("source_hash") == _build.source_hash(files):
             return rec.get("dram_bytes_per_launch"), rec
-    except (OSError, ValueError):
+    except (OSError, ValueError, KeyError):
         pass
     return None, None
 
@@ -266,21 +270,22 @@ def run_ours(args, w, rank, local_rank, world):
 
 
 def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
-    """Same metric through the C ABI with host buffers: pinned H2D, softmax, D2H."""
+    """Same metric through the C ABI with host buffers: softmax_rows_host streams the
+    pinned host matrix through a device workspace (copy-in, compute and copy-out of
+    consecutive chunks overlapped), and the result lands back in pinned host memory."""
     import torch
+    import memory_bound_row_rows_gb300 as sr
     x_pin = host_tensor(x).pin_memory()
     y_pin = torch.empty((w.M, w.ld_out), dtype=tdt).pin_memory()
-    x_dev = torch.empty((w.M, w.ld_in), dtype=tdt, device=dev)
-    y_dev = torch.empty((w.M, w.ld_out), dtype=tdt, device=dev)
+    need = sr.softmax_rows_host_workspace_bytes(w.M, w.N, w.dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        x_dev.copy_(x_pin, non_blocking=True)
-        st = lib.softmax_rows(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in, w.ld_out,
-                              w.dtype, stream.cuda_stream)
+        st = lib.softmax_rows_host(x_pin.data_ptr(), y_pin.data_ptr(), w.M, w.N, w.ld_in,
+                                   w.ld_out, w.dtype, ws.data_ptr(), need, stream.cuda_stream)
         if st != 0:
-            raise RuntimeError("softmax_rows failed")
-        y_pin.copy_(y_dev, non_blocking=True)
+            raise RuntimeError("softmax_rows_host failed: %s" % sr.softmax_rows_strerror(st))
 
     for _ in range(3):
         step()
@@ -296,8 +301,10 @@ def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
     sec = t0.elapsed_time(t1) / 1e3 / k
     eb = w.elem_bytes
     return {"value": round(w.fused_bytes / sec / 1e9, 2), "unit": "GB/s",
-            "h2d_bytes_per_step": w.M * w.ld_in * eb, "d2h_bytes_per_step": w.M * w.ld_out * eb,
-            "ms_per_step": round(sec * 1e3, 4), "steps": k}
+            "h2d_bytes_per_step": w.M * w.N * eb, "d2h_bytes_per_step": w.M * w.N * eb,
+            "ms_per_step": round(sec * 1e3, 4), "steps": k,
+            "path": "softmax_rows_host: pinned host -> device workspace -> pinned host, "
+                    "chunks overlapped on three streams"}
 
 
 def parity_vs_oracle(w, y_dev, y_ref, max_elements: int = 1 << 25):
@@ -325,6 +332,22 @@ def parity_vs_oracle(w, y_dev, y_ref, max_elements: int = 1 << 25):
             "max_abs_err": float(np.nanmax(np.abs(g - r)))}
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest of every rank's value (identity without a process group)."""
+    import torch
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(fused_bytes: int, steps: int, world: int, slowest_total_s: float) -> float:
+    """Whole-job GB/s when every rank runs the full workload (weak scaling):
+    all ranks' bytes over the slowest rank's time."""
+    return world * fused_bytes * steps / slowest_total_s / 1e9
+
+
 def bench_ours(args, w):
     import torch
     rank, local_rank, world = dist_env()
@@ -333,19 +356,15 @@ def bench_ours(args, w):
     from memory_bound_row_rows_gb300 import _build
     res = run_ours(args, w, rank, local_rank, world)
     ms = res["ms"]
-    total_s = sum(ms) / 1e3
-    if world > 1:
-        t = torch.tensor([total_s], dtype=torch.float64, device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_s = float(t.item())
+    total_s = max_over_ranks(sum(ms) / 1e3, device="cuda" if world > 1 else "cpu")
     if rank != 0:
         return None
     steps = len(ms)
     mean_s = total_s / steps
-    value = world * w.fused_bytes * steps / total_s / 1e9
+    value = replica_throughput(w.fused_bytes, steps, world, total_s)
     peaks = measured_peaks()
-    src_hash = _build.source_hash()
-    traffic, rec = recorded_traffic(w.name, src_hash)
+    src_hash = _build.source_hash(_build.PLAN_SOURCES.get(res["plan"]))
+    traffic, rec = recorded_traffic(w.name, res["plan"])
     achieved = w.fused_bytes / (sum(ms) / 1e3 / steps) / 1e9
     line = {
         "metric": "cold-L2 softmax GB/s (2*M*N*bytes/time)" if args.lane == "cold"

@@ -153,6 +153,33 @@ SR_API int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_
                              int64_t ld_out, int dtype, int plan, uint64_t timeout_ns,
                              sr_stream_t stream);
 
+/*
+ * The same softmax for matrices in HOST memory (h_in, h_out: host pointers,
+ * same layout rules as softmax_rows). Rows are streamed through the device
+ * in chunks: copied host -> device into the caller's device workspace
+ * `d_work` (work_bytes bytes, 16-byte aligned, owned by the caller), reduced
+ * there, and copied back, with copy-in, compute and copy-out of consecutive
+ * chunks overlapped on three streams the library creates once per device.
+ * Host buffers must be page-locked (cudaHostAlloc or cudaHostRegister) for
+ * the copies to run asynchronously and overlap. The call returns once the
+ * work is enqueued: `stream` waits for the whole pipeline, so synchronise it
+ * before reading h_out; work queued on `stream` earlier runs first. Calls on
+ * one device are enqueued one at a time (a library lock); calls that share a
+ * workspace must be ordered by the caller (for example on one stream).
+ * work_bytes must hold at least two staged rows; softmax_rows_host_workspace_bytes
+ * gives the size for full overlap. Returns like softmax_rows, or SR_EINVAL for
+ * a missing or too small workspace.
+ */
+SR_API int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,
+                             int64_t ld_out, int dtype, void* d_work, int64_t work_bytes,
+                             sr_stream_t stream);
+
+/*
+ * Device workspace size (bytes) with which softmax_rows_host overlaps its
+ * copies at full depth for M rows of N elements, or a negative sr_status.
+ */
+SR_API int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype);
+
 /* A static, human-readable name for an sr_status value. */
 SR_API const char* softmax_rows_strerror(int status);
 

@@ -18,7 +18,8 @@ __all__ = [
     "PLAN_NAMES", "SoftmaxRowsError", "load", "lib_path",
     "softmax_rows", "softmax_rows_ex", "softmax_rows_plan", "softmax_rows_plan_check",
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
-    "softmax_rows_version", "softmax", "dtype_code",
+    "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes", "softmax",
+    "dtype_code",
 ]
 
 SR_F32, SR_BF16, SR_F16 = 0, 1, 2
@@ -64,12 +65,15 @@ def load():
         "softmax_rows_last_device_error": [vp],
         "softmax_rows_test_expiry": [vp, vp, i64, i64, i64, i64, c_int, c_int, u64, vp],
         "softmax_rows_strerror": [c_int],
+        "softmax_rows_host": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
+        "softmax_rows_host_workspace_bytes": [i64, i64, c_int],
         "softmax_rows_version": [],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
-        fn.restype = ctypes.c_char_p if name == "softmax_rows_strerror" else c_int
+        fn.restype = {"softmax_rows_strerror": ctypes.c_char_p,
+                      "softmax_rows_host_workspace_bytes": i64}.get(name, c_int)
     _lib = lib
     return lib
 
@@ -131,6 +135,18 @@ def softmax_rows_test_expiry(in_, out, M, N, ld_in, ld_out, dtype, plan, timeout
     return _check(load().softmax_rows_test_expiry(_ptr(in_), _ptr(out), M, N, ld_in, ld_out,
                                                   dtype, plan, timeout_ns, _stream(stream)),
                   "softmax_rows_test_expiry")
+
+
+def softmax_rows_host(h_in, h_out, M, N, ld_in, ld_out, dtype, d_work, work_bytes,
+                      stream=None) -> int:
+    """Host-memory variant: h_in/h_out are host pointers (page-locked for overlap)."""
+    return _check(load().softmax_rows_host(_ptr(h_in), _ptr(h_out), M, N, ld_in, ld_out, dtype,
+                                           _ptr(d_work), work_bytes, _stream(stream)),
+                  "softmax_rows_host")
+
+
+def softmax_rows_host_workspace_bytes(M, N, dtype) -> int:
+    return int(load().softmax_rows_host_workspace_bytes(M, N, dtype))
 
 
 def softmax_rows_strerror(status: int) -> str:

@@ -20,7 +20,7 @@ LIB = os.path.join(LIBDIR, "libsoftmax_rows.so")
 HEADER = os.path.join(ROOT, "include", "softmax_rows.h")
 
 UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu", "smem_rows.cu",
-         "block_rows.cu"]
+         "block_rows.cu", "host_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]
@@ -44,9 +44,28 @@ def _stamp(extra_flags) -> str:
     return h.hexdigest()
 
 
-def source_hash() -> str:
-    """Hash of the kernel sources (used to tie profiler counters to a build)."""
-    return _stamp([])[:16]
+# Sources each plan's kernel is built from (besides the shared headers).
+PLAN_SOURCES = {
+    "row": ["block_rows.cu"], "warp": ["warp_rows.cu"], "cta": ["tma_rows.cu"],
+    "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
+}
+SHARED_SOURCES = ["device.cuh", "internal.h"]
+
+
+def source_hash(files=None) -> str:
+    """Hash of kernel sources and build flags, tying profiler counters to a build.
+
+    ``files`` (names under csrc/) limits it to one kernel's sources plus the
+    shared device headers; None hashes every source.
+    """
+    if files is None:
+        return _stamp([])[:16]
+    h = hashlib.sha256()
+    for name in sorted(set(files) | set(SHARED_SOURCES)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    h.update(" ".join(ARCH + NVCC_FLAGS).encode())
+    return h.hexdigest()[:16]
 
 
 def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: bool = False) -> str:

@@ -217,6 +217,11 @@ int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t 
     return e == cudaSuccess ? SR_OK : SR_ECUDA;
 }
 
+int launch_auto(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
+                int dtype, cudaStream_t stream) {
+    return run(in, out, M, N, ld_in, ld_out, dtype, SR_PLAN_AUTO, stream, kDefaultTimeoutNs, 0);
+}
+
 }  // namespace
 }  // namespace sr
 
@@ -270,6 +275,22 @@ int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, in
     if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER && plan != SR_PLAN_SMEM) return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    (unsigned long long)timeout_ns, sr::kFlagNoCopy);
+}
+
+int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype) {
+    if (dtype != SR_F32 && dtype != SR_BF16 && dtype != SR_F16) return -SR_EDTYPE;
+    if (M < 0 || N < 1) return -SR_EINVAL;
+    return sr::host_workspace_bytes(M, N, dtype);
+}
+
+int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,
+                      int64_t ld_out, int dtype, void* d_work, int64_t work_bytes,
+                      sr_stream_t stream) {
+    const int bad = sr::check_args(h_in, h_out, M, N, ld_in, ld_out, dtype);
+    if (bad) return bad;
+    if (M == 0) return SR_OK;
+    return sr::run_host(h_in, h_out, M, N, ld_in, ld_out, dtype, d_work, work_bytes,
+                        (cudaStream_t)stream, sr::launch_auto);
 }
 
 const char* softmax_rows_strerror(int status) {

@@ -292,6 +292,16 @@ __device__ __forceinline__ void st_async_f4(uint32_t remote_addr, float4 v, uint
         : "memory");
 }
 
+// The same for an 8-byte pair.
+__device__ __forceinline__ void st_async_f2(uint32_t remote_addr, float a, float b,
+                                            uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+            remote_addr),
+        "f"(a), "f"(b), "r"(remote_bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::

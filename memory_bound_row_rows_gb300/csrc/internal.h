@@ -86,5 +86,10 @@ cudaError_t launch_online(const Problem& p);
 cudaError_t launch_smem(const Problem& p);
 cudaError_t launch_row(const Problem& p);
 bool row_plan_fits(int64_t N, int dtype);
+int64_t host_workspace_bytes(int64_t M, int64_t N, int dtype);
+int run_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
+             int dtype, void* d_work, int64_t work_bytes, cudaStream_t stream,
+             int (*launch)(const void*, void*, int64_t, int64_t, int64_t, int64_t, int,
+                           cudaStream_t));
 
 }  // namespace sr
