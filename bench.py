@@ -53,7 +53,11 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=synth.HEADLINE,
-                    help="one of %s, or 'all'" % ", ".join(synth.WORKLOADS))
+                    help="one of %s; 'all' (those five) or 'wide' (%s)"
+                         % (", ".join(synth.WORKLOADS), ", ".join(synth.WIDE_FEW)))
+    ap.add_argument("--api", choices=("rows", "split"), default="rows",
+                    help="rows: softmax_rows / softmax_rows_ex; split: softmax_rows_split "
+                         "with a device workspace (the split plan for few, wide rows)")
     ap.add_argument("--lane", choices=("cold", "warm"), default="cold")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--plan", type=int, default=0, help="forced plan (0 = automatic)")
@@ -215,6 +219,11 @@ def run_ours(args, w, rank, local_rank, world):
 
     x_dev = host_tensor(x).to(dev)
     y_dev = torch.empty((w.M, w.ld_out), dtype=tdt, device=dev)
+    ws, ws_bytes = None, 0
+    if args.api == "split":
+        ws_bytes = sr.softmax_rows_split_workspace_bytes(x_dev, y_dev, w.M, w.N, w.ld_in,
+                                                         w.ld_out, w.dtype)
+        ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
     # float32 so the reduction reads the buffer directly (an int32 sum would
     # first widen it to int64, writing 1 GiB and leaving dirty lines in L2).
     flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -224,8 +233,12 @@ def run_ours(args, w, rank, local_rank, world):
         if args.plan == 0 else args.plan
 
     def step():
-        st = lib.softmax_rows_ex(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
-                                 w.ld_out, w.dtype, args.plan, sh)
+        if args.api == "split":
+            st = lib.softmax_rows_split(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
+                                        w.ld_out, w.dtype, ws.data_ptr(), ws_bytes, sh)
+        else:
+            st = lib.softmax_rows_ex(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
+                                     w.ld_out, w.dtype, args.plan, sh)
         if st != 0:
             raise RuntimeError("softmax_rows failed: %s" % sr.softmax_rows_strerror(st))
 
@@ -265,7 +278,10 @@ def run_ours(args, w, rank, local_rank, world):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, x, dev, lib, host_tensor, tdt)
-    return {"ms": ms, "clocks": clk.summary(), "plan": sr.PLAN_NAMES.get(plan_used, str(plan_used)),
+    if args.api == "split":
+        plan_used = "split"
+    return {"ms": ms, "clocks": clk.summary(),
+            "plan": plan_used if isinstance(plan_used, str) else sr.PLAN_NAMES.get(plan_used, str(plan_used)),
             "y_dev": y_dev, "e2e": e2e, "x": x}
 
 
@@ -391,7 +407,7 @@ def bench_ours(args, w):
         "median_step_us": round(statistics.median(ms) * 1e3, 3),
         "p10_p90_step_us": [round(float(np.percentile(ms, 10)) * 1e3, 3),
                             round(float(np.percentile(ms, 90)) * 1e3, 3)],
-        "gpu_launches": steps,
+        "gpu_launches": steps * (2 if res["plan"] == "split" else 1),
         "clocks": res["clocks"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -446,9 +462,11 @@ def bench_reference(args, w):
 
 def main(argv=None):
     args = parse_args(argv)
-    names = list(synth.WORKLOADS) if args.workload == "all" else [args.workload]
+    catalog = dict(synth.WORKLOADS, **synth.WIDE_FEW)
+    names = (list(synth.WORKLOADS) if args.workload == "all" else
+             list(synth.WIDE_FEW) if args.workload == "wide" else [args.workload])
     for name in names:
-        w = synth.WORKLOADS[name]
+        w = catalog[name]
         if args.rows:
             w = w.with_rows(min(args.rows, w.M))
         line = bench_reference(args, w) if args.impl == "reference" else bench_ours(args, w)

@@ -180,6 +180,34 @@ SR_API int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N
  */
 SR_API int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype);
 
+/*
+ * The split plan for few, wide rows ("Measured optimization case studies",
+ * Wide rows: split across programs when there are fewer rows than SMs).
+ * Every row is cut into chunks handled by separate thread blocks; a first
+ * kernel writes each chunk's online (max, sum) pair into `workspace`, a second
+ * kernel has every chunk merge its row's pairs (with the all -inf guard) and
+ * write exp(x - M) / S for its chunk, rereading the input. Same arguments and
+ * layout rules as softmax_rows, plus a caller-owned DEVICE workspace of at
+ * least softmax_rows_split_workspace_bytes(...) bytes, 16-byte aligned, whose
+ * contents on entry do not matter. In-place use (in == out) is rejected
+ * (SR_EINVAL): the second kernel rereads the input. Calls that share a
+ * workspace must not overlap on the GPU. Returns like softmax_rows, or
+ * SR_EINVAL for a missing, misaligned or too small workspace.
+ */
+SR_API int softmax_rows_split(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                              int64_t ld_out, int dtype, void* workspace, int64_t workspace_bytes,
+                              sr_stream_t stream);
+
+/*
+ * Workspace bytes softmax_rows_split needs for these arguments (M * chunks
+ * pairs of floats; the chunking depends only on the arguments, not on the
+ * device), or a negative sr_status. Pure host logic; pointers are read only
+ * for alignment.
+ */
+SR_API int64_t softmax_rows_split_workspace_bytes(const void* in, const void* out, int64_t M,
+                                                  int64_t N, int64_t ld_in, int64_t ld_out,
+                                                  int dtype);
+
 /* A static, human-readable name for an sr_status value. */
 SR_API const char* softmax_rows_strerror(int status);
 

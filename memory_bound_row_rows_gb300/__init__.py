@@ -18,7 +18,8 @@ __all__ = [
     "PLAN_NAMES", "SoftmaxRowsError", "load", "lib_path",
     "softmax_rows", "softmax_rows_ex", "softmax_rows_plan", "softmax_rows_plan_check",
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
-    "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes", "softmax",
+    "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
+    "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax",
     "dtype_code",
 ]
 
@@ -67,13 +68,16 @@ def load():
         "softmax_rows_strerror": [c_int],
         "softmax_rows_host": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
         "softmax_rows_host_workspace_bytes": [i64, i64, c_int],
+        "softmax_rows_split": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
+        "softmax_rows_split_workspace_bytes": [vp, vp, i64, i64, i64, i64, c_int],
         "softmax_rows_version": [],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = {"softmax_rows_strerror": ctypes.c_char_p,
-                      "softmax_rows_host_workspace_bytes": i64}.get(name, c_int)
+                      "softmax_rows_host_workspace_bytes": i64,
+                      "softmax_rows_split_workspace_bytes": i64}.get(name, c_int)
     _lib = lib
     return lib
 
@@ -143,6 +147,19 @@ def softmax_rows_host(h_in, h_out, M, N, ld_in, ld_out, dtype, d_work, work_byte
     return _check(load().softmax_rows_host(_ptr(h_in), _ptr(h_out), M, N, ld_in, ld_out, dtype,
                                            _ptr(d_work), work_bytes, _stream(stream)),
                   "softmax_rows_host")
+
+
+def softmax_rows_split(in_, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,
+                       stream=None) -> int:
+    """Split plan for few, wide rows; `workspace` is a device buffer."""
+    return _check(load().softmax_rows_split(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
+                                            _ptr(workspace), workspace_bytes, _stream(stream)),
+                  "softmax_rows_split")
+
+
+def softmax_rows_split_workspace_bytes(in_, out, M, N, ld_in, ld_out, dtype) -> int:
+    return int(load().softmax_rows_split_workspace_bytes(_ptr(in_), _ptr(out), M, N, ld_in,
+                                                         ld_out, dtype))
 
 
 def softmax_rows_host_workspace_bytes(M, N, dtype) -> int:

@@ -277,6 +277,33 @@ int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, in
                    (unsigned long long)timeout_ns, sr::kFlagNoCopy);
 }
 
+int64_t softmax_rows_split_workspace_bytes(const void* in, const void* out, int64_t M, int64_t N,
+                                           int64_t ld_in, int64_t ld_out, int dtype) {
+    const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return -bad;
+    const sr::SplitShape sh = sr::split_shape(M, N, ld_in, ld_out, dtype, in, out);
+    return M * sh.chunks * (int64_t)sizeof(float2);
+}
+
+int softmax_rows_split(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                       int64_t ld_out, int dtype, void* workspace, int64_t workspace_bytes,
+                       sr_stream_t stream) {
+    const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return bad;
+    if (M == 0) return SR_OK;
+    const sr::SplitShape sh = sr::split_shape(M, N, ld_in, ld_out, dtype, in, out);
+    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 16 != 0 ||
+        workspace_bytes < M * sh.chunks * (int64_t)sizeof(float2))
+        return SR_EINVAL;
+    if (in == out) return SR_EINVAL;  // the second pass rereads the input
+    cudaError_t e;
+    const sr::DeviceInfo* dev = sr::device_info(&e);
+    if (!dev) return SR_ECUDA;
+    sr::Problem p{in, out, M, N, ld_in, ld_out, dtype, (cudaStream_t)stream, dev,
+                  sr::kDefaultTimeoutNs, 0};
+    return sr::launch_split(p, sh, workspace) == cudaSuccess ? SR_OK : SR_ECUDA;
+}
+
 int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype) {
     if (dtype != SR_F32 && dtype != SR_BF16 && dtype != SR_F16) return -SR_EDTYPE;
     if (M < 0 || N < 1) return -SR_EINVAL;

@@ -87,6 +87,21 @@ cudaError_t launch_smem(const Problem& p);
 cudaError_t launch_row(const Problem& p);
 bool row_plan_fits(int64_t N, int dtype);
 int64_t host_workspace_bytes(int64_t M, int64_t N, int dtype);
+
+// SPLIT plan: chunks per row and chunk length (in 16-byte vectors when vec > 1,
+// else in elements); the workspace holds M * chunks (max, sum) pairs.
+constexpr int64_t kSplitTargetBlocks = 640;
+constexpr int64_t kSplitMinUnits = 256;
+constexpr int64_t kSplitMaxChunks = 4096;
+constexpr int64_t kSplitMaxGridRows = 65535;
+struct SplitShape {
+    int64_t chunks = 1;
+    int64_t chunk_units = 1;
+    int vec = 1;
+};
+SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int dtype,
+                       const void* in, const void* out);
+cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws);
 int run_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
              int dtype, void* d_work, int64_t work_bytes, cudaStream_t stream,
              int (*launch)(const void*, void*, int64_t, int64_t, int64_t, int64_t, int,

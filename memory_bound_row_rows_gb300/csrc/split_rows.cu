@@ -1,0 +1,179 @@
+// SPLIT plan: rows cut into chunks across many blocks, statistics through a
+// workspace, two launches.
+//
+// The split plan of "Measured optimization case studies" (Wide rows): when
+// there are fewer rows than SMs, one program per row cannot fill the GPU, so
+// every row is split into chunks; the first kernel writes each chunk's
+// statistics, and in the second every chunk merges its row's statistics
+// itself and writes its part of the output. The statistics are online
+// (max, sum) pairs merged with the same section's rule and its guard for
+// chunks that are entirely -inf.
+//
+// stats_kernel: block (row r, chunk c) reduces its chunk to (m, s) with
+//   s = sum exp(x - m) and stores it at ws[r * C + c].
+// apply_kernel: block (row r, chunk c) merges ws[r * C .. r * C + C) into
+//   the row's (M, S), rereads its chunk (from L2 for the few-row shapes this
+//   plan is for) and writes exp(x - M) / S.
+// The grid is (C, M): block x = chunk, y = row. Chunks are whole 16-byte
+// vectors when rows are 16-byte aligned (VEC = 16 / sizeof(T)), else
+// elements (VEC = 1).
+#include "device.cuh"
+#include "internal.h"
+
+namespace sr {
+namespace {
+
+constexpr int kSplitThreads = 256;
+constexpr int kSplitNW = kSplitThreads / 32;
+
+template <typename T, int VEC>
+__device__ __forceinline__ void load_vec(const T* p, float* f) {
+    if constexpr (VEC == 1) {
+        f[0] = Elem<T>::load1(p);
+    } else {
+        Elem<T>::unpack(ldg_stream(p), f);
+    }
+}
+
+// Block-wide online (max, sum) merge; every thread returns the result.
+__device__ __forceinline__ void block_merge(float& m, float& s, float2* red) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        merge_ms(m, s, m2, s2);
+    }
+    if (lane == 0) red[warp] = make_float2(m, s);
+    __syncthreads();
+    m = red[0].x;
+    s = red[0].y;
+#pragma unroll
+    for (int w = 1; w < kSplitNW; ++w) merge_ms(m, s, red[w].x, red[w].y);
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kSplitThreads)
+    split_stats_kernel(const T* __restrict__ in, int64_t N, int64_t ld_in, int64_t chunk_units,
+                       float2* __restrict__ ws) {
+    __shared__ float2 red[kSplitNW];
+    const int64_t r = blockIdx.y, c = blockIdx.x, C = gridDim.x;
+    const int64_t units = N / VEC;  // VEC divides N when VEC > 1
+    const int64_t u0 = c * chunk_units;
+    const int64_t u1 = (u0 + chunk_units < units) ? u0 + chunk_units : units;
+    const T* rin = in + r * ld_in;
+    float m = neg_inf(), s = 0.0f;
+    for (int64_t u = u0 + threadIdx.x; u < u1; u += kSplitThreads) {
+        float f[VEC];
+        load_vec<T, VEC>(rin + u * VEC, f);
+        float cm = f[0];
+#pragma unroll
+        for (int e = 1; e < VEC; ++e) cm = fmaxf(cm, f[e]);
+        const float mn = fmaxf(m, cm);
+        const float shift = (mn == neg_inf()) ? 0.0f : mn;
+        float cs = 0.0f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) cs += expf(f[e] - shift);
+        s = s * merge_scale(m, mn) + cs;
+        m = mn;
+    }
+    block_merge(m, s, red);
+    if (threadIdx.x == 0) ws[r * C + c] = make_float2(m, s);
+}
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kSplitThreads)
+    split_apply_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t N, int64_t ld_in,
+                       int64_t ld_out, int64_t chunk_units, const float2* __restrict__ ws) {
+    __shared__ float2 red[kSplitNW];
+    const int64_t r = blockIdx.y, c = blockIdx.x, C = gridDim.x;
+    // The row's (M, S) from all of its chunks' pairs.
+    float m = neg_inf(), s = 0.0f;
+    for (int64_t k = threadIdx.x; k < C; k += kSplitThreads) {
+        const float2 q = ws[r * C + k];
+        merge_ms(m, s, q.x, q.y);
+    }
+    block_merge(m, s, red);
+    const float rs = final_rcp(m, s);
+    const float m_l2 = m * kLog2e;
+
+    const int64_t units = N / VEC;
+    const int64_t u0 = c * chunk_units;
+    const int64_t u1 = (u0 + chunk_units < units) ? u0 + chunk_units : units;
+    const T* rin = in + r * ld_in;
+    T* rout = out + r * ld_out;
+    for (int64_t u = u0 + threadIdx.x; u < u1; u += kSplitThreads) {
+        float f[VEC];
+        load_vec<T, VEC>(rin + u * VEC, f);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) f[e] = exp_shifted<T>(f[e], m, m_l2) * rs;
+        if constexpr (VEC == 1) {
+            Elem<T>::store1(rout + u, f[0]);
+        } else {
+            stg_stream(rout + u * VEC, Elem<T>::pack(f));
+        }
+    }
+}
+
+template <typename T, int VEC>
+cudaError_t launch_vec(const Problem& p, const SplitShape& sh, float2* ws) {
+    const dim3 grid((unsigned)sh.chunks, (unsigned)p.M, 1);
+    split_stats_kernel<T, VEC><<<grid, kSplitThreads, 0, p.stream>>>(
+        static_cast<const T*>(p.in), p.N, p.ld_in, sh.chunk_units, ws);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    split_apply_kernel<T, VEC><<<grid, kSplitThreads, 0, p.stream>>>(
+        static_cast<const T*>(p.in), static_cast<T*>(p.out), p.N, p.ld_in, p.ld_out,
+        sh.chunk_units, ws);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const Problem& p, const SplitShape& sh, float2* ws) {
+    if (sh.vec > 1) return launch_vec<T, 16 / sizeof(T)>(p, sh, ws);
+    return launch_vec<T, 1>(p, sh, ws);
+}
+
+}  // namespace
+
+// Chunking (host logic, the same on every device): about kSplitTargetBlocks
+// blocks in total, chunks of at least kSplitMinUnits vectors (or elements),
+// at most kSplitMaxChunks chunks per row.
+SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int dtype,
+                       const void* in, const void* out) {
+    SplitShape sh;
+    const bool vec = rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
+    sh.vec = vec ? 16 / elem_bytes(dtype) : 1;
+    const int64_t units = N / sh.vec;
+    const int64_t target_blocks = kSplitTargetBlocks;
+    int64_t chunks = M > 0 ? (target_blocks + M - 1) / M : 1;
+    const int64_t max_chunks = (units + kSplitMinUnits - 1) / kSplitMinUnits;
+    if (chunks > max_chunks) chunks = max_chunks;
+    if (chunks > kSplitMaxChunks) chunks = kSplitMaxChunks;
+    if (chunks < 1) chunks = 1;
+    sh.chunk_units = (units + chunks - 1) / chunks;
+    sh.chunks = (units + sh.chunk_units - 1) / sh.chunk_units;
+    return sh;
+}
+
+// Rows go in batches of at most kSplitMaxGridRows (the grid's y dimension).
+cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws) {
+    const int64_t es = elem_bytes(p.dtype);
+    for (int64_t r0 = 0; r0 < p.M; r0 += kSplitMaxGridRows) {
+        Problem q = p;
+        q.M = (p.M - r0 < kSplitMaxGridRows) ? p.M - r0 : kSplitMaxGridRows;
+        q.in = static_cast<const char*>(p.in) + r0 * p.ld_in * es;
+        q.out = static_cast<char*>(p.out) + r0 * p.ld_out * es;
+        float2* w = static_cast<float2*>(ws) + r0 * sh.chunks;
+        cudaError_t e = cudaErrorInvalidValue;
+        switch (p.dtype) {
+            case kF32: e = launch_typed<float>(q, sh, w); break;
+            case kBF16: e = launch_typed<__nv_bfloat16>(q, sh, w); break;
+            case kF16: e = launch_typed<__half>(q, sh, w); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace sr

@@ -178,6 +178,18 @@ WORKLOADS = {
     ]
 }
 
+# Few, wide rows (the wide-row shapes of "Measured optimization case studies",
+# FP16, N(0, 1)), for the split plan.
+WIDE_FEW = {
+    w.name: w
+    for w in [
+        Workload("f16_4x32769", F16, 4, 32769, 32769, 32769, 5, DIST_NORMAL, 0.0, 1.0),
+        Workload("f16_64x131072", F16, 64, 131072, 131072, 131072, 6, DIST_NORMAL, 0.0, 1.0),
+        Workload("f16_128x32769", F16, 128, 32769, 32769, 32769, 7, DIST_NORMAL, 0.0, 1.0),
+        Workload("f16_1024x16384", F16, 1024, 16384, 16384, 16384, 8, DIST_NORMAL, 0.0, 1.0),
+    ]
+}
+
 # The workload the headline throughput is quoted on (square FP32 matrix, 4096 x 4096).
 HEADLINE = "f32_4096x4096"
 

@@ -131,3 +131,19 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sr, "_lib", None)
     with pytest.raises(RuntimeError, match="not found"):
         sr.softmax_rows(1, 2, 1, 8, 8, 8, 0, 0)
+
+
+def test_split_workspace_is_host_logic(lib):
+    A, B = ALIGNED_IN, ALIGNED_OUT
+    W = sr.softmax_rows_split_workspace_bytes
+    # 4 rows x 32769 f16 (unaligned: chunks of elements): 129 chunks of 255 elements.
+    assert W(A, B, 4, 32769, 32769, 32769, 2) == 4 * 129 * 8
+    # 64 rows x 131072 f16 (aligned): 10 chunks per row.
+    assert W(A, B, 64, 131072, 131072, 131072, 2) == 64 * 10 * 8
+    # Many short rows: one chunk per row.
+    assert W(A, B, 100000, 64, 64, 64, 1) == 100000 * 8
+    assert W(A, B, 4, 0, 8, 8, 0) == -sr.SR_EINVAL
+    assert W(A, B, 4, 8, 8, 8, 9) == -sr.SR_EDTYPE
+    L = lib
+    assert L.softmax_rows_split(A, B, 0, 8, 8, 8, 0, None, 0, None) == sr.SR_OK
+    assert L.softmax_rows_split(A, B, 4, 8, 8, 8, 0, None, 1024, None) == sr.SR_EINVAL
