@@ -208,6 +208,32 @@ SR_API int64_t softmax_rows_split_workspace_bytes(const void* in, const void* ou
                                                   int64_t N, int64_t ld_in, int64_t ld_out,
                                                   int dtype);
 
+/*
+ * The split plan without a caller workspace, for callers that cannot
+ * allocate device memory: code held to a fixed device-memory budget reserved
+ * at start-up (inference servers, plugins inside another framework's memory
+ * pool), code that must not change the device's memory footprint while it
+ * runs, and code for which a cudaMalloc could implicitly synchronise the
+ * device. The source pages have no counterpart; this entry point only
+ * changes where the split plan keeps its statistics.
+ *
+ * Same arguments, results and layout rules as softmax_rows_split, without
+ * the workspace: the statistics live in a 512 KiB array built into the
+ * library's device image (every GPU that loads the library holds it until
+ * the process exits). This call allocates nothing and calls no allocating
+ * routine. Limit: softmax_rows_split_workspace_bytes(...) for the same
+ * arguments must be at most 524288 (65536 pairs, i.e. M * chunks); larger
+ * problems are rejected with SR_EINVAL, launching nothing. The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array and leaves its statistics in
+ * it; nothing in it needs to start at zero. Calls whose kernels overlap on
+ * the GPU (other streams, other host threads) race on the array: order them.
+ */
+SR_API int softmax_rows_split_noalloc(const void* in, void* out, int64_t M, int64_t N,
+                                      int64_t ld_in, int64_t ld_out, int dtype,
+                                      sr_stream_t stream);
+
 /* A static, human-readable name for an sr_status value. */
 SR_API const char* softmax_rows_strerror(int status);
 

@@ -19,7 +19,8 @@ __all__ = [
     "softmax_rows", "softmax_rows_ex", "softmax_rows_plan", "softmax_rows_plan_check",
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
-    "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax",
+    "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
+    "softmax",
     "dtype_code",
 ]
 
@@ -70,6 +71,7 @@ def load():
         "softmax_rows_host_workspace_bytes": [i64, i64, c_int],
         "softmax_rows_split": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
         "softmax_rows_split_workspace_bytes": [vp, vp, i64, i64, i64, i64, c_int],
+        "softmax_rows_split_noalloc": [vp, vp, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_version": [],
     }
     for name, args in sig.items():
@@ -155,6 +157,13 @@ def softmax_rows_split(in_, out, M, N, ld_in, ld_out, dtype, workspace, workspac
     return _check(load().softmax_rows_split(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
                                             _ptr(workspace), workspace_bytes, _stream(stream)),
                   "softmax_rows_split")
+
+
+def softmax_rows_split_noalloc(in_, out, M, N, ld_in, ld_out, dtype, stream=None) -> int:
+    """Split plan with the library's built-in scratch: allocates nothing (see the C header)."""
+    return _check(load().softmax_rows_split_noalloc(_ptr(in_), _ptr(out), M, N, ld_in, ld_out,
+                                                    dtype, _stream(stream)),
+                  "softmax_rows_split_noalloc")
 
 
 def softmax_rows_split_workspace_bytes(in_, out, M, N, ld_in, ld_out, dtype) -> int:

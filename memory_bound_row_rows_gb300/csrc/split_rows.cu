@@ -17,6 +17,9 @@
 // The grid is (C, M): block x = chunk, y = row. Chunks are whole 16-byte
 // vectors when rows are 16-byte aligned (VEC = 16 / sizeof(T)), else
 // elements (VEC = 1).
+#include <mutex>
+
+#include "../../include/softmax_rows.h"
 #include "device.cuh"
 #include "internal.h"
 
@@ -177,3 +180,60 @@ cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws) {
 }
 
 }  // namespace sr
+
+// ---------------------------------------------------------------------------
+// softmax_rows_split_noalloc: the split plan with built-in scratch.
+//
+// For callers that must not allocate device memory at all: code that runs
+// under a fixed memory budget reserved up front (inference servers, plugins
+// living inside another framework's memory pool), code that may not change
+// the device's memory footprint once it is running, and code called from
+// places where a cudaMalloc would implicitly synchronise the device and
+// stall other work. They pass only the input and the output; the
+// statistics live in the array below, which is part of the library's device
+// image: every GPU that loads the library holds it until the process exits.
+// ---------------------------------------------------------------------------
+namespace sr {
+namespace {
+
+// Room for this many (max, sum) pairs: M * chunks of a call must fit.
+constexpr int64_t kNoAllocPairs = 65536;  // 512 KiB
+static __device__ __align__(256) float2 g_noalloc_scratch[kNoAllocPairs];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[64];  // the array's device address, per device, once set up
+
+// Device address of the array on the current device (set up on first use,
+// with that device current). In host code the array's name is only a
+// stand-in, never a device address.
+int noalloc_scratch(void** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SR_ECUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (g_noalloc_addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+            return SR_ECUDA;
+        g_noalloc_addr[dev] = ptr;
+    }
+    *out = g_noalloc_addr[dev];
+    return SR_OK;
+}
+
+}  // namespace
+}  // namespace sr
+
+extern "C" int softmax_rows_split_noalloc(const void* in, void* out, int64_t M, int64_t N,
+                                          int64_t ld_in, int64_t ld_out, int dtype,
+                                          sr_stream_t stream) {
+    const int64_t need = softmax_rows_split_workspace_bytes(in, out, M, N, ld_in, ld_out, dtype);
+    if (need < 0) return (int)-need;
+    if (M == 0) return SR_OK;
+    if (need > sr::kNoAllocPairs * (int64_t)sizeof(float2)) return SR_EINVAL;  // too big
+    void* scratch = nullptr;
+    const int st = sr::noalloc_scratch(&scratch);
+    if (st != SR_OK) return st;
+    // Nothing in the scratch has to start at zero: the first kernel writes
+    // every pair the second one reads.
+    return softmax_rows_split(in, out, M, N, ld_in, ld_out, dtype, scratch, need, stream);
+}

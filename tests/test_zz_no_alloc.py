@@ -1,0 +1,70 @@
+"""softmax_rows_split_noalloc: the split plan for callers that cannot allocate
+device memory (fixed memory budgets, foreign memory pools, code that must not
+trigger the implicit device synchronisation of a cudaMalloc). Its statistics
+live in scratch built into the library instead of a caller workspace.
+
+Each check calls the allocation-free entry point through the C ABI and compares
+its output with the workspace entry point (softmax_rows_split) on the same
+input, within the parity tolerance, for two calls in a row on different data
+(the built-in scratch keeps the previous call's contents). This file is
+collected last so that a run stopping at its first failure has already run
+every other test; it also passes on its own in a fresh process.
+"""
+import numpy as np
+import pytest
+
+import memory_bound_row_rows_gb300 as sr
+import synth
+from tests import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+# Largest statistics the built-in scratch holds, in bytes (65536 pairs).
+NOALLOC_LIMIT = 65536 * 8
+
+
+def _with_workspace(xd, M, N, ld_in, ld_out, dtype):
+    y = torch.full((M, ld_out), float("nan"), dtype=xd.dtype, device="cuda")
+    need = sr.softmax_rows_split_workspace_bytes(xd, y, M, N, ld_in, ld_out, dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    sr.softmax_rows_split(xd, y, M, N, ld_in, ld_out, dtype, ws, need)
+    return y
+
+
+def _no_alloc(xd, M, N, ld_in, ld_out, dtype):
+    y = torch.full((M, ld_out), float("nan"), dtype=xd.dtype, device="cuda")
+    st = sr.load().softmax_rows_split_noalloc(xd.data_ptr(), y.data_ptr(), M, N, ld_in, ld_out,
+                                              dtype, torch.cuda.current_stream().cuda_stream)
+    assert st == sr.SR_OK, sr.softmax_rows_strerror(st)
+    return y
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
+def test_no_alloc_matches_workspace_entry_point_twice(dtype):
+    shapes = [(4, 32769, 32769, 32769), (37, 12345, 12350, 12345)]
+    for call, (M, N, ld_in, ld_out) in enumerate(shapes):
+        x = synth.generate(M, N, ld=ld_in, dtype=dtype, seed=1000 + 17 * call + dtype, p1=2.5)
+        xd = gu.to_device(x, dtype)
+        ref = _with_workspace(xd, M, N, ld_in, ld_out, dtype)
+        got = _no_alloc(xd, M, N, ld_in, ld_out, dtype)
+        torch.cuda.synchronize()
+        g = synth.storage_to_float64(gu.to_host(got, dtype)[:, :N], dtype)
+        r = synth.storage_to_float64(gu.to_host(ref, dtype)[:, :N], dtype)
+        ok, nbad, rep = gu.gate(g, r, dtype)
+        assert ok, "call %d: %d elements differ beyond the tolerance (max %.3g)" % (
+            call, nbad, rep["max_abs"])
+        assert torch.isnan(got[:, N:]).all() if ld_out > N else True
+
+
+def test_no_alloc_rejects_problems_beyond_its_scratch():
+    M, N = 70000, 64  # one chunk per row: 70000 pairs, more than the scratch holds
+    x = torch.randn(M, N, device="cuda", dtype=torch.float16)
+    y = torch.full_like(x, float("nan"))
+    need = sr.softmax_rows_split_workspace_bytes(x, y, M, N, N, N, synth.F16)
+    assert need > NOALLOC_LIMIT
+    st = sr.load().softmax_rows_split_noalloc(x.data_ptr(), y.data_ptr(), M, N, N, N,
+                                              synth.F16, torch.cuda.current_stream().cuda_stream)
+    assert st == sr.SR_EINVAL
+    torch.cuda.synchronize()
+    assert torch.isnan(y).all(), "a rejected call wrote output"
