@@ -52,6 +52,9 @@ class Oracle:
             fn = getattr(lib, name)
             fn.restype = c_int
             fn.argtypes = [vp, vp, i64, i64, i64, i64, c_int, c_int]
+        fn = lib.oracle_softmax_rows_masked
+        fn.restype = c_int
+        fn.argtypes = [vp, vp, i64, i64, i64, i64, c_int, vp, i64, c_int]
         for name in ("oracle_cast", "oracle_decode"):
             fn = getattr(lib, name)
             fn.restype = c_int
@@ -74,6 +77,24 @@ class Oracle:
                                           ld_out, dtype, nthreads)
         if rc != 0:
             raise ValueError("oracle_softmax_rows returned %d" % rc)
+        return out
+
+    def softmax_rows_masked(self, x: np.ndarray, M: int, N: int, ld_in: int, ld_out: int,
+                            dtype: int, lens=None, causal_period: int = 0,
+                            nthreads: int = 1) -> np.ndarray:
+        """Masked softmax (entries past each row's valid length are -inf, never read)."""
+        x = np.ascontiguousarray(x)
+        assert x.dtype == _STORAGE[dtype] and x.size >= M * ld_in
+        out = np.zeros((M, ld_out), dtype=_STORAGE[dtype])
+        lp = None
+        if lens is not None:
+            lens = np.ascontiguousarray(lens, dtype=np.int32)
+            assert lens.size >= M
+            lp = lens.ctypes.data
+        rc = self.lib.oracle_softmax_rows_masked(x.ctypes.data, out.ctypes.data, M, N, ld_in,
+                                                 ld_out, dtype, lp, causal_period, nthreads)
+        if rc != 0:
+            raise ValueError("oracle_softmax_rows_masked returned %d" % rc)
         return out
 
     def softmax_rows_f64(self, x: np.ndarray, M: int, N: int, ld_in: int, dtype: int,

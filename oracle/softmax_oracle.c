@@ -147,15 +147,29 @@ typedef struct {
     int dtype;
     int64_t row_begin, row_end;
     double* work;   /* 2*N doubles */
+    const int32_t* lens;   /* per-row valid lengths, or NULL */
+    int64_t causal_period; /* used when lens is NULL: row i keeps i mod period + 1 entries */
 } job_t;
+
+/* Number of leading entries of row i that take part (the rest are -inf). */
+static int64_t valid_length(const job_t* jb, int64_t i) {
+    int64_t v = jb->N;
+    if (jb->lens) v = jb->lens[i];
+    else if (jb->causal_period > 0) v = i % jb->causal_period + 1;
+    if (v < 0) v = 0;
+    if (v > jb->N) v = jb->N;
+    return v;
+}
 
 static void* run_rows(void* arg) {
     job_t* jb = (job_t*)arg;
     double* x = jb->work;
     double* y = jb->work + jb->N;
     for (int64_t i = jb->row_begin; i < jb->row_end; ++i) {
+        /* Masked entries are -inf by definition and are never read. */
+        const int64_t v = valid_length(jb, i);
         for (int64_t j = 0; j < jb->N; ++j)
-            x[j] = decode(jb->in, i * jb->ld_in + j, jb->dtype);
+            x[j] = j < v ? decode(jb->in, i * jb->ld_in + j, jb->dtype) : -INFINITY;
         softmax_row_f64(x, y, jb->N);
         for (int64_t j = 0; j < jb->N; ++j) {
             if (jb->out) encode(jb->out, i * jb->ld_out + j, jb->dtype, y[j]);
@@ -166,7 +180,8 @@ static void* run_rows(void* arg) {
 }
 
 static int run(const void* in, void* out, double* out64, int64_t M, int64_t N,
-               int64_t ld_in, int64_t ld_out, int dtype, int nthreads) {
+               int64_t ld_in, int64_t ld_out, int dtype, int nthreads, const int32_t* lens,
+               int64_t causal_period) {
     if (M < 0 || N < 1 || ld_in < N || ld_out < N) return 1;
     if (dtype < OR_F32 || dtype > OR_F16) return 2;
     if (M == 0) return 0;
@@ -184,7 +199,8 @@ static int run(const void* in, void* out, double* out64, int64_t M, int64_t N,
         int64_t b = t * per, e = (t + 1) * per;
         if (b > M) b = M;
         if (e > M) e = M;
-        job_t jb = {in, out, out64, N, ld_in, ld_out, dtype, b, e, work + 2 * N * (int64_t)t};
+        job_t jb = {in, out, out64, N, ld_in, ld_out, dtype, b, e, work + 2 * N * (int64_t)t,
+                    lens, causal_period};
         jobs[t] = jb;
     }
     if (nthreads == 1) {
@@ -212,13 +228,26 @@ static int run(const void* in, void* out, double* out64, int64_t M, int64_t N,
  */
 int oracle_softmax_rows(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                         int64_t ld_out, int dtype, int nthreads) {
-    return run(in, out, NULL, M, N, ld_in, ld_out, dtype, nthreads);
+    return run(in, out, NULL, M, N, ld_in, ld_out, dtype, nthreads, NULL, 0);
+}
+
+/*
+ * Masked softmax: in row i only the first L_i entries take part; the others
+ * are -inf (never read) and so come out as exact zeros. L_i = lens[i] when
+ * lens is not NULL, else i mod causal_period + 1 when causal_period > 0
+ * (the causal attention mask of rows holding query positions i mod period),
+ * else N; L_i is clamped to [0, N]. L_i = 0 leaves an all -inf row: NaN.
+ */
+int oracle_softmax_rows_masked(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                               int64_t ld_out, int dtype, const int32_t* lens,
+                               int64_t causal_period, int nthreads) {
+    return run(in, out, NULL, M, N, ld_in, ld_out, dtype, nthreads, lens, causal_period);
 }
 
 /* The same, returning the double values before the final cast (for diagnostics). */
 int oracle_softmax_rows_f64(const void* in, double* out64, int64_t M, int64_t N,
                             int64_t ld_in, int64_t ld_out, int dtype, int nthreads) {
-    return run(in, NULL, out64, M, N, ld_in, ld_out, dtype, nthreads);
+    return run(in, NULL, out64, M, N, ld_in, ld_out, dtype, nthreads, NULL, 0);
 }
 
 /* Step 5 alone: round doubles to `dtype` storage (f32 values or 16-bit patterns). */

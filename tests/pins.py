@@ -289,8 +289,59 @@ def check_thread_independence(orc):
     assert same(a, b)
 
 
+# ---- masked softmax (valid lengths, causal rows) ------------------------------
+
+def check_masked_brute(orc):
+    rng = np.random.default_rng(21)
+    for dtype in DTYPES:
+        for N in (1, 3, 8, 13):
+            M = 6
+            vals = to_grid(rng.normal(0, 3, size=(M, N)), dtype)
+            lens = np.array([0, 1, N, N + 5, -2, max(1, N // 2)], dtype=np.int32)
+            # Masked entries hold poison: they must never be read.
+            poisoned = vals.copy()
+            for i, L in enumerate(lens):
+                poisoned[i, max(0, min(L, N)):] = math.nan
+            x = encode_exact(poisoned, dtype)
+            got = decode(orc.softmax_rows_masked(x.reshape(-1), M, N, N, N, dtype, lens=lens), dtype)
+            for i, L in enumerate(lens):
+                L = max(0, min(int(L), N))
+                if L == 0:
+                    assert np.all(np.isnan(got[i])), "masked row of length 0 must be NaN"
+                    continue
+                want = np.zeros(N)
+                want[:L] = brute.softmax_exact_cast(vals[i, :L], dtype)
+                assert same(got[i], want), "masked brute dtype %d N=%d L=%d: %r vs %r" % (
+                    dtype, N, L, got[i], want)
+
+
+def check_masked_causal(orc):
+    for dtype in DTYPES:
+        P, N, M = 5, 7, 12
+        x = encode_exact(np.zeros((M, N)), dtype)  # constant rows: 1/L on the first L entries
+        got = decode(orc.softmax_rows_masked(x.reshape(-1), M, N, N, N, dtype, causal_period=P),
+                     dtype)
+        for i in range(M):
+            L = min(N, i % P + 1)
+            want = np.zeros(N)
+            want[:L] = brute.round_exact(Fraction(1, L), dtype)
+            assert same(got[i], want), "causal dtype %d row %d" % (dtype, i)
+        # The causal generator's rows: masking by period equals the data's own -inf mask.
+        w = synth.WORKLOADS["f16_causal_524288x2048"]
+        rows = w.generate_rows([0, 5, 2047, 2048, 4000])
+        lens = np.array([r % 2048 + 1 for r in (0, 5, 2047, 2048, 4000)], dtype=np.int32)
+        a = orc.softmax_rows_masked(rows.reshape(-1), 5, w.N, w.N, w.N, w.dtype, lens=lens)
+        vals = decode(rows, w.dtype)
+        for k in range(5):
+            L = int(lens[k])
+            assert np.all(decode(a[k, L:], w.dtype) == 0.0)
+            assert same(decode(a[k, :L], w.dtype), brute.softmax_exact_cast(vals[k, :L], w.dtype)) \
+                if L <= 16 else np.allclose(decode(a[k, :L], w.dtype).sum(), 1.0, atol=2e-3)
+
+
 ALL_CHECKS = [
     check_decode, check_cast, check_brute_random, check_brute_extremes, check_uniform_rows,
     check_two_entries, check_tied_maxima, check_causal_rows, check_nan_rows,
     check_row_sums_and_range, check_shift_invariance, check_strides, check_thread_independence,
+    check_masked_brute, check_masked_causal,
 ]

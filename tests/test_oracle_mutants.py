@@ -32,6 +32,9 @@ MUTANTS = {
     "f16_bias_off_by_one": ("e - 25);", "e - 24);"),
     "bf16_decode_shift": ("(uint32_t)h << 16;", "(uint32_t)h << 15;"),
     "f32_output_truncated": ("float f = (float)y;", "float f = (float)(y * (1.0 - 0x1p-30));"),
+    "masked_as_zero": ("decode(jb->in, i * jb->ld_in + j, jb->dtype) : -INFINITY;",
+                       "decode(jb->in, i * jb->ld_in + j, jb->dtype) : 0.0;"),
+    "causal_off_by_one": ("v = i % jb->causal_period + 1;", "v = i % jb->causal_period;"),
 }
 
 
