@@ -55,9 +55,11 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=synth.HEADLINE,
                     help="one of %s; 'all' (those five) or 'wide' (%s)"
                          % (", ".join(synth.WORKLOADS), ", ".join(synth.WIDE_FEW)))
-    ap.add_argument("--api", choices=("rows", "split"), default="rows",
+    ap.add_argument("--api", choices=("rows", "split", "masked"), default="rows",
                     help="rows: softmax_rows / softmax_rows_ex; split: softmax_rows_split "
-                         "with a device workspace (the split plan for few, wide rows)")
+                         "with a device workspace (the split plan for few, wide rows); masked: "
+                         "softmax_rows_masked with the workload's causal period (masked "
+                         "entries are not read)")
     ap.add_argument("--lane", choices=("cold", "warm"), default="cold")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--plan", type=int, default=0, help="forced plan (0 = automatic)")
@@ -236,6 +238,9 @@ def run_ours(args, w, rank, local_rank, world):
         if args.api == "split":
             st = lib.softmax_rows_split(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
                                         w.ld_out, w.dtype, ws.data_ptr(), ws_bytes, sh)
+        elif args.api == "masked":
+            st = lib.softmax_rows_masked(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
+                                         w.ld_out, w.dtype, None, w.causal_period, args.plan, sh)
         else:
             st = lib.softmax_rows_ex(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
                                      w.ld_out, w.dtype, args.plan, sh)
@@ -280,6 +285,8 @@ def run_ours(args, w, rank, local_rank, world):
         e2e = run_e2e(args, w, x, dev, lib, host_tensor, tdt)
     if args.api == "split":
         plan_used = "split"
+    elif args.api == "masked":
+        plan_used = "masked-" + sr.PLAN_NAMES.get(plan_used, str(plan_used))
     return {"ms": ms, "clocks": clk.summary(),
             "plan": plan_used if isinstance(plan_used, str) else sr.PLAN_NAMES.get(plan_used, str(plan_used)),
             "y_dev": y_dev, "e2e": e2e, "x": x}
@@ -348,6 +355,19 @@ def parity_vs_oracle(w, y_dev, y_ref, max_elements: int = 1 << 25):
             "max_abs_err": float(np.nanmax(np.abs(g - r)))}
 
 
+def algorithmic_bytes(w, api: str) -> int:
+    """Bytes one call must move: every element read once and written once; with
+    the causal mask applied in the kernel, only the valid entries are read."""
+    if api == "masked" and w.causal_period > 0:
+        P = w.causal_period
+        full, rest = divmod(w.M, P)
+        def valid_sum(rows):  # rows 0..rows-1 of one period
+            return sum(min(w.N, q + 1) for q in range(rows))
+        valid = full * valid_sum(P) + valid_sum(rest)
+        return w.elem_bytes * (valid + w.M * w.N)
+    return w.fused_bytes
+
+
 def max_over_ranks(value: float, device="cpu") -> float:
     """The largest of every rank's value (identity without a process group)."""
     import torch
@@ -377,14 +397,16 @@ def bench_ours(args, w):
         return None
     steps = len(ms)
     mean_s = total_s / steps
-    value = replica_throughput(w.fused_bytes, steps, world, total_s)
+    nbytes = algorithmic_bytes(w, args.api)
+    value = replica_throughput(nbytes, steps, world, total_s)
     peaks = measured_peaks()
     src_hash = _build.source_hash(_build.PLAN_SOURCES.get(res["plan"]))
     traffic, rec = recorded_traffic(w.name, res["plan"])
-    achieved = w.fused_bytes / (sum(ms) / 1e3 / steps) / 1e9
+    achieved = nbytes / (sum(ms) / 1e3 / steps) / 1e9
     line = {
-        "metric": "cold-L2 softmax GB/s (2*M*N*bytes/time)" if args.lane == "cold"
-        else "warm-L2 softmax GB/s (2*M*N*bytes/time)",
+        "metric": ("cold-L2 softmax GB/s (2*M*N*bytes/time)" if args.lane == "cold"
+                   else "warm-L2 softmax GB/s (2*M*N*bytes/time)") if args.api != "masked"
+        else "cold-L2 masked softmax GB/s ((valid reads + M*N writes)*bytes/time)",
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
@@ -404,6 +426,8 @@ def bench_ours(args, w):
         "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "rows_per_s": round(world * w.M * steps / total_s, 1),
+        "bytes_per_step": nbytes,
+        "dense_equivalent_gbs": round(world * w.fused_bytes * steps / total_s / 1e9, 2),
         "median_step_us": round(statistics.median(ms) * 1e3, 3),
         "p10_p90_step_us": [round(float(np.percentile(ms, 10)) * 1e3, 3),
                             round(float(np.percentile(ms, 90)) * 1e3, 3)],

@@ -181,6 +181,27 @@ SR_API int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N
 SR_API int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype);
 
 /*
+ * Masked softmax: in row i only the first L_i entries take part, the others
+ * count as -inf; they are never read and are written as exact zeros. This is
+ * the attention-score softmax with its mask applied in the kernel instead of
+ * in the data (the -inf prefixes and masks of "Measured optimization case
+ * studies", Wide rows); a row reads only its valid bytes.
+ *   lengths: DEVICE array of M int32 lengths (L_i = lengths[i], clamped to
+ *            [0, N]), caller-owned; or NULL.
+ *   causal_period: with lengths == NULL and causal_period > 0, row i keeps
+ *            L_i = min(N, i mod causal_period + 1) entries (rows holding query
+ *            positions i mod causal_period of causal attention over N keys).
+ *            Neither given: no mask (same as softmax_rows_ex).
+ * L_i = 0 leaves an all -inf row, which is NaN like any all -inf row.
+ * plan: SR_PLAN_AUTO, SR_PLAN_WARP, SR_PLAN_ROW or SR_PLAN_ONLINE.
+ * Other arguments and results as softmax_rows_ex; SR_EINVAL also for a
+ * negative causal_period or for lengths and causal_period both given.
+ */
+SR_API int softmax_rows_masked(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                               int64_t ld_out, int dtype, const int32_t* lengths,
+                               int64_t causal_period, int plan, sr_stream_t stream);
+
+/*
  * The split plan for few, wide rows ("Measured optimization case studies",
  * Wide rows: split across programs when there are fewer rows than SMs).
  * Every row is cut into chunks handled by separate thread blocks; a first

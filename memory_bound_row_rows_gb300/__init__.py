@@ -20,6 +20,7 @@ __all__ = [
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
     "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
+    "softmax_rows_masked",
     "softmax",
     "dtype_code",
 ]
@@ -72,6 +73,7 @@ def load():
         "softmax_rows_split": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
         "softmax_rows_split_workspace_bytes": [vp, vp, i64, i64, i64, i64, c_int],
         "softmax_rows_split_noalloc": [vp, vp, i64, i64, i64, i64, c_int, vp],
+        "softmax_rows_masked": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, c_int, vp],
         "softmax_rows_version": [],
     }
     for name, args in sig.items():
@@ -149,6 +151,14 @@ def softmax_rows_host(h_in, h_out, M, N, ld_in, ld_out, dtype, d_work, work_byte
     return _check(load().softmax_rows_host(_ptr(h_in), _ptr(h_out), M, N, ld_in, ld_out, dtype,
                                            _ptr(d_work), work_bytes, _stream(stream)),
                   "softmax_rows_host")
+
+
+def softmax_rows_masked(in_, out, M, N, ld_in, ld_out, dtype, lengths=None, causal_period=0,
+                        plan=SR_PLAN_AUTO, stream=None) -> int:
+    """Masked softmax; `lengths` is a device int32 array of M valid lengths (or None)."""
+    return _check(load().softmax_rows_masked(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
+                                             _ptr(lengths), causal_period, plan, _stream(stream)),
+                  "softmax_rows_masked")
 
 
 def softmax_rows_split(in_, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,

@@ -217,6 +217,20 @@ int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t 
     return e == cudaSuccess ? SR_OK : SR_ECUDA;
 }
 
+// Plans that take a row mask, and the automatic choice among them.
+bool masked_plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_in,
+                      int64_t ld_out, int dtype) {
+    return plan == SR_PLAN_WARP || plan == SR_PLAN_ROW || plan == SR_PLAN_ONLINE
+               ? plan_fits(plan, in, out, N, ld_in, ld_out, dtype)
+               : false;
+}
+
+int choose_masked_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
+                       int dtype) {
+    const int plan = choose_plan(in, out, N, ld_in, ld_out, dtype);
+    return (plan == SR_PLAN_ROW || plan == SR_PLAN_WARP) ? plan : SR_PLAN_ONLINE;
+}
+
 int launch_auto(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype, cudaStream_t stream) {
     return run(in, out, M, N, ld_in, ld_out, dtype, SR_PLAN_AUTO, stream, kDefaultTimeoutNs, 0);
@@ -275,6 +289,36 @@ int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, in
     if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER && plan != SR_PLAN_SMEM) return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    (unsigned long long)timeout_ns, sr::kFlagNoCopy);
+}
+
+int softmax_rows_masked(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
+                        int64_t ld_out, int dtype, const int32_t* lengths, int64_t causal_period,
+                        int plan, sr_stream_t stream) {
+    const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return bad;
+    if (causal_period < 0 || (lengths != nullptr && causal_period != 0)) return SR_EINVAL;
+    if (plan == SR_PLAN_AUTO) {
+        plan = sr::choose_masked_plan(in, out, N, ld_in, ld_out, dtype);
+    } else if (!sr::masked_plan_fits(plan, in, out, N, ld_in, ld_out, dtype)) {
+        return SR_EPLAN;
+    }
+    if (M == 0) return SR_OK;
+    if (M > 0 && lengths == nullptr && causal_period == 0)  // no mask: the plain softmax
+        return softmax_rows_ex(in, out, M, N, ld_in, ld_out, dtype, plan, stream);
+    cudaError_t e;
+    const sr::DeviceInfo* dev = sr::device_info(&e);
+    if (!dev) return SR_ECUDA;
+    sr::Problem p{in, out, M, N, ld_in, ld_out, dtype, (cudaStream_t)stream, dev,
+                  sr::kDefaultTimeoutNs, 0};
+    p.mask.lens = lengths;
+    p.mask.period = causal_period;
+    switch (plan) {
+        case SR_PLAN_WARP: e = sr::launch_warp(p); break;
+        case SR_PLAN_ROW: e = sr::launch_row(p); break;
+        case SR_PLAN_ONLINE: e = sr::launch_online(p); break;
+        default: return SR_EPLAN;
+    }
+    return e == cudaSuccess ? SR_OK : SR_ECUDA;
 }
 
 int64_t softmax_rows_split_workspace_bytes(const void* in, const void* out, int64_t M, int64_t N,

@@ -28,10 +28,10 @@ constexpr int kRowMaxKV = 8;
 namespace sr {
 namespace {
 
-template <typename T, int NT, int KV>
+template <typename T, int NT, int KV, bool MASKED>
 __global__ void __launch_bounds__(NT)
     block_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
-                      int64_t ld_in, int64_t ld_out) {
+                      int64_t ld_in, int64_t ld_out, RowMask mask) {
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NW = NT / 32;
     __shared__ float red_m[NW], red_s[NW];
@@ -40,12 +40,21 @@ __global__ void __launch_bounds__(NT)
 
     for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
         const T* rin = in + r * ld_in;
+        // Masked rows read only the vectors that hold valid entries (rows of
+        // this plan are short enough for 32-bit element counts).
+        const int valid = MASKED ? (int)mask.valid(r, N) : 0;
         float v[KV][VEC];
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + NT * k;
-            if (idx < nvec) {
+            const int rem = MASKED ? valid - idx * VEC : VEC;  // valid entries in this vector
+            if (idx < nvec && (!MASKED || rem > 0)) {
                 Elem<T>::unpack(ldg_stream(rin + (int64_t)idx * VEC), v[k]);
+                if constexpr (MASKED) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e)
+                        if (e >= rem) v[k][e] = neg_inf();
+                }
             } else {
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) v[k][e] = neg_inf();
@@ -100,16 +109,22 @@ __global__ void __launch_bounds__(NT)
     }
 }
 
-template <typename T, int NT, int KV>
-cudaError_t launch_nt_kv(const Problem& p) {
-    auto kern = block_rows_kernel<T, NT, KV>;
-    // One block per row, capped at the largest grid dimension; rows beyond it
-    // are walked with a grid stride.
+// One block per row, capped at the largest grid dimension; rows beyond it
+// are walked with a grid stride.
+template <typename T>
+cudaError_t launch_grid(void (*kern)(const T*, T*, int64_t, int64_t, int64_t, int64_t, RowMask),
+                        int nt, const Problem& p) {
     const int64_t cap = 0x7fffffff;
     const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
-    kern<<<grid, NT, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
-                                    p.N, p.ld_in, p.ld_out);
+    kern<<<grid, nt, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
+                                    p.N, p.ld_in, p.ld_out, p.mask);
     return cudaGetLastError();
+}
+
+template <typename T, int NT, int KV>
+cudaError_t launch_nt_kv(const Problem& p) {
+    if (p.mask.active()) return launch_grid(block_rows_kernel<T, NT, KV, true>, NT, p);
+    return launch_grid(block_rows_kernel<T, NT, KV, false>, NT, p);
 }
 
 template <typename T, int NT>

@@ -36,6 +36,29 @@ struct DeviceInfo {
     unsigned int* err = nullptr;  // device address of the error word
 };
 
+// Masked softmax: in row r only the first valid(r) entries take part; the
+// rest count as -inf, are never loaded (a 16-byte vector with no valid entry
+// is skipped) and come out as zeros.
+struct RowMask {
+    const int32_t* lens = nullptr;  // device array of M valid lengths, or null
+    int64_t period = 0;             // without lens: row r keeps r mod period + 1 entries
+    __host__ __device__ bool active() const { return lens != nullptr || period > 0; }
+    __device__ __forceinline__ int64_t valid(int64_t r, int64_t N) const {
+        int64_t v = N;
+        if (lens) {
+            v = lens[r];
+        } else if (period > 0) {
+            // 32-bit division when both fit: a 64-bit one costs as much as the
+            // rest of a short row's work.
+            if (r <= 0x7fffffff && period <= 0x7fffffff)
+                v = (int64_t)((uint32_t)r % (uint32_t)period) + 1;
+            else
+                v = r % period + 1;
+        }
+        return v < 0 ? 0 : (v > N ? N : v);
+    }
+};
+
 struct Problem {
     const void* in;
     void* out;
@@ -45,6 +68,7 @@ struct Problem {
     const DeviceInfo* dev;
     unsigned long long timeout_ns;
     int flags;
+    RowMask mask = RowMask();
 };
 
 inline int elem_bytes(int dtype) { return dtype == kF32 ? 4 : 2; }

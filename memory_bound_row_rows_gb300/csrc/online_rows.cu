@@ -17,10 +17,10 @@ namespace {
 constexpr int kOnlineThreads = 256;
 constexpr int kChunk = 8;  // elements per thread per step of pass 1
 
-template <typename T>
+template <typename T, bool MASKED>
 __global__ void __launch_bounds__(kOnlineThreads)
     online_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
-                       int64_t ld_in, int64_t ld_out) {
+                       int64_t ld_in, int64_t ld_out, RowMask mask) {
     constexpr int NW = kOnlineThreads / 32;
     __shared__ float2 red[NW];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -28,16 +28,18 @@ __global__ void __launch_bounds__(kOnlineThreads)
     for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
         const T* rin = in + r * ld_in;
         T* rout = out + r * ld_out;
+        // Masked rows: entries at or past `valid` are -inf and never read.
+        const int64_t valid = MASKED ? mask.valid(r, N) : N;
 
         // Pass 1: online (m, s) per thread over elements tid + NT*k.
         float m = neg_inf(), s = 0.0f;
-        for (int64_t j0 = tid; j0 < N; j0 += (int64_t)kOnlineThreads * kChunk) {
+        for (int64_t j0 = tid; j0 < valid; j0 += (int64_t)kOnlineThreads * kChunk) {
             float x[kChunk];
             float cm = neg_inf();
 #pragma unroll
             for (int u = 0; u < kChunk; ++u) {
                 const int64_t j = j0 + (int64_t)kOnlineThreads * u;
-                x[u] = j < N ? Elem<T>::load1(rin + j) : neg_inf();
+                x[u] = j < valid ? Elem<T>::load1(rin + j) : neg_inf();
                 cm = fmaxf(cm, x[u]);
             }
             const float mn = fmaxf(m, cm);
@@ -65,22 +67,30 @@ __global__ void __launch_bounds__(kOnlineThreads)
 
         // Pass 2: normalise and write.
         const float rs = final_rcp(Mr, Sr);
-        for (int64_t j = tid; j < N; j += kOnlineThreads)
-            Elem<T>::store1(rout + j, expf(Elem<T>::load1(rin + j) - Mr) * rs);
+        for (int64_t j = tid; j < N; j += kOnlineThreads) {
+            const float x = (!MASKED || j < valid) ? Elem<T>::load1(rin + j) : neg_inf();
+            Elem<T>::store1(rout + j, expf(x - Mr) * rs);
+        }
     }
 }
 
-template <typename T>
-cudaError_t launch_typed(const Problem& p) {
-    auto kern = online_rows_kernel<T>;
+template <typename T, bool MASKED>
+cudaError_t launch_m(const Problem& p) {
+    auto kern = online_rows_kernel<T, MASKED>;
     const int per_sm = blocks_per_sm(reinterpret_cast<const void*>(kern), kOnlineThreads, 0);
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
     const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
     kern<<<grid, kOnlineThreads, 0, p.stream>>>(static_cast<const T*>(p.in),
                                                 static_cast<T*>(p.out), p.M, p.N, p.ld_in,
-                                                p.ld_out);
+                                                p.ld_out, p.mask);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_typed(const Problem& p) {
+    if (p.mask.active()) return launch_m<T, true>(p);
+    return launch_m<T, false>(p);
 }
 
 }  // namespace

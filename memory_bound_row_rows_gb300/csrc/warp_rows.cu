@@ -26,10 +26,10 @@ constexpr int kWarpBlock = 256;  // 8 warps per block
 #define SR_WARP_PERSISTENT 1
 #endif
 
-template <typename T, int VEC, int KV>
+template <typename T, int VEC, int KV, bool MASKED>
 __global__ void __launch_bounds__(kWarpBlock)
     warp_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
-                     int64_t ld_in, int64_t ld_out) {
+                     int64_t ld_in, int64_t ld_out, RowMask mask) {
     const int lane = threadIdx.x & 31;
     const int64_t first = ((int64_t)blockIdx.x * kWarpBlock + threadIdx.x) >> 5;
     const int64_t stride = ((int64_t)gridDim.x * kWarpBlock) >> 5;
@@ -39,17 +39,26 @@ __global__ void __launch_bounds__(kWarpBlock)
         const T* rin = in + r * ld_in;
         T* rout = out + r * ld_out;
         float v[KV][VEC];
+        // Masked rows read only the vectors that hold valid entries.
+        const int valid = MASKED ? (int)mask.valid(r, N) : N;
 
         // Row load (masked lanes read -inf, which adds exp(-inf) = 0 to the sum).
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int idx = lane + 32 * k;
-            if (idx < nvec) {
+            const int rem = MASKED ? valid - idx * VEC : VEC;  // valid entries in this vector
+            if (idx < nvec && (!MASKED || rem > 0)) {
                 if constexpr (VEC == 1) {
                     v[k][0] = Elem<T>::load1(rin + idx);
+                    if (MASKED && rem <= 0) v[k][0] = neg_inf();
                 } else {
                     uint4 u = ldg_stream(rin + (int64_t)idx * VEC);
                     Elem<T>::unpack(u, v[k]);
+                    if constexpr (MASKED) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e)
+                            if (e >= rem) v[k][e] = neg_inf();
+                    }
                 }
             } else {
 #pragma unroll
@@ -107,9 +116,9 @@ __global__ void __launch_bounds__(kWarpBlock)
     }
 }
 
-template <typename T, int VEC, int KV>
-cudaError_t launch_one(const Problem& p) {
-    auto kern = warp_rows_kernel<T, VEC, KV>;
+template <typename T, int VEC, int KV, bool MASKED>
+cudaError_t launch_one_m(const Problem& p) {
+    auto kern = warp_rows_kernel<T, VEC, KV, MASKED>;
     const int64_t warps_per_block = kWarpBlock / 32;
     const int64_t need = (p.M + warps_per_block - 1) / warps_per_block;
     int64_t cap = 0x7fffffff;
@@ -120,8 +129,14 @@ cudaError_t launch_one(const Problem& p) {
     }
     const unsigned grid = (unsigned)(need < cap ? need : cap);
     kern<<<grid, kWarpBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
-                                            p.M, (int)p.N, p.ld_in, p.ld_out);
+                                            p.M, (int)p.N, p.ld_in, p.ld_out, p.mask);
     return cudaGetLastError();
+}
+
+template <typename T, int VEC, int KV>
+cudaError_t launch_one(const Problem& p) {
+    if (p.mask.active()) return launch_one_m<T, VEC, KV, true>(p);
+    return launch_one_m<T, VEC, KV, false>(p);
 }
 
 // Vectors per lane: the smallest power of two that covers the row.
