@@ -55,6 +55,9 @@ class Oracle:
         fn = lib.oracle_softmax_rows_masked
         fn.restype = c_int
         fn.argtypes = [vp, vp, i64, i64, i64, i64, c_int, vp, i64, c_int]
+        fn = lib.oracle_softmax_backward
+        fn.restype = c_int
+        fn.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, c_int]
         for name in ("oracle_cast", "oracle_decode"):
             fn = getattr(lib, name)
             fn.restype = c_int
@@ -96,6 +99,20 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_softmax_rows_masked returned %d" % rc)
         return out
+
+    def softmax_backward(self, y: np.ndarray, dy: np.ndarray, M: int, N: int, ld_y: int,
+                         ld_dy: int, ld_dx: int, dtype: int) -> np.ndarray:
+        """dx = y * (dy - sum(y * dy)) per row, FP64, one cast; an (M, ld_dx) array."""
+        y = np.ascontiguousarray(y)
+        dy = np.ascontiguousarray(dy)
+        assert y.dtype == _STORAGE[dtype] and dy.dtype == _STORAGE[dtype]
+        assert y.size >= M * ld_y and dy.size >= M * ld_dy
+        dx = np.zeros((M, ld_dx), dtype=_STORAGE[dtype])
+        rc = self.lib.oracle_softmax_backward(y.ctypes.data, dy.ctypes.data, dx.ctypes.data, M, N,
+                                              ld_y, ld_dy, ld_dx, dtype)
+        if rc != 0:
+            raise ValueError("oracle_softmax_backward returned %d" % rc)
+        return dx
 
     def softmax_rows_f64(self, x: np.ndarray, M: int, N: int, ld_in: int, dtype: int,
                          nthreads: int = 1) -> np.ndarray:

@@ -28,6 +28,10 @@
  * dtype 0 = f32 (IEEE binary32), 1 = bf16 (upper half of binary32),
  * 2 = f16 (IEEE binary16); bf16 and f16 are 16-bit patterns.
  *
+ * Also here: the masked softmax (entries past a row's valid length count as
+ * -inf) and the softmax backward dx = y * (dy - sum_j y_j dy_j), each stated
+ * and cited where it is defined below.
+ *
  * Parity pins (tests/test_oracle_pins.py) check this code against 60-digit
  * decimal brute force, closed forms and invariants, not against itself.
  */
@@ -248,6 +252,37 @@ int oracle_softmax_rows_masked(const void* in, void* out, int64_t M, int64_t N, 
 int oracle_softmax_rows_f64(const void* in, double* out64, int64_t M, int64_t N,
                             int64_t ld_in, int64_t ld_out, int dtype, int nthreads) {
     return run(in, NULL, out64, M, N, ld_in, ld_out, dtype, nthreads, NULL, 0);
+}
+
+/*
+ * Softmax backward ("Measured optimization case studies", Training: softmax
+ * saves its output y and computes y * (dy - sum(y * dy))): for every row i,
+ *     dot_i = sum_j y[i,j] * dy[i,j],   dx[i,j] = y[i,j] * (dy[i,j] - dot_i),
+ * computed in FP64 (sequential sum) and cast once to the dtype. y, dy and dx
+ * are M x N with their own pitches (elements).
+ */
+static void backward_rows(const void* y, const void* dy, void* dx, int64_t row_begin,
+                          int64_t row_end, int64_t N, int64_t ld_y, int64_t ld_dy,
+                          int64_t ld_dx, int dtype) {
+    for (int64_t i = row_begin; i < row_end; ++i) {
+        double dot = 0.0;
+        for (int64_t j = 0; j < N; ++j)
+            dot += decode(y, i * ld_y + j, dtype) * decode(dy, i * ld_dy + j, dtype);
+        for (int64_t j = 0; j < N; ++j) {
+            const double yj = decode(y, i * ld_y + j, dtype);
+            const double gj = decode(dy, i * ld_dy + j, dtype);
+            encode(dx, i * ld_dx + j, dtype, yj * (gj - dot));
+        }
+    }
+}
+
+int oracle_softmax_backward(const void* y, const void* dy, void* dx, int64_t M, int64_t N,
+                            int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype) {
+    if (M < 0 || N < 1 || ld_y < N || ld_dy < N || ld_dx < N) return 1;
+    if (dtype < OR_F32 || dtype > OR_F16) return 2;
+    if (M > 0 && (!y || !dy || !dx)) return 1;
+    backward_rows(y, dy, dx, 0, M, N, ld_y, ld_dy, ld_dx, dtype);
+    return 0;
 }
 
 /* Step 5 alone: round doubles to `dtype` storage (f32 values or 16-bit patterns). */

@@ -339,9 +339,83 @@ def check_masked_causal(orc):
                 if L <= 16 else np.allclose(decode(a[k, :L], w.dtype).sum(), 1.0, atol=2e-3)
 
 
+# ---- softmax backward -------------------------------------------------------------
+
+def _bwd_decimal(y, dy):
+    import decimal
+    with decimal.localcontext(brute.CTX):
+        Y = [decimal.Decimal(float(v)) for v in y]
+        G = [decimal.Decimal(float(v)) for v in dy]
+        dot = sum(a * b for a, b in zip(Y, G))
+        return [a * (b - dot) for a, b in zip(Y, G)]
+
+
+def check_backward_brute(orc):
+    rng = np.random.default_rng(31)
+    for dtype in DTYPES:
+        for N in (1, 2, 5, 13):
+            M = 4
+            y = to_grid(rng.uniform(0, 1, size=(M, N)), dtype)
+            dy = to_grid(rng.normal(0, 2, size=(M, N)), dtype)
+            got = decode(orc.softmax_backward(encode_exact(y, dtype), encode_exact(dy, dtype),
+                                              M, N, N, N, N, dtype), dtype)
+            for i in range(M):
+                want = [brute.round_exact(Fraction(v), dtype) for v in _bwd_decimal(y[i], dy[i])]
+                assert same(got[i], want), "backward brute dtype %d N=%d" % (dtype, N)
+
+
+def check_backward_is_softmax_vjp(orc):
+    """dx equals the vector-Jacobian product of softmax, by central differences
+    of the 60-digit softmax: dx_k = d/dt [softmax(x + t e_k) . dy] at t = 0."""
+    import decimal
+    rng = np.random.default_rng(32)
+    for N in (2, 3, 6):
+        x = rng.normal(0, 1.5, size=N)
+        dy = rng.normal(0, 1, size=N)
+        y = np.array([float(v) for v in brute.softmax_decimal(x)])
+        got = orc.softmax_backward(y.astype(np.float32), dy.astype(np.float32), 1, N, N, N, N,
+                                   F32).astype(np.float64)[0]
+        with decimal.localcontext(brute.CTX):
+            h = decimal.Decimal("1e-25")
+            G = [decimal.Decimal(float(v)) for v in dy.astype(np.float32)]
+            for k in range(N):
+                def f(t):
+                    xs = [decimal.Decimal(float(v)) for v in x]
+                    xs[k] += t
+                    m = max(xs)
+                    e = [(v - m).exp() for v in xs]
+                    s = sum(e)
+                    return sum((a / s) * g for a, g in zip(e, G))
+                fd = float((f(h) - f(-h)) / (2 * h))
+                # y and dy were rounded to f32 before the oracle saw them.
+                assert abs(got[k] - fd) <= 2e-6 * (1 + abs(fd)), "vjp N=%d k=%d: %g vs %g" % (
+                    N, k, got[k], fd)
+
+
+def check_backward_closed_forms(orc):
+    for dtype in DTYPES:
+        N = 9
+        y = np.zeros((3, N))
+        y[0, 4] = 1.0                       # one-hot y: dx = 0 whatever dy is
+        y[1, :] = 0.0                       # zero y: dx = 0
+        y[2, :3] = [0.25, 0.25, 0.5]        # dy = constant c: dx_j = c*y_j*(1 - sum y) = 0
+        dy = np.array([np.linspace(-3, 3, N), np.linspace(1, 2, N), np.full(N, 1.5)])
+        got = decode(orc.softmax_backward(encode_exact(to_grid(y, dtype), dtype),
+                                          encode_exact(to_grid(dy, dtype), dtype),
+                                          3, N, N, N, N, dtype), dtype)
+        assert np.all(got == 0.0), "backward closed forms dtype %d: %r" % (dtype, got)
+        # Row sums of dx vanish when y sums to one (exactly representable y).
+        y2 = np.array([[0.5, 0.25, 0.125, 0.125]])
+        dy2 = np.array([[1.0, -2.0, 0.5, 4.0]])
+        d = decode(orc.softmax_backward(encode_exact(y2, dtype), encode_exact(dy2, dtype), 1, 4, 4, 4,
+                                        4, dtype), dtype)
+        assert abs(d.sum()) <= 4 * UNIT_ROUNDOFF[dtype] * np.abs(d).max()
+
+
 ALL_CHECKS = [
     check_decode, check_cast, check_brute_random, check_brute_extremes, check_uniform_rows,
     check_two_entries, check_tied_maxima, check_causal_rows, check_nan_rows,
     check_row_sums_and_range, check_shift_invariance, check_strides, check_thread_independence,
     check_masked_brute, check_masked_causal,
+    check_backward_brute, check_backward_is_softmax_vjp, check_backward_closed_forms,
 ]

@@ -35,6 +35,12 @@ MUTANTS = {
     "masked_as_zero": ("decode(jb->in, i * jb->ld_in + j, jb->dtype) : -INFINITY;",
                        "decode(jb->in, i * jb->ld_in + j, jb->dtype) : 0.0;"),
     "causal_off_by_one": ("v = i % jb->causal_period + 1;", "v = i % jb->causal_period;"),
+    "backward_drops_dot": ("encode(dx, i * ld_dx + j, dtype, yj * (gj - dot));",
+                           "encode(dx, i * ld_dx + j, dtype, yj * gj);"),
+    "backward_sign": ("encode(dx, i * ld_dx + j, dtype, yj * (gj - dot));",
+                      "encode(dx, i * ld_dx + j, dtype, yj * (dot - gj));"),
+    "backward_dot_skips_last": ("for (int64_t j = 0; j < N; ++j)\n            dot +=",
+                                "for (int64_t j = 0; j + 1 < N; ++j)\n            dot +="),
 }
 
 
