@@ -52,14 +52,16 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=synth.HEADLINE,
+    ap.add_argument("--workload", default=None,
                     help="one of %s; 'all' (those five) or 'wide' (%s)"
                          % (", ".join(synth.WORKLOADS), ", ".join(synth.WIDE_FEW)))
-    ap.add_argument("--api", choices=("rows", "split", "masked"), default="rows",
+    ap.add_argument("--api", choices=("rows", "split", "masked", "backward"), default="rows",
                     help="rows: softmax_rows / softmax_rows_ex; split: softmax_rows_split "
                          "with a device workspace (the split plan for few, wide rows); masked: "
                          "softmax_rows_masked with the workload's causal period (masked "
-                         "entries are not read)")
+                         "entries are not read); backward: softmax_rows_backward_ex on the "
+                         "backward shapes (%s; 'all' for every one)"
+                         % ", ".join(synth.BACKWARD))
     ap.add_argument("--lane", choices=("cold", "warm"), default="cold")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--plan", type=int, default=0, help="forced plan (0 = automatic)")
@@ -204,6 +206,39 @@ def gpu_uuid(device_index: int):
         return None
 
 
+def timed_steps(args, step, flush_l2, stream, rank, local_rank, world):
+    """Warm-up, a burst of load, then exactly args.steps steps, each between a
+    pair of CUDA events on `stream` (the L2 flush, if any, outside the pair),
+    with nvidia-smi sampling the clocks throughout. Returns (ms list, clocks)."""
+    import torch
+    for _ in range(max(3, args.warmup)):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    clk = ClockSampler(gpu_uuid(local_rank) if rank == 0 else None)
+    with clk:
+        t_end = time.perf_counter() + args.burst
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                flush_l2()
+                step()
+            torch.cuda.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            flush_l2()
+            starts[k].record(stream)
+            step()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)], clk.summary()
+
+
 def run_ours(args, w, rank, local_rank, world):
     import torch
 
@@ -251,33 +286,7 @@ def run_ours(args, w, rank, local_rank, world):
         if args.lane == "cold":
             torch.sum(flush)  # reads 512 MiB: L2 now holds clean lines only
 
-    for _ in range(max(3, args.warmup)):
-        flush_l2()
-        step()
-    torch.cuda.synchronize()
-
-    clk = ClockSampler(gpu_uuid(local_rank) if rank == 0 else None)
-    with clk:
-        t_end = time.perf_counter() + args.burst
-        while time.perf_counter() < t_end:
-            for _ in range(20):
-                flush_l2()
-                step()
-            torch.cuda.synchronize()
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        if world > 1:
-            torch.distributed.barrier()
-        torch.cuda.synchronize()
-        for k in range(args.steps):
-            flush_l2()
-            starts[k].record(stream)
-            step()
-            ends[k].record(stream)
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms, clocks = timed_steps(args, step, flush_l2, stream, rank, local_rank, world)
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
     e2e = None
@@ -287,7 +296,7 @@ def run_ours(args, w, rank, local_rank, world):
         plan_used = "split"
     elif args.api == "masked":
         plan_used = "masked-" + sr.PLAN_NAMES.get(plan_used, str(plan_used))
-    return {"ms": ms, "clocks": clk.summary(),
+    return {"ms": ms, "clocks": clocks,
             "plan": plan_used if isinstance(plan_used, str) else sr.PLAN_NAMES.get(plan_used, str(plan_used)),
             "y_dev": y_dev, "e2e": e2e, "x": x}
 
@@ -451,6 +460,174 @@ def bench_ours(args, w):
     return line
 
 
+# ---- softmax backward lane -------------------------------------------------------
+
+def backward_outside_gate(g, r, y, dy, dtype) -> int:
+    """Elements outside the backward parity gate (FP32 dot product, one cast):
+    |g - r| <= |y|(2^-17 S + 2^-22 |dy - d|) + 2^-22 |r| + 2 ulp_dtype(r), with
+    d = sum y*dy and S = sum |y*dy| per row. Decoded float64 (rows, N) arrays."""
+    mant = {synth.F32: 23, synth.BF16: 7, synth.F16: 10}[dtype]
+    emin = {synth.F32: -126, synth.BF16: -126, synth.F16: -14}[dtype]
+    d = (y * dy).sum(axis=1, keepdims=True)
+    S = np.abs(y * dy).sum(axis=1, keepdims=True)
+    a = np.abs(r)
+    ulp = np.exp2(np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), emin) - mant)
+    tol = np.abs(y) * (2.0 ** -17 * S + 2.0 ** -22 * np.abs(dy - d)) + 2.0 ** -22 * a + 2 * ulp
+    bad = ~(np.abs(g - r) <= tol) & ~(np.isnan(g) & np.isnan(r))
+    return int(bad.sum())
+
+
+def oracle_backward_rows(w, y, dy, rows):
+    import oracle
+    return oracle.load().softmax_backward(np.ascontiguousarray(y[rows]).reshape(-1),
+                                          np.ascontiguousarray(dy[rows]).reshape(-1), len(rows),
+                                          w.N, w.ld, w.ld, w.N, w.dtype)
+
+
+def backward_cpu_baseline(w, y, dy, budget_s: float):
+    """The oracle's backward as it stands (one thread) on leading rows of the
+    workload, repeated for about budget_s."""
+    per_row = 3 * w.N * w.elem_bytes
+    rows = np.arange(min(w.M, max(1, (8 << 20) // per_row)))  # about 8 MB per pass
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle_backward_rows(w, y, dy, rows)
+        times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start >= budget_s:
+            break
+    gbs = per_row * rows.size * len(times) / sum(times) / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d rows of %s, %d pass(es) of the FP64 C oracle's backward, "
+                      "1 thread" % (rows.size, w.M, w.name, len(times))}
+
+
+def bench_backward(args, w):
+    """dx = y * (dy - sum(y * dy)) per row: one softmax_rows_backward_ex call per step."""
+    import torch
+
+    import memory_bound_row_rows_gb300 as sr
+    from memory_bound_row_rows_gb300 import _build
+    rank, local_rank, world = dist_env()
+    if world > 1 and not torch.distributed.is_initialized():
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = sr.load()
+    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[w.dtype]
+
+    def host_tensor(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t if w.dtype == synth.F32 else t.view(torch.int16).view(tdt)
+
+    y, dy = w.y_rows(0, w.M), w.dy_rows(0, w.M)
+    y_dev, dy_dev = host_tensor(y).to(dev), host_tensor(dy).to(dev)
+    dx_dev = torch.empty((w.M, w.N), dtype=tdt, device=dev)
+    flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    plan = sr.softmax_rows_backward_plan(y_dev, dy_dev, dx_dev, w.M, w.N, w.ld, w.ld, w.N,
+                                         w.dtype, args.plan, 0)
+    if plan < 0:
+        raise RuntimeError("backward plan %d cannot take %s" % (args.plan, w.name))
+
+    def step():
+        st = lib.softmax_rows_backward_ex(y_dev.data_ptr(), dy_dev.data_ptr(), dx_dev.data_ptr(),
+                                          w.M, w.N, w.ld, w.ld, w.N, w.dtype, args.plan, sh)
+        if st != 0:
+            raise RuntimeError("softmax_rows_backward failed: %s" % sr.softmax_rows_strerror(st))
+
+    def flush_l2():
+        if args.lane == "cold":
+            torch.sum(flush)
+
+    ms, clocks = timed_steps(args, step, flush_l2, stream, rank, local_rank, world)
+    total_s = max_over_ranks(sum(ms) / 1e3, device="cuda" if world > 1 else "cpu")
+
+    e2e = None
+    if not args.no_e2e:
+        # Host buffers: pinned y and dy copied in, the call, dx copied back, each step.
+        y_pin, dy_pin = host_tensor(y).pin_memory(), host_tensor(dy).pin_memory()
+        dx_pin = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
+
+        def e2e_step():
+            y_dev.copy_(y_pin, non_blocking=True)
+            dy_dev.copy_(dy_pin, non_blocking=True)
+            step()
+            dx_pin.copy_(dx_dev, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        k = max(3, min(args.steps, 20))
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(k):
+            e2e_step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        sec = t0.elapsed_time(t1) / 1e3 / k
+        e2e = {"value": round(w.fused_bytes / sec / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": 2 * w.M * w.N * w.elem_bytes,
+               "d2h_bytes_per_step": w.M * w.N * w.elem_bytes,
+               "ms_per_step": round(sec * 1e3, 4), "steps": k,
+               "path": "pinned host y, dy -> device (copies), softmax_rows_backward_ex, "
+                       "dx -> pinned host, in order on one stream"}
+    if rank != 0:
+        return None
+    steps = len(ms)
+    value = replica_throughput(w.fused_bytes, steps, world, total_s)
+    achieved = w.fused_bytes / (sum(ms) / 1e3 / steps) / 1e9
+    peaks = measured_peaks()
+    pname = "backward-" + sr.PLAN_NAMES[plan]
+    traffic, rec = recorded_traffic("backward:" + w.name, "backward")
+    line = {
+        "metric": "cold-L2 softmax backward GB/s (3*M*N*bytes/time)" if args.lane == "cold"
+        else "warm-L2 softmax backward GB/s (3*M*N*bytes/time)",
+        "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total_s / steps * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": synth.DTYPE_NAMES[w.dtype],
+        "data": "synthetic: y ~ U[0, 2/N), dy ~ N(0, 1), seeded SplitMix64 (seed %d)" % w.seed,
+        "config": {"workload": "backward " + w.name, "M": w.M, "N": w.N, "ld": w.ld,
+                   "plan": pname, "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": ("flushed: a 512 MiB device buffer is read before every step, outside "
+                          "the event pair") if args.lane == "cold" else "warm (no flush)",
+                   "inputs_resident_in_hbm": True},
+        "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
+        "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
+        "bytes_per_step": w.fused_bytes,
+        "median_step_us": round(statistics.median(ms) * 1e3, 3),
+        "p10_p90_step_us": [round(float(np.percentile(ms, 10)) * 1e3, 3),
+                            round(float(np.percentile(ms, 90)) * 1e3, 3)],
+        "gpu_launches": steps,
+        "clocks": clocks,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic,
+                     "traffic_note": (rec or {}).get("note") if traffic else
+                     "null: no ncu capture recorded for this build of the kernels"},
+        "source_hash": _build.source_hash(_build.PLAN_SOURCES["backward"]),
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if world == 1:
+        line["cpu_baseline"] = backward_cpu_baseline(w, y, dy, args.cpu_budget)
+        rows = np.unique(np.concatenate([np.linspace(0, w.M - 1, 64).astype(np.int64),
+                                         [w.M - 1]]))
+        g = dx_dev[torch.from_numpy(rows).to(dev)].cpu()
+        g = g.numpy() if w.dtype == synth.F32 else g.view(torch.int16).numpy().view(np.uint16)
+        r = oracle_backward_rows(w, y, dy, rows)
+        dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :w.N]), w.dtype)
+        line["parity"] = {"rows": int(rows.size), "of_rows": w.M,
+                          "outside_tolerance": backward_outside_gate(
+                              dec(g), dec(r), dec(y[rows]), dec(dy[rows]), w.dtype),
+                          "gate": "FP32 dot-product error bound plus 2 ulp of the dtype"}
+    return line
+
+
 def bench_reference(args, w):
     """The CPU oracle as the reference arm: each step is one oracle pass over the workload."""
     rank, _, world = dist_env()
@@ -484,16 +661,63 @@ def bench_reference(args, w):
     }
 
 
+def bench_reference_backward(args, w):
+    """The CPU oracle's backward as the reference arm, each step a bounded sample."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return None
+    y, dy = w.y_rows(0, w.M), w.dy_rows(0, w.M)
+    per_row = 3 * w.N * w.elem_bytes
+    rows = np.arange(min(w.M, max(1, (8 << 20) // per_row)))
+    for _ in range(max(0, args.warmup)):
+        oracle_backward_rows(w, y, dy, rows)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_backward_rows(w, y, dy, rows)
+        times.append(time.perf_counter() - t0)
+    value = per_row * rows.size * len(times) / sum(times) / 1e9
+    sample = "first %d of %d rows of %s per step, FP64 C oracle's backward, 1 thread" % (
+        rows.size, w.M, w.name)
+    return {
+        "impl": "reference",
+        "metric": "cold-L2 softmax backward GB/s (3*M*N*bytes/time)",
+        "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": synth.DTYPE_NAMES[w.dtype],
+        "data": "synthetic: y ~ U[0, 2/N), dy ~ N(0, 1), seeded SplitMix64 (seed %d)" % w.seed,
+        "config": {"workload": "backward " + w.name, "M": w.M, "N": w.N, "ld": w.ld},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def main(argv=None):
     args = parse_args(argv)
-    catalog = dict(synth.WORKLOADS, **synth.WIDE_FEW)
-    names = (list(synth.WORKLOADS) if args.workload == "all" else
-             list(synth.WIDE_FEW) if args.workload == "wide" else [args.workload])
+    if args.api == "backward":
+        catalog = synth.BACKWARD
+        names = (list(synth.BACKWARD) if args.workload == "all" else
+                 [args.workload or synth.BACKWARD_HEADLINE])
+    else:
+        catalog = dict(synth.WORKLOADS, **synth.WIDE_FEW)
+        wl = args.workload or synth.HEADLINE
+        names = (list(synth.WORKLOADS) if wl == "all" else
+                 list(synth.WIDE_FEW) if wl == "wide" else [wl])
     for name in names:
         w = catalog[name]
         if args.rows:
             w = w.with_rows(min(args.rows, w.M))
-        line = bench_reference(args, w) if args.impl == "reference" else bench_ours(args, w)
+        if args.impl == "reference" and args.api == "backward":
+            line = bench_reference_backward(args, w)
+        elif args.impl == "reference":
+            line = bench_reference(args, w)
+        elif args.api == "backward":
+            line = bench_backward(args, w)
+        else:
+            line = bench_ours(args, w)
         if line is not None:
             print(json.dumps(line), flush=True)
     if args.impl == "ours":

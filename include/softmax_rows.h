@@ -256,6 +256,53 @@ SR_API int softmax_rows_split_noalloc(const void* in, void* out, int64_t M, int6
                                       sr_stream_t stream);
 
 /* A static, human-readable name for an sr_status value. */
+/*
+ * Softmax backward ("Measured optimization case studies", Training: backward
+ * kernels through autograd: the softmax keeps its output y and forms
+ * y * (dy - sum(y * dy))). For every row i,
+ *     dx[i,j] = y[i,j] * (dy[i,j] - sum_k y[i,k] * dy[i,k]),
+ * with the sum (a dot product) held in FP32 and each dx rounded once to the
+ * dtype. y, dy and dx are DEVICE M x N row-major matrices in the same dtype,
+ * with pitches ld_y, ld_dy, ld_dx (elements, each >= N), caller-owned; dx
+ * must not overlap y or dy (dx equal to y or dy is rejected with SR_EINVAL).
+ * Pad columns [N, ld_dx) are not written. y need not be a softmax output: the
+ * formula is applied as written (a NaN or infinity in a row's y or dy makes
+ * that row's dot product, and so its dx, NaN or infinite).
+ * Enqueued on `stream`; asynchronous like softmax_rows. Returns SR_OK,
+ * SR_EDTYPE, SR_EINVAL (sizes, pitches, null pointers, aliasing, or a last
+ * addressed byte beyond INT64_MAX) or SR_ECUDA.
+ */
+SR_API int softmax_rows_backward(const void* y, const void* dy, void* dx, int64_t M, int64_t N,
+                                 int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype,
+                                 sr_stream_t stream);
+
+/*
+ * softmax_rows_backward with a chosen plan: SR_PLAN_AUTO, SR_PLAN_ROW (a
+ * team of threads per row, the row held in registers; rows up to 16384
+ * elements), SR_PLAN_CLUSTER (a thread-block cluster of 2..16 blocks per row,
+ * partial dot products exchanged in distributed shared memory; rows up to
+ * 131072 elements) or SR_PLAN_ONLINE (any row: y and dy are read twice).
+ * Rows are read as 16-byte vectors when the three matrices' bases and pitches
+ * agree modulo 16 bytes (an element-aligned head and tail are read singly);
+ * otherwise element by element, and the limits halve (8192 and 65536).
+ * SR_EPLAN when the plan cannot take the shape.
+ */
+SR_API int softmax_rows_backward_ex(const void* y, const void* dy, void* dx, int64_t M,
+                                    int64_t N, int64_t ld_y, int64_t ld_dy, int64_t ld_dx,
+                                    int dtype, int plan, sr_stream_t stream);
+
+/*
+ * Host-only query: the plan softmax_rows_backward_ex would run for `plan`
+ * (SR_PLAN_AUTO resolves to a concrete plan), or a negative sr_status
+ * (-SR_EPLAN when the plan cannot take the shape). The pointers are only
+ * inspected for alignment. sm_count > 0 stands for the device's SM count (it
+ * steers the automatic choice and the cluster size); sm_count <= 0 queries
+ * the current device.
+ */
+SR_API int softmax_rows_backward_plan(const void* y, const void* dy, const void* dx, int64_t M,
+                                      int64_t N, int64_t ld_y, int64_t ld_dy, int64_t ld_dx,
+                                      int dtype, int plan, int sm_count);
+
 SR_API const char* softmax_rows_strerror(int status);
 
 /* Library version as major*10000 + minor*100 + patch. */

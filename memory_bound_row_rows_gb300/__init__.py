@@ -20,8 +20,9 @@ __all__ = [
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
     "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
-    "softmax_rows_masked",
-    "softmax",
+    "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
+    "softmax_rows_backward_plan",
+    "softmax", "softmax_backward",
     "dtype_code",
 ]
 
@@ -74,6 +75,9 @@ def load():
         "softmax_rows_split_workspace_bytes": [vp, vp, i64, i64, i64, i64, c_int],
         "softmax_rows_split_noalloc": [vp, vp, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_masked": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, c_int, vp],
+        "softmax_rows_backward": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, vp],
+        "softmax_rows_backward_ex": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, vp],
+        "softmax_rows_backward_plan": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, c_int],
         "softmax_rows_version": [],
     }
     for name, args in sig.items():
@@ -161,6 +165,27 @@ def softmax_rows_masked(in_, out, M, N, ld_in, ld_out, dtype, lengths=None, caus
                   "softmax_rows_masked")
 
 
+def softmax_rows_backward(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, stream=None) -> int:
+    """dx = y * (dy - sum(y * dy)) per row; y, dy, dx are device matrices."""
+    return _check(load().softmax_rows_backward(_ptr(y), _ptr(dy), _ptr(dx), M, N, ld_y, ld_dy,
+                                               ld_dx, dtype, _stream(stream)),
+                  "softmax_rows_backward")
+
+
+def softmax_rows_backward_ex(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan,
+                             stream=None) -> int:
+    return _check(load().softmax_rows_backward_ex(_ptr(y), _ptr(dy), _ptr(dx), M, N, ld_y, ld_dy,
+                                                  ld_dx, dtype, plan, _stream(stream)),
+                  "softmax_rows_backward_ex")
+
+
+def softmax_rows_backward_plan(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan=SR_PLAN_AUTO,
+                               sm_count=0) -> int:
+    """The plan the backward would run (> 0), or a negative status (host logic)."""
+    return int(load().softmax_rows_backward_plan(_ptr(y), _ptr(dy), _ptr(dx), M, N, ld_y, ld_dy,
+                                                 ld_dx, dtype, plan, sm_count))
+
+
 def softmax_rows_split(in_, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,
                        stream=None) -> int:
     """Split plan for few, wide rows; `workspace` is a device buffer."""
@@ -222,3 +247,26 @@ def softmax(x, out=None, plan: int = SR_PLAN_AUTO, stream=None):
     ld_out = out.stride(0) if M > 1 else N
     softmax_rows_ex(x, out, M, N, ld_in, ld_out, dtype_code(x.dtype), plan, stream)
     return out
+
+
+def softmax_backward(y, dy, dx=None, plan: int = SR_PLAN_AUTO, stream=None):
+    """Softmax backward of 2-D CUDA tensors with unit column stride.
+
+    ``y`` is the softmax output and ``dy`` the gradient of the loss with
+    respect to it; returns dx (a new contiguous tensor unless ``dx`` is given).
+    """
+    import torch
+    for name, t in (("y", y), ("dy", dy)):
+        if t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+            raise ValueError("%s: expected a 2-D CUDA tensor with unit column stride" % name)
+    if dy.shape != y.shape or dy.dtype != y.dtype:
+        raise ValueError("y and dy must have the same shape and dtype")
+    M, N = y.shape
+    if dx is None:
+        dx = torch.empty((M, N), dtype=y.dtype, device=y.device)
+    if dx.shape != y.shape or dx.dtype != y.dtype or dx.stride(1) != 1:
+        raise ValueError("dx must match y in shape and dtype, with unit column stride")
+    ld = lambda t: t.stride(0) if M > 1 else N
+    softmax_rows_backward_ex(y, dy, dx, M, N, ld(y), ld(dy), ld(dx), dtype_code(y.dtype), plan,
+                             stream)
+    return dx

@@ -5,6 +5,7 @@
 #include <unordered_map>
 
 #include "../../include/softmax_rows.h"
+#include "rowpair.h"
 #include "internal.h"
 
 namespace sr {
@@ -231,6 +232,71 @@ int choose_masked_plan(const void* in, const void* out, int64_t N, int64_t ld_in
     return (plan == SR_PLAN_ROW || plan == SR_PLAN_WARP) ? plan : SR_PLAN_ONLINE;
 }
 
+// Argument check of the softmax backward: 0 or a positive sr_status.
+int check_bwd_args(const void* y, const void* dy, const void* dx, int64_t M, int64_t N,
+                   int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype) {
+    if (dtype != SR_F32 && dtype != SR_BF16 && dtype != SR_F16) return SR_EDTYPE;
+    if (M < 0 || N < 1 || ld_y < N || ld_dy < N || ld_dx < N) return SR_EINVAL;
+    if (M > 0 && (y == nullptr || dy == nullptr || dx == nullptr)) return SR_EINVAL;
+    if (M > 0 && (dx == y || dx == dy)) return SR_EINVAL;
+    if (M > 0) {
+        __int128 ld = ld_y > ld_dy ? ld_y : ld_dy;
+        if (ld_dx > ld) ld = ld_dx;
+        const __int128 last = ((__int128)(M - 1) * ld + N) * elem_bytes(dtype);
+        if (last > (__int128)INT64_MAX) return SR_EINVAL;
+    }
+    return 0;
+}
+
+// Resolve `plan` for a row-pair operation (SR_PLAN_AUTO included): the plan,
+// or a negative status.
+int resolve_pair_plan(const rp::Args& p, int plan, int sm_count, rp::Shape* sh) {
+    if (plan == SR_PLAN_AUTO) plan = rp::choose_plan(p, sm_count);
+    if (plan != SR_PLAN_ROW && plan != SR_PLAN_CLUSTER && plan != SR_PLAN_ONLINE) return -SR_EPLAN;
+    if (!rp::shape_for(p, plan, sm_count, sh)) return -SR_EPLAN;
+    return plan;
+}
+
+// Plan and launch one row-pair operation (arguments already checked).
+template <class Launch>
+int run_pair(const rp::Args& a, int plan, Launch&& launch) {
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return SR_EPLAN;
+    rp::Shape sh;
+    if (a.M == 0) {  // nothing to launch; the plan is still checked against the shape
+        return resolve_pair_plan(a, plan, 1, &sh) < 0 ? SR_EPLAN : SR_OK;
+    }
+    cudaError_t e;
+    const DeviceInfo* dev = device_info(&e);
+    if (!dev) return SR_ECUDA;
+    const int chosen = resolve_pair_plan(a, plan, dev->sm_count, &sh);
+    if (chosen < 0) return -chosen;
+    return launch(a, sh) == cudaSuccess ? SR_OK : SR_ECUDA;
+}
+
+int run_bwd(const void* y, const void* dy, void* dx, int64_t M, int64_t N, int64_t ld_y,
+            int64_t ld_dy, int64_t ld_dx, int dtype, int plan, cudaStream_t stream) {
+    const int bad = check_bwd_args(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype);
+    if (bad) return bad;
+    const rp::Args a{y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, stream};
+    return run_pair(a, plan, [](const rp::Args& q, const rp::Shape& sh) {
+        return launch_backward(q, sh);
+    });
+}
+
+// The plan a row-pair call would run, or a negative status (host logic; the
+// current device's SM count when sm_count <= 0).
+int pair_plan_query(const rp::Args& a, int plan, int sm_count) {
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return -SR_EPLAN;
+    if (sm_count <= 0) {
+        cudaError_t e;
+        const DeviceInfo* dev = device_info(&e);
+        if (!dev) return -SR_ECUDA;
+        sm_count = dev->sm_count;
+    }
+    rp::Shape sh;
+    return resolve_pair_plan(a, plan, sm_count, &sh);
+}
+
 int launch_auto(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype, cudaStream_t stream) {
     return run(in, out, M, N, ld_in, ld_out, dtype, SR_PLAN_AUTO, stream, kDefaultTimeoutNs, 0);
@@ -362,6 +428,28 @@ int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64
     if (M == 0) return SR_OK;
     return sr::run_host(h_in, h_out, M, N, ld_in, ld_out, dtype, d_work, work_bytes,
                         (cudaStream_t)stream, sr::launch_auto);
+}
+
+int softmax_rows_backward(const void* y, const void* dy, void* dx, int64_t M, int64_t N,
+                          int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype,
+                          sr_stream_t stream) {
+    return sr::run_bwd(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, SR_PLAN_AUTO,
+                       (cudaStream_t)stream);
+}
+
+int softmax_rows_backward_ex(const void* y, const void* dy, void* dx, int64_t M, int64_t N,
+                             int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype, int plan,
+                             sr_stream_t stream) {
+    return sr::run_bwd(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan, (cudaStream_t)stream);
+}
+
+int softmax_rows_backward_plan(const void* y, const void* dy, const void* dx, int64_t M,
+                               int64_t N, int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype,
+                               int plan, int sm_count) {
+    const int bad = sr::check_bwd_args(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype);
+    if (bad) return -bad;
+    const sr::rp::Args a{y, dy, const_cast<void*>(dx), M, N, ld_y, ld_dy, ld_dx, dtype, nullptr};
+    return sr::pair_plan_query(a, plan, sm_count);
 }
 
 const char* softmax_rows_strerror(int status) {

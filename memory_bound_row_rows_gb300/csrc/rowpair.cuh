@@ -1,0 +1,501 @@
+// Row-pair engine: kernels for operations that read two M x N matrices A and
+// B, reduce each row to one FP32 number, and write C = f(A, B, that number)
+// elementwise. The softmax backward (A = y, B = dy, the number is the dot
+// product) and the residual RMSNorm (A = x, B = residual, the number is the
+// inverse RMS) are such operations; an Op type supplies the arithmetic:
+//
+//   struct Op {
+//     // acc += the element's contribution to the row's reduction
+//     __device__ void accumulate(float& acc, float a, float b) const;
+//     // the row's number from the FP32 sum of all contributions
+//     __device__ float finish(float total, int64_t N) const;
+//     // out[e] = the result at columns col .. col + n - 1 (n = 1 or VEC)
+//     template <int n> __device__ void apply(const float* a, const float* b, float s,
+//                                            int64_t col, float* out) const;
+//   };
+//
+// Three plans, each reading A and B once (ONLINE: twice) and writing C once:
+//  ROW      a team of 32..512 threads per row holds the row in registers and
+//           reduces with shuffles (plus one shared-memory step for teams
+//           wider than a warp); one-warp teams share a block four to one.
+//  CLUSTER  the C blocks of a thread-block cluster hold a row in C slices;
+//           each block stores its partial into every block's shared memory
+//           (distributed shared memory) and one hardware cluster barrier
+//           makes them visible; every block adds the C partials in rank order,
+//           so all blocks of a row use the same number.
+//  ONLINE   one block per row reads the row to reduce it, then again to write.
+//
+// Units: with Mode::kAligned every row of all three matrices starts on a
+// 16-byte boundary and holds whole 16-byte vectors; with Mode::kShifted the
+// rows of the three matrices share the same offset from a 16-byte boundary
+// (the same base offset and pitch modulo 16 bytes), so each row is a head of
+// fewer than VEC elements, 16-byte vectors, and a tail of fewer than VEC
+// elements; the head and tail elements go one per thread. Mode::kScalar
+// loads single elements.
+#pragma once
+
+#include "device.cuh"
+#include "internal.h"
+#include "rowpair.h"
+
+namespace sr {
+namespace rp {
+
+// Units per thread a plan aims for, and the most it holds. Eight 16-byte
+// vectors of 16-bit data per matrix widen to 128 floats, more than a thread
+// keeps without spilling, so 16-bit vectors stop at four.
+template <typename T, Mode MODE>
+struct KvTarget {
+    static constexpr bool kWide = MODE != Mode::kScalar;
+    static constexpr int kTarget = kWide ? 4 : 8;
+    static constexpr int kMax = kWide ? (sizeof(T) == 4 ? 8 : 4) : 16;
+};
+
+// One load unit: a 16-byte vector or a single element.
+template <typename T, bool WIDE>
+struct Unit;
+
+template <typename T>
+struct Unit<T, true> {
+    static constexpr int kN = Elem<T>::kVec;
+    uint4 raw;
+    __device__ __forceinline__ void zero() { raw = make_uint4(0u, 0u, 0u, 0u); }
+    __device__ __forceinline__ void load(const T* p) { raw = ldg_stream(p); }
+    __device__ __forceinline__ void get(float* f) const { Elem<T>::unpack(raw, f); }
+    __device__ __forceinline__ static void put(T* p, const float* f) {
+        stg_stream(p, Elem<T>::pack(f));
+    }
+};
+
+template <typename T>
+struct Unit<T, false> {
+    static constexpr int kN = 1;
+    float v;
+    __device__ __forceinline__ void zero() { v = 0.0f; }
+    __device__ __forceinline__ void load(const T* p) { v = Elem<T>::load1(p); }
+    __device__ __forceinline__ void get(float* f) const { f[0] = v; }
+    __device__ __forceinline__ static void put(T* p, const float* f) { Elem<T>::store1(p, f[0]); }
+};
+
+// Where a row's units and its head/tail elements are.
+template <typename T, Mode MODE>
+struct Layout {
+    static constexpr int VEC = MODE == Mode::kScalar ? 1 : Elem<T>::kVec;
+    int head = 0;      // elements before the first 16-byte boundary
+    int64_t nv = 0;    // units (vectors, or elements with kScalar)
+    int extra = 0;     // head + tail elements
+    __device__ __forceinline__ Layout(const T* row, int64_t N) {
+        if constexpr (MODE == Mode::kShifted) {
+            const int off = (int)((reinterpret_cast<uintptr_t>(row) & 15u) / sizeof(T));
+            head = off ? VEC - off : 0;
+            if (head > N) head = (int)N;
+            nv = (N - head) / VEC;
+            extra = (int)(N - nv * VEC);
+        } else {
+            nv = N / VEC;
+        }
+    }
+    __device__ __forceinline__ int64_t unit_col(int64_t i) const { return head + i * VEC; }
+    __device__ __forceinline__ int64_t extra_col(int k) const {
+        return k < head ? k : head + nv * VEC + (k - head);
+    }
+};
+
+template <int VEC>
+__device__ __forceinline__ float fold(float* acc) {
+#pragma unroll
+    for (int w = VEC / 2; w > 0; w >>= 1)
+#pragma unroll
+        for (int e = 0; e < w; ++e) acc[e] += acc[e + w];
+    return acc[0];
+}
+
+// Sum of one value per thread over the NW warps starting at warp w0, through
+// red[] (callers alternate two buffers per row, so a warp may write the next
+// row's partial before a slower warp has read this row's).
+template <int NW>
+__device__ __forceinline__ float team_sum(float v, float* red, int w0) {
+    v = warp_sum(v);
+    if constexpr (NW == 1) {
+        return v;
+    } else {
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+        __syncthreads();
+        float s = red[w0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) s += red[w0 + w];
+        return s;
+    }
+}
+
+template <class Op, typename T, bool WIDE>
+__device__ __forceinline__ void accumulate_unit(const Op& op, const Unit<T, WIDE>& a,
+                                                const Unit<T, WIDE>& b, float* acc) {
+    constexpr int VEC = Unit<T, WIDE>::kN;
+    float fa[VEC], fb[VEC];
+    a.get(fa);
+    b.get(fb);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) op.accumulate(acc[e], fa[e], fb[e]);
+}
+
+template <class Op, typename T, bool WIDE>
+__device__ __forceinline__ void write_unit(const Op& op, const Unit<T, WIDE>& a,
+                                           const Unit<T, WIDE>& b, float s, int64_t col, T* p) {
+    constexpr int VEC = Unit<T, WIDE>::kN;
+    float fa[VEC], fb[VEC], f[VEC];
+    a.get(fa);
+    b.get(fb);
+    op.template apply<VEC>(fa, fb, s, col, f);
+    Unit<T, WIDE>::put(p, f);
+}
+
+// The head/tail element a thread owns (if any) in a kShifted row.
+template <class Op, typename T>
+struct Extra {
+    float a = 0.0f, b = 0.0f;
+    int64_t col = -1;
+    __device__ __forceinline__ void load(const T* ra, const T* rb, int64_t c) {
+        col = c;
+        a = Elem<T>::load1(ra + c);
+        b = Elem<T>::load1(rb + c);
+    }
+    __device__ __forceinline__ void accumulate(const Op& op, float* acc) const {
+        if (col >= 0) op.accumulate(acc[0], a, b);
+    }
+    __device__ __forceinline__ void write(const Op& op, float s, T* rc) const {
+        if (col >= 0) {
+            float f;
+            op.template apply<1>(&a, &b, s, col, &f);
+            Elem<T>::store1(rc + col, f);
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// ROW plan.
+// ---------------------------------------------------------------------------
+template <class Op, typename T, Mode MODE, int TPR, int KV>
+__global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
+    team_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
+                int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    constexpr bool WIDE = MODE != Mode::kScalar;
+    using U = Unit<T, WIDE>;
+    using L = Layout<T, MODE>;
+    constexpr int VEC = U::kN;
+    constexpr int NT = TPR < 128 ? 128 : TPR;
+    constexpr int RPB = NT / TPR;  // rows per block
+    constexpr int NW = TPR / 32;   // warps per team
+    __shared__ float red[2][NT / 32];
+    const int tid = threadIdx.x, t = tid % TPR;
+    const int w0 = (tid / TPR) * NW;
+    int parity = 0;
+    for (int64_t r0 = (int64_t)blockIdx.x * RPB; r0 < M; r0 += (int64_t)gridDim.x * RPB) {
+        const int64_t r = r0 + tid / TPR;
+        const bool live = r < M;
+        const T* ra = A + r * lda;
+        const T* rb = B + r * ldb;
+        const L lay(ra, live ? N : 0);
+        U a[KV], b[KV];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int64_t idx = t + TPR * k;
+            if (idx < lay.nv) {
+                a[k].load(ra + lay.unit_col(idx));
+                b[k].load(rb + lay.unit_col(idx));
+            } else {
+                a[k].zero();
+                b[k].zero();
+            }
+        }
+        Extra<Op, T> ex;
+        if constexpr (MODE == Mode::kShifted)
+            if (t < lay.extra) ex.load(ra, rb, lay.extra_col(t));
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) accumulate_unit<Op, T, WIDE>(op, a[k], b[k], acc);
+        if constexpr (MODE == Mode::kShifted) ex.accumulate(op, acc);
+        const float s = op.finish(team_sum<NW>(fold<VEC>(acc), red[parity], w0), N);
+        parity ^= 1;
+        T* rc = C + r * ldc;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int64_t idx = t + TPR * k;
+            if (idx < lay.nv)
+                write_unit<Op, T, WIDE>(op, a[k], b[k], s, lay.unit_col(idx), rc + lay.unit_col(idx));
+        }
+        if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// CLUSTER plan: csize blocks per row, `slice` units per block; the head and
+// tail elements of a kShifted row belong to rank 0.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+template <class Op, typename T, Mode MODE, int KV>
+__global__ void __launch_bounds__(kClusterThreads)
+    cluster_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
+                   int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
+                   int64_t slice) {
+    constexpr bool WIDE = MODE != Mode::kScalar;
+    using U = Unit<T, WIDE>;
+    using L = Layout<T, MODE>;
+    constexpr int VEC = U::kN;
+    constexpr int NT = kClusterThreads;
+    constexpr int NW = NT / 32;
+    __shared__ float red[2][NW];
+    __shared__ float part[2][kMaxCluster];  // part[p][q]: block q's partial of this row
+    const int tid = threadIdx.x;
+    const int rank = (int)cluster_ctarank();
+    const int64_t nclusters = gridDim.x / csize;
+    // A block may store into a peer's shared memory only once the peer is
+    // running; the first row's loads overlap this start-up barrier.
+    cluster_arrive_relaxed();
+    bool started = false;
+    int parity = 0;
+    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters) {
+        const T* ra = A + r * lda;
+        const T* rb = B + r * ldb;
+        const L lay(ra, N);
+        const int64_t u0 = (int64_t)rank * slice;
+        const int64_t u1 = (u0 + slice < lay.nv) ? u0 + slice : lay.nv;
+        U a[KV], b[KV];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int64_t idx = u0 + tid + NT * k;
+            if (idx < u1) {
+                a[k].load(ra + lay.unit_col(idx));
+                b[k].load(rb + lay.unit_col(idx));
+            } else {
+                a[k].zero();
+                b[k].zero();
+            }
+        }
+        Extra<Op, T> ex;
+        if constexpr (MODE == Mode::kShifted)
+            if (rank == 0 && tid < lay.extra) ex.load(ra, rb, lay.extra_col(tid));
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) accumulate_unit<Op, T, WIDE>(op, a[k], b[k], acc);
+        if constexpr (MODE == Mode::kShifted) ex.accumulate(op, acc);
+        const float mine = team_sum<NW>(fold<VEC>(acc), red[parity], 0);
+        if (!started) {
+            cluster_wait();
+            started = true;
+        }
+        if (tid < csize)
+            st_cluster_f32(map_to_rank(smem_addr(&part[parity][rank]), (uint32_t)tid), mine);
+        // Release this block's stores, acquire the peers' (every thread of
+        // every block of the cluster arrives once per row).
+        cluster_sync_all();
+        float total = part[parity][0];
+        for (int q = 1; q < csize; ++q) total += part[parity][q];
+        const float s = op.finish(total, N);
+        parity ^= 1;
+        T* rc = C + r * ldc;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int64_t idx = u0 + tid + NT * k;
+            if (idx < u1)
+                write_unit<Op, T, WIDE>(op, a[k], b[k], s, lay.unit_col(idx), rc + lay.unit_col(idx));
+        }
+        if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
+    }
+    if (!started) cluster_wait();
+}
+
+// ---------------------------------------------------------------------------
+// ONLINE plan: one block per row, two passes.
+// ---------------------------------------------------------------------------
+template <class Op, typename T, Mode MODE>
+__global__ void __launch_bounds__(kLoopThreads)
+    loop_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
+                int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    constexpr bool WIDE = MODE != Mode::kScalar;
+    using U = Unit<T, WIDE>;
+    using L = Layout<T, MODE>;
+    constexpr int VEC = U::kN;
+    constexpr int NT = kLoopThreads;
+    constexpr int NW = NT / 32;
+    constexpr int UR = kLoopUnroll;
+    __shared__ float red[2][NW];
+    const int tid = threadIdx.x;
+    int parity = 0;
+    for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
+        const T* ra = A + r * lda;
+        const T* rb = B + r * ldb;
+        const L lay(ra, N);
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+        for (int64_t base = 0; base < lay.nv; base += (int64_t)NT * UR) {
+            U a[UR], b[UR];
+#pragma unroll
+            for (int j = 0; j < UR; ++j) {
+                const int64_t idx = base + tid + NT * j;
+                if (idx < lay.nv) {
+                    a[j].load(ra + lay.unit_col(idx));
+                    b[j].load(rb + lay.unit_col(idx));
+                } else {
+                    a[j].zero();
+                    b[j].zero();
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < UR; ++j) accumulate_unit<Op, T, WIDE>(op, a[j], b[j], acc);
+        }
+        Extra<Op, T> ex;
+        if constexpr (MODE == Mode::kShifted)
+            if (tid < lay.extra) ex.load(ra, rb, lay.extra_col(tid));
+        if constexpr (MODE == Mode::kShifted) ex.accumulate(op, acc);
+        const float s = op.finish(team_sum<NW>(fold<VEC>(acc), red[parity], 0), N);
+        parity ^= 1;
+        T* rc = C + r * ldc;
+        for (int64_t base = 0; base < lay.nv; base += (int64_t)NT * UR) {
+            U a[UR], b[UR];
+#pragma unroll
+            for (int j = 0; j < UR; ++j) {
+                const int64_t idx = base + tid + NT * j;
+                if (idx < lay.nv) {
+                    a[j].load(ra + lay.unit_col(idx));
+                    b[j].load(rb + lay.unit_col(idx));
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < UR; ++j) {
+                const int64_t idx = base + tid + NT * j;
+                if (idx < lay.nv)
+                    write_unit<Op, T, WIDE>(op, a[j], b[j], s, lay.unit_col(idx), rc + lay.unit_col(idx));
+            }
+        }
+        if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
+    }
+}
+
+// One block (or cluster) per row up to the largest grid; more rows are
+// walked with a grid stride.
+inline unsigned grid_for(int64_t rows, int64_t blocks_per_unit) {
+    const int64_t cap = 0x7fffffff / blocks_per_unit;
+    return (unsigned)((rows < cap ? rows : cap) * blocks_per_unit);
+}
+
+template <class Op, typename T, Mode MODE, int TPR, int KV>
+cudaError_t launch_team_kv(const Op& op, const Args& p) {
+    constexpr int NT = TPR < 128 ? 128 : TPR;
+    constexpr int RPB = NT / TPR;
+    team_kernel<Op, T, MODE, TPR, KV><<<grid_for((p.M + RPB - 1) / RPB, 1), NT, 0, p.stream>>>(
+        op, static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.c), p.M,
+        p.N, p.lda, p.ldb, p.ldc);
+    return cudaGetLastError();
+}
+
+template <class Op, typename T, Mode MODE, int TPR>
+cudaError_t launch_team_tpr(const Op& op, const Args& p, int kv) {
+    constexpr int KT = KvTarget<T, MODE>::kTarget;
+    constexpr int KM = KvTarget<T, MODE>::kMax;
+    if constexpr (TPR == 32) {
+        if (kv == 1) return launch_team_kv<Op, T, MODE, TPR, 1>(op, p);
+        if (kv == 2) return launch_team_kv<Op, T, MODE, TPR, 2>(op, p);
+        if (kv == 4) return launch_team_kv<Op, T, MODE, TPR, 4>(op, p);
+        if constexpr (KT > 4) if (kv == KT) return launch_team_kv<Op, T, MODE, TPR, KT>(op, p);
+    } else {
+        if (kv == KT) return launch_team_kv<Op, T, MODE, TPR, KT>(op, p);
+        if constexpr (TPR == kTeamMaxThreads && KM > KT)
+            if (kv == KM) return launch_team_kv<Op, T, MODE, TPR, KM>(op, p);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <class Op, typename T, Mode MODE>
+cudaError_t launch_team(const Op& op, const Args& p, const Shape& sh) {
+    switch (sh.tpr) {
+        case 32: return launch_team_tpr<Op, T, MODE, 32>(op, p, sh.kv);
+        case 64: return launch_team_tpr<Op, T, MODE, 64>(op, p, sh.kv);
+        case 128: return launch_team_tpr<Op, T, MODE, 128>(op, p, sh.kv);
+        case 256: return launch_team_tpr<Op, T, MODE, 256>(op, p, sh.kv);
+        case 512: return launch_team_tpr<Op, T, MODE, 512>(op, p, sh.kv);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <class Op, typename T, Mode MODE, int KV>
+cudaError_t launch_cluster_kv(const Op& op, const Args& p, const Shape& sh) {
+    auto kern = cluster_kernel<Op, T, MODE, KV>;
+    const void* fn = reinterpret_cast<const void*>(kern);
+    cudaError_t e = ensure_smem_limit(fn, 0, sh.csize > 8);
+    if (e != cudaSuccess) return e;
+    if (max_active_clusters(fn, kClusterThreads, 0, sh.csize) <= 0)
+        return cudaErrorInvalidConfiguration;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid_for(p.M, sh.csize), 1, 1);
+    cfg.blockDim = dim3(kClusterThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)sh.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
+                           static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc, sh.csize,
+                           sh.slice);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+template <class Op, typename T, Mode MODE>
+cudaError_t launch_cluster(const Op& op, const Args& p, const Shape& sh) {
+    constexpr int KM = KvTarget<T, MODE>::kMax;
+    if (sh.kv == 1) return launch_cluster_kv<Op, T, MODE, 1>(op, p, sh);
+    if (sh.kv == 2) return launch_cluster_kv<Op, T, MODE, 2>(op, p, sh);
+    if (sh.kv == 4) return launch_cluster_kv<Op, T, MODE, 4>(op, p, sh);
+    if constexpr (KM >= 8) if (sh.kv == 8) return launch_cluster_kv<Op, T, MODE, 8>(op, p, sh);
+    if constexpr (KM >= 16) if (sh.kv == 16) return launch_cluster_kv<Op, T, MODE, 16>(op, p, sh);
+    return cudaErrorInvalidValue;
+}
+
+template <class Op, typename T, Mode MODE>
+cudaError_t launch_mode(const Op& op, const Args& p, const Shape& sh) {
+    switch (sh.plan) {
+        case SR_PLAN_ROW: return launch_team<Op, T, MODE>(op, p, sh);
+        case SR_PLAN_CLUSTER: return launch_cluster<Op, T, MODE>(op, p, sh);
+        case SR_PLAN_ONLINE:
+            loop_kernel<Op, T, MODE><<<grid_for(p.M, 1), kLoopThreads, 0, p.stream>>>(
+                op, static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.c),
+                p.M, p.N, p.lda, p.ldb, p.ldc);
+            return cudaGetLastError();
+    }
+    return cudaErrorInvalidValue;
+}
+
+// Launch `sh` with the Op the factory makes for element type T.
+template <typename T, class Op>
+cudaError_t launch(const Op& op, const Args& p, const Shape& sh) {
+    switch (sh.mode) {
+        case (int)Mode::kAligned: return launch_mode<Op, T, Mode::kAligned>(op, p, sh);
+        case (int)Mode::kShifted: return launch_mode<Op, T, Mode::kShifted>(op, p, sh);
+        case (int)Mode::kScalar: return launch_mode<Op, T, Mode::kScalar>(op, p, sh);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace rp
+}  // namespace sr

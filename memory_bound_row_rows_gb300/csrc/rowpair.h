@@ -1,0 +1,149 @@
+// Host-side logic of the row-pair engine (rowpair.cuh): the problem, the
+// load mode the matrices allow, and the shape each plan runs with. Plain host
+// code, shared by the C ABI (plan queries) and the launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/softmax_rows.h"
+#include "internal.h"
+
+namespace sr {
+namespace rp {
+
+enum class Mode : int { kAligned = 0, kShifted = 1, kScalar = 2 };
+
+constexpr int kTeamMaxThreads = 512;
+constexpr int kClusterThreads = 256;
+constexpr int kLoopThreads = 512;
+constexpr int kLoopUnroll = 4;
+
+inline int kv_target(int mode) { return mode != (int)Mode::kScalar ? 4 : 8; }
+inline int kv_max(int mode, int dtype) {
+    return mode != (int)Mode::kScalar ? (elem_bytes(dtype) == 4 ? 8 : 4) : 16;
+}
+
+// One problem: C = f(A, B, the row's reduction), M x N, pitches in elements.
+struct Args {
+    const void* a;
+    const void* b;
+    void* c;
+    int64_t M, N, lda, ldb, ldc;
+    int dtype;
+    cudaStream_t stream;
+};
+
+// How one plan runs one problem (host logic only, the same on every device).
+struct Shape {
+    int plan = 0;  // SR_PLAN_ROW, SR_PLAN_CLUSTER or SR_PLAN_ONLINE
+    int mode = 0;  // Mode
+    int tpr = 0;   // ROW: threads per row
+    int kv = 0;    // ROW, CLUSTER: units per thread
+    int csize = 0; // CLUSTER: blocks per row
+    int64_t slice = 0;  // CLUSTER: units per block
+};
+
+// The load mode the three matrices allow.
+inline int mode_for(const Args& p) {
+    const int64_t es = elem_bytes(p.dtype);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p.a), b = reinterpret_cast<uintptr_t>(p.b),
+                    c = reinterpret_cast<uintptr_t>(p.c);
+    const int64_t pa = p.lda * es % 16, pb = p.ldb * es % 16, pc = p.ldc * es % 16;
+    if (a % 16 == 0 && b % 16 == 0 && c % 16 == 0 && pa == 0 && pb == 0 && pc == 0 &&
+        (p.N * es) % 16 == 0)
+        return (int)Mode::kAligned;
+    if (a % 16 == b % 16 && a % 16 == c % 16 && pa == pb && pa == pc && a % es == 0)
+        return (int)Mode::kShifted;
+    return (int)Mode::kScalar;
+}
+
+// Most units a row of the matrices can hold (a shifted row's vectors are at
+// most N / VEC).
+inline int64_t max_units(const Args& p, int mode) {
+    return mode == (int)Mode::kScalar ? p.N : p.N / (16 / elem_bytes(p.dtype));
+}
+
+inline int64_t pow2_at_least(int64_t v) {
+    int64_t k = 1;
+    while (k < v) k *= 2;
+    return k;
+}
+
+// Shapes:
+//  ROW: the smallest power-of-two team (32..512 threads) that gives each
+//    thread at most the target units (4 vectors, or 8 elements), the units
+//    per thread rounded up to a power of two; rows up to 512 x the most a
+//    thread holds (8 f32 vectors, 4 16-bit vectors, 16 elements).
+//  CLUSTER: 256-thread blocks; the smallest power-of-two cluster (2..16)
+//    whose slices fit the target units per thread (else the most a thread
+//    holds, in 16 blocks). While there are too few rows to give every SM two
+//    blocks, the cluster doubles (up to 16) as long as each block keeps at
+//    least one unit per thread; the units per thread follow the slice.
+inline bool shape_for(const Args& p, int plan, int sm_count, Shape* out) {
+    Shape sh;
+    sh.plan = plan;
+    sh.mode = mode_for(p);
+    const int64_t units = max_units(p, sh.mode);
+    const int kt = kv_target(sh.mode);
+    const int km = kv_max(sh.mode, p.dtype);
+    switch (plan) {
+        case SR_PLAN_ROW: {
+            if (units > (int64_t)kTeamMaxThreads * km) return false;
+            int tpr = 32;
+            while (tpr < kTeamMaxThreads && (int64_t)tpr * kt < units) tpr *= 2;
+            int64_t kv = pow2_at_least((units + tpr - 1) / tpr);
+            if (tpr > 32 && kv < kt) kv = kt;
+            sh.tpr = tpr;
+            sh.kv = (int)kv;
+            break;
+        }
+        case SR_PLAN_CLUSTER: {
+            int c = 0, kv = kt;
+            for (int cc = 2; cc <= kMaxCluster; cc *= 2)
+                if ((int64_t)cc * kClusterThreads * kt >= units) {
+                    c = cc;
+                    break;
+                }
+            if (c == 0) {
+                if ((int64_t)kMaxCluster * kClusterThreads * km < units) return false;
+                c = kMaxCluster;
+                kv = km;
+            }
+            while (c < kMaxCluster && p.M * c < 2 * (int64_t)sm_count &&
+                   units / (2 * c) >= kClusterThreads)
+                c *= 2;
+            sh.csize = c;
+            sh.slice = (units + c - 1) / c;
+            const int64_t k = pow2_at_least((sh.slice + kClusterThreads - 1) / kClusterThreads);
+            if (k > kv) return false;
+            sh.kv = (int)k;
+            break;
+        }
+        case SR_PLAN_ONLINE: break;
+        default: return false;
+    }
+    *out = sh;
+    return true;
+}
+
+// Automatic plan: ROW when the row fits one team and there are rows enough
+// for the GPU (or the row is short); CLUSTER for wider rows and for rows too
+// few to fill the GPU; ONLINE otherwise.
+inline int choose_plan(const Args& p, int sm_count) {
+    Shape sh;
+    const bool row = shape_for(p, SR_PLAN_ROW, sm_count, &sh);
+    const int64_t units = max_units(p, mode_for(p));
+    if (row && (p.M >= sm_count || units < 2 * kClusterThreads)) return SR_PLAN_ROW;
+    if (shape_for(p, SR_PLAN_CLUSTER, sm_count, &sh)) return SR_PLAN_CLUSTER;
+    if (row) return SR_PLAN_ROW;
+    return SR_PLAN_ONLINE;
+}
+
+}  // namespace rp
+
+// Launchers of the two row-pair operations (backward_rows.cu, rmsnorm_rows.cu).
+cudaError_t launch_backward(const rp::Args& p, const rp::Shape& sh);
+cudaError_t launch_rmsnorm(const rp::Args& p, const rp::Shape& sh, const void* weight, float eps);
+
+}  // namespace sr

@@ -190,6 +190,67 @@ WIDE_FEW = {
     ]
 }
 
+@dataclass(frozen=True)
+class BackwardWorkload:
+    """Inputs of the softmax backward: y (a stand-in for softmax output, U[0, 2/N),
+    so rows sum to about one) and the incoming gradient dy ~ N(0, 1); both M x N
+    with pitch ``ld``."""
+    name: str
+    dtype: int
+    M: int
+    N: int
+    ld: int
+    seed: int
+
+    @property
+    def elem_bytes(self) -> int:
+        return ELEM_BYTES[self.dtype]
+
+    @property
+    def fused_bytes(self) -> int:
+        """Algorithmic HBM bytes: y and dy read once, dx written once."""
+        return 3 * self.M * self.N * self.elem_bytes
+
+    def with_rows(self, M: int) -> "BackwardWorkload":
+        d = dict(self.__dict__)
+        d["M"] = M
+        return BackwardWorkload(**d)
+
+    def _rows(self, which: int, row0: int, count: int, nthreads=None) -> np.ndarray:
+        count = max(0, min(count, self.M - row0))
+        buf = np.zeros((count, self.ld), dtype=NP_STORAGE[self.dtype])
+        if count:
+            if which == 0:
+                kw = dict(dist=DIST_UNIFORM, p0=0.0, p1=2.0 / self.N)
+            else:
+                kw = dict(dist=DIST_NORMAL, p0=0.0, p1=1.0)
+            generate_into(buf.reshape(-1), row0, count, self.N, self.ld, self.dtype,
+                          self.seed * 2 + which, nthreads=nthreads, **kw)
+        return buf
+
+    def y_rows(self, row0: int, count: int, nthreads=None) -> np.ndarray:
+        return self._rows(0, row0, count, nthreads)
+
+    def dy_rows(self, row0: int, count: int, nthreads=None) -> np.ndarray:
+        return self._rows(1, row0, count, nthreads)
+
+
+# Softmax-backward shapes: the FP16 training-step shapes of "Measured
+# optimization case studies" (Training), plus the 4096 x 4096 FP32 square.
+BACKWARD = {
+    w.name: w
+    for w in [
+        BackwardWorkload("f16_16384x4096", F16, 16384, 4096, 4096, 20),
+        BackwardWorkload("f32_4096x4096", F32, 4096, 4096, 4096, 21),
+        BackwardWorkload("f16_64x131072", F16, 64, 131072, 131072, 22),
+        BackwardWorkload("f16_4x32769", F16, 4, 32769, 32769, 23),
+        BackwardWorkload("f16_512x4097", F16, 512, 4097, 4097, 24),
+        BackwardWorkload("f16_1024x1024", F16, 1024, 1024, 1024, 25),
+        BackwardWorkload("f16_32x127", F16, 32, 127, 127, 26),
+    ]
+}
+BACKWARD_HEADLINE = "f16_16384x4096"
+
 # The workload the headline throughput is quoted on (square FP32 matrix, 4096 x 4096).
 HEADLINE = "f32_4096x4096"
 

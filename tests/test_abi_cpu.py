@@ -147,3 +147,74 @@ def test_split_workspace_is_host_logic(lib):
     L = lib
     assert L.softmax_rows_split(A, B, 0, 8, 8, 8, 0, None, 0, None) == sr.SR_OK
     assert L.softmax_rows_split(A, B, 4, 8, 8, 8, 0, None, 1024, None) == sr.SR_EINVAL
+
+
+ALIGNED_DY = 0x7F0200000000
+
+
+def test_backward_rejected_arguments_touch_no_device(lib):
+    L = lib
+    y, g, x = ALIGNED_IN, ALIGNED_DY, ALIGNED_OUT
+    assert L.softmax_rows_backward(None, None, None, 0, 8, 8, 8, 8, 0, None) == sr.SR_OK
+    assert L.softmax_rows_backward(y, g, x, 4, 0, 8, 8, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows_backward(y, g, x, -1, 8, 8, 8, 8, 0, None) == sr.SR_EINVAL
+    for lds in ((7, 8, 8), (8, 7, 8), (8, 8, 7)):
+        assert L.softmax_rows_backward(y, g, x, 4, 8, *lds, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows_backward(y, None, x, 4, 8, 8, 8, 8, 0, None) == sr.SR_EINVAL
+    assert L.softmax_rows_backward(y, g, y, 4, 8, 8, 8, 8, 0, None) == sr.SR_EINVAL  # dx is y
+    assert L.softmax_rows_backward(y, g, g, 4, 8, 8, 8, 8, 0, None) == sr.SR_EINVAL  # dx is dy
+    assert L.softmax_rows_backward(y, g, x, 4, 8, 8, 8, 8, 3, None) == sr.SR_EDTYPE
+    assert L.softmax_rows_backward(y, g, x, 2**40, 2**30, 2**30, 2**30, 2**30, 0,
+                                   None) == sr.SR_EINVAL  # last byte beyond int64
+    assert L.softmax_rows_backward_ex(y, g, x, 4, 8, 8, 8, 8, 0, 9, None) == sr.SR_EPLAN
+    assert L.softmax_rows_backward_ex(y, g, x, 0, 8, 8, 8, 8, 0, sr.SR_PLAN_WARP,
+                                      None) == sr.SR_EPLAN
+    # Empty, with a plan that takes the shape: nothing is launched.
+    assert L.softmax_rows_backward_ex(y, g, x, 0, 8, 8, 8, 8, 0, sr.SR_PLAN_ROW,
+                                      None) == sr.SR_OK
+
+
+def _bwd_plan(M, N, dtype, plan=sr.SR_PLAN_AUTO, sm=152, ld=None, offset=0):
+    ld = N if ld is None else ld
+    return sr.softmax_rows_backward_plan(ALIGNED_IN + offset, ALIGNED_DY, ALIGNED_OUT, M, N, ld,
+                                         ld, ld, dtype, plan, sm)
+
+
+def test_backward_plan_choice(lib):
+    F32, BF16, F16 = sr.SR_F32, sr.SR_BF16, sr.SR_F16
+    ROW, CL, ON = sr.SR_PLAN_ROW, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_ONLINE
+    # Many rows that fit one team: ROW.
+    assert _bwd_plan(4096, 4096, F32) == ROW
+    assert _bwd_plan(16384, 4096, F16) == ROW
+    assert _bwd_plan(1024, 1024, F16) == ROW
+    assert _bwd_plan(32, 127, F16) == ROW          # short rows, even if few
+    assert _bwd_plan(512, 4097, F16) == ROW        # unaligned, 4097 elements
+    # Team limits: 16384 elements of any dtype when aligned, 8192 unaligned.
+    assert _bwd_plan(1024, 16384, F32, ROW) == ROW
+    assert _bwd_plan(1024, 16384, F16, ROW) == ROW
+    assert _bwd_plan(1024, 16392, F16, ROW) == -sr.SR_EPLAN
+    # Odd widths with the same pitch in all three matrices: rows share their
+    # offset from a 16-byte boundary and are loaded as vectors.
+    assert _bwd_plan(1024, 8193, F16, ROW) == ROW
+    assert _bwd_plan(1024, 16391, F16, ROW) == ROW
+    # Incongruent layouts (y 2 bytes off, dy and dx aligned) load elements:
+    # 8192 elements per team at most.
+    assert _bwd_plan(1024, 8192, F16, ROW, offset=2) == ROW
+    assert _bwd_plan(1024, 8193, F16, ROW, offset=2) == -sr.SR_EPLAN
+    # Wide or few rows: CLUSTER; beyond its limit: ONLINE.
+    assert _bwd_plan(64, 131072, F16) == CL
+    assert _bwd_plan(4, 32769, F16) == CL
+    assert _bwd_plan(1024, 131072, BF16) == CL
+    assert _bwd_plan(8, 4096, F32) == CL           # too few rows for one team each
+    assert _bwd_plan(64, 131080, F16) == ON
+    assert _bwd_plan(4, 65537, F16) == CL
+    assert _bwd_plan(4, 65537, F16, offset=2) == ON
+    assert _bwd_plan(4, 65536, F16, offset=2) == CL
+    assert _bwd_plan(64, 131080, F16, CL) == -sr.SR_EPLAN
+    # ONLINE takes anything.
+    assert _bwd_plan(3, 1 << 22, F32, ON) == ON
+    # A misaligned y base makes every row unaligned (element units).
+    assert _bwd_plan(1024, 16384, F16, ROW, offset=2) == -sr.SR_EPLAN
+    # Query errors.
+    assert _bwd_plan(4, 8, 7) == -sr.SR_EDTYPE
+    assert _bwd_plan(4, 8, F32, plan=sr.SR_PLAN_SMEM) == -sr.SR_EPLAN
