@@ -58,6 +58,9 @@ class Oracle:
         fn = lib.oracle_softmax_backward
         fn.restype = c_int
         fn.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, c_int]
+        fn = lib.oracle_rmsnorm_residual
+        fn.restype = c_int
+        fn.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_double, c_int]
         for name in ("oracle_cast", "oracle_decode"):
             fn = getattr(lib, name)
             fn.restype = c_int
@@ -113,6 +116,21 @@ class Oracle:
         if rc != 0:
             raise ValueError("oracle_softmax_backward returned %d" % rc)
         return dx
+
+    def rmsnorm_residual(self, x: np.ndarray, r: np.ndarray, w: np.ndarray, M: int, N: int,
+                         ld_x: int, ld_r: int, ld_y: int, eps: float, dtype: int) -> np.ndarray:
+        """y = dtype(h * w / sqrt(mean(h^2) + eps)), h = dtype(x + r); an (M, ld_y) array."""
+        x, r, w = (np.ascontiguousarray(a) for a in (x, r, w))
+        for a in (x, r, w):
+            assert a.dtype == _STORAGE[dtype]
+        assert x.size >= M * ld_x and r.size >= M * ld_r and w.size >= N
+        y = np.zeros((M, ld_y), dtype=_STORAGE[dtype])
+        rc = self.lib.oracle_rmsnorm_residual(x.ctypes.data, r.ctypes.data, w.ctypes.data,
+                                              y.ctypes.data, M, N, ld_x, ld_r, ld_y, float(eps),
+                                              dtype)
+        if rc != 0:
+            raise ValueError("oracle_rmsnorm_residual returned %d" % rc)
+        return y
 
     def softmax_rows_f64(self, x: np.ndarray, M: int, N: int, ld_in: int, dtype: int,
                          nthreads: int = 1) -> np.ndarray:

@@ -29,8 +29,8 @@
  * 2 = f16 (IEEE binary16); bf16 and f16 are 16-bit patterns.
  *
  * Also here: the masked softmax (entries past a row's valid length count as
- * -inf) and the softmax backward dx = y * (dy - sum_j y_j dy_j), each stated
- * and cited where it is defined below.
+ * -inf), the softmax backward dx = y * (dy - sum_j y_j dy_j) and the residual
+ * RMSNorm forward, each stated and cited where it is defined below.
  *
  * Parity pins (tests/test_oracle_pins.py) check this code against 60-digit
  * decimal brute force, closed forms and invariants, not against itself.
@@ -282,6 +282,50 @@ int oracle_softmax_backward(const void* y, const void* dy, void* dx, int64_t M, 
     if (dtype < OR_F32 || dtype > OR_F16) return 2;
     if (M > 0 && (!y || !dy || !dx)) return 1;
     backward_rows(y, dy, dx, 0, M, N, ld_y, ld_dy, ld_dx, dtype);
+    return 0;
+}
+
+/*
+ * Residual RMSNorm forward (the "Warpline" README's K1 kernel: one program per
+ * row adds the input and the residual in FP32, rounds that sum once to the
+ * input dtype, reduces the RMS, applies the weight and writes one rounded
+ * result; "Measured optimization case studies", Residual RMSNorm). For every
+ * row i, with w the N weights:
+ *     h_j    = dtype(x[i,j] + r[i,j])                 (one rounding of the sum)
+ *     ms     = (1/N) * sum_j h_j^2                      (FP64, sequential)
+ *     y[i,j] = dtype(h_j * w_j / sqrt(ms + eps))       (FP64, one rounding)
+ * The pages add in FP32 and then round to the dtype. For bf16 and f16 inputs
+ * that equals one rounding of the exact sum (FP32 carries at least twice
+ * their precision plus two bits, so rounding twice changes nothing), and for
+ * f32 inputs it is the FP32 sum; the double sum below, rounded once, gives
+ * both (53 >= 2 * 24 + 2 bits). x, r, y are M x N with their own pitches.
+ */
+static double to_dtype(double v, int dtype) {
+    unsigned char buf[4];
+    encode(buf, 0, dtype, v);
+    return decode(buf, 0, dtype);
+}
+
+int oracle_rmsnorm_residual(const void* x, const void* r, const void* w, void* y, int64_t M,
+                            int64_t N, int64_t ld_x, int64_t ld_r, int64_t ld_y, double eps,
+                            int dtype) {
+    if (M < 0 || N < 1 || ld_x < N || ld_r < N || ld_y < N || !(eps >= 0.0)) return 1;
+    if (dtype < OR_F32 || dtype > OR_F16) return 2;
+    if (M > 0 && (!x || !r || !w || !y)) return 1;
+    double* h = (double*)malloc((size_t)N * sizeof(double));
+    if (!h) return 3;
+    for (int64_t i = 0; i < M; ++i) {
+        double ms = 0.0;
+        for (int64_t j = 0; j < N; ++j) {
+            h[j] = to_dtype(decode(x, i * ld_x + j, dtype) + decode(r, i * ld_r + j, dtype), dtype);
+            ms += h[j] * h[j];
+        }
+        ms /= (double)N;
+        const double rms = sqrt(ms + eps);
+        for (int64_t j = 0; j < N; ++j)
+            encode(y, i * ld_y + j, dtype, h[j] * decode(w, j, dtype) / rms);
+    }
+    free(h);
     return 0;
 }
 

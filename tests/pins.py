@@ -412,10 +412,96 @@ def check_backward_closed_forms(orc):
         assert abs(d.sum()) <= 4 * UNIT_ROUNDOFF[dtype] * np.abs(d).max()
 
 
+# ---- residual RMSNorm -------------------------------------------------------------
+
+def _rms_brute(x, r, w, eps, dtype):
+    """60-digit RMSNorm of one row: h = dtype(exact x + r), y = dtype(h w / sqrt(mean h^2 + eps))."""
+    import decimal
+    h = [brute.round_exact(Fraction(float(a)) + Fraction(float(b)), dtype) for a, b in zip(x, r)]
+    with decimal.localcontext(brute.CTX):
+        H = [decimal.Decimal(v) for v in h]
+        ms = sum(v * v for v in H) / len(H)
+        rms = (ms + decimal.Decimal(float(eps))).sqrt()
+        out = []
+        for v, wj in zip(H, w):
+            q = v * decimal.Decimal(float(wj)) / rms if rms != 0 else decimal.Decimal("NaN")
+            out.append(math.nan if q.is_nan() else brute.round_exact(Fraction(q), dtype))
+    return np.array(out)
+
+
+def _rms(orc, x, r, w, eps, dtype):
+    M, N = x.shape
+    return decode(orc.rmsnorm_residual(encode_exact(x, dtype), encode_exact(r, dtype),
+                                       encode_exact(w, dtype), M, N, N, N, N, eps, dtype), dtype)
+
+
+def check_rmsnorm_brute(orc):
+    rng = np.random.default_rng(41)
+    for dtype in DTYPES:
+        for N in (1, 3, 8, 17):
+            M = 3
+            # Magnitudes spread over several binades so that x + r often needs rounding.
+            x = to_grid(rng.normal(0, 1, size=(M, N)) * 2.0 ** rng.integers(-6, 7, size=(M, N)),
+                        dtype)
+            r = to_grid(rng.normal(0, 1, size=(M, N)) * 2.0 ** rng.integers(-6, 7, size=(M, N)),
+                        dtype)
+            w = to_grid(rng.uniform(0.5, 1.5, size=N), dtype)
+            for eps in (0.0, 1e-6, 0.25):
+                got = _rms(orc, x, r, w, eps, dtype)
+                for i in range(M):
+                    want = _rms_brute(x[i], r[i], w, eps, dtype)
+                    assert same(got[i], want), "rmsnorm brute dtype %d N=%d eps=%g" % (dtype, N, eps)
+
+
+def check_rmsnorm_closed_forms(orc):
+    for dtype in DTYPES:
+        w = np.array([1.0, 2.0, 0.5, -1.0, 0.75, 1.5])
+        N = w.size
+        # A constant row of c (c = x + r exactly), eps = 0: h / rms = sign(c), so y = sign(c) w.
+        x = np.array([[3.0] * N, [-0.375] * N, [96.0] * N])
+        r = np.array([[1.0] * N, [-0.125] * N, [32.0] * N])
+        y = _rms(orc, to_grid(x, dtype), to_grid(r, dtype), to_grid(w, dtype), 0.0, dtype)
+        assert np.array_equal(y, np.sign(x + r) * w), "rmsnorm constant rows dtype %d" % dtype
+        # Alternating +-c: mean square c^2 again.
+        x2 = np.array([[2.0, -2.0] * (N // 2)])
+        y2 = _rms(orc, to_grid(x2, dtype), np.zeros_like(x2), to_grid(w, dtype), 0.0, dtype)
+        assert np.array_equal(y2[0], np.sign(x2[0]) * w)
+        # N = 1: y = w h / sqrt(h^2 + eps); with h = 3, eps = 16: y = 3/5 w.
+        y3 = _rms(orc, np.array([[1.0]]), np.array([[2.0]]), np.array([5.0]), 16.0, dtype)
+        assert y3[0, 0] == brute.round_exact(Fraction(3), dtype)
+        # Zero row: 0/0 with eps = 0, zeros with eps > 0.
+        z = np.zeros((1, 4))
+        assert np.isnan(_rms(orc, z, z, np.ones(4), 0.0, dtype)).all()
+        assert (_rms(orc, z, z, np.ones(4), 1e-6, dtype) == 0.0).all()
+
+
+def check_rmsnorm_invariants(orc):
+    rng = np.random.default_rng(42)
+    for dtype in DTYPES:
+        M, N = 4, 64
+        x = to_grid(rng.normal(0, 1, size=(M, N)), dtype)
+        r = to_grid(rng.normal(0, 1, size=(M, N)), dtype)
+        w1 = np.ones(N)
+        y = _rms(orc, x, r, w1, 0.0, dtype)
+        # Unit weight, eps = 0: each output row has mean square one (up to the casts).
+        ms = (y * y).mean(axis=1)
+        assert np.all(np.abs(ms - 1.0) <= 4 * UNIT_ROUNDOFF[dtype]), (dtype, ms)
+        # Scaling x and r by a power of two leaves y unchanged (eps = 0).
+        y4 = _rms(orc, x * 4.0, r * 4.0, w1, 0.0, dtype)
+        assert np.array_equal(y, y4)
+        # Doubling the weight doubles y exactly; a zero residual gives RMSNorm of x.
+        w = to_grid(rng.uniform(0.5, 1.5, size=N), dtype)
+        assert np.array_equal(_rms(orc, x, r, 2 * w, 1e-5, dtype),
+                              2 * _rms(orc, x, r, w, 1e-5, dtype))
+        assert np.array_equal(_rms(orc, x, np.zeros_like(x), w, 1e-5, dtype),
+                              _rms(orc, np.zeros_like(x), x, w, 1e-5, dtype))
+
+
 ALL_CHECKS = [
     check_decode, check_cast, check_brute_random, check_brute_extremes, check_uniform_rows,
     check_two_entries, check_tied_maxima, check_causal_rows, check_nan_rows,
     check_row_sums_and_range, check_shift_invariance, check_strides, check_thread_independence,
     check_masked_brute, check_masked_causal,
     check_backward_brute, check_backward_is_softmax_vjp, check_backward_closed_forms,
+    check_rmsnorm_brute, check_rmsnorm_closed_forms, check_rmsnorm_invariants,
 ]

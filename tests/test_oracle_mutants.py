@@ -35,6 +35,13 @@ MUTANTS = {
     "masked_as_zero": ("decode(jb->in, i * jb->ld_in + j, jb->dtype) : -INFINITY;",
                        "decode(jb->in, i * jb->ld_in + j, jb->dtype) : 0.0;"),
     "causal_off_by_one": ("v = i % jb->causal_period + 1;", "v = i % jb->causal_period;"),
+    "rmsnorm_no_residual": ("decode(x, i * ld_x + j, dtype) + decode(r, i * ld_r + j, dtype), dtype)",
+                            "decode(x, i * ld_x + j, dtype), dtype)"),
+    "rmsnorm_unrounded_sum": ("h[j] = to_dtype(decode(x, i * ld_x + j, dtype) + decode(r, i * ld_r + j, dtype), dtype);",
+                              "h[j] = decode(x, i * ld_x + j, dtype) + decode(r, i * ld_r + j, dtype);"),
+    "rmsnorm_sum_not_mean": ("ms /= (double)N;", "ms /= 1.0;"),
+    "rmsnorm_eps_outside": ("sqrt(ms + eps);", "sqrt(ms) + eps;"),
+    "rmsnorm_weight_index": ("decode(w, j, dtype)", "decode(w, N - 1 - j, dtype)"),
     "backward_drops_dot": ("encode(dx, i * ld_dx + j, dtype, yj * (gj - dot));",
                            "encode(dx, i * ld_dx + j, dtype, yj * gj);"),
     "backward_sign": ("encode(dx, i * ld_dx + j, dtype, yj * (gj - dot));",
