@@ -55,13 +55,15 @@ def parse_args(argv=None):
     ap.add_argument("--workload", default=None,
                     help="one of %s; 'all' (those five) or 'wide' (%s)"
                          % (", ".join(synth.WORKLOADS), ", ".join(synth.WIDE_FEW)))
-    ap.add_argument("--api", choices=("rows", "split", "masked", "backward"), default="rows",
+    ap.add_argument("--api", choices=("rows", "split", "masked", "backward", "rmsnorm"),
+                    default="rows",
                     help="rows: softmax_rows / softmax_rows_ex; split: softmax_rows_split "
                          "with a device workspace (the split plan for few, wide rows); masked: "
                          "softmax_rows_masked with the workload's causal period (masked "
                          "entries are not read); backward: softmax_rows_backward_ex on the "
-                         "backward shapes (%s; 'all' for every one)"
-                         % ", ".join(synth.BACKWARD))
+                         "backward shapes (%s); rmsnorm: rmsnorm_residual_rows_ex on the RMSNorm "
+                         "shapes (%s); 'all' for every shape of the lane"
+                         % (", ".join(synth.BACKWARD), ", ".join(synth.RMSNORM)))
     ap.add_argument("--lane", choices=("cold", "warm"), default="cold")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--plan", type=int, default=0, help="forced plan (0 = automatic)")
@@ -460,55 +462,139 @@ def bench_ours(args, w):
     return line
 
 
-# ---- softmax backward lane -------------------------------------------------------
+# ---- row-pair lanes: softmax backward and residual RMSNorm ----------------------
 
-def backward_outside_gate(g, r, y, dy, dtype) -> int:
-    """Elements outside the backward parity gate (FP32 dot product, one cast):
-    |g - r| <= |y|(2^-17 S + 2^-22 |dy - d|) + 2^-22 |r| + 2 ulp_dtype(r), with
-    d = sum y*dy and S = sum |y*dy| per row. Decoded float64 (rows, N) arrays."""
+def _ulp(r, dtype):
     mant = {synth.F32: 23, synth.BF16: 7, synth.F16: 10}[dtype]
     emin = {synth.F32: -126, synth.BF16: -126, synth.F16: -14}[dtype]
-    d = (y * dy).sum(axis=1, keepdims=True)
-    S = np.abs(y * dy).sum(axis=1, keepdims=True)
     a = np.abs(r)
-    ulp = np.exp2(np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), emin) - mant)
-    tol = np.abs(y) * (2.0 ** -17 * S + 2.0 ** -22 * np.abs(dy - d)) + 2.0 ** -22 * a + 2 * ulp
-    bad = ~(np.abs(g - r) <= tol) & ~(np.isnan(g) & np.isnan(r))
-    return int(bad.sum())
+    return np.exp2(np.maximum(np.floor(np.log2(np.where(a > 0, a, 1.0))), emin) - mant)
 
 
-def oracle_backward_rows(w, y, dy, rows):
-    import oracle
-    return oracle.load().softmax_backward(np.ascontiguousarray(y[rows]).reshape(-1),
-                                          np.ascontiguousarray(dy[rows]).reshape(-1), len(rows),
-                                          w.N, w.ld, w.ld, w.N, w.dtype)
+class BackwardLane:
+    """dx = y * (dy - sum(y * dy)) per row: y ~ U[0, 2/N), dy ~ N(0, 1)."""
+    api = "backward"
+    catalog = synth.BACKWARD
+    headline = synth.BACKWARD_HEADLINE
+    label = "softmax backward"
+    model = "3*M*N*bytes"
+
+    def __init__(self, w):
+        self.w = w
+        self.mats = [w.y_rows(0, w.M), w.dy_rows(0, w.M)]
+        self.vecs = []
+
+    data = property(lambda self: "synthetic: y ~ U[0, 2/N), dy ~ N(0, 1), seeded SplitMix64 "
+                                 "(seed %d)" % self.w.seed)
+
+    def call(self, lib, dev_mats, dev_vecs, out, plan, stream):
+        w = self.w
+        return lib.softmax_rows_backward_ex(dev_mats[0].data_ptr(), dev_mats[1].data_ptr(),
+                                            out.data_ptr(), w.M, w.N, w.ld, w.ld, w.N, w.dtype,
+                                            plan, stream)
+
+    def plan(self, sr, dev_mats, dev_vecs, out, plan):
+        w = self.w
+        return sr.softmax_rows_backward_plan(dev_mats[0], dev_mats[1], out, w.M, w.N, w.ld, w.ld,
+                                             w.N, w.dtype, plan, 0)
+
+    def oracle_rows(self, rows):
+        import oracle
+        w = self.w
+        y, dy = (np.ascontiguousarray(m[rows]).reshape(-1) for m in self.mats)
+        return oracle.load().softmax_backward(y, dy, len(rows), w.N, w.ld, w.ld, w.N, w.dtype)
+
+    def outside_gate(self, g, r, rows):
+        """|g - r| <= |y|(2^-17 S + 2^-22 |dy - d|) + 2^-22 |r| + 2 ulp(r), d = sum y*dy and
+        S = sum |y*dy| per row (the FP32 dot product's error bound, one cast)."""
+        dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :self.w.N]),
+                                                 self.w.dtype)
+        y, dy = dec(self.mats[0][rows]), dec(self.mats[1][rows])
+        d = (y * dy).sum(axis=1, keepdims=True)
+        S = np.abs(y * dy).sum(axis=1, keepdims=True)
+        tol = (np.abs(y) * (2.0 ** -17 * S + 2.0 ** -22 * np.abs(dy - d)) + 2.0 ** -22 * np.abs(r)
+               + 2 * _ulp(r, self.w.dtype))
+        return int((~(np.abs(g - r) <= tol) & ~(np.isnan(g) & np.isnan(r))).sum())
+
+    gate = "FP32 dot-product error bound plus 2 ulp of the dtype"
 
 
-def backward_cpu_baseline(w, y, dy, budget_s: float):
-    """The oracle's backward as it stands (one thread) on leading rows of the
-    workload, repeated for about budget_s."""
+class RmsNormLane(BackwardLane):
+    """y = dtype(h * w / sqrt(mean(h^2) + eps)), h = dtype(x + residual)."""
+    api = "rmsnorm"
+    catalog = synth.RMSNORM
+    headline = synth.RMSNORM_HEADLINE
+    label = "residual RMSNorm"
+    model = "(3*M*N + N)*bytes"
+
+    def __init__(self, w):
+        self.w = w
+        self.mats = [w.x_rows(0, w.M), w.residual_rows(0, w.M)]
+        self.vecs = [w.weight()]
+
+    data = property(lambda self: "synthetic: x, residual ~ N(0, 1), weight ~ U[0.5, 1.5), "
+                                 "eps %g, seeded SplitMix64 (seed %d)" % (self.w.eps, self.w.seed))
+
+    def call(self, lib, dev_mats, dev_vecs, out, plan, stream):
+        w = self.w
+        return lib.rmsnorm_residual_rows_ex(dev_mats[0].data_ptr(), dev_mats[1].data_ptr(),
+                                            dev_vecs[0].data_ptr(), out.data_ptr(), w.M, w.N, w.ld,
+                                            w.ld, w.N, w.eps, w.dtype, plan, stream)
+
+    def plan(self, sr, dev_mats, dev_vecs, out, plan):
+        w = self.w
+        return sr.rmsnorm_residual_rows_plan(dev_mats[0], dev_mats[1], dev_vecs[0], out, w.M, w.N,
+                                             w.ld, w.ld, w.N, w.eps, w.dtype, plan, 0)
+
+    def oracle_rows(self, rows):
+        import oracle
+        w = self.w
+        x, r = (np.ascontiguousarray(m[rows]).reshape(-1) for m in self.mats)
+        return oracle.load().rmsnorm_residual(x, r, self.vecs[0], len(rows), w.N, w.ld, w.ld, w.N,
+                                              float(np.float32(w.eps)), w.dtype)
+
+    def outside_gate(self, g, r, rows):
+        """|g - r| <= 2^-16 |r| + ulp(r): FP32 reduction and scaling, one cast."""
+        tol = 2.0 ** -16 * np.abs(r) + _ulp(r, self.w.dtype)
+        return int((~(np.abs(g - r) <= tol) & ~(np.isnan(g) & np.isnan(r))).sum())
+
+    gate = "FP32 RMS error bound plus 1 ulp of the dtype"
+
+
+LANES = {"backward": BackwardLane, "rmsnorm": RmsNormLane}
+
+
+def pair_cpu_sample(lane):
+    """Leading rows of the workload, about 8 MB of algorithmic traffic."""
+    w = lane.w
     per_row = 3 * w.N * w.elem_bytes
-    rows = np.arange(min(w.M, max(1, (8 << 20) // per_row)))  # about 8 MB per pass
+    return np.arange(min(w.M, max(1, (8 << 20) // per_row))), per_row
+
+
+def pair_cpu_baseline(lane, budget_s: float):
+    """The oracle as it stands (one thread) on leading rows, repeated for about budget_s."""
+    rows, per_row = pair_cpu_sample(lane)
     times = []
     t_start = time.perf_counter()
     while True:
         t0 = time.perf_counter()
-        oracle_backward_rows(w, y, dy, rows)
+        lane.oracle_rows(rows)
         times.append(time.perf_counter() - t0)
         if time.perf_counter() - t_start >= budget_s:
             break
     gbs = per_row * rows.size * len(times) / sum(times) / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "first %d of %d rows of %s, %d pass(es) of the FP64 C oracle's backward, "
-                      "1 thread" % (rows.size, w.M, w.name, len(times))}
+            "sample": "first %d of %d rows of %s, %d pass(es) of the FP64 C oracle's %s, 1 thread"
+                      % (rows.size, lane.w.M, lane.w.name, len(times), lane.label)}
 
 
-def bench_backward(args, w):
-    """dx = y * (dy - sum(y * dy)) per row: one softmax_rows_backward_ex call per step."""
+def bench_pair(args, lane):
+    """One row-pair call per step (softmax_rows_backward_ex or rmsnorm_residual_rows_ex)."""
     import torch
 
     import memory_bound_row_rows_gb300 as sr
     from memory_bound_row_rows_gb300 import _build
+    w = lane.w
     rank, local_rank, world = dist_env()
     if world > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group("nccl")
@@ -521,22 +607,20 @@ def bench_backward(args, w):
         t = torch.from_numpy(np.ascontiguousarray(a))
         return t if w.dtype == synth.F32 else t.view(torch.int16).view(tdt)
 
-    y, dy = w.y_rows(0, w.M), w.dy_rows(0, w.M)
-    y_dev, dy_dev = host_tensor(y).to(dev), host_tensor(dy).to(dev)
-    dx_dev = torch.empty((w.M, w.N), dtype=tdt, device=dev)
+    dev_mats = [host_tensor(m).to(dev) for m in lane.mats]
+    dev_vecs = [host_tensor(v).to(dev) for v in lane.vecs]
+    out = torch.empty((w.M, w.N), dtype=tdt, device=dev)
     flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    plan = sr.softmax_rows_backward_plan(y_dev, dy_dev, dx_dev, w.M, w.N, w.ld, w.ld, w.N,
-                                         w.dtype, args.plan, 0)
+    plan = lane.plan(sr, dev_mats, dev_vecs, out, args.plan)
     if plan < 0:
-        raise RuntimeError("backward plan %d cannot take %s" % (args.plan, w.name))
+        raise RuntimeError("plan %d cannot take %s %s" % (args.plan, lane.api, w.name))
 
     def step():
-        st = lib.softmax_rows_backward_ex(y_dev.data_ptr(), dy_dev.data_ptr(), dx_dev.data_ptr(),
-                                          w.M, w.N, w.ld, w.ld, w.N, w.dtype, args.plan, sh)
+        st = lane.call(lib, dev_mats, dev_vecs, out, args.plan, sh)
         if st != 0:
-            raise RuntimeError("softmax_rows_backward failed: %s" % sr.softmax_rows_strerror(st))
+            raise RuntimeError("%s failed: %s" % (lane.api, sr.softmax_rows_strerror(st)))
 
     def flush_l2():
         if args.lane == "cold":
@@ -547,15 +631,16 @@ def bench_backward(args, w):
 
     e2e = None
     if not args.no_e2e:
-        # Host buffers: pinned y and dy copied in, the call, dx copied back, each step.
-        y_pin, dy_pin = host_tensor(y).pin_memory(), host_tensor(dy).pin_memory()
-        dx_pin = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
+        # Host buffers: the pinned inputs copied in, the call, the output copied back.
+        pins = [host_tensor(m).pin_memory() for m in lane.mats + lane.vecs]
+        out_pin = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
+        targets = dev_mats + dev_vecs
 
         def e2e_step():
-            y_dev.copy_(y_pin, non_blocking=True)
-            dy_dev.copy_(dy_pin, non_blocking=True)
+            for d, h in zip(targets, pins):
+                d.copy_(h, non_blocking=True)
             step()
-            dx_pin.copy_(dx_dev, non_blocking=True)
+            out_pin.copy_(out, non_blocking=True)
 
         for _ in range(3):
             e2e_step()
@@ -569,28 +654,27 @@ def bench_backward(args, w):
         torch.cuda.synchronize()
         sec = t0.elapsed_time(t1) / 1e3 / k
         e2e = {"value": round(w.fused_bytes / sec / 1e9, 2), "unit": "GB/s",
-               "h2d_bytes_per_step": 2 * w.M * w.N * w.elem_bytes,
+               "h2d_bytes_per_step": sum(p.numel() * p.element_size() for p in pins),
                "d2h_bytes_per_step": w.M * w.N * w.elem_bytes,
                "ms_per_step": round(sec * 1e3, 4), "steps": k,
-               "path": "pinned host y, dy -> device (copies), softmax_rows_backward_ex, "
-                       "dx -> pinned host, in order on one stream"}
+               "path": "pinned host inputs -> device (copies), %s call, output -> pinned host, "
+                       "in order on one stream" % lane.api}
     if rank != 0:
         return None
     steps = len(ms)
     value = replica_throughput(w.fused_bytes, steps, world, total_s)
     achieved = w.fused_bytes / (sum(ms) / 1e3 / steps) / 1e9
     peaks = measured_peaks()
-    pname = "backward-" + sr.PLAN_NAMES[plan]
-    traffic, rec = recorded_traffic("backward:" + w.name, "backward")
+    pname = "%s-%s" % (lane.api, sr.PLAN_NAMES[plan])
+    traffic, rec = recorded_traffic("%s:%s" % (lane.api, w.name), lane.api)
+    lanename = "cold-L2" if args.lane == "cold" else "warm-L2"
     line = {
-        "metric": "cold-L2 softmax backward GB/s (3*M*N*bytes/time)" if args.lane == "cold"
-        else "warm-L2 softmax backward GB/s (3*M*N*bytes/time)",
+        "metric": "%s %s GB/s (%s/time)" % (lanename, lane.label, lane.model),
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
         "warmup": args.warmup, "ms_per_step": round(total_s / steps * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": synth.DTYPE_NAMES[w.dtype],
-        "data": "synthetic: y ~ U[0, 2/N), dy ~ N(0, 1), seeded SplitMix64 (seed %d)" % w.seed,
-        "config": {"workload": "backward " + w.name, "M": w.M, "N": w.N, "ld": w.ld,
+        "dtype": synth.DTYPE_NAMES[w.dtype], "data": lane.data,
+        "config": {"workload": "%s %s" % (lane.api, w.name), "M": w.M, "N": w.N, "ld": w.ld,
                    "plan": pname, "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": ("flushed: a 512 MiB device buffer is read before every step, outside "
                           "the event pair") if args.lane == "cold" else "warm (no flush)",
@@ -609,22 +693,21 @@ def bench_backward(args, w):
                      "traffic": traffic,
                      "traffic_note": (rec or {}).get("note") if traffic else
                      "null: no ncu capture recorded for this build of the kernels"},
-        "source_hash": _build.source_hash(_build.PLAN_SOURCES["backward"]),
+        "source_hash": _build.source_hash(_build.PLAN_SOURCES[lane.api]),
     }
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1:
-        line["cpu_baseline"] = backward_cpu_baseline(w, y, dy, args.cpu_budget)
+        line["cpu_baseline"] = pair_cpu_baseline(lane, args.cpu_budget)
         rows = np.unique(np.concatenate([np.linspace(0, w.M - 1, 64).astype(np.int64),
                                          [w.M - 1]]))
-        g = dx_dev[torch.from_numpy(rows).to(dev)].cpu()
+        g = out[torch.from_numpy(rows).to(dev)].cpu()
         g = g.numpy() if w.dtype == synth.F32 else g.view(torch.int16).numpy().view(np.uint16)
-        r = oracle_backward_rows(w, y, dy, rows)
+        r = lane.oracle_rows(rows)
         dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :w.N]), w.dtype)
         line["parity"] = {"rows": int(rows.size), "of_rows": w.M,
-                          "outside_tolerance": backward_outside_gate(
-                              dec(g), dec(r), dec(y[rows]), dec(dy[rows]), w.dtype),
-                          "gate": "FP32 dot-product error bound plus 2 ulp of the dtype"}
+                          "outside_tolerance": lane.outside_gate(dec(g), dec(r), rows),
+                          "gate": lane.gate}
     return line
 
 
@@ -661,33 +744,31 @@ def bench_reference(args, w):
     }
 
 
-def bench_reference_backward(args, w):
-    """The CPU oracle's backward as the reference arm, each step a bounded sample."""
+def bench_reference_pair(args, lane):
+    """The CPU oracle as the reference arm of a row-pair lane, each step a bounded sample."""
     rank, _, world = dist_env()
     if rank != 0:
         return None
-    y, dy = w.y_rows(0, w.M), w.dy_rows(0, w.M)
-    per_row = 3 * w.N * w.elem_bytes
-    rows = np.arange(min(w.M, max(1, (8 << 20) // per_row)))
+    w = lane.w
+    rows, per_row = pair_cpu_sample(lane)
     for _ in range(max(0, args.warmup)):
-        oracle_backward_rows(w, y, dy, rows)
+        lane.oracle_rows(rows)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle_backward_rows(w, y, dy, rows)
+        lane.oracle_rows(rows)
         times.append(time.perf_counter() - t0)
     value = per_row * rows.size * len(times) / sum(times) / 1e9
-    sample = "first %d of %d rows of %s per step, FP64 C oracle's backward, 1 thread" % (
-        rows.size, w.M, w.name)
+    sample = "first %d of %d rows of %s per step, FP64 C oracle's %s, 1 thread" % (
+        rows.size, w.M, w.name, lane.label)
     return {
         "impl": "reference",
-        "metric": "cold-L2 softmax backward GB/s (3*M*N*bytes/time)",
+        "metric": "cold-L2 %s GB/s (%s/time)" % (lane.label, lane.model),
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
         "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": synth.DTYPE_NAMES[w.dtype],
-        "data": "synthetic: y ~ U[0, 2/N), dy ~ N(0, 1), seeded SplitMix64 (seed %d)" % w.seed,
-        "config": {"workload": "backward " + w.name, "M": w.M, "N": w.N, "ld": w.ld},
+        "dtype": synth.DTYPE_NAMES[w.dtype], "data": lane.data,
+        "config": {"workload": "%s %s" % (lane.api, w.name), "M": w.M, "N": w.N, "ld": w.ld},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -697,10 +778,11 @@ def bench_reference_backward(args, w):
 
 def main(argv=None):
     args = parse_args(argv)
-    if args.api == "backward":
-        catalog = synth.BACKWARD
-        names = (list(synth.BACKWARD) if args.workload == "all" else
-                 [args.workload or synth.BACKWARD_HEADLINE])
+    if args.api in LANES:
+        lane_cls = LANES[args.api]
+        catalog = lane_cls.catalog
+        names = (list(catalog) if args.workload == "all" else
+                 [args.workload or lane_cls.headline])
     else:
         catalog = dict(synth.WORKLOADS, **synth.WIDE_FEW)
         wl = args.workload or synth.HEADLINE
@@ -710,12 +792,12 @@ def main(argv=None):
         w = catalog[name]
         if args.rows:
             w = w.with_rows(min(args.rows, w.M))
-        if args.impl == "reference" and args.api == "backward":
-            line = bench_reference_backward(args, w)
+        if args.impl == "reference" and args.api in LANES:
+            line = bench_reference_pair(args, LANES[args.api](w))
         elif args.impl == "reference":
             line = bench_reference(args, w)
-        elif args.api == "backward":
-            line = bench_backward(args, w)
+        elif args.api in LANES:
+            line = bench_pair(args, LANES[args.api](w))
         else:
             line = bench_ours(args, w)
         if line is not None:

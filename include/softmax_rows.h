@@ -303,6 +303,37 @@ SR_API int softmax_rows_backward_plan(const void* y, const void* dy, const void*
                                       int64_t N, int64_t ld_y, int64_t ld_dy, int64_t ld_dx,
                                       int dtype, int plan, int sm_count);
 
+/*
+ * Residual RMSNorm forward, the second row reduction on the same plans (the
+ * "Warpline" README's K1 kernel; "Measured optimization case studies",
+ * Residual RMSNorm: the input and the residual are added in FP32 and the sum
+ * rounded once to the input dtype, the RMS is reduced in FP32, the weight
+ * applied and the result rounded once). For every row i,
+ *     h[j]   = dtype(x[i,j] + residual[i,j])
+ *     y[i,j] = dtype(h[j] * weight[j] / sqrt(mean_j h[j]^2 + eps))
+ * The sum h is not written anywhere. x, residual and y are DEVICE M x N
+ * row-major matrices with pitches ld_x, ld_r, ld_y (elements, >= N); weight
+ * is a DEVICE vector of N elements; all in the one dtype, caller-owned. y
+ * must not overlap x or residual (y equal to either is rejected). eps must be
+ * finite and >= 0 (eps = 0 and a zero row give NaN, 0/0). Pad columns of y
+ * are not written. Plans and limits as softmax_rows_backward_ex. Returns
+ * SR_OK, SR_EDTYPE, SR_EINVAL, SR_EPLAN or SR_ECUDA.
+ */
+SR_API int rmsnorm_residual_rows(const void* x, const void* residual, const void* weight, void* y,
+                                 int64_t M, int64_t N, int64_t ld_x, int64_t ld_r, int64_t ld_y,
+                                 float eps, int dtype, sr_stream_t stream);
+
+SR_API int rmsnorm_residual_rows_ex(const void* x, const void* residual, const void* weight,
+                                    void* y, int64_t M, int64_t N, int64_t ld_x, int64_t ld_r,
+                                    int64_t ld_y, float eps, int dtype, int plan,
+                                    sr_stream_t stream);
+
+/* Host-only plan query for rmsnorm_residual_rows_ex, as softmax_rows_backward_plan. */
+SR_API int rmsnorm_residual_rows_plan(const void* x, const void* residual, const void* weight,
+                                      const void* y, int64_t M, int64_t N, int64_t ld_x,
+                                      int64_t ld_r, int64_t ld_y, float eps, int dtype, int plan,
+                                      int sm_count);
+
 SR_API const char* softmax_rows_strerror(int status);
 
 /* Library version as major*10000 + minor*100 + patch. */

@@ -21,8 +21,9 @@ __all__ = [
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
     "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
-    "softmax_rows_backward_plan",
-    "softmax", "softmax_backward",
+    "softmax_rows_backward_plan", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
+    "rmsnorm_residual_rows_plan",
+    "softmax", "softmax_backward", "rmsnorm_residual",
     "dtype_code",
 ]
 
@@ -61,6 +62,7 @@ def load():
             "`python -c 'import __graft_entry__ as g; g.build()'`" % path)
     lib = ctypes.CDLL(path)
     vp, i64, c_int, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_uint64
+    f32 = ctypes.c_float
     sig = {
         "softmax_rows": [vp, vp, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_ex": [vp, vp, i64, i64, i64, i64, c_int, c_int, vp],
@@ -78,6 +80,11 @@ def load():
         "softmax_rows_backward": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_backward_ex": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, vp],
         "softmax_rows_backward_plan": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, c_int],
+        "rmsnorm_residual_rows": [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, c_int, vp],
+        "rmsnorm_residual_rows_ex": [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, c_int, c_int,
+                                     vp],
+        "rmsnorm_residual_rows_plan": [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, c_int, c_int,
+                                       c_int],
         "softmax_rows_version": [],
     }
     for name, args in sig.items():
@@ -186,6 +193,29 @@ def softmax_rows_backward_plan(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan=
                                                  ld_dx, dtype, plan, sm_count))
 
 
+def rmsnorm_residual_rows(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype,
+                          stream=None) -> int:
+    """y = dtype(h * w / sqrt(mean(h^2) + eps)), h = dtype(x + residual); device pointers."""
+    return _check(load().rmsnorm_residual_rows(_ptr(x), _ptr(residual), _ptr(weight), _ptr(y), M,
+                                               N, ld_x, ld_r, ld_y, eps, dtype, _stream(stream)),
+                  "rmsnorm_residual_rows")
+
+
+def rmsnorm_residual_rows_ex(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype, plan,
+                             stream=None) -> int:
+    return _check(load().rmsnorm_residual_rows_ex(_ptr(x), _ptr(residual), _ptr(weight), _ptr(y),
+                                                  M, N, ld_x, ld_r, ld_y, eps, dtype, plan,
+                                                  _stream(stream)),
+                  "rmsnorm_residual_rows_ex")
+
+
+def rmsnorm_residual_rows_plan(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype,
+                               plan=SR_PLAN_AUTO, sm_count=0) -> int:
+    return int(load().rmsnorm_residual_rows_plan(_ptr(x), _ptr(residual), _ptr(weight), _ptr(y),
+                                                 M, N, ld_x, ld_r, ld_y, eps, dtype, plan,
+                                                 sm_count))
+
+
 def softmax_rows_split(in_, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,
                        stream=None) -> int:
     """Split plan for few, wide rows; `workspace` is a device buffer."""
@@ -270,3 +300,26 @@ def softmax_backward(y, dy, dx=None, plan: int = SR_PLAN_AUTO, stream=None):
     softmax_rows_backward_ex(y, dy, dx, M, N, ld(y), ld(dy), ld(dx), dtype_code(y.dtype), plan,
                              stream)
     return dx
+
+
+def rmsnorm_residual(x, residual, weight, eps: float = 1e-6, y=None, plan: int = SR_PLAN_AUTO,
+                     stream=None):
+    """Residual RMSNorm of 2-D CUDA tensors with unit column stride; weight is 1-D."""
+    import torch
+    for name, t in (("x", x), ("residual", residual)):
+        if t.dim() != 2 or t.stride(1) != 1 or not t.is_cuda:
+            raise ValueError("%s: expected a 2-D CUDA tensor with unit column stride" % name)
+    if residual.shape != x.shape or residual.dtype != x.dtype:
+        raise ValueError("x and residual must have the same shape and dtype")
+    M, N = x.shape
+    if weight.dim() != 1 or weight.shape[0] != N or weight.dtype != x.dtype or \
+            not weight.is_contiguous():
+        raise ValueError("weight must be a contiguous vector of N elements of x's dtype")
+    if y is None:
+        y = torch.empty((M, N), dtype=x.dtype, device=x.device)
+    if y.shape != x.shape or y.dtype != x.dtype or y.stride(1) != 1:
+        raise ValueError("y must match x in shape and dtype, with unit column stride")
+    ld = lambda t: t.stride(0) if M > 1 else N
+    rmsnorm_residual_rows_ex(x, residual, weight, y, M, N, ld(x), ld(residual), ld(y), eps,
+                             dtype_code(x.dtype), plan, stream)
+    return y

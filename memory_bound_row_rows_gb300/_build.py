@@ -21,7 +21,7 @@ HEADER = os.path.join(ROOT, "include", "softmax_rows.h")
 
 UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu", "smem_rows.cu",
          "block_rows.cu", "host_stream.cu",
-         "split_rows.cu", "backward_rows.cu"]
+         "split_rows.cu", "backward_rows.cu", "rmsnorm_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]
@@ -51,6 +51,7 @@ PLAN_SOURCES = {
     "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
     "split": ["split_rows.cu"],
     "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],
+    "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h"],
 }
 SHARED_SOURCES = ["device.cuh", "internal.h"]
 

@@ -262,9 +262,10 @@ template <class Launch>
 int run_pair(const rp::Args& a, int plan, Launch&& launch) {
     if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return SR_EPLAN;
     rp::Shape sh;
-    if (a.M == 0) {  // nothing to launch; the plan is still checked against the shape
-        return resolve_pair_plan(a, plan, 1, &sh) < 0 ? SR_EPLAN : SR_OK;
-    }
+    // Whether a plan fits does not depend on the device (only the cluster
+    // size does), so a plan that cannot run is refused before any CUDA call.
+    if (resolve_pair_plan(a, plan, 1, &sh) < 0) return SR_EPLAN;
+    if (a.M == 0) return SR_OK;
     cudaError_t e;
     const DeviceInfo* dev = device_info(&e);
     if (!dev) return SR_ECUDA;
@@ -281,6 +282,17 @@ int run_bwd(const void* y, const void* dy, void* dx, int64_t M, int64_t N, int64
     return run_pair(a, plan, [](const rp::Args& q, const rp::Shape& sh) {
         return launch_backward(q, sh);
     });
+}
+
+// Argument check of the residual RMSNorm: 0 or a positive sr_status.
+int check_rms_args(const void* x, const void* r, const void* w, const void* y, int64_t M,
+                   int64_t N, int64_t ld_x, int64_t ld_r, int64_t ld_y, float eps, int dtype) {
+    const int bad = check_bwd_args(x, r, y, M, N, ld_x, ld_r, ld_y, dtype);
+    if (bad) return bad;
+    if (!(eps >= 0.0f) || eps == INFINITY) return SR_EINVAL;
+    if (M > 0 && (w == nullptr || reinterpret_cast<uintptr_t>(w) % elem_bytes(dtype) != 0))
+        return SR_EINVAL;
+    return 0;
 }
 
 // The plan a row-pair call would run, or a negative status (host logic; the
@@ -449,6 +461,33 @@ int softmax_rows_backward_plan(const void* y, const void* dy, const void* dx, in
     const int bad = sr::check_bwd_args(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype);
     if (bad) return -bad;
     const sr::rp::Args a{y, dy, const_cast<void*>(dx), M, N, ld_y, ld_dy, ld_dx, dtype, nullptr};
+    return sr::pair_plan_query(a, plan, sm_count);
+}
+
+int rmsnorm_residual_rows_ex(const void* x, const void* residual, const void* weight, void* y,
+                             int64_t M, int64_t N, int64_t ld_x, int64_t ld_r, int64_t ld_y,
+                             float eps, int dtype, int plan, sr_stream_t stream) {
+    const int bad = sr::check_rms_args(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype);
+    if (bad) return bad;
+    const sr::rp::Args a{x, residual, y, M, N, ld_x, ld_r, ld_y, dtype, (cudaStream_t)stream};
+    return sr::run_pair(a, plan, [weight, eps](const sr::rp::Args& q, const sr::rp::Shape& sh) {
+        return sr::launch_rmsnorm(q, sh, weight, eps);
+    });
+}
+
+int rmsnorm_residual_rows(const void* x, const void* residual, const void* weight, void* y,
+                          int64_t M, int64_t N, int64_t ld_x, int64_t ld_r, int64_t ld_y,
+                          float eps, int dtype, sr_stream_t stream) {
+    return rmsnorm_residual_rows_ex(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype,
+                                    SR_PLAN_AUTO, stream);
+}
+
+int rmsnorm_residual_rows_plan(const void* x, const void* residual, const void* weight,
+                               const void* y, int64_t M, int64_t N, int64_t ld_x, int64_t ld_r,
+                               int64_t ld_y, float eps, int dtype, int plan, int sm_count) {
+    const int bad = sr::check_rms_args(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype);
+    if (bad) return -bad;
+    const sr::rp::Args a{x, residual, const_cast<void*>(y), M, N, ld_x, ld_r, ld_y, dtype, nullptr};
     return sr::pair_plan_query(a, plan, sm_count);
 }
 

@@ -19,8 +19,12 @@ struct BackwardOp {
     }
     __device__ __forceinline__ float finish(float dot, int64_t) const { return dot; }
     template <int n>
-    __device__ __forceinline__ void apply(const float* y, const float* dy, float dot, int64_t,
-                                          float* dx) const {
+    struct Aux {};  // no per-column data
+    template <int n>
+    __device__ __forceinline__ Aux<n> load_aux(int64_t) const { return {}; }
+    template <int n>
+    __device__ __forceinline__ void apply(const float* y, const float* dy, float dot,
+                                          const Aux<n>&, float* dx) const {
 #pragma unroll
         for (int e = 0; e < n; ++e) dx[e] = y[e] * (dy[e] - dot);
     }

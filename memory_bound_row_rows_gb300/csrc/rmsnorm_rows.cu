@@ -1,0 +1,101 @@
+// Residual RMSNorm forward: y = dtype(h * w / sqrt(mean(h^2) + eps)) with
+// h = dtype(x + residual), row by row.
+//
+// The "Warpline" README's K1 kernel (one program per row adds the input and
+// the residual in FP32, rounds that sum once to the input dtype, reduces the
+// RMS in FP32, applies the weight and writes one rounded result) and the
+// residual RMSNorm of "Measured optimization case studies": fusing the
+// residual addition, the reduction and the scaling means the sum h is never
+// written to memory. This is the row-pair engine's shape (rowpair.cuh) with
+// A = x, B = residual, C = y: per row one reduction (the sum of h^2, one FMA
+// per element) and one elementwise pass, h recomputed from the registers.
+// Algorithmic traffic: x and the residual read once, y written once, plus
+// the N weights (read once from DRAM, then from cache).
+#include "rowpair.cuh"
+
+namespace sr {
+namespace {
+
+template <typename T>
+__device__ __forceinline__ float round_to(float v);
+template <>
+__device__ __forceinline__ float round_to<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ float round_to<__nv_bfloat16>(float v) {
+    return __bfloat162float(__float2bfloat16_rn(v));
+}
+template <>
+__device__ __forceinline__ float round_to<__half>(float v) {
+    return __half2float(__float2half_rn(v));
+}
+
+// The weights of a unit travel as the unit does: n weights in storage format
+// (one 16-byte vector for a vector unit, one element otherwise). WVEC: a
+// vector unit's weights are one aligned 16-byte vector (rows in the aligned
+// mode with an aligned weight vector); otherwise they are gathered one by
+// one. They are read through the cache: every row uses the same N weights.
+template <typename T, bool WVEC>
+struct RmsNormOp {
+    const T* w;
+    float eps;
+    template <int n>
+    struct Aux {
+        uint4 raw;  // n == kVec: n weights packed as stored
+    };
+    template <int n>
+    __device__ __forceinline__ Aux<n> load_aux(int64_t col) const {
+        Aux<n> a;
+        if constexpr (n == 1) {
+            a.raw.x = __float_as_uint(Elem<T>::load1(w + col));
+        } else if constexpr (WVEC) {
+            a.raw = __ldg(reinterpret_cast<const uint4*>(w + col));
+        } else {
+            float f[n];
+#pragma unroll
+            for (int e = 0; e < n; ++e) f[e] = Elem<T>::load1(w + col + e);
+            a.raw = Elem<T>::pack(f);  // exact: each f[e] is a T value
+        }
+        return a;
+    }
+    __device__ __forceinline__ void accumulate(float& acc, float x, float r) const {
+        const float h = round_to<T>(x + r);
+        acc = fmaf(h, h, acc);
+    }
+    __device__ __forceinline__ float finish(float sumsq, int64_t N) const {
+        return 1.0f / sqrtf(sumsq / (float)N + eps);
+    }
+    template <int n>
+    __device__ __forceinline__ void apply(const float* x, const float* r, float rstd,
+                                          const Aux<n>& aux, float* y) const {
+        float wv[n];
+        if constexpr (n == 1) {
+            wv[0] = __uint_as_float(aux.raw.x);
+        } else {
+            Elem<T>::unpack(aux.raw, wv);
+        }
+#pragma unroll
+        for (int e = 0; e < n; ++e) y[e] = (round_to<T>(x[e] + r[e]) * rstd) * wv[e];
+    }
+};
+
+template <typename T>
+cudaError_t launch_typed(const rp::Args& p, const rp::Shape& sh, const void* weight, float eps) {
+    const T* w = static_cast<const T*>(weight);
+    if (sh.mode == (int)rp::Mode::kAligned && reinterpret_cast<uintptr_t>(weight) % 16 == 0)
+        return rp::launch_mode<RmsNormOp<T, true>, T, rp::Mode::kAligned>(
+            RmsNormOp<T, true>{w, eps}, p, sh);
+    return rp::launch<T>(RmsNormOp<T, false>{w, eps}, p, sh);
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm(const rp::Args& p, const rp::Shape& sh, const void* weight, float eps) {
+    switch (p.dtype) {
+        case kF32: return launch_typed<float>(p, sh, weight, eps);
+        case kBF16: return launch_typed<__nv_bfloat16>(p, sh, weight, eps);
+        case kF16: return launch_typed<__half>(p, sh, weight, eps);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace sr

@@ -9,9 +9,13 @@
 //     __device__ void accumulate(float& acc, float a, float b) const;
 //     // the row's number from the FP32 sum of all contributions
 //     __device__ float finish(float total, int64_t N) const;
-//     // out[e] = the result at columns col .. col + n - 1 (n = 1 or VEC)
+//     // per-column data of n columns (the RMSNorm weights; empty otherwise),
+//     // loaded together with the row so that no load waits on the reduction
+//     template <int n> struct Aux;
+//     template <int n> __device__ Aux<n> load_aux(int64_t col) const;
+//     // out[e] = the result at the n columns the unit covers
 //     template <int n> __device__ void apply(const float* a, const float* b, float s,
-//                                            int64_t col, float* out) const;
+//                                            const Aux<n>& aux, float* out) const;
 //   };
 //
 // Three plans, each reading A and B once (ONLINE: twice) and writing C once:
@@ -31,7 +35,8 @@
 // (the same base offset and pitch modulo 16 bytes), so each row is a head of
 // fewer than VEC elements, 16-byte vectors, and a tail of fewer than VEC
 // elements; the head and tail elements go one per thread. Mode::kScalar
-// loads single elements.
+// loads single elements. A thread's columns are the same in every row in the
+// aligned mode, so its per-column data is loaded once, before the first row.
 #pragma once
 
 #include "device.cuh"
@@ -41,9 +46,7 @@
 namespace sr {
 namespace rp {
 
-// Units per thread a plan aims for, and the most it holds. Eight 16-byte
-// vectors of 16-bit data per matrix widen to 128 floats, more than a thread
-// keeps without spilling, so 16-bit vectors stop at four.
+// Units per thread a plan aims for, and the most it holds.
 template <typename T, Mode MODE>
 struct KvTarget {
     static constexpr bool kWide = MODE != Mode::kScalar;
@@ -62,6 +65,16 @@ struct Unit<T, true> {
     __device__ __forceinline__ void zero() { raw = make_uint4(0u, 0u, 0u, 0u); }
     __device__ __forceinline__ void load(const T* p) { raw = ldg_stream(p); }
     __device__ __forceinline__ void get(float* f) const { Elem<T>::unpack(raw, f); }
+    // The same values, widened again from the stored vector. For 16-bit data
+    // the empty asm hides that they equal an earlier get(), so the compiler
+    // keeps the packed vector (4 registers) across the row's reduction
+    // instead of the widened floats (8), which lets more blocks share an SM.
+    __device__ __forceinline__ void get_again(float* f) const {
+        uint4 r = raw;
+        if constexpr (sizeof(T) == 2)
+            asm volatile("" : "+r"(r.x), "+r"(r.y), "+r"(r.z), "+r"(r.w));
+        Elem<T>::unpack(r, f);
+    }
     __device__ __forceinline__ static void put(T* p, const float* f) {
         stg_stream(p, Elem<T>::pack(f));
     }
@@ -74,6 +87,7 @@ struct Unit<T, false> {
     __device__ __forceinline__ void zero() { v = 0.0f; }
     __device__ __forceinline__ void load(const T* p) { v = Elem<T>::load1(p); }
     __device__ __forceinline__ void get(float* f) const { f[0] = v; }
+    __device__ __forceinline__ void get_again(float* f) const { f[0] = v; }
     __device__ __forceinline__ static void put(T* p, const float* f) { Elem<T>::store1(p, f[0]); }
 };
 
@@ -141,12 +155,14 @@ __device__ __forceinline__ void accumulate_unit(const Op& op, const Unit<T, WIDE
 
 template <class Op, typename T, bool WIDE>
 __device__ __forceinline__ void write_unit(const Op& op, const Unit<T, WIDE>& a,
-                                           const Unit<T, WIDE>& b, float s, int64_t col, T* p) {
+                                           const Unit<T, WIDE>& b, float s,
+                                           const typename Op::template Aux<Unit<T, WIDE>::kN>& aux,
+                                           T* p) {
     constexpr int VEC = Unit<T, WIDE>::kN;
     float fa[VEC], fb[VEC], f[VEC];
-    a.get(fa);
-    b.get(fb);
-    op.template apply<VEC>(fa, fb, s, col, f);
+    a.get_again(fa);
+    b.get_again(fb);
+    op.template apply<VEC>(fa, fb, s, aux, f);
     Unit<T, WIDE>::put(p, f);
 }
 
@@ -155,10 +171,12 @@ template <class Op, typename T>
 struct Extra {
     float a = 0.0f, b = 0.0f;
     int64_t col = -1;
-    __device__ __forceinline__ void load(const T* ra, const T* rb, int64_t c) {
+    typename Op::template Aux<1> aux;
+    __device__ __forceinline__ void load(const Op& op, const T* ra, const T* rb, int64_t c) {
         col = c;
         a = Elem<T>::load1(ra + c);
         b = Elem<T>::load1(rb + c);
+        aux = op.template load_aux<1>(c);
     }
     __device__ __forceinline__ void accumulate(const Op& op, float* acc) const {
         if (col >= 0) op.accumulate(acc[0], a, b);
@@ -166,7 +184,7 @@ struct Extra {
     __device__ __forceinline__ void write(const Op& op, float s, T* rc) const {
         if (col >= 0) {
             float f;
-            op.template apply<1>(&a, &b, s, col, &f);
+            op.template apply<1>(&a, &b, s, aux, &f);
             Elem<T>::store1(rc + col, f);
         }
     }
@@ -183,12 +201,22 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;
     constexpr int VEC = U::kN;
+    using AuxV = typename Op::template Aux<VEC>;
     constexpr int NT = TPR < 128 ? 128 : TPR;
     constexpr int RPB = NT / TPR;  // rows per block
     constexpr int NW = TPR / 32;   // warps per team
     __shared__ float red[2][NT / 32];
     const int tid = threadIdx.x, t = tid % TPR;
     const int w0 = (tid / TPR) * NW;
+    AuxV aux[KV];
+    if constexpr (MODE == Mode::kAligned) {  // the same columns in every row
+        const L lay(A, N);
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int64_t idx = t + TPR * k;
+            if (idx < lay.nv) aux[k] = op.template load_aux<VEC>(lay.unit_col(idx));
+        }
+    }
     int parity = 0;
     for (int64_t r0 = (int64_t)blockIdx.x * RPB; r0 < M; r0 += (int64_t)gridDim.x * RPB) {
         const int64_t r = r0 + tid / TPR;
@@ -203,6 +231,8 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
             if (idx < lay.nv) {
                 a[k].load(ra + lay.unit_col(idx));
                 b[k].load(rb + lay.unit_col(idx));
+                if constexpr (MODE != Mode::kAligned)
+                    aux[k] = op.template load_aux<VEC>(lay.unit_col(idx));
             } else {
                 a[k].zero();
                 b[k].zero();
@@ -210,7 +240,7 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
         }
         Extra<Op, T> ex;
         if constexpr (MODE == Mode::kShifted)
-            if (t < lay.extra) ex.load(ra, rb, lay.extra_col(t));
+            if (t < lay.extra) ex.load(op, ra, rb, lay.extra_col(t));
         float acc[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
@@ -224,7 +254,7 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
         for (int k = 0; k < KV; ++k) {
             const int64_t idx = t + TPR * k;
             if (idx < lay.nv)
-                write_unit<Op, T, WIDE>(op, a[k], b[k], s, lay.unit_col(idx), rc + lay.unit_col(idx));
+                write_unit<Op, T, WIDE>(op, a[k], b[k], s, aux[k], rc + lay.unit_col(idx));
         }
         if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
     }
@@ -255,6 +285,7 @@ __global__ void __launch_bounds__(kClusterThreads)
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;
     constexpr int VEC = U::kN;
+    using AuxV = typename Op::template Aux<VEC>;
     constexpr int NT = kClusterThreads;
     constexpr int NW = NT / 32;
     __shared__ float red[2][NW];
@@ -262,6 +293,17 @@ __global__ void __launch_bounds__(kClusterThreads)
     const int tid = threadIdx.x;
     const int rank = (int)cluster_ctarank();
     const int64_t nclusters = gridDim.x / csize;
+    const int64_t u0 = (int64_t)rank * slice;
+    AuxV aux[KV];
+    if constexpr (MODE == Mode::kAligned) {
+        const L lay(A, N);
+        const int64_t u1 = (u0 + slice < lay.nv) ? u0 + slice : lay.nv;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int64_t idx = u0 + tid + NT * k;
+            if (idx < u1) aux[k] = op.template load_aux<VEC>(lay.unit_col(idx));
+        }
+    }
     // A block may store into a peer's shared memory only once the peer is
     // running; the first row's loads overlap this start-up barrier.
     cluster_arrive_relaxed();
@@ -271,7 +313,6 @@ __global__ void __launch_bounds__(kClusterThreads)
         const T* ra = A + r * lda;
         const T* rb = B + r * ldb;
         const L lay(ra, N);
-        const int64_t u0 = (int64_t)rank * slice;
         const int64_t u1 = (u0 + slice < lay.nv) ? u0 + slice : lay.nv;
         U a[KV], b[KV];
 #pragma unroll
@@ -280,6 +321,8 @@ __global__ void __launch_bounds__(kClusterThreads)
             if (idx < u1) {
                 a[k].load(ra + lay.unit_col(idx));
                 b[k].load(rb + lay.unit_col(idx));
+                if constexpr (MODE != Mode::kAligned)
+                    aux[k] = op.template load_aux<VEC>(lay.unit_col(idx));
             } else {
                 a[k].zero();
                 b[k].zero();
@@ -287,7 +330,7 @@ __global__ void __launch_bounds__(kClusterThreads)
         }
         Extra<Op, T> ex;
         if constexpr (MODE == Mode::kShifted)
-            if (rank == 0 && tid < lay.extra) ex.load(ra, rb, lay.extra_col(tid));
+            if (rank == 0 && tid < lay.extra) ex.load(op, ra, rb, lay.extra_col(tid));
         float acc[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
@@ -312,8 +355,7 @@ __global__ void __launch_bounds__(kClusterThreads)
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int64_t idx = u0 + tid + NT * k;
-            if (idx < u1)
-                write_unit<Op, T, WIDE>(op, a[k], b[k], s, lay.unit_col(idx), rc + lay.unit_col(idx));
+            if (idx < u1) write_unit<Op, T, WIDE>(op, a[k], b[k], s, aux[k], rc + lay.unit_col(idx));
         }
         if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
     }
@@ -331,6 +373,7 @@ __global__ void __launch_bounds__(kLoopThreads)
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;
     constexpr int VEC = U::kN;
+    using AuxV = typename Op::template Aux<VEC>;
     constexpr int NT = kLoopThreads;
     constexpr int NW = NT / 32;
     constexpr int UR = kLoopUnroll;
@@ -362,26 +405,28 @@ __global__ void __launch_bounds__(kLoopThreads)
         }
         Extra<Op, T> ex;
         if constexpr (MODE == Mode::kShifted)
-            if (tid < lay.extra) ex.load(ra, rb, lay.extra_col(tid));
+            if (tid < lay.extra) ex.load(op, ra, rb, lay.extra_col(tid));
         if constexpr (MODE == Mode::kShifted) ex.accumulate(op, acc);
         const float s = op.finish(team_sum<NW>(fold<VEC>(acc), red[parity], 0), N);
         parity ^= 1;
         T* rc = C + r * ldc;
         for (int64_t base = 0; base < lay.nv; base += (int64_t)NT * UR) {
             U a[UR], b[UR];
+            AuxV aux[UR];
 #pragma unroll
             for (int j = 0; j < UR; ++j) {
                 const int64_t idx = base + tid + NT * j;
                 if (idx < lay.nv) {
                     a[j].load(ra + lay.unit_col(idx));
                     b[j].load(rb + lay.unit_col(idx));
+                    aux[j] = op.template load_aux<VEC>(lay.unit_col(idx));
                 }
             }
 #pragma unroll
             for (int j = 0; j < UR; ++j) {
                 const int64_t idx = base + tid + NT * j;
                 if (idx < lay.nv)
-                    write_unit<Op, T, WIDE>(op, a[j], b[j], s, lay.unit_col(idx), rc + lay.unit_col(idx));
+                    write_unit<Op, T, WIDE>(op, a[j], b[j], s, aux[j], rc + lay.unit_col(idx));
             }
         }
         if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);

@@ -251,6 +251,75 @@ BACKWARD = {
 }
 BACKWARD_HEADLINE = "f16_16384x4096"
 
+@dataclass(frozen=True)
+class RmsNormWorkload:
+    """Inputs of the residual RMSNorm: x ~ N(0, 1), residual ~ N(0, 1) (M x N,
+    pitch ``ld``), weight ~ U[0.5, 1.5) (N), and eps."""
+    name: str
+    dtype: int
+    M: int
+    N: int
+    ld: int
+    seed: int
+    eps: float = 1e-6
+
+    @property
+    def elem_bytes(self) -> int:
+        return ELEM_BYTES[self.dtype]
+
+    @property
+    def fused_bytes(self) -> int:
+        """Algorithmic HBM bytes: x and the residual read once, y written once, weights once."""
+        return (3 * self.M * self.N + self.N) * self.elem_bytes
+
+    def with_rows(self, M: int) -> "RmsNormWorkload":
+        d = dict(self.__dict__)
+        d["M"] = M
+        return RmsNormWorkload(**d)
+
+    def _rows(self, which: int, row0: int, count: int, nthreads=None) -> np.ndarray:
+        count = max(0, min(count, self.M - row0))
+        buf = np.zeros((count, self.ld), dtype=NP_STORAGE[self.dtype])
+        if count:
+            generate_into(buf.reshape(-1), row0, count, self.N, self.ld, self.dtype,
+                          self.seed * 3 + which, nthreads=nthreads)
+        return buf
+
+    def x_rows(self, row0: int, count: int, nthreads=None) -> np.ndarray:
+        return self._rows(0, row0, count, nthreads)
+
+    def residual_rows(self, row0: int, count: int, nthreads=None) -> np.ndarray:
+        return self._rows(1, row0, count, nthreads)
+
+    def weight(self) -> np.ndarray:
+        buf = np.zeros(self.N, dtype=NP_STORAGE[self.dtype])
+        generate_into(buf, 0, 1, self.N, self.N, self.dtype, self.seed * 3 + 2,
+                      dist=DIST_UNIFORM, p0=0.5, p1=1.5)
+        return buf
+
+
+# Residual RMSNorm shapes: the FP16 shapes of "Measured optimization case
+# studies" (Residual RMSNorm) and the BF16 batch x hidden shapes of the
+# "Warpline" README (K1).
+RMSNORM = {
+    w.name: w
+    for w in [
+        RmsNormWorkload("f16_16384x4096", F16, 16384, 4096, 4096, 30),
+        RmsNormWorkload("f16_1024x1024", F16, 1024, 1024, 1024, 31),
+        RmsNormWorkload("f16_512x4097", F16, 512, 4097, 4097, 32),
+        RmsNormWorkload("f16_32x127", F16, 32, 127, 127, 33),
+        RmsNormWorkload("f16_4x32769", F16, 4, 32769, 32769, 34),
+        RmsNormWorkload("f16_64x131072", F16, 64, 131072, 131072, 35),
+        RmsNormWorkload("bf16_1x1024", BF16, 1, 1024, 1024, 36),
+        RmsNormWorkload("bf16_8x1024", BF16, 8, 1024, 1024, 37),
+        RmsNormWorkload("bf16_16x2048", BF16, 16, 2048, 2048, 38),
+        RmsNormWorkload("bf16_32x4096", BF16, 32, 4096, 4096, 39),
+        RmsNormWorkload("bf16_64x4096", BF16, 64, 4096, 4096, 40),
+        RmsNormWorkload("bf16_64x8192", BF16, 64, 8192, 8192, 41),
+    ]
+}
+RMSNORM_HEADLINE = "f16_16384x4096"
+
 # The workload the headline throughput is quoted on (square FP32 matrix, 4096 x 4096).
 HEADLINE = "f32_4096x4096"
 

@@ -218,3 +218,22 @@ def test_backward_plan_choice(lib):
     # Query errors.
     assert _bwd_plan(4, 8, 7) == -sr.SR_EDTYPE
     assert _bwd_plan(4, 8, F32, plan=sr.SR_PLAN_SMEM) == -sr.SR_EPLAN
+
+
+def test_rmsnorm_rejected_arguments_touch_no_device(lib):
+    L = lib
+    x, r, y, w = ALIGNED_IN, ALIGNED_DY, ALIGNED_OUT, 0x7F0300000000
+    ok = (x, r, w, y, 4, 8, 8, 8, 8)
+    assert L.rmsnorm_residual_rows(None, None, None, None, 0, 8, 8, 8, 8, 1e-6, 0, None) == sr.SR_OK
+    assert L.rmsnorm_residual_rows(*ok, 1e-6, 3, None) == sr.SR_EDTYPE
+    assert L.rmsnorm_residual_rows(x, r, None, y, 4, 8, 8, 8, 8, 1e-6, 0, None) == sr.SR_EINVAL
+    assert L.rmsnorm_residual_rows(x, r, w + 1, y, 4, 8, 8, 8, 8, 1e-6, 1, None) == sr.SR_EINVAL
+    assert L.rmsnorm_residual_rows(x, r, w, x, 4, 8, 8, 8, 8, 1e-6, 0, None) == sr.SR_EINVAL
+    assert L.rmsnorm_residual_rows(x, r, w, r, 4, 8, 8, 8, 8, 1e-6, 0, None) == sr.SR_EINVAL
+    assert L.rmsnorm_residual_rows(x, r, w, y, 4, 8, 7, 8, 8, 1e-6, 0, None) == sr.SR_EINVAL
+    for eps in (-1.0, float("nan"), float("inf")):
+        assert L.rmsnorm_residual_rows(*ok, eps, 0, None) == sr.SR_EINVAL
+    assert L.rmsnorm_residual_rows_ex(*ok, 1e-6, 0, sr.SR_PLAN_SMEM, None) == sr.SR_EPLAN
+    assert sr.rmsnorm_residual_rows_plan(*ok, 1e-6, 0, sr.SR_PLAN_AUTO, 152) == sr.SR_PLAN_ROW
+    assert sr.rmsnorm_residual_rows_plan(x, r, w, y, 64, 131072, 131072, 131072, 131072, 1e-6,
+                                         2, sr.SR_PLAN_AUTO, 152) == sr.SR_PLAN_CLUSTER

@@ -187,9 +187,10 @@ def test_offset_views(dtype):
     for all three the rows are read as vectors after a short head; with
     different k element by element."""
     M, N = 40, 4096
-    y = synth.generate(M, N + 8, dtype=dtype, seed=80, dist=synth.DIST_UNIFORM, p0=0.0,
+    # One spare row, so that a view starting k elements in still holds M full rows.
+    y = synth.generate(M + 1, N + 8, dtype=dtype, seed=80, dist=synth.DIST_UNIFORM, p0=0.0,
                        p1=2.0 / N)
-    dy = synth.generate(M, N + 8, dtype=dtype, seed=81)
+    dy = synth.generate(M + 1, N + 8, dtype=dtype, seed=81)
     tdt = gu.torch_dtype(dtype)
     yd, gd = gu.to_device(y, dtype).reshape(-1), gu.to_device(dy, dtype).reshape(-1)
     for ky, kg, kx in ((1, 1, 1), (3, 3, 3), (1, 2, 3), (0, 5, 0)):
