@@ -70,7 +70,7 @@ enum sr_status {
 
 /*
  * Kernel plans. AUTO picks by row width, dtype and alignment: ROW for
- * aligned rows of 4 KiB to 32 KiB, WARP for shorter rows, CLUSTER for aligned
+ * aligned rows of 4 KiB to 32 KiB, WARP for shorter rows, WIDE for aligned
  * rows up to 512 KiB, ONLINE otherwise. Every plan computes the same
  * function; forcing one (softmax_rows_ex) only changes the schedule:
  *   WARP    one warp per row, the row resident in registers; rows up to 2048 elements.
@@ -86,7 +86,13 @@ enum sr_status {
  *           no block barrier at all; aligned rows up to 32 KiB.
  *   ROW     one thread block per row loaded straight into registers, one
  *           block per row in the grid; aligned rows up to 2048 vectors.
- * All plans but ROW run a persistent grid sized to the device's SM count.
+ *   WIDE    one thread-block cluster per row, each block holding a slice
+ *           (staged in shared memory by a bulk asynchronous copy), warp
+ *           (max, sum) pairs merged across the cluster, the exponential
+ *           recomputed for the output; aligned rows up to 512 KiB. One HBM
+ *           read per element.
+ * All plans but ROW and WIDE run a persistent grid sized to the device's SM
+ * count.
  */
 enum sr_plan {
     SR_PLAN_AUTO = 0,
@@ -95,7 +101,8 @@ enum sr_plan {
     SR_PLAN_CLUSTER = 3,
     SR_PLAN_ONLINE = 4,
     SR_PLAN_SMEM = 5,
-    SR_PLAN_ROW = 6
+    SR_PLAN_ROW = 6,
+    SR_PLAN_WIDE = 7
 };
 
 /*
@@ -143,7 +150,7 @@ SR_API int softmax_rows_plan_check(const void* in, const void* out, int64_t M, i
 SR_API int softmax_rows_last_device_error(sr_stream_t stream);
 
 /*
- * Test hook for the bounded-wait path: runs `plan` (CTA, CLUSTER or SMEM) on the
+ * Test hook for the bounded-wait path: runs `plan` (CTA, CLUSTER, SMEM or WIDE) on the
  * given arguments with its bulk copies switched off, so every wait for a copy
  * expires after `timeout_ns` nanoseconds; the kernel then records
  * SR_EDEVICE_TIMEOUT and returns without writing `out`. Nothing hangs and

@@ -14,7 +14,7 @@ import os
 __all__ = [
     "SR_F32", "SR_BF16", "SR_F16", "SR_OK", "SR_EINVAL", "SR_EDTYPE", "SR_ECUDA",
     "SR_EDEVICE_TIMEOUT", "SR_EPLAN", "SR_PLAN_AUTO", "SR_PLAN_WARP", "SR_PLAN_CTA",
-    "SR_PLAN_CLUSTER", "SR_PLAN_ONLINE", "SR_PLAN_SMEM", "SR_PLAN_ROW",
+    "SR_PLAN_CLUSTER", "SR_PLAN_ONLINE", "SR_PLAN_SMEM", "SR_PLAN_ROW", "SR_PLAN_WIDE",
     "PLAN_NAMES", "SoftmaxRowsError", "load", "lib_path",
     "softmax_rows", "softmax_rows_ex", "softmax_rows_plan", "softmax_rows_plan_check",
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
@@ -30,10 +30,10 @@ __all__ = [
 SR_F32, SR_BF16, SR_F16 = 0, 1, 2
 SR_OK, SR_EINVAL, SR_EDTYPE, SR_ECUDA, SR_EDEVICE_TIMEOUT, SR_EPLAN = 0, 1, 2, 3, 4, 5
 SR_PLAN_AUTO, SR_PLAN_WARP, SR_PLAN_CTA, SR_PLAN_CLUSTER, SR_PLAN_ONLINE = 0, 1, 2, 3, 4
-SR_PLAN_SMEM, SR_PLAN_ROW = 5, 6
+SR_PLAN_SMEM, SR_PLAN_ROW, SR_PLAN_WIDE = 5, 6, 7
 PLAN_NAMES = {SR_PLAN_AUTO: "auto", SR_PLAN_WARP: "warp", SR_PLAN_CTA: "cta",
               SR_PLAN_CLUSTER: "cluster", SR_PLAN_ONLINE: "online", SR_PLAN_SMEM: "smem",
-              SR_PLAN_ROW: "row"}
+              SR_PLAN_ROW: "row", SR_PLAN_WIDE: "wide"}
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "lib", "libsoftmax_rows.so")

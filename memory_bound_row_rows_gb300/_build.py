@@ -21,7 +21,7 @@ HEADER = os.path.join(ROOT, "include", "softmax_rows.h")
 
 UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu", "smem_rows.cu",
          "block_rows.cu", "host_stream.cu",
-         "split_rows.cu", "backward_rows.cu", "rmsnorm_rows.cu"]
+         "split_rows.cu", "backward_rows.cu", "rmsnorm_rows.cu", "wide_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]
@@ -49,7 +49,7 @@ def _stamp(extra_flags) -> str:
 PLAN_SOURCES = {
     "row": ["block_rows.cu"], "warp": ["warp_rows.cu"], "cta": ["tma_rows.cu"],
     "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
-    "split": ["split_rows.cu"],
+    "split": ["split_rows.cu"], "wide": ["wide_rows.cu"],
     "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],
     "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h"],
 }

@@ -173,6 +173,10 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
         case SR_PLAN_ONLINE: return true;
         case SR_PLAN_SMEM: return vec && row_bytes <= kSmemMaxRowBytes;
         case SR_PLAN_ROW: return vec && row_plan_fits(N, dtype);
+        case SR_PLAN_WIDE: {
+            WideShape sh;
+            return vec && wide_shape(N, dtype, &sh);
+        }
     }
     return false;
 }
@@ -180,7 +184,8 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
 // Automatic plan (from plan sweeps on GB300, cold L2):
 //  - aligned rows of 256..2048 16-byte vectors: ROW (one block per row);
 //  - shorter rows (or unaligned rows up to 2048 elements): WARP;
-//  - aligned rows up to 512 KiB: CLUSTER;
+//  - aligned rows up to 512 KiB: WIDE (one register-resident cluster per row;
+//    faster than CLUSTER on every wide shape measured);
 //  - anything else: ONLINE.
 int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype) {
@@ -188,6 +193,7 @@ int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64
     const int64_t nvec = N * elem_bytes(dtype) / 16;
     if (vec && nvec >= kRowMinVectors && row_plan_fits(N, dtype)) return SR_PLAN_ROW;
     if (N <= kWarpMaxN) return SR_PLAN_WARP;
+    if (plan_fits(SR_PLAN_WIDE, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_WIDE;
     if (plan_fits(SR_PLAN_CLUSTER, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CLUSTER;
     return SR_PLAN_ONLINE;
 }
@@ -213,6 +219,7 @@ int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t 
         case SR_PLAN_ONLINE: e = launch_online(p); break;
         case SR_PLAN_SMEM: e = launch_smem(p); break;
         case SR_PLAN_ROW: e = launch_row(p); break;
+        case SR_PLAN_WIDE: e = launch_wide(p); break;
         default: return SR_EPLAN;
     }
     return e == cudaSuccess ? SR_OK : SR_ECUDA;
@@ -327,7 +334,7 @@ int softmax_rows(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
 
 int softmax_rows_ex(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                     int64_t ld_out, int dtype, int plan, sr_stream_t stream) {
-    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return SR_EPLAN;
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_WIDE) return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    sr::kDefaultTimeoutNs, 0);
 }
@@ -344,7 +351,7 @@ int softmax_rows_plan_check(const void* in, const void* out, int64_t M, int64_t 
     const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
     if (bad) return -bad;
     if (plan == SR_PLAN_AUTO) return sr::choose_plan(in, out, N, ld_in, ld_out, dtype);
-    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return -SR_EPLAN;
+    if (plan < SR_PLAN_AUTO || plan > SR_PLAN_WIDE) return -SR_EPLAN;
     return sr::plan_fits(plan, in, out, N, ld_in, ld_out, dtype) ? plan : -SR_EPLAN;
 }
 
@@ -364,7 +371,9 @@ int softmax_rows_last_device_error(sr_stream_t stream) {
 int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                              int64_t ld_out, int dtype, int plan, uint64_t timeout_ns,
                              sr_stream_t stream) {
-    if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER && plan != SR_PLAN_SMEM) return SR_EPLAN;
+    if (plan != SR_PLAN_CTA && plan != SR_PLAN_CLUSTER && plan != SR_PLAN_SMEM &&
+        plan != SR_PLAN_WIDE)
+        return SR_EPLAN;
     return sr::run(in, out, M, N, ld_in, ld_out, dtype, plan, (cudaStream_t)stream,
                    (unsigned long long)timeout_ns, sr::kFlagNoCopy);
 }

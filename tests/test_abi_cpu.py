@@ -67,7 +67,7 @@ def test_rejected_arguments_touch_no_device(lib):
     assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 4096, 4096, 4096, 0, sr.SR_PLAN_WARP,
                              None) == sr.SR_EPLAN
     assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, 9, None) == sr.SR_EPLAN
-    assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, 7, None) == sr.SR_EPLAN
+    assert L.softmax_rows_ex(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, 8, None) == sr.SR_EPLAN
     assert L.softmax_rows_test_expiry(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, sr.SR_PLAN_WARP,
                                       1000, None) == sr.SR_EPLAN
 
@@ -76,7 +76,7 @@ EXPECTED_PLANS = {
     "f32_1024x256": sr.SR_PLAN_WARP,
     "f32_4096x4096": sr.SR_PLAN_ROW,
     "bf16_16384x1000_ld1024": sr.SR_PLAN_WARP,
-    "bf16_1024x131072": sr.SR_PLAN_CLUSTER,
+    "bf16_1024x131072": sr.SR_PLAN_WIDE,
     "f16_causal_524288x2048": sr.SR_PLAN_ROW,
 }
 
@@ -97,8 +97,8 @@ def test_plan_depends_on_alignment_and_width(lib):
     assert P(A + 4, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_ONLINE   # misaligned input
     assert P(A, B, 10, 4096, 4097, 4096, 0) == sr.SR_PLAN_ONLINE       # odd pitch
     assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_ROW          # 32 KiB rows
-    assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_CLUSTER      # just over 32 KiB
-    assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_CLUSTER  # 512 KiB bf16
+    assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_WIDE         # just over 32 KiB
+    assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_WIDE   # 512 KiB bf16
     assert P(A, B, 10, 262152, 262152, 262152, 1) == sr.SR_PLAN_ONLINE  # wider than a cluster
     assert P(A, B, 10, 2048, 2048, 2048, 2) == sr.SR_PLAN_ROW
     assert P(A, B, 10, 2040, 2040, 2040, 2) == sr.SR_PLAN_WARP         # 255 vectors
@@ -119,7 +119,12 @@ def test_forced_plan_checks(lib):
     assert C(A, B, 5, 8, 8, 8, 1, sr.SR_PLAN_SMEM) == sr.SR_PLAN_SMEM
     assert C(A, B, 5, 16384, 16384, 16384, 1, sr.SR_PLAN_SMEM) == sr.SR_PLAN_SMEM
     assert C(A, B, 5, 16392, 16392, 16392, 1, sr.SR_PLAN_SMEM) == -sr.SR_EPLAN  # > 32 KiB
-    assert C(A, B, 5, 8, 8, 8, 1, 7) == -sr.SR_EPLAN
+    assert C(A, B, 5, 8, 8, 8, 1, 8) == -sr.SR_EPLAN  # no such plan
+    assert C(A, B, 5, 8, 8, 8, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE
+    assert C(A, B, 5, 131072, 131072, 131072, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE
+    assert C(A, B, 5, 262144, 262144, 262144, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE  # 512 KiB
+    assert C(A, B, 5, 262152, 262152, 262152, 1, sr.SR_PLAN_WIDE) == -sr.SR_EPLAN
+    assert C(A + 2, B, 5, 131072, 131072, 131072, 1, sr.SR_PLAN_WIDE) == -sr.SR_EPLAN
     assert C(A, B, 5, 4096, 4096, 4096, 0, sr.SR_PLAN_ROW) == sr.SR_PLAN_ROW
     assert C(A, B, 5, 16384, 16384, 16384, 1, sr.SR_PLAN_ROW) == sr.SR_PLAN_ROW
     assert C(A, B, 5, 16392, 16392, 16392, 1, sr.SR_PLAN_ROW) == -sr.SR_EPLAN

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
 
 PLANS = [sr.SR_PLAN_AUTO, sr.SR_PLAN_WARP, sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_ONLINE,
-         sr.SR_PLAN_SMEM, sr.SR_PLAN_ROW]
+         sr.SR_PLAN_SMEM, sr.SR_PLAN_ROW, sr.SR_PLAN_WIDE]
 
 
 def nan_filled(M, ld, dtype):
@@ -105,6 +105,23 @@ def test_full_size_sampled(name):
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
 
+@pytest.mark.parametrize("name,plan", [("bf16_1024x131072", sr.SR_PLAN_WIDE),
+                                       ("bf16_1024x131072", sr.SR_PLAN_CLUSTER)])
+def test_full_size_forced_wide_plans(name, plan):
+    """Both wide-row plans on the whole wide workload, checked on sampled rows."""
+    w = synth.WORKLOADS[name]
+    x = w.generate()
+    xd = gu.to_device(x, w.dtype)
+    st, y = run_plan(xd, w.M, w.N, w.ld_in, w.ld_out, w.dtype, plan)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    sample = np.unique(np.concatenate([np.arange(8), np.arange(w.M - 8, w.M),
+                                       np.random.default_rng(5).integers(0, w.M, 48)]))
+    ys = gu.to_host(y[torch.from_numpy(sample).to("cuda")], w.dtype)
+    gu.check_rows(ys, x[sample], w.N, w.ld_in, w.dtype, "%s plan %s" % (name, sr.PLAN_NAMES[plan]))
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
 # ---- edge shapes: widths around every plan boundary, odd row counts ----
 
 EDGE_N = [1, 2, 3, 7, 31, 33, 127, 255, 1000, 2047, 2048, 2049, 4095, 4104, 8192, 8193, 16384,
@@ -144,7 +161,7 @@ def test_misaligned_rows(dtype, N):
     for plan in PLANS:
         if not plan_applies(xd, yd, M, N, ld_in, ld_out, dtype, plan):
             assert plan in (sr.SR_PLAN_CTA, sr.SR_PLAN_CLUSTER, sr.SR_PLAN_WARP, sr.SR_PLAN_SMEM,
-                            sr.SR_PLAN_ROW)
+                            sr.SR_PLAN_ROW, sr.SR_PLAN_WIDE)
             continue
         yb.fill_(float("nan"))
         st = sr.load().softmax_rows_ex(xd.data_ptr(), yd.data_ptr(), M, N, ld_in, ld_out, dtype,
@@ -272,6 +289,7 @@ def test_side_stream_and_empty_calls():
 
 @pytest.mark.parametrize("name,plan", [("f32_4096x4096", sr.SR_PLAN_CTA),
                                        ("bf16_1024x131072", sr.SR_PLAN_CLUSTER),
+                                       ("bf16_1024x131072", sr.SR_PLAN_WIDE),
                                        ("f32_4096x4096", sr.SR_PLAN_SMEM),
                                        ("f16_causal_524288x2048", sr.SR_PLAN_SMEM)])
 def test_bounded_wait_expiry(name, plan):
