@@ -53,17 +53,6 @@
 #ifndef SR_CLUSTER_MIN_BLOCKS_PARKED
 #define SR_CLUSTER_MIN_BLOCKS_PARKED 3
 #endif
-// Recompute variant (RC) for the widest 16-bit slices: 1 selects it, and the
-// resident blocks per SM it is compiled for.
-#ifndef SR_CLUSTER_RC
-#define SR_CLUSTER_RC 1
-#endif
-#ifndef SR_CLUSTER_MIN_BLOCKS_RC
-#define SR_CLUSTER_MIN_BLOCKS_RC 4
-#endif
-#ifndef SR_CLUSTER_RC_STAGE_BUDGET
-#define SR_CLUSTER_RC_STAGE_BUDGET (32 * 1024)
-#endif
 // Vectors per thread whose exponentials are parked in shared memory for the
 // widest 16-bit slices (KV = 8), and the stage budget in that case.
 #ifndef SR_CLUSTER_PARK
@@ -95,13 +84,8 @@ struct SmemLayout {
 // KS: of each thread's KV vectors, the last KS keep their FP32 exponentials
 // in shared memory instead of registers between the exchange and the store,
 // which lets more blocks share an SM's register file.
-// RC: instead of keeping FP32 exponentials until the row's (M, S) arrives,
-// keep the staged inputs in registers as packed 16-byte vectors and
-// exponentiate them a second time for the output (half the on-chip bytes per
-// element for 16-bit data; the output is still rounded once, from FP32).
-template <typename T, int NT, int KV, bool CLUSTER, int KS, bool RC = false>
+template <typename T, int NT, int KV, bool CLUSTER, int KS>
 __global__ void __launch_bounds__(NT, !CLUSTER ? 1
-                                       : RC ? SR_CLUSTER_MIN_BLOCKS_RC
                                        : (KS > 0 ? SR_CLUSTER_MIN_BLOCKS_PARKED
                                           : KV * Elem<T>::kVec >= 64 ? SR_CLUSTER_MIN_BLOCKS
                                                                      : SR_CLUSTER_MIN_BLOCKS_SMALL))
@@ -173,44 +157,12 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
             local_fail = !ok;
         }
 
-        float v[RC ? 1 : KV][VEC];
-        uint4 raw[RC ? KV : 1];
+        float v[KV][VEC];
         // Slice values into registers (vectors tid, tid+NT, ...). Vectors
         // k >= KV - KS are only read here for the max; their exponentials are
         // computed from a second read of the staged slice and parked.
         const uint32_t stage = sbase + (uint32_t)s * L.stage_bytes;
         float mx = neg_inf();
-        float m_w, s_w;
-        if constexpr (RC) {
-#pragma unroll
-            for (int k = 0; k < KV; ++k) {
-                const int idx = tid + NT * k;
-                if (ok && idx < cnt) {
-                    raw[k] = lds128(stage + 16u * idx);
-                    float f[VEC];
-                    Elem<T>::unpack(raw[k], f);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, f[e]);
-                }
-            }
-            m_w = warp_max(mx);
-            const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
-            const float shift_l2 = shift * kLog2e;
-            float sa = 0.0f, sb = 0.0f;
-#pragma unroll
-            for (int k = 0; k < KV; ++k) {
-                if (ok && tid + NT * k < cnt) {
-                    float f[VEC];
-                    Elem<T>::unpack(raw[k], f);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) {
-                        const float x = exp_shifted<T>(f[e], shift, shift_l2);
-                        if (e & 1) sb += x; else sa += x;
-                    }
-                }
-            }
-            s_w = warp_sum(sa + sb);
-        } else {
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + NT * k;
@@ -229,7 +181,7 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
         }
 
         // Warp partial: m_w, then e = exp(x - shift) and s_w (all -inf guard).
-        m_w = warp_max(mx);
+        const float m_w = warp_max(mx);
         const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
         const float shift_l2 = shift * kLog2e;
         // Two partial sums per thread keep the register count low (the
@@ -264,8 +216,7 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
                              "f"(f[4 * h]), "f"(f[4 * h + 1]), "f"(f[4 * h + 2]), "f"(f[4 * h + 3])
                              : "memory");
         }
-        s_w = warp_sum(sa + sb);
-        }  // RC
+        const float s_w = warp_sum(sa + sb);
         if constexpr (!CLUSTER) {
             if (lane == 0) red[p * 32 + warp] = make_float2(m_w, s_w);
         }
@@ -312,28 +263,8 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
             Sr = warp_sum(q.y * merge_scale(q.x, Mr));
         }
 
-        T* rout = out + r * ld_out + v0 * VEC + (int64_t)tid * VEC;
-        if constexpr (RC) {
-            const float rs = final_rcp(Mr, Sr);
-            const float m_l2 = Mr * kLog2e;
-#pragma unroll
-            for (int k = 0; k < KV; ++k) {
-                if (tid + NT * k < cnt) {
-                    // Widened again from the packed vector (the empty asm keeps
-                    // the compiler from holding the first pass's floats).
-                    uint4 rr = raw[k];
-                    if constexpr (sizeof(T) == 2)
-                        asm volatile("" : "+r"(rr.x), "+r"(rr.y), "+r"(rr.z), "+r"(rr.w));
-                    float f[VEC];
-                    Elem<T>::unpack(rr, f);
-#pragma unroll
-                    for (int e = 0; e < VEC; ++e) f[e] = exp_shifted<T>(f[e], Mr, m_l2) * rs;
-                    stg_stream(rout + k * NT * VEC, Elem<T>::pack(f));
-                }
-            }
-            continue;
-        }
         const float f = merge_scale(m_w, Mr) * final_rcp(Mr, Sr);
+        T* rout = out + r * ld_out + v0 * VEC + (int64_t)tid * VEC;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             if (k >= KR) {  // bring a parked vector back
@@ -365,9 +296,9 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
     if constexpr (CLUSTER) cluster_sync_all();
 }
 
-template <typename T, int KV, bool CLUSTER, int KS, bool RC = false>
+template <typename T, int KV, bool CLUSTER, int KS>
 cudaError_t launch_kv(const Problem& p, int csize, SmemLayout L) {
-    auto kern = tma_rows_kernel<T, kTmaThreads, KV, CLUSTER, KS, RC>;
+    auto kern = tma_rows_kernel<T, kTmaThreads, KV, CLUSTER, KS>;
     const void* fn = reinterpret_cast<const void*>(kern);
     const size_t smem = L.total();
     cudaError_t e = ensure_smem_limit(fn, smem, csize > 8);
@@ -421,15 +352,8 @@ cudaError_t launch_typed(const Problem& p, int csize) {
     };
     const bool wide16 = CLUSTER && VEC == 8 && kv > 4;
     if constexpr (CLUSTER && VEC == 8) {
-        // The widest 16-bit slices keep their packed inputs in registers and
-        // exponentiate twice (one stage: the next row streams in while this
-        // one is exchanged and written), or park part of their exponentials
-        // in shared memory so that three blocks share an SM's register file.
-        if (wide16 && SR_CLUSTER_RC) {
-            L.stages = stages_for(SR_CLUSTER_RC_STAGE_BUDGET, 1);
-            L.ebuf_bytes = 0u;
-            return launch_kv<T, 8, CLUSTER, 0, true>(p, csize, L);
-        }
+        // The widest 16-bit slices park part of their exponentials in shared
+        // memory, so that three blocks share an SM's register file.
         if (wide16 && SR_CLUSTER_PARK > 0) {
             L.stages = stages_for(SR_CLUSTER_PARK_STAGE_BUDGET, 1);
             L.ebuf_bytes = (uint32_t)(SR_CLUSTER_PARK * kTmaThreads * VEC * 4);
