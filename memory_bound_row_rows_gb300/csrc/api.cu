@@ -278,7 +278,10 @@ int run_pair(const rp::Args& a, int plan, Launch&& launch) {
     if (!dev) return SR_ECUDA;
     const int chosen = resolve_pair_plan(a, plan, dev->sm_count, &sh);
     if (chosen < 0) return -chosen;
-    return launch(a, sh) == cudaSuccess ? SR_OK : SR_ECUDA;
+    rp::Args q = a;
+    q.err = dev->err;
+    q.timeout_ns = kDefaultTimeoutNs;
+    return launch(q, sh) == cudaSuccess ? SR_OK : SR_ECUDA;
 }
 
 int run_bwd(const void* y, const void* dy, void* dx, int64_t M, int64_t N, int64_t ld_y,

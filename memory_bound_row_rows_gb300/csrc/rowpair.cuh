@@ -272,15 +272,26 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// Asynchronous 4-byte store into a peer's shared memory, completing 4
+// transaction bytes on the peer's mbarrier (both shared::cluster addresses).
+__device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(
+            remote_addr),
+        "f"(v), "r"(remote_bar)
+        : "memory");
 }
 
+// The partials travel by st.async and complete on each receiver's exchange
+// mbarrier (no cluster barrier and no release fence in the row); a receiver's
+// wait is bounded, and a block whose wait expires writes nothing more,
+// records the failure in the error word and waits once more (bounded) before
+// it leaves, so that a late partial cannot land after it exits.
 template <class Op, typename T, Mode MODE, int KV>
 __global__ void __launch_bounds__(kClusterThreads)
     cluster_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                    int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
-                   int64_t slice) {
+                   int64_t slice, unsigned int* err, unsigned long long timeout_ns) {
     constexpr bool WIDE = MODE != Mode::kScalar;
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;
@@ -290,6 +301,7 @@ __global__ void __launch_bounds__(kClusterThreads)
     constexpr int NW = NT / 32;
     __shared__ float red[2][NW];
     __shared__ float part[2][kMaxCluster];  // part[p][q]: block q's partial of this row
+    __shared__ __align__(8) unsigned long long xbar[2];
     const int tid = threadIdx.x;
     const int rank = (int)cluster_ctarank();
     const int64_t nclusters = gridDim.x / csize;
@@ -304,12 +316,20 @@ __global__ void __launch_bounds__(kClusterThreads)
             if (idx < u1) aux[k] = op.template load_aux<VEC>(lay.unit_col(idx));
         }
     }
-    // A block may store into a peer's shared memory only once the peer is
-    // running; the first row's loads overlap this start-up barrier.
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // A block may send to a peer only once the peer runs and its barriers are
+    // initialised; the first row's loads overlap this start-up barrier.
     cluster_arrive_relaxed();
-    bool started = false;
+    bool started = false, failed = false;
+    uint32_t fail_bar = 0, fail_phase = 0;
     int parity = 0;
-    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters) {
+    int64_t it = 0;
+    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters, ++it) {
         const T* ra = A + r * lda;
         const T* rb = B + r * ldb;
         const L lay(ra, N);
@@ -342,11 +362,21 @@ __global__ void __launch_bounds__(kClusterThreads)
             cluster_wait();
             started = true;
         }
+        const uint32_t xb = smem_addr(&xbar[parity]);
+        const uint32_t phase = (uint32_t)((it >> 1) & 1);
+        if (tid == 0) mbar_expect_tx(xb, (uint32_t)csize * 4u);
         if (tid < csize)
-            st_cluster_f32(map_to_rank(smem_addr(&part[parity][rank]), (uint32_t)tid), mine);
-        // Release this block's stores, acquire the peers' (every thread of
-        // every block of the cluster arrives once per row).
-        cluster_sync_all();
+            st_async_f32(map_to_rank(smem_addr(&part[parity][rank]), (uint32_t)tid), mine,
+                         map_to_rank(xb, (uint32_t)tid));
+        if (!failed && !mbar_wait_bounded(xb, phase, timeout_ns)) {
+            failed = true;
+            fail_bar = xb;
+            fail_phase = phase;
+        }
+        if (failed) {  // no output; keep sending, so peers do not wait in vain
+            parity ^= 1;
+            continue;
+        }
         float total = part[parity][0];
         for (int q = 1; q < csize; ++q) total += part[parity][q];
         const float s = op.finish(total, N);
@@ -360,6 +390,10 @@ __global__ void __launch_bounds__(kClusterThreads)
         if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
     }
     if (!started) cluster_wait();
+    if (failed) {
+        if (tid == 0) atomicOr(err, 1u);
+        mbar_wait_bounded(fail_bar, fail_phase, timeout_ns);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -501,7 +535,7 @@ cudaError_t launch_cluster_kv(const Op& op, const Args& p, const Shape& sh) {
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, kern, op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
                            static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc, sh.csize,
-                           sh.slice);
+                           sh.slice, p.err, p.timeout_ns);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }

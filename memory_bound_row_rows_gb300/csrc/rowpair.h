@@ -32,6 +32,8 @@ struct Args {
     int64_t M, N, lda, ldb, ldc;
     int dtype;
     cudaStream_t stream;
+    unsigned int* err = nullptr;            // device error word (CLUSTER plan's bounded waits)
+    unsigned long long timeout_ns = 0;      // limit of one bounded wait
 };
 
 // How one plan runs one problem (host logic only, the same on every device).
