@@ -49,7 +49,7 @@ def _stamp(extra_flags) -> str:
 PLAN_SOURCES = {
     "row": ["block_rows.cu"], "warp": ["warp_rows.cu"], "cta": ["tma_rows.cu"],
     "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
-    "split": ["split_rows.cu"], "wide": ["wide_rows.cu"],
+    "split": ["split_rows.cu"], "wide": ["wide_rows.cu", "wide.h"],
     "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],
     "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h"],
 }

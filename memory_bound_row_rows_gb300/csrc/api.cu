@@ -6,6 +6,7 @@
 
 #include "../../include/softmax_rows.h"
 #include "rowpair.h"
+#include "wide.h"
 #include "internal.h"
 
 namespace sr {

@@ -104,19 +104,6 @@ int max_active_clusters(const void* func, int threads, size_t smem, int cluster)
 // Raise a kernel's dynamic shared memory limit once per device.
 cudaError_t ensure_smem_limit(const void* func, size_t smem, bool nonportable_cluster);
 
-// WIDE plan: clusters of `csize` blocks, `slice` 16-byte vectors per block,
-// `kv` vectors per thread. SR_WIDE_KV: the most vectors a thread holds.
-#ifndef SR_WIDE_KV
-#define SR_WIDE_KV 8
-#endif
-struct WideShape {
-    int csize = 0;
-    int kv = 0;
-    int64_t slice = 0;
-};
-bool wide_shape(int64_t N, int dtype, WideShape* out);
-cudaError_t launch_wide(const Problem& p);
-
 cudaError_t launch_warp(const Problem& p);
 cudaError_t launch_tma(const Problem& p, int cluster);
 cudaError_t launch_online(const Problem& p);

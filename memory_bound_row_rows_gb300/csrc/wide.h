@@ -1,0 +1,24 @@
+// Host-side interface of the WIDE plan (wide_rows.cu) for the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+
+namespace sr {
+
+// WIDE plan: clusters of `csize` blocks, `slice` 16-byte vectors per block,
+// `kv` vectors per thread. SR_WIDE_KV: the most vectors a thread holds.
+#ifndef SR_WIDE_KV
+#define SR_WIDE_KV 8
+#endif
+struct WideShape {
+    int csize = 0;
+    int kv = 0;
+    int64_t slice = 0;
+};
+bool wide_shape(int64_t N, int dtype, WideShape* out);
+cudaError_t launch_wide(const Problem& p);
+
+}  // namespace sr

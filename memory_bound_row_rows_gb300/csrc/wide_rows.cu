@@ -22,6 +22,7 @@
 // more (bounded) so that a late peer's pair cannot land after it exits.
 #include "device.cuh"
 #include "internal.h"
+#include "wide.h"
 
 namespace sr {
 namespace {
