@@ -20,12 +20,19 @@
 // Failure: a wait that expires marks the block failed; it writes nothing
 // more, records the failure in the error word and, before leaving, waits once
 // more (bounded) so that a late peer's pair cannot land after it exits.
+#include <type_traits>
+
 #include "device.cuh"
 #include "internal.h"
 #include "wide.h"
 
 namespace sr {
 namespace {
+
+// Cluster scheduling policy of the launch (a cudaClusterSchedulingPolicy).
+#ifndef SR_WIDE_POLICY
+#define SR_WIDE_POLICY 2
+#endif
 
 // Resident blocks per SM the kernel is compiled for (bounds its registers).
 #ifndef SR_WIDE_MIN_BLOCKS
@@ -49,37 +56,59 @@ __device__ __forceinline__ float lg2_approx(float x) {
     return y;
 }
 
-// Largest element of a packed vector (NaN elements are ignored, as fmaxf
-// does). 16-bit data compares pairs in their own format: exact, and one
-// instruction per two elements.
+// Running maximum over packed vectors (NaN elements are ignored, as fmaxf
+// does). 16-bit data is compared in pairs in its own format (exact, one
+// instruction per two elements) and widened once at the end.
 template <typename T>
-__device__ __forceinline__ float vec_max(const uint4& u);
+struct VecMax {
+    uint32_t m = sizeof(T) == 2 ? (std::is_same<T, __half>::value ? 0xFC00FC00u : 0xFF80FF80u)
+                                : 0xFF800000u;  // -inf (pair)
+    __device__ __forceinline__ void add(const uint4& u);
+    __device__ __forceinline__ float get() const;
+};
 
 template <>
-__device__ __forceinline__ float vec_max<float>(const uint4& u) {
-    return fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
-                 fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+__device__ __forceinline__ void VecMax<float>::add(const uint4& u) {
+    const float a = fmaxf(fmaxf(__uint_as_float(u.x), __uint_as_float(u.y)),
+                          fmaxf(__uint_as_float(u.z), __uint_as_float(u.w)));
+    m = __float_as_uint(fmaxf(__uint_as_float(m), a));
 }
+template <>
+__device__ __forceinline__ float VecMax<float>::get() const { return __uint_as_float(m); }
 
 template <typename H2>
 __device__ __forceinline__ H2 as_h2(uint32_t w) {
     return *reinterpret_cast<H2*>(&w);
 }
-
-template <>
-__device__ __forceinline__ float vec_max<__nv_bfloat16>(const uint4& u) {
-    using H2 = __nv_bfloat162;
-    const H2 m = __hmax2(__hmax2(as_h2<H2>(u.x), as_h2<H2>(u.y)),
-                         __hmax2(as_h2<H2>(u.z), as_h2<H2>(u.w)));
-    return fmaxf(__low2float(m), __high2float(m));
+template <typename H2>
+__device__ __forceinline__ uint32_t from_h2(H2 h) {
+    return *reinterpret_cast<uint32_t*>(&h);
 }
 
 template <>
-__device__ __forceinline__ float vec_max<__half>(const uint4& u) {
-    using H2 = __half2;
-    const H2 m = __hmax2(__hmax2(as_h2<H2>(u.x), as_h2<H2>(u.y)),
+__device__ __forceinline__ void VecMax<__nv_bfloat16>::add(const uint4& u) {
+    using H2 = __nv_bfloat162;
+    const H2 a = __hmax2(__hmax2(as_h2<H2>(u.x), as_h2<H2>(u.y)),
                          __hmax2(as_h2<H2>(u.z), as_h2<H2>(u.w)));
-    return fmaxf(__low2float(m), __high2float(m));
+    m = from_h2(__hmax2(as_h2<H2>(m), a));
+}
+template <>
+__device__ __forceinline__ float VecMax<__nv_bfloat16>::get() const {
+    const __nv_bfloat162 h = as_h2<__nv_bfloat162>(m);
+    return fmaxf(__low2float(h), __high2float(h));
+}
+
+template <>
+__device__ __forceinline__ void VecMax<__half>::add(const uint4& u) {
+    using H2 = __half2;
+    const H2 a = __hmax2(__hmax2(as_h2<H2>(u.x), as_h2<H2>(u.y)),
+                         __hmax2(as_h2<H2>(u.z), as_h2<H2>(u.w)));
+    m = from_h2(__hmax2(as_h2<H2>(m), a));
+}
+template <>
+__device__ __forceinline__ float VecMax<__half>::get() const {
+    const __half2 h = as_h2<__half2>(m);
+    return fmaxf(__low2float(h), __high2float(h));
 }
 
 // Values of a packed vector, widened again for the output pass. The empty
@@ -93,7 +122,9 @@ __device__ __forceinline__ void unpack_again(const uint4& raw, float* f) {
 }
 
 // KV: 16-byte vectors per thread; `slice`: vectors per block (<= 256 * KV).
-template <typename T, int KV>
+// FULL: every block's slice is exactly 256 * KV vectors, so no vector needs a
+// bounds check (straight-line loads, math and stores).
+template <typename T, int KV, bool FULL>
 __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     wide_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
@@ -135,20 +166,20 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int64_t idx = u0 + tid + NT * k;
-            if (idx < u1) raw[k] = ldg_stream(rin + idx * VEC);
+            if (FULL || idx < u1) raw[k] = ldg_stream(rin + idx * VEC);
         }
         // Warp partial (m_w, s_w): max, then sum of exp(x - m_w).
-        float mx = neg_inf();
+        VecMax<T> vm;
 #pragma unroll
         for (int k = 0; k < KV; ++k)
-            if (u0 + tid + NT * k < u1) mx = fmaxf(mx, vec_max<T>(raw[k]));
-        const float m_w = warp_max(mx);
+            if (FULL || u0 + tid + NT * k < u1) vm.add(raw[k]);
+        const float m_w = warp_max(vm.get());
         const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
         const float shift_l2 = shift * kLog2e;
         float sa = 0.0f, sb = 0.0f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-            if (u0 + tid + NT * k < u1) {
+            if (FULL || u0 + tid + NT * k < u1) {
                 float f[VEC];
                 Elem<T>::unpack(raw[k], f);
 #pragma unroll
@@ -191,7 +222,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
 #pragma unroll
             for (int k = 0; k < KV; ++k) {
                 const int64_t idx = u0 + tid + NT * k;
-                if (idx < u1) {
+                if (FULL || idx < u1) {
                     float f[VEC];
                     unpack_again<T>(raw[k], f);
 #pragma unroll
@@ -207,7 +238,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
 #pragma unroll
             for (int k = 0; k < KV; ++k) {
                 const int64_t idx = u0 + tid + NT * k;
-                if (idx < u1) {
+                if (FULL || idx < u1) {
                     float f[VEC];
                     unpack_again<T>(raw[k], f);
 #pragma unroll
@@ -226,9 +257,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     }
 }
 
-template <typename T, int KV>
+template <typename T, int KV, bool FULL>
 cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
-    auto kern = wide_rows_kernel<T, KV>;
+    auto kern = wide_rows_kernel<T, KV, FULL>;
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = ensure_smem_limit(fn, 0, csize > 8);
     if (e != cudaSuccess) return e;
@@ -241,13 +272,18 @@ cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
     cfg.blockDim = dim3(kWideThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = p.stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // Let the hardware balance a cluster's blocks over the SMs of a GPC
+    // (measured: 1.5 % faster than the default policy on 1024 x 131072 bf16).
+    attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+    attr[1].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)SR_WIDE_POLICY;
+    cfg.numAttrs = 2;
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
                            p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
                            p.flags);
@@ -257,10 +293,18 @@ cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
 
 template <typename T>
 cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
+    const int64_t nvec = p.N / Elem<T>::kVec;
+    const bool full = sh.slice == (int64_t)kWideThreads * sh.kv && nvec == sh.slice * sh.csize;
     switch (sh.kv) {
-        case 2: return launch_kv<T, 2>(p, sh.csize, sh.slice);
-        case 4: return launch_kv<T, 4>(p, sh.csize, sh.slice);
-        case 8: return launch_kv<T, 8>(p, sh.csize, sh.slice);
+        case 2:
+            return full ? launch_kv<T, 2, true>(p, sh.csize, sh.slice)
+                        : launch_kv<T, 2, false>(p, sh.csize, sh.slice);
+        case 4:
+            return full ? launch_kv<T, 4, true>(p, sh.csize, sh.slice)
+                        : launch_kv<T, 4, false>(p, sh.csize, sh.slice);
+        case 8:
+            return full ? launch_kv<T, 8, true>(p, sh.csize, sh.slice)
+                        : launch_kv<T, 8, false>(p, sh.csize, sh.slice);
     }
     return cudaErrorInvalidValue;
 }
