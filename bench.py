@@ -190,10 +190,18 @@ def cpu_baseline(w, x, budget_s: float):
         if time.perf_counter() - t_start >= budget_s:
             break
     gbs = w.fused_bytes * len(times) / sum(times) / 1e9
+    # The same oracle on one core, over the leading rows (about a tenth of the budget).
+    import oracle
+    rows = max(1, min(w.M, int(w.M * 0.1 * budget_s / max(1e-9, 16 * sum(times) / len(times)))))
+    t0 = time.perf_counter()
+    oracle.softmax_rows(x[:rows].reshape(-1), rows, w.N, w.ld_in, w.ld_out, w.dtype, nthreads=1)
+    t1 = time.perf_counter() - t0
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": nthreads, "kind": "oracle",
             "sample": "whole %s matrix (%d x %d), %d pass(es) of the FP64 C oracle, %d threads"
                       % (w.name, w.M, w.N, len(times), nthreads),
-            "rows_per_s": round(w.M * len(times) / sum(times), 1)}, y
+            "rows_per_s": round(w.M * len(times) / sum(times), 1),
+            "serial": {"value": round(2 * rows * w.N * w.elem_bytes / t1 / 1e9, 4), "unit": "GB/s",
+                       "cores": 1, "sample": "first %d rows, one pass" % rows}}, y
 
 
 # ---- GPU leg ----------------------------------------------------------------------
@@ -206,6 +214,17 @@ def gpu_uuid(device_index: int):
         return s if s.startswith("GPU-") else "GPU-" + s
     except Exception:
         return None
+
+
+def step_stats(ms) -> dict:
+    """Per-step time statistics in µs: median, p10/p90, MAD, min, max."""
+    us = np.asarray(ms, dtype=np.float64) * 1e3
+    med = float(np.median(us))
+    return {"median_step_us": round(med, 3),
+            "p10_p90_step_us": [round(float(np.percentile(us, 10)), 3),
+                                round(float(np.percentile(us, 90)), 3)],
+            "mad_step_us": round(float(np.median(np.abs(us - med))), 3),
+            "min_max_step_us": [round(float(us.min()), 3), round(float(us.max()), 3)]}
 
 
 def timed_steps(args, step, flush_l2, stream, rank, local_rank, world):
@@ -439,9 +458,7 @@ def bench_ours(args, w):
         "rows_per_s": round(world * w.M * steps / total_s, 1),
         "bytes_per_step": nbytes,
         "dense_equivalent_gbs": round(world * w.fused_bytes * steps / total_s / 1e9, 2),
-        "median_step_us": round(statistics.median(ms) * 1e3, 3),
-        "p10_p90_step_us": [round(float(np.percentile(ms, 10)) * 1e3, 3),
-                            round(float(np.percentile(ms, 90)) * 1e3, 3)],
+        **step_stats(ms),
         "gpu_launches": steps * (2 if res["plan"] == "split" else 1),
         "clocks": res["clocks"],
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
@@ -682,9 +699,7 @@ def bench_pair(args, lane):
         "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "bytes_per_step": w.fused_bytes,
-        "median_step_us": round(statistics.median(ms) * 1e3, 3),
-        "p10_p90_step_us": [round(float(np.percentile(ms, 10)) * 1e3, 3),
-                            round(float(np.percentile(ms, 90)) * 1e3, 3)],
+        **step_stats(ms),
         "gpu_launches": steps,
         "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
