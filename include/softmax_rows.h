@@ -299,6 +299,20 @@ SR_API int softmax_rows_backward_ex(const void* y, const void* dy, void* dx, int
                                     int dtype, int plan, sr_stream_t stream);
 
 /*
+ * Test hook for the bounded waits of the row-pair CLUSTER plan: runs the
+ * softmax backward with SR_PLAN_CLUSTER and its partial dot products not sent,
+ * so every block's wait for its peers expires after `timeout_ns` nanoseconds;
+ * the kernel then records SR_EDEVICE_TIMEOUT (see softmax_rows_last_device_error)
+ * and returns without writing dx. Nothing hangs and nothing faults. Returns
+ * like softmax_rows_backward_ex (SR_EPLAN when the CLUSTER plan cannot take
+ * the shape).
+ */
+SR_API int softmax_rows_backward_test_expiry(const void* y, const void* dy, void* dx, int64_t M,
+                                             int64_t N, int64_t ld_y, int64_t ld_dy,
+                                             int64_t ld_dx, int dtype, uint64_t timeout_ns,
+                                             sr_stream_t stream);
+
+/*
  * Host-only query: the plan softmax_rows_backward_ex would run for `plan`
  * (SR_PLAN_AUTO resolves to a concrete plan), or a negative sr_status
  * (-SR_EPLAN when the plan cannot take the shape). The pointers are only

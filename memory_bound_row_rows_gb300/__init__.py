@@ -21,7 +21,7 @@ __all__ = [
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
     "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
-    "softmax_rows_backward_plan", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
+    "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
     "rmsnorm_residual_rows_plan",
     "softmax", "softmax_backward", "rmsnorm_residual",
     "dtype_code",
@@ -80,6 +80,7 @@ def load():
         "softmax_rows_backward": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_backward_ex": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, vp],
         "softmax_rows_backward_plan": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, c_int],
+        "softmax_rows_backward_test_expiry": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, u64, vp],
         "rmsnorm_residual_rows": [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, c_int, vp],
         "rmsnorm_residual_rows_ex": [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, c_int, c_int,
                                      vp],
@@ -184,6 +185,15 @@ def softmax_rows_backward_ex(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan,
     return _check(load().softmax_rows_backward_ex(_ptr(y), _ptr(dy), _ptr(dx), M, N, ld_y, ld_dy,
                                                   ld_dx, dtype, plan, _stream(stream)),
                   "softmax_rows_backward_ex")
+
+
+def softmax_rows_backward_test_expiry(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, timeout_ns,
+                                      stream=None) -> int:
+    """Test hook: the CLUSTER plan with its partials not sent (every wait expires)."""
+    return _check(load().softmax_rows_backward_test_expiry(_ptr(y), _ptr(dy), _ptr(dx), M, N,
+                                                           ld_y, ld_dy, ld_dx, dtype, timeout_ns,
+                                                           _stream(stream)),
+                  "softmax_rows_backward_test_expiry")
 
 
 def softmax_rows_backward_plan(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan=SR_PLAN_AUTO,

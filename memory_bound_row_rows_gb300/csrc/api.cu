@@ -267,7 +267,8 @@ int resolve_pair_plan(const rp::Args& p, int plan, int sm_count, rp::Shape* sh) 
 
 // Plan and launch one row-pair operation (arguments already checked).
 template <class Launch>
-int run_pair(const rp::Args& a, int plan, Launch&& launch) {
+int run_pair(const rp::Args& a, int plan, Launch&& launch,
+             unsigned long long timeout_ns = kDefaultTimeoutNs) {
     if (plan < SR_PLAN_AUTO || plan > SR_PLAN_ROW) return SR_EPLAN;
     rp::Shape sh;
     // Whether a plan fits does not depend on the device (only the cluster
@@ -281,7 +282,7 @@ int run_pair(const rp::Args& a, int plan, Launch&& launch) {
     if (chosen < 0) return -chosen;
     rp::Args q = a;
     q.err = dev->err;
-    q.timeout_ns = kDefaultTimeoutNs;
+    q.timeout_ns = timeout_ns;
     return launch(q, sh) == cudaSuccess ? SR_OK : SR_ECUDA;
 }
 
@@ -466,6 +467,19 @@ int softmax_rows_backward_ex(const void* y, const void* dy, void* dx, int64_t M,
                              int64_t ld_y, int64_t ld_dy, int64_t ld_dx, int dtype, int plan,
                              sr_stream_t stream) {
     return sr::run_bwd(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, plan, (cudaStream_t)stream);
+}
+
+int softmax_rows_backward_test_expiry(const void* y, const void* dy, void* dx, int64_t M,
+                                      int64_t N, int64_t ld_y, int64_t ld_dy, int64_t ld_dx,
+                                      int dtype, uint64_t timeout_ns, sr_stream_t stream) {
+    const int bad = sr::check_bwd_args(y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype);
+    if (bad) return bad;
+    sr::rp::Args a{y, dy, dx, M, N, ld_y, ld_dy, ld_dx, dtype, (cudaStream_t)stream};
+    a.flags = sr::kFlagNoCopy;
+    return sr::run_pair(
+        a, SR_PLAN_CLUSTER,
+        [](const sr::rp::Args& q, const sr::rp::Shape& sh) { return sr::launch_backward(q, sh); },
+        (unsigned long long)timeout_ns);
 }
 
 int softmax_rows_backward_plan(const void* y, const void* dy, const void* dx, int64_t M,

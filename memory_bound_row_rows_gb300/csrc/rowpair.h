@@ -34,6 +34,7 @@ struct Args {
     cudaStream_t stream;
     unsigned int* err = nullptr;            // device error word (CLUSTER plan's bounded waits)
     unsigned long long timeout_ns = 0;      // limit of one bounded wait
+    int flags = 0;                          // kFlagNoCopy: the CLUSTER plan sends no partials
 };
 
 // How one plan runs one problem (host logic only, the same on every device).

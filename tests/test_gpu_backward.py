@@ -214,3 +214,21 @@ def test_offset_views(dtype):
             dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :N]), dtype)
             bwd_gate(dec(got), dec(ref), dec(ys), dec(gs), dtype,
                      "offsets %s/%s" % ((ky, kg, kx), sr.PLAN_NAMES[plan]))
+
+
+@pytest.mark.parametrize("name", ["f16_64x131072", "f16_4x32769"])
+def test_cluster_wait_expiry(name):
+    """The CLUSTER plan's bounded waits: with the partials not sent every wait
+    expires, the status is reported, nothing is written, and the context still
+    runs a normal call afterwards."""
+    w = synth.BACKWARD[name].with_rows(4)
+    y, dy = w.y_rows(0, w.M), w.dy_rows(0, w.M)
+    yd, gd = gu.to_device(y, w.dtype), gu.to_device(dy, w.dtype)
+    dx = torch.full((w.M, w.N), float("nan"), dtype=gu.torch_dtype(w.dtype), device="cuda")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    sr.softmax_rows_backward_test_expiry(yd, gd, dx, w.M, w.N, w.ld, w.ld, w.N, w.dtype,
+                                         2_000_000)
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert torch.isnan(dx).all(), "an expired kernel wrote output"
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    check_case(y, dy, w.M, w.N, w.ld, w.ld, w.N, w.dtype, sr.SR_PLAN_CLUSTER, "after expiry")
