@@ -9,12 +9,17 @@
 // is persistent ("Fused Softmax on GPU", Persistent Triton Kernel): blocks
 // resident on every SM walk the rows with a grid stride.
 //
+// Aligned rows without a mask take a packed variant (warp_packed_kernel):
+// the row stays in registers as packed 16-byte vectors and the exponential is
+// computed twice, which doubles the rows in flight per SM.
+//
 // Lane l owns 16-byte vectors l, l+32, ..., so every load and store
 // instruction of a warp covers 512 contiguous bytes. A row of up to
 // 32 * KV * VEC elements fits; VEC == 1 is the scalar variant used when rows
 // are not 16-byte aligned.
 #include "device.cuh"
 #include "internal.h"
+#include "packed.cuh"
 
 namespace sr {
 namespace {
@@ -24,6 +29,14 @@ constexpr int kWarpBlock = 256;  // 8 warps per block
 // 0: one warp per row, the hardware scheduler hands out the rows.
 #ifndef SR_WARP_PERSISTENT
 #define SR_WARP_PERSISTENT 1
+#endif
+// 1: aligned, unmasked rows take the packed variant; the resident blocks per
+// SM it is compiled for.
+#ifndef SR_WARP_PACKED
+#define SR_WARP_PACKED 1
+#endif
+#ifndef SR_WARP_PACKED_MIN_BLOCKS
+#define SR_WARP_PACKED_MIN_BLOCKS 6
 #endif
 
 template <typename T, int VEC, int KV, bool MASKED>
@@ -116,6 +129,96 @@ __global__ void __launch_bounds__(kWarpBlock)
     }
 }
 
+// Packed variant for aligned, unmasked rows: the row stays in registers as
+// packed 16-byte vectors (4 registers per 16 bytes instead of one per element
+// for 16-bit data), so about twice as many rows are in flight per SM; the
+// exponential is computed twice, once for the sum and once for the output
+// (16-bit data: 1/S folded into the exponent, one FMA and one ex2 per element),
+// and the result is still rounded once, from FP32.
+template <typename T, int KV>
+__global__ void __launch_bounds__(kWarpBlock, KV <= 4 ? SR_WARP_PACKED_MIN_BLOCKS : 2)
+    warp_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
+                       int64_t ld_in, int64_t ld_out) {
+    constexpr int VEC = Elem<T>::kVec;
+    const int lane = threadIdx.x & 31;
+    const int64_t first = ((int64_t)blockIdx.x * kWarpBlock + threadIdx.x) >> 5;
+    const int64_t stride = ((int64_t)gridDim.x * kWarpBlock) >> 5;
+    const int nvec = N / VEC;
+    for (int64_t r = first; r < M; r += stride) {
+        const T* rin = in + r * ld_in;
+        uint4 raw[KV];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = lane + 32 * k;
+            if (idx < nvec) raw[k] = ldg_stream(rin + (int64_t)idx * VEC);
+        }
+        VecMax<T> vm;
+#pragma unroll
+        for (int k = 0; k < KV; ++k)
+            if (lane + 32 * k < nvec) vm.add(raw[k]);
+        const float m = warp_max(vm.get());
+        const float m_l2 = m * kLog2e;
+        float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            if (lane + 32 * k < nvec) {
+                float f[VEC];
+                Elem<T>::unpack(raw[k], f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float x = exp_shifted<T>(f[e], m, m_l2);
+                    if (e & 1) sb += x; else sa += x;
+                }
+            }
+        }
+        const float s = warp_sum(sa + sb);
+        T* rout = out + r * ld_out;
+        if constexpr (Elem<T>::kAccurateExp) {
+            const float rs = __frcp_rn(s);
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int idx = lane + 32 * k;
+                if (idx < nvec) {
+                    float f[VEC];
+                    unpack_again<T>(raw[k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) f[e] = expf(f[e] - m) * rs;
+                    stg_stream(rout + (int64_t)idx * VEC, Elem<T>::pack(f));
+                }
+            }
+        } else {
+            // y = 2^(x log2(e) - (m log2(e) + log2(S))); an all -inf row gives
+            // -inf - -inf = NaN, as 0/0 does.
+            const float c = fmaf(m, kLog2e, lg2_approx(s));
+#pragma unroll
+            for (int k = 0; k < KV; ++k) {
+                const int idx = lane + 32 * k;
+                if (idx < nvec) {
+                    float f[VEC];
+                    unpack_again<T>(raw[k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
+                    stg_stream(rout + (int64_t)idx * VEC, Elem<T>::pack(f));
+                }
+            }
+        }
+    }
+}
+
+// One warp per row and no row loop (measured faster than the persistent grid
+// for this variant: the hardware hands out rows as blocks retire).
+template <typename T, int KV>
+cudaError_t launch_packed(const Problem& p) {
+    auto kern = warp_packed_kernel<T, KV>;
+    const int64_t warps_per_block = kWarpBlock / 32;
+    const int64_t need = (p.M + warps_per_block - 1) / warps_per_block;
+    const int64_t cap = 0x7fffffff;
+    const unsigned grid = (unsigned)(need < cap ? need : cap);
+    kern<<<grid, kWarpBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
+                                            p.M, (int)p.N, p.ld_in, p.ld_out);
+    return cudaGetLastError();
+}
+
 template <typename T, int VEC, int KV, bool MASKED>
 cudaError_t launch_one_m(const Problem& p) {
     auto kern = warp_rows_kernel<T, VEC, KV, MASKED>;
@@ -136,6 +239,7 @@ cudaError_t launch_one_m(const Problem& p) {
 template <typename T, int VEC, int KV>
 cudaError_t launch_one(const Problem& p) {
     if (p.mask.active()) return launch_one_m<T, VEC, KV, true>(p);
+    if constexpr (VEC > 1 && SR_WARP_PACKED) return launch_packed<T, KV>(p);
     return launch_one_m<T, VEC, KV, false>(p);
 }
 
