@@ -323,9 +323,12 @@ def run_ours(args, w, rank, local_rank, world):
 
 
 def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
-    """Same metric through the C ABI with host buffers: softmax_rows_host streams the
-    pinned host matrix through a device workspace (copy-in, compute and copy-out of
-    consecutive chunks overlapped), and the result lands back in pinned host memory."""
+    """Same metric through the C ABI with host buffers, timed around whole calls with the
+    input in pinned host memory and the result landing back in pinned host memory. Two
+    public entry points: softmax_rows_host_mapped (the kernel reads and writes the mapped
+    host buffers itself, zero copy) and softmax_rows_host (staged through a device
+    workspace, copy-in, compute and copy-out of chunks overlapped on three streams).
+    The line reports the faster, and both figures."""
     import torch
     import memory_bound_row_rows_gb300 as sr
     x_pin = host_tensor(x).pin_memory()
@@ -334,30 +337,46 @@ def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
     ws = torch.empty(need, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def staged():
         st = lib.softmax_rows_host(x_pin.data_ptr(), y_pin.data_ptr(), w.M, w.N, w.ld_in,
                                    w.ld_out, w.dtype, ws.data_ptr(), need, stream.cuda_stream)
         if st != 0:
             raise RuntimeError("softmax_rows_host failed: %s" % sr.softmax_rows_strerror(st))
 
-    for _ in range(3):
-        step()
-    torch.cuda.synchronize()
-    k = max(3, min(args.steps, 20))
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for _ in range(k):
-        step()
-    t1.record(stream)
-    torch.cuda.synchronize()
-    sec = t0.elapsed_time(t1) / 1e3 / k
+    def mapped():
+        st = lib.softmax_rows_host_mapped(x_pin.data_ptr(), y_pin.data_ptr(), w.M, w.N, w.ld_in,
+                                          w.ld_out, w.dtype, stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError("softmax_rows_host_mapped failed: %s" % sr.softmax_rows_strerror(st))
+
+    def timed(step):
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        k = max(3, min(args.steps, 20))
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(k):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / 1e3 / k, k
+
+    sec_m, k = timed(mapped)
+    sec_s, _ = timed(staged)
     eb = w.elem_bytes
+    best_mapped = sec_m <= sec_s
+    sec = sec_m if best_mapped else sec_s
     return {"value": round(w.fused_bytes / sec / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": w.M * w.N * eb, "d2h_bytes_per_step": w.M * w.N * eb,
             "ms_per_step": round(sec * 1e3, 4), "steps": k,
-            "path": "softmax_rows_host: pinned host -> device workspace -> pinned host, "
-                    "chunks overlapped on three streams"}
+            "path": ("softmax_rows_host_mapped: the kernel reads pinned host input and writes "
+                     "pinned host output over the host link (zero copy)") if best_mapped else
+                    ("softmax_rows_host: pinned host -> device workspace -> pinned host, "
+                     "chunks overlapped on three streams"),
+            "mapped_gbs": round(w.fused_bytes / sec_m / 1e9, 2),
+            "staged_gbs": round(w.fused_bytes / sec_s / 1e9, 2)}
 
 
 def parity_vs_oracle(w, y_dev, y_ref, max_elements: int = 1 << 25):

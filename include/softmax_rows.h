@@ -182,6 +182,20 @@ SR_API int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N
                              sr_stream_t stream);
 
 /*
+ * Host-resident matrices read and written by the kernel itself (zero copy):
+ * h_in and h_out must be page-locked host memory mapped into the device's
+ * address space (cudaHostAlloc / cudaHostRegister with mapping, which is the
+ * default under unified addressing) or managed memory; the kernel loads the
+ * input over the host link and stores the output back, with no staging copies
+ * and no workspace. Each pointer is checked with cudaPointerGetAttributes
+ * before anything is launched; memory the device cannot address is refused
+ * with SR_EINVAL. The plan is chosen as for softmax_rows. Asynchronous on
+ * `stream`: synchronise it before reading h_out. Returns like softmax_rows.
+ */
+SR_API int softmax_rows_host_mapped(const void* h_in, void* h_out, int64_t M, int64_t N,
+                                    int64_t ld_in, int64_t ld_out, int dtype, sr_stream_t stream);
+
+/*
  * Device workspace size (bytes) with which softmax_rows_host overlaps its
  * copies at full depth for M rows of N elements, or a negative sr_status.
  */

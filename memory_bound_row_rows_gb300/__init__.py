@@ -20,6 +20,7 @@ __all__ = [
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
     "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
+    "softmax_rows_host_mapped",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
     "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
     "rmsnorm_residual_rows_plan",
@@ -73,6 +74,7 @@ def load():
         "softmax_rows_strerror": [c_int],
         "softmax_rows_host": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
         "softmax_rows_host_workspace_bytes": [i64, i64, c_int],
+        "softmax_rows_host_mapped": [vp, vp, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_split": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
         "softmax_rows_split_workspace_bytes": [vp, vp, i64, i64, i64, i64, c_int],
         "softmax_rows_split_noalloc": [vp, vp, i64, i64, i64, i64, c_int, vp],
@@ -163,6 +165,13 @@ def softmax_rows_host(h_in, h_out, M, N, ld_in, ld_out, dtype, d_work, work_byte
     return _check(load().softmax_rows_host(_ptr(h_in), _ptr(h_out), M, N, ld_in, ld_out, dtype,
                                            _ptr(d_work), work_bytes, _stream(stream)),
                   "softmax_rows_host")
+
+
+def softmax_rows_host_mapped(h_in, h_out, M, N, ld_in, ld_out, dtype, stream=None) -> int:
+    """Zero-copy variant: the kernel reads and writes mapped page-locked host memory."""
+    return _check(load().softmax_rows_host_mapped(_ptr(h_in), _ptr(h_out), M, N, ld_in, ld_out,
+                                                  dtype, _stream(stream)),
+                  "softmax_rows_host_mapped")
 
 
 def softmax_rows_masked(in_, out, M, N, ld_in, ld_out, dtype, lengths=None, causal_period=0,

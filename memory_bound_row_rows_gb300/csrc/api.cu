@@ -446,6 +446,30 @@ int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype) {
     return sr::host_workspace_bytes(M, N, dtype);
 }
 
+int softmax_rows_host_mapped(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,
+                             int64_t ld_out, int dtype, sr_stream_t stream) {
+    const int bad = sr::check_args(h_in, h_out, M, N, ld_in, ld_out, dtype);
+    if (bad) return bad;
+    if (M == 0) return SR_OK;
+    // Only memory the device can address: page-locked host memory mapped into
+    // the device's address space (or managed memory). Anything else is
+    // refused before a kernel could touch it.
+    void* dptr[2] = {nullptr, nullptr};
+    const void* hptr[2] = {h_in, h_out};
+    for (int i = 0; i < 2; ++i) {
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, hptr[i]) != cudaSuccess) {
+            (void)cudaGetLastError();  // clear the sticky-free error of an unknown pointer
+            return SR_EINVAL;
+        }
+        if ((at.type != cudaMemoryTypeHost && at.type != cudaMemoryTypeManaged) ||
+            at.devicePointer == nullptr)
+            return SR_EINVAL;
+        dptr[i] = at.devicePointer;
+    }
+    return sr::launch_auto(dptr[0], dptr[1], M, N, ld_in, ld_out, dtype, (cudaStream_t)stream);
+}
+
 int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,
                       int64_t ld_out, int dtype, void* d_work, int64_t work_bytes,
                       sr_stream_t stream) {

@@ -242,3 +242,12 @@ def test_rmsnorm_rejected_arguments_touch_no_device(lib):
     assert sr.rmsnorm_residual_rows_plan(*ok, 1e-6, 0, sr.SR_PLAN_AUTO, 152) == sr.SR_PLAN_ROW
     assert sr.rmsnorm_residual_rows_plan(x, r, w, y, 64, 131072, 131072, 131072, 131072, 1e-6,
                                          2, sr.SR_PLAN_AUTO, 152) == sr.SR_PLAN_CLUSTER
+
+
+def test_host_mapped_refuses_without_a_device(lib):
+    # No device here: the pointer check fails and nothing is launched.
+    assert lib.softmax_rows_host_mapped(ALIGNED_IN, ALIGNED_OUT, 4, 8, 8, 8, 0, None) == \
+        sr.SR_EINVAL
+    assert lib.softmax_rows_host_mapped(None, None, 0, 8, 8, 8, 0, None) == sr.SR_OK
+    assert lib.softmax_rows_host_mapped(ALIGNED_IN, ALIGNED_OUT, 4, 8, 7, 8, 0, None) == \
+        sr.SR_EINVAL
