@@ -174,10 +174,7 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
         case SR_PLAN_ONLINE: return true;
         case SR_PLAN_SMEM: return vec && row_bytes <= kSmemMaxRowBytes;
         case SR_PLAN_ROW: return vec && row_plan_fits(N, dtype);
-        case SR_PLAN_WIDE: {
-            WideShape sh;
-            return vec && wide_shape(N, dtype, &sh);
-        }
+        case SR_PLAN_WIDE: return wide_fits(in, out, N, ld_in, ld_out, dtype);
     }
     return false;
 }

@@ -18,7 +18,9 @@ struct WideShape {
     int kv = 0;
     int64_t slice = 0;
 };
-bool wide_shape(int64_t N, int dtype, WideShape* out);
+bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out);
+bool wide_fits(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
+               int dtype);
 cudaError_t launch_wide(const Problem& p);
 
 }  // namespace sr

@@ -49,10 +49,17 @@ __device__ __forceinline__ void cluster_wait() {
     asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
 }
 
+// Row layouts: kAligned, every row of both matrices on a 16-byte boundary
+// and whole vectors (kFull when, besides, every block's slice is exactly
+// 256 * KV vectors, so no vector needs a bounds check); kShifted, the rows of
+// the input and the output share their offset from a 16-byte boundary, so a
+// row is a head of fewer than VEC elements, 16-byte vectors and a tail of
+// fewer than VEC elements; rank 0's first threads take the head and tail
+// elements one each.
+enum : int { kAligned = 0, kFull = 1, kShifted = 2 };
+
 // KV: 16-byte vectors per thread; `slice`: vectors per block (<= 256 * KV).
-// FULL: every block's slice is exactly 256 * KV vectors, so no vector needs a
-// bounds check (straight-line loads, math and stores).
-template <typename T, int KV, bool FULL>
+template <typename T, int KV, int MODE>
 __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     wide_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
@@ -60,6 +67,8 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NT = kWideThreads;
     constexpr int NW = kWideWarps;
+    constexpr bool FULL = MODE == kFull;
+    constexpr bool SHIFTED = MODE == kShifted;
     // pairs[p][q * NW + w]: warp w of block q for rows of parity p (a cluster
     // walks more than one row only when the grid is capped), and the two
     // exchange barriers they complete on.
@@ -70,7 +79,6 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     const int64_t nclusters = gridDim.x / csize;
     const int64_t nvec = N / VEC;
     const int64_t u0 = (int64_t)rank * slice;
-    const int64_t u1 = (u0 + slice < nvec) ? u0 + slice : nvec;
     const int npairs = csize * NW;
     const bool send = !(flags & kFlagNoCopy);  // test hook: send nothing, every wait expires
 
@@ -90,18 +98,39 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
         const int p = (int)(it & 1);
         const uint32_t phase = (uint32_t)((it >> 1) & 1);
         const T* rin = in + r * ld_in;
+        // The row's vectors start `head` elements in; `nvb` of them, then
+        // `extra` = head + tail single elements.
+        int head = 0, extra = 0;
+        int64_t nvb = nvec;
+        if constexpr (SHIFTED) {
+            const int off = (int)((reinterpret_cast<uintptr_t>(rin) & 15u) / sizeof(T));
+            head = off ? VEC - off : 0;
+            if (head > N) head = (int)N;
+            nvb = (N - head) / VEC;
+            extra = (int)(N - nvb * VEC);
+        }
+        const T* rbody = rin + head;
+        const int64_t u1 = (u0 + slice < nvb) ? u0 + slice : nvb;
         uint4 raw[KV];
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int64_t idx = u0 + tid + NT * k;
-            if (FULL || idx < u1) raw[k] = ldg_stream(rin + idx * VEC);
+            if (FULL || idx < u1) raw[k] = ldg_stream(rbody + idx * VEC);
+        }
+        float xe = neg_inf();  // this thread's head or tail element, if any
+        int64_t ce = -1;
+        if constexpr (SHIFTED) {
+            if (rank == 0 && tid < extra) {
+                ce = tid < head ? tid : head + nvb * VEC + (tid - head);
+                xe = Elem<T>::load1(rin + ce);
+            }
         }
         // Warp partial (m_w, s_w): max, then sum of exp(x - m_w).
         VecMax<T> vm;
 #pragma unroll
         for (int k = 0; k < KV; ++k)
             if (FULL || u0 + tid + NT * k < u1) vm.add(raw[k]);
-        const float m_w = warp_max(vm.get());
+        const float m_w = warp_max(fmaxf(vm.get(), xe));
         const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
         const float shift_l2 = shift * kLog2e;
         float sa = 0.0f, sb = 0.0f;
@@ -117,6 +146,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
                 }
             }
         }
+        if (SHIFTED && ce >= 0) sa += exp_shifted<T>(xe, shift, shift_l2);
         const float s_w = warp_sum(sa + sb);
         if (!started) {
             cluster_wait();
@@ -144,6 +174,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
         }
         const float Sr = warp_sum(sloc);
         T* rout = out + r * ld_out;
+        T* obody = rout + head;
         if constexpr (Elem<T>::kAccurateExp) {
             // FP32 data: exp of the exact difference, times the rounded 1/S.
             const float rs = final_rcp(Mr, Sr);
@@ -155,9 +186,10 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
                     unpack_again<T>(raw[k], f);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) f[e] = expf(f[e] - Mr) * rs;
-                    stg_stream(rout + idx * VEC, Elem<T>::pack(f));
+                    stg_stream(obody + idx * VEC, Elem<T>::pack(f));
                 }
             }
+            if (SHIFTED && ce >= 0) Elem<T>::store1(rout + ce, expf(xe - Mr) * rs);
         } else {
             // 16-bit data: 1/S folded into the exponent,
             // y = 2^(x log2(e) - (M log2(e) + log2(S))), one FMA and one ex2 per
@@ -171,9 +203,10 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
                     unpack_again<T>(raw[k], f);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
-                    stg_stream(rout + idx * VEC, Elem<T>::pack(f));
+                    stg_stream(obody + idx * VEC, Elem<T>::pack(f));
                 }
             }
+            if (SHIFTED && ce >= 0) Elem<T>::store1(rout + ce, ex2_approx(fmaf(xe, kLog2e, -c)));
         }
     }
     if (!started) cluster_wait();
@@ -185,9 +218,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     }
 }
 
-template <typename T, int KV, bool FULL>
+template <typename T, int KV, int MODE>
 cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
-    auto kern = wide_rows_kernel<T, KV, FULL>;
+    auto kern = wide_rows_kernel<T, KV, MODE>;
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = ensure_smem_limit(fn, 0, csize > 8);
     if (e != cudaSuccess) return e;
@@ -219,20 +252,28 @@ cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
     return cudaGetLastError();
 }
 
+template <typename T, int KV>
+cudaError_t launch_mode(const Problem& p, const WideShape& sh, int mode) {
+    switch (mode) {
+        case kAligned: return launch_kv<T, KV, kAligned>(p, sh.csize, sh.slice);
+        case kFull: return launch_kv<T, KV, kFull>(p, sh.csize, sh.slice);
+        case kShifted: return launch_kv<T, KV, kShifted>(p, sh.csize, sh.slice);
+    }
+    return cudaErrorInvalidValue;
+}
+
 template <typename T>
 cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     const int64_t nvec = p.N / Elem<T>::kVec;
-    const bool full = sh.slice == (int64_t)kWideThreads * sh.kv && nvec == sh.slice * sh.csize;
+    int mode = kShifted;
+    if (rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype))
+        mode = (sh.slice == (int64_t)kWideThreads * sh.kv && nvec == sh.slice * sh.csize) ? kFull
+                                                                                          : kAligned;
     switch (sh.kv) {
-        case 2:
-            return full ? launch_kv<T, 2, true>(p, sh.csize, sh.slice)
-                        : launch_kv<T, 2, false>(p, sh.csize, sh.slice);
-        case 4:
-            return full ? launch_kv<T, 4, true>(p, sh.csize, sh.slice)
-                        : launch_kv<T, 4, false>(p, sh.csize, sh.slice);
-        case 8:
-            return full ? launch_kv<T, 8, true>(p, sh.csize, sh.slice)
-                        : launch_kv<T, 8, false>(p, sh.csize, sh.slice);
+        case 1: return launch_mode<T, 1>(p, sh, mode);
+        case 2: return launch_mode<T, 2>(p, sh, mode);
+        case 4: return launch_mode<T, 4>(p, sh, mode);
+        case 8: return launch_mode<T, 8>(p, sh, mode);
     }
     return cudaErrorInvalidValue;
 }
@@ -241,26 +282,40 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
 
 // Shape (host logic): clusters of 2..16 blocks of 256 threads; the smallest
 // power-of-two cluster whose slices give each thread at most SR_WIDE_KV
-// vectors, the vectors per thread rounded up to 2, 4 or 8. Rows up to
-// 16 x 256 x 8 vectors (512 KiB) fit.
-bool wide_shape(int64_t N, int dtype, WideShape* out) {
+// vectors. While there are too few rows to give every SM two blocks, the
+// cluster doubles (up to 8: larger clusters are scheduled poorly) as long as
+// each thread keeps at least one vector. The vectors per thread are rounded
+// up to 1, 2, 4 or 8. Rows up to 16 x 256 x 8 vectors (512 KiB) fit.
+bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
     const int64_t nvec = N * elem_bytes(dtype) / 16;
     for (int c = 2; c <= kMaxCluster; c *= 2) {
+        if ((nvec + c - 1) / c > (int64_t)kWideThreads * SR_WIDE_KV) continue;
+        while (c < 8 && M * c < 2 * (int64_t)sm_count && nvec / (2 * c) >= kWideThreads) c *= 2;
         const int64_t per = (nvec + c - 1) / c;
-        if (per <= (int64_t)kWideThreads * SR_WIDE_KV) {
-            const int64_t kv = (per + kWideThreads - 1) / kWideThreads;
-            out->csize = c;
-            out->slice = per;
-            out->kv = kv <= 2 ? 2 : kv <= 4 ? 4 : 8;
-            return true;
-        }
+        const int64_t kv = (per + kWideThreads - 1) / kWideThreads;
+        out->csize = c;
+        out->slice = per;
+        out->kv = kv <= 1 ? 1 : kv <= 2 ? 2 : kv <= 4 ? 4 : 8;
+        return true;
     }
     return false;
 }
 
+// Whether the WIDE plan takes these rows: aligned, or sharing their offset
+// from a 16-byte boundary (input and output), and at most 512 KiB.
+bool wide_fits(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
+               int dtype) {
+    WideShape sh;
+    if (!wide_shape(1, N, dtype, 0, &sh)) return false;
+    if (rows_vector_aligned(in, out, N, ld_in, ld_out, dtype)) return true;
+    const int64_t es = elem_bytes(dtype);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
+    return a % 16 == b % 16 && a % es == 0 && (ld_in * es) % 16 == (ld_out * es) % 16;
+}
+
 cudaError_t launch_wide(const Problem& p) {
     WideShape sh;
-    if (!wide_shape(p.N, p.dtype, &sh)) return cudaErrorInvalidValue;
+    if (!wide_shape(p.M, p.N, p.dtype, p.dev->sm_count, &sh)) return cudaErrorInvalidValue;
     switch (p.dtype) {
         case kF32: return launch_typed<float>(p, sh);
         case kBF16: return launch_typed<__nv_bfloat16>(p, sh);

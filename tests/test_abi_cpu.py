@@ -96,6 +96,11 @@ def test_plan_depends_on_alignment_and_width(lib):
     assert P(A, B, 10, 1020, 1020, 1020, 0) == sr.SR_PLAN_WARP         # 255 vectors
     assert P(A + 4, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_ONLINE   # misaligned input
     assert P(A, B, 10, 4096, 4097, 4096, 0) == sr.SR_PLAN_ONLINE       # odd pitch
+    # Rows that share their offset from a 16-byte boundary (odd widths, equal
+    # pitches, or bases equally misaligned): WIDE reads them as shifted vectors.
+    assert P(A, B, 4, 32769, 32769, 32769, 2) == sr.SR_PLAN_WIDE
+    assert P(A + 4, B + 4, 10, 4096, 4097, 4097, 0) == sr.SR_PLAN_WIDE
+    assert P(A + 2, B + 4, 10, 4096, 4096, 4096, 2) == sr.SR_PLAN_ONLINE  # not congruent
     assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_ROW          # 32 KiB rows
     assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_WIDE         # just over 32 KiB
     assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_WIDE   # 512 KiB bf16

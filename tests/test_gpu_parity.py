@@ -122,6 +122,32 @@ def test_full_size_forced_wide_plans(name, plan):
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
 
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
+@pytest.mark.parametrize("N,M", [(2049, 37), (4097, 64), (32769, 4), (40000, 3), (131071, 2)])
+def test_wide_shifted_rows(dtype, N, M):
+    """Odd widths with equal pitches, and views starting k elements past a
+    16-byte boundary: the WIDE plan reads them as shifted vectors."""
+    vec = 4 if dtype == synth.F32 else 8
+    x = synth.generate(M + 1, N, dtype=dtype, seed=N + M, p1=2.5)
+    base = gu.to_device(x.reshape(-1), dtype)
+    for k in (0, 1, vec - 1):
+        xd = base[k:]
+        yb = torch.full(((M + 1) * N,), float("nan"), dtype=gu.torch_dtype(dtype), device="cuda")
+        yd = yb[k:]
+        for plan in (sr.SR_PLAN_WIDE, sr.SR_PLAN_AUTO):
+            assert sr.softmax_rows_plan_check(xd, yd, M, N, N, N, dtype, plan) == sr.SR_PLAN_WIDE
+            yb.fill_(float("nan"))
+            st = sr.load().softmax_rows_ex(xd.data_ptr(), yd.data_ptr(), M, N, N, N, dtype, plan,
+                                           torch.cuda.current_stream().cuda_stream)
+            assert st == sr.SR_OK
+            torch.cuda.synchronize()
+            got = gu.to_host(yd[:M * N].reshape(M, N), dtype)
+            xs = gu.to_host(xd[:M * N].reshape(M, N), dtype)
+            gu.check_rows(got, xs, N, N, dtype, "shifted N=%d k=%d" % (N, k))
+            # Nothing written outside the M rows.
+            assert torch.isnan(yb[:k]).all() and torch.isnan(yd[M * N:]).all()
+
+
 # ---- edge shapes: widths around every plan boundary, odd row counts ----
 
 EDGE_N = [1, 2, 3, 7, 31, 33, 127, 255, 1000, 2047, 2048, 2049, 4095, 4104, 8192, 8193, 16384,
