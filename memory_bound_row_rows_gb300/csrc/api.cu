@@ -162,6 +162,15 @@ int check_args(const void* in, const void* out, int64_t M, int64_t N, int64_t ld
     return 0;
 }
 
+// True when the rows of `in` and `out` sit at the same offset from a 16-byte
+// boundary (the same base offset, pitches equal modulo 16 bytes) on element
+// boundaries: such rows are read as a head, 16-byte vectors and a tail.
+bool rows_congruent(const void* in, const void* out, int64_t ld_in, int64_t ld_out, int dtype) {
+    const int64_t es = elem_bytes(dtype);
+    const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
+    return a % 16 == b % 16 && a % es == 0 && (ld_in * es) % 16 == (ld_out * es) % 16;
+}
+
 // Whether a plan can run the arguments (host logic only).
 bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_in,
                int64_t ld_out, int dtype) {
@@ -173,7 +182,8 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
         case SR_PLAN_CLUSTER: return vec && cluster_size_for(N, dtype, 2) > 0;
         case SR_PLAN_ONLINE: return true;
         case SR_PLAN_SMEM: return vec && row_bytes <= kSmemMaxRowBytes;
-        case SR_PLAN_ROW: return vec && row_plan_fits(N, dtype);
+        case SR_PLAN_ROW: return (vec || rows_congruent(in, out, ld_in, ld_out, dtype)) &&
+                                 row_plan_fits(N, dtype);
         case SR_PLAN_WIDE: return wide_fits(in, out, N, ld_in, ld_out, dtype);
     }
     return false;
@@ -189,7 +199,9 @@ int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64
                 int dtype) {
     const bool vec = rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
     const int64_t nvec = N * elem_bytes(dtype) / 16;
-    if (vec && nvec >= kRowMinVectors && row_plan_fits(N, dtype)) return SR_PLAN_ROW;
+    if ((vec || rows_congruent(in, out, ld_in, ld_out, dtype)) && nvec >= kRowMinVectors &&
+        row_plan_fits(N, dtype))
+        return SR_PLAN_ROW;
     if (N <= kWarpMaxN) return SR_PLAN_WARP;
     if (plan_fits(SR_PLAN_WIDE, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_WIDE;
     if (plan_fits(SR_PLAN_CLUSTER, in, out, N, ld_in, ld_out, dtype)) return SR_PLAN_CLUSTER;
@@ -226,7 +238,9 @@ int run(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t 
 // Plans that take a row mask, and the automatic choice among them.
 bool masked_plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_in,
                       int64_t ld_out, int dtype) {
-    return plan == SR_PLAN_WARP || plan == SR_PLAN_ROW || plan == SR_PLAN_ONLINE
+    if (plan == SR_PLAN_ROW)  // the masked ROW kernel reads aligned rows only
+        return rows_vector_aligned(in, out, N, ld_in, ld_out, dtype) && row_plan_fits(N, dtype);
+    return plan == SR_PLAN_WARP || plan == SR_PLAN_ONLINE
                ? plan_fits(plan, in, out, N, ld_in, ld_out, dtype)
                : false;
 }
@@ -234,6 +248,8 @@ bool masked_plan_fits(int plan, const void* in, const void* out, int64_t N, int6
 int choose_masked_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
                        int dtype) {
     const int plan = choose_plan(in, out, N, ld_in, ld_out, dtype);
+    if (plan == SR_PLAN_ROW && !rows_vector_aligned(in, out, N, ld_in, ld_out, dtype))
+        return N <= kWarpMaxN ? SR_PLAN_WARP : SR_PLAN_ONLINE;
     return (plan == SR_PLAN_ROW || plan == SR_PLAN_WARP) ? plan : SR_PLAN_ONLINE;
 }
 

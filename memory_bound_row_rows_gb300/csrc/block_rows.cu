@@ -28,7 +28,11 @@ constexpr int kRowMaxKV = 8;
 namespace sr {
 namespace {
 
-template <typename T, int NT, int KV, bool MASKED>
+// SHIFTED (unmasked only): the input and output rows share their offset from
+// a 16-byte boundary but are not aligned; each row is a head of fewer than
+// VEC elements, 16-byte vectors and a tail of fewer than VEC elements, and the
+// first threads of the block take the head and tail elements one each.
+template <typename T, int NT, int KV, bool MASKED, bool SHIFTED = false>
 __global__ void __launch_bounds__(NT)
     block_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                       int64_t ld_in, int64_t ld_out, RowMask mask) {
@@ -36,10 +40,27 @@ __global__ void __launch_bounds__(NT)
     constexpr int NW = NT / 32;
     __shared__ float red_m[NW], red_s[NW];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nvec = (int)(N / VEC);
+    static_assert(!(MASKED && SHIFTED), "masked rows are aligned");
 
     for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
-        const T* rin = in + r * ld_in;
+        const T* rin0 = in + r * ld_in;
+        int head = 0;
+        if constexpr (SHIFTED) {
+            const int off = (int)((reinterpret_cast<uintptr_t>(rin0) & 15u) / sizeof(T));
+            head = off ? VEC - off : 0;
+            if (head > N) head = (int)N;
+        }
+        const T* rin = rin0 + head;  // the row's first 16-byte boundary
+        const int nvec = (int)((N - head) / VEC);
+        const int extra = (int)(N - (int64_t)nvec * VEC);  // head + tail elements
+        float xe = neg_inf();
+        int ce = -1;
+        if constexpr (SHIFTED) {
+            if (tid < extra) {
+                ce = tid < head ? tid : head + nvec * VEC + (tid - head);
+                xe = Elem<T>::load1(rin0 + ce);
+            }
+        }
         // Masked rows read only the vectors that hold valid entries (rows of
         // this plan are short enough for 32-bit element counts).
         const int valid = MASKED ? (int)mask.valid(r, N) : 0;
@@ -65,6 +86,7 @@ __global__ void __launch_bounds__(NT)
         for (int k = 0; k < KV; ++k)
 #pragma unroll
             for (int e = 0; e < VEC; ++e) mx = fmaxf(mx, v[k][e]);
+        if constexpr (SHIFTED) mx = fmaxf(mx, xe);
         mx = warp_max(mx);
         if (lane == 0) red_m[warp] = mx;
         __syncthreads();
@@ -87,6 +109,10 @@ __global__ void __launch_bounds__(NT)
         for (int w = VEC / 2; w > 0; w >>= 1)
 #pragma unroll
             for (int e = 0; e < w; ++e) sv[e] += sv[e + w];
+        if constexpr (SHIFTED) {
+            xe = exp_shifted<T>(xe, m, m_l2);  // 0 for a thread without an element
+            sv[0] += xe;
+        }
         const float sw = warp_sum(sv[0]);
         if (lane == 0) red_s[warp] = sw;
         __syncthreads();
@@ -95,7 +121,8 @@ __global__ void __launch_bounds__(NT)
         for (int w = 1; w < NW; ++w) s += red_s[w];
         const float rs = __frcp_rn(s);
 
-        T* rout = out + r * ld_out;
+        T* rout0 = out + r * ld_out;
+        T* rout = rout0 + head;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
             const int idx = tid + NT * k;
@@ -105,6 +132,9 @@ __global__ void __launch_bounds__(NT)
                 for (int e = 0; e < VEC; ++e) y[e] = v[k][e] * rs;
                 stg_stream(rout + (int64_t)idx * VEC, Elem<T>::pack(y));
             }
+        }
+        if constexpr (SHIFTED) {
+            if (ce >= 0) Elem<T>::store1(rout0 + ce, xe * rs);
         }
     }
 }
@@ -124,6 +154,8 @@ cudaError_t launch_grid(void (*kern)(const T*, T*, int64_t, int64_t, int64_t, in
 template <typename T, int NT, int KV>
 cudaError_t launch_nt_kv(const Problem& p) {
     if (p.mask.active()) return launch_grid(block_rows_kernel<T, NT, KV, true>, NT, p);
+    if (!rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype))
+        return launch_grid(block_rows_kernel<T, NT, KV, false, true>, NT, p);
     return launch_grid(block_rows_kernel<T, NT, KV, false>, NT, p);
 }
 

@@ -97,9 +97,12 @@ def test_plan_depends_on_alignment_and_width(lib):
     assert P(A + 4, B, 10, 4096, 4096, 4096, 0) == sr.SR_PLAN_ONLINE   # misaligned input
     assert P(A, B, 10, 4096, 4097, 4096, 0) == sr.SR_PLAN_ONLINE       # odd pitch
     # Rows that share their offset from a 16-byte boundary (odd widths, equal
-    # pitches, or bases equally misaligned): WIDE reads them as shifted vectors.
+    # pitches, or bases equally misaligned) are read as shifted vectors: ROW up
+    # to 32 KiB, WIDE beyond.
     assert P(A, B, 4, 32769, 32769, 32769, 2) == sr.SR_PLAN_WIDE
-    assert P(A + 4, B + 4, 10, 4096, 4097, 4097, 0) == sr.SR_PLAN_WIDE
+    assert P(A + 4, B + 4, 10, 4096, 4097, 4097, 0) == sr.SR_PLAN_ROW
+    assert P(A, B, 10, 4097, 4097, 4097, 2) == sr.SR_PLAN_ROW
+    assert P(A + 4, B + 4, 10, 40000, 40001, 40001, 0) == sr.SR_PLAN_WIDE
     assert P(A + 2, B + 4, 10, 4096, 4096, 4096, 2) == sr.SR_PLAN_ONLINE  # not congruent
     assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_ROW          # 32 KiB rows
     assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_WIDE         # just over 32 KiB
@@ -134,6 +137,7 @@ def test_forced_plan_checks(lib):
     assert C(A, B, 5, 16384, 16384, 16384, 1, sr.SR_PLAN_ROW) == sr.SR_PLAN_ROW
     assert C(A, B, 5, 16392, 16392, 16392, 1, sr.SR_PLAN_ROW) == -sr.SR_EPLAN
     assert C(A + 2, B, 5, 4096, 4096, 4096, 1, sr.SR_PLAN_ROW) == -sr.SR_EPLAN
+    assert C(A + 2, B + 2, 5, 4096, 4096, 4096, 1, sr.SR_PLAN_ROW) == sr.SR_PLAN_ROW  # shifted
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):
