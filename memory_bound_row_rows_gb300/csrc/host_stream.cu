@@ -117,10 +117,9 @@ int run_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,
 
     char* base = static_cast<char*>(d_work);
     const int64_t slot_bytes = rows * row_bytes;
-    cudaError_t e;
-    if ((e = cudaEventRecord(p->start, stream)) || (e = cudaStreamWaitEvent(p->s_in, p->start, 0)) ||
-        (e = cudaStreamWaitEvent(p->s_run, p->start, 0)) ||
-        (e = cudaStreamWaitEvent(p->s_out, p->start, 0)))
+    if (cudaEventRecord(p->start, stream) || cudaStreamWaitEvent(p->s_in, p->start, 0) ||
+        cudaStreamWaitEvent(p->s_run, p->start, 0) ||
+        cudaStreamWaitEvent(p->s_out, p->start, 0))
         return SR_ECUDA;
 
     for (int64_t c = 0; c < nchunks; ++c) {
@@ -132,22 +131,22 @@ int run_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,
         const char* src = static_cast<const char*>(h_in) + r0 * ld_in * es;
         char* dst = static_cast<char*>(h_out) + r0 * ld_out * es;
         // Copy in once the slot's previous chunk has been copied out.
-        if (c >= slots && (e = cudaStreamWaitEvent(p->s_in, p->copied_out[k], 0))) return SR_ECUDA;
-        if ((e = copy_rows(d_in, ldd, src, ld_in, N, nr, dtype, cudaMemcpyHostToDevice, p->s_in)) ||
-            (e = cudaEventRecord(p->copied_in[k], p->s_in)))
+        if (c >= slots && cudaStreamWaitEvent(p->s_in, p->copied_out[k], 0)) return SR_ECUDA;
+        if (copy_rows(d_in, ldd, src, ld_in, N, nr, dtype, cudaMemcpyHostToDevice, p->s_in) ||
+            cudaEventRecord(p->copied_in[k], p->s_in))
             return SR_ECUDA;
         // Compute.
-        if ((e = cudaStreamWaitEvent(p->s_run, p->copied_in[k], 0))) return SR_ECUDA;
+        if (cudaStreamWaitEvent(p->s_run, p->copied_in[k], 0)) return SR_ECUDA;
         const int st = launch(d_in, d_out, nr, N, ldd, ldd, dtype, p->s_run);
         if (st != SR_OK) return st;
-        if ((e = cudaEventRecord(p->computed[k], p->s_run))) return SR_ECUDA;
+        if (cudaEventRecord(p->computed[k], p->s_run)) return SR_ECUDA;
         // Copy out.
-        if ((e = cudaStreamWaitEvent(p->s_out, p->computed[k], 0)) ||
-            (e = copy_rows(dst, ld_out, d_out, ldd, N, nr, dtype, cudaMemcpyDeviceToHost, p->s_out)) ||
-            (e = cudaEventRecord(p->copied_out[k], p->s_out)))
+        if (cudaStreamWaitEvent(p->s_out, p->computed[k], 0) ||
+            copy_rows(dst, ld_out, d_out, ldd, N, nr, dtype, cudaMemcpyDeviceToHost, p->s_out) ||
+            cudaEventRecord(p->copied_out[k], p->s_out))
             return SR_ECUDA;
     }
-    if ((e = cudaEventRecord(p->done, p->s_out)) || (e = cudaStreamWaitEvent(stream, p->done, 0)))
+    if (cudaEventRecord(p->done, p->s_out) || cudaStreamWaitEvent(stream, p->done, 0))
         return SR_ECUDA;
     return SR_OK;
 }
