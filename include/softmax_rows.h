@@ -189,7 +189,9 @@ SR_API int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N
  * input over the host link and stores the output back, with no staging copies
  * and no workspace. Each pointer is checked with cudaPointerGetAttributes
  * before anything is launched; memory the device cannot address is refused
- * with SR_EINVAL. The plan is chosen as for softmax_rows. Asynchronous on
+ * with SR_EINVAL. The host link bounds every plan here. Matrices of at
+ * least 8 MiB whose rows the WIDE plan takes run on WIDE, which keeps the link
+ * busiest. Other matrices get the plan softmax_rows would choose. Asynchronous on
  * `stream`: synchronise it before reading h_out. Returns like softmax_rows.
  */
 SR_API int softmax_rows_host_mapped(const void* h_in, void* h_out, int64_t M, int64_t N,

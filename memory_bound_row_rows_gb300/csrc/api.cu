@@ -334,6 +334,23 @@ int pair_plan_query(const rp::Args& a, int plan, int sm_count) {
     return resolve_pair_plan(a, plan, sm_count, &sh);
 }
 
+// Plan for matrices read and written over the host link. There every plan is
+// bound by the link (about 210 GB/s host-to-device and 193 GB/s back, 340 GB/s
+// both at once, the same as the copy engines). With both matrices on the host,
+// one cluster per row comes closest to that. Measured on GB300 against the
+// device plans: 325 vs 290 GB/s on f32 4096 x 4096, 301 vs 239 GB/s on bf16
+// 16384 x 1000, and 342 vs 333 GB/s on f16 65536 x 2048. Below a few MiB the
+// call is launch-bound and the device choice stays.
+constexpr int64_t kMappedWideMinBytes = 8ll << 20;
+
+int mapped_plan(const void* in, const void* out, int64_t M, int64_t N, int64_t ld_in,
+                int64_t ld_out, int dtype) {
+    if (M * N * elem_bytes(dtype) >= kMappedWideMinBytes &&
+        plan_fits(SR_PLAN_WIDE, in, out, N, ld_in, ld_out, dtype))
+        return SR_PLAN_WIDE;
+    return SR_PLAN_AUTO;
+}
+
 int launch_auto(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype, cudaStream_t stream) {
     return run(in, out, M, N, ld_in, ld_out, dtype, SR_PLAN_AUTO, stream, kDefaultTimeoutNs, 0);
@@ -480,7 +497,9 @@ int softmax_rows_host_mapped(const void* h_in, void* h_out, int64_t M, int64_t N
             return SR_EINVAL;
         dptr[i] = at.devicePointer;
     }
-    return sr::launch_auto(dptr[0], dptr[1], M, N, ld_in, ld_out, dtype, (cudaStream_t)stream);
+    return sr::run(dptr[0], dptr[1], M, N, ld_in, ld_out, dtype,
+                   sr::mapped_plan(dptr[0], dptr[1], M, N, ld_in, ld_out, dtype),
+                   (cudaStream_t)stream, sr::kDefaultTimeoutNs, 0);
 }
 
 int softmax_rows_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in,

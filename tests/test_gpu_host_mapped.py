@@ -12,7 +12,10 @@ torch = pytest.importorskip("torch")
 
 @pytest.mark.parametrize("name,rows", [("f32_4096x4096", 64), ("bf16_16384x1000_ld1024", 300),
                                        ("bf16_1024x131072", 6), ("f16_causal_524288x2048", 300),
-                                       ("f32_1024x256", 1024)])
+                                       ("f32_1024x256", 1024),
+                                       # 8 MiB and more: these run on the WIDE plan
+                                       ("f32_4096x4096", 1024), ("bf16_16384x1000_ld1024", 8192),
+                                       ("f16_causal_524288x2048", 4096)])
 def test_mapped_matches_oracle(name, rows):
     w = synth.WORKLOADS[name].with_rows(rows)
     x = w.generate()
