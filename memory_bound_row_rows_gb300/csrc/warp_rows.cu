@@ -11,7 +11,8 @@
 //
 // Aligned rows without a mask take a packed variant (warp_packed_kernel):
 // the row stays in registers as packed 16-byte vectors and the exponential is
-// computed twice, which doubles the rows in flight per SM.
+// computed twice, which doubles the rows in flight per SM. Its rows of at most
+// 64 vectors are taken by 8 or 16 lanes each (two or four rows per warp).
 //
 // Lane l owns 16-byte vectors l, l+32, ..., so every load and store
 // instruction of a warp covers 512 contiguous bytes. A row of up to
@@ -129,39 +130,68 @@ __global__ void __launch_bounds__(kWarpBlock)
     }
 }
 
+// Resident blocks per SM the packed variant with 8 vectors per lane is
+// compiled for (64 registers at 4).
+#ifndef SR_WARP_PACKED_MIN_BLOCKS_KV8
+#define SR_WARP_PACKED_MIN_BLOCKS_KV8 4
+#endif
+
+// Butterfly max / sum over aligned groups of W lanes (W = 32: the whole warp,
+// in the same order as warp_max / warp_sum).
+template <int W>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+template <int W>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
 // Packed variant for aligned, unmasked rows: the row stays in registers as
 // packed 16-byte vectors (4 registers per 16 bytes instead of one per element
 // for 16-bit data), so about twice as many rows are in flight per SM; the
 // exponential is computed twice, once for the sum and once for the output
 // (16-bit data: 1/S folded into the exponent, one FMA and one ex2 per element),
-// and the result is still rounded once, from FP32.
-template <typename T, int KV>
-__global__ void __launch_bounds__(kWarpBlock, KV <= 4 ? SR_WARP_PACKED_MIN_BLOCKS : 2)
+// and the result is still rounded once, from FP32. LPR lanes take a row; the
+// row loop is uniform over the warp so that every lane joins the shuffles.
+template <typename T, int KV, int LPR>
+__global__ void __launch_bounds__(kWarpBlock, KV <= 4   ? SR_WARP_PACKED_MIN_BLOCKS
+                                              : KV == 8 ? SR_WARP_PACKED_MIN_BLOCKS_KV8
+                                                        : 2)
     warp_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
                        int64_t ld_in, int64_t ld_out) {
     constexpr int VEC = Elem<T>::kVec;
+    constexpr int RPW = 32 / LPR;  // rows per warp
     const int lane = threadIdx.x & 31;
-    const int64_t first = ((int64_t)blockIdx.x * kWarpBlock + threadIdx.x) >> 5;
-    const int64_t stride = ((int64_t)gridDim.x * kWarpBlock) >> 5;
+    const int sub = lane & (LPR - 1);
+    const int64_t wfirst = ((int64_t)blockIdx.x * kWarpBlock + threadIdx.x) >> 5;
+    const int64_t wstride = ((int64_t)gridDim.x * kWarpBlock) >> 5;
     const int nvec = N / VEC;
-    for (int64_t r = first; r < M; r += stride) {
-        const T* rin = in + r * ld_in;
+    for (int64_t w = wfirst; w * RPW < M; w += wstride) {
+        const int64_t r = w * RPW + lane / LPR;
+        const bool live = r < M;
+        const T* rin = in + (live ? r : 0) * ld_in;
         uint4 raw[KV];
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-            const int idx = lane + 32 * k;
-            if (idx < nvec) raw[k] = ldg_stream(rin + (int64_t)idx * VEC);
+            const int idx = sub + LPR * k;
+            if (live && idx < nvec) raw[k] = ldg_stream(rin + (int64_t)idx * VEC);
         }
         VecMax<T> vm;
 #pragma unroll
         for (int k = 0; k < KV; ++k)
-            if (lane + 32 * k < nvec) vm.add(raw[k]);
-        const float m = warp_max(vm.get());
+            if (live && sub + LPR * k < nvec) vm.add(raw[k]);
+        const float m = group_max<LPR>(vm.get());
         const float m_l2 = m * kLog2e;
         float sa = 0.0f, sb = 0.0f;
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
-            if (lane + 32 * k < nvec) {
+            if (live && sub + LPR * k < nvec) {
                 float f[VEC];
                 Elem<T>::unpack(raw[k], f);
 #pragma unroll
@@ -171,13 +201,14 @@ __global__ void __launch_bounds__(kWarpBlock, KV <= 4 ? SR_WARP_PACKED_MIN_BLOCK
                 }
             }
         }
-        const float s = warp_sum(sa + sb);
+        const float s = group_sum<LPR>(sa + sb);
+        if (!live) continue;
         T* rout = out + r * ld_out;
         if constexpr (Elem<T>::kAccurateExp) {
             const float rs = __frcp_rn(s);
 #pragma unroll
             for (int k = 0; k < KV; ++k) {
-                const int idx = lane + 32 * k;
+                const int idx = sub + LPR * k;
                 if (idx < nvec) {
                     float f[VEC];
                     unpack_again<T>(raw[k], f);
@@ -192,7 +223,7 @@ __global__ void __launch_bounds__(kWarpBlock, KV <= 4 ? SR_WARP_PACKED_MIN_BLOCK
             const float c = fmaf(m, kLog2e, lg2_approx(s));
 #pragma unroll
             for (int k = 0; k < KV; ++k) {
-                const int idx = lane + 32 * k;
+                const int idx = sub + LPR * k;
                 if (idx < nvec) {
                     float f[VEC];
                     unpack_again<T>(raw[k], f);
@@ -205,18 +236,35 @@ __global__ void __launch_bounds__(kWarpBlock, KV <= 4 ? SR_WARP_PACKED_MIN_BLOCK
     }
 }
 
-// One warp per row and no row loop (measured faster than the persistent grid
-// for this variant: the hardware hands out rows as blocks retire).
-template <typename T, int KV>
-cudaError_t launch_packed(const Problem& p) {
-    auto kern = warp_packed_kernel<T, KV>;
-    const int64_t warps_per_block = kWarpBlock / 32;
-    const int64_t need = (p.M + warps_per_block - 1) / warps_per_block;
+template <typename T, int KV, int LPR>
+cudaError_t launch_packed_lpr(const Problem& p) {
+    auto kern = warp_packed_kernel<T, KV * 32 / LPR, LPR>;
+    const int64_t rows_per_block = kWarpBlock / LPR;
+    const int64_t need = (p.M + rows_per_block - 1) / rows_per_block;
     const int64_t cap = 0x7fffffff;
     const unsigned grid = (unsigned)(need < cap ? need : cap);
     kern<<<grid, kWarpBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
                                             p.M, (int)p.N, p.ld_in, p.ld_out);
     return cudaGetLastError();
+}
+
+// No row loop: the hardware hands out rows as blocks retire (measured faster
+// than a persistent grid for this variant). KV counts the vectors a lane
+// holds when 32 lanes take a row. Rows of at most 64 vectors are shared by
+// fewer lanes, so that each lane holds 4 vectors and every SM has more rows
+// in flight. This needs rows enough for 4 blocks per SM at the narrower
+// layout. Measured on GB300, cold L2: bf16 131072 x 256 went from 27.5 to
+// 20.7 µs with 8 lanes per row.
+template <typename T, int KV>
+cudaError_t launch_packed(const Problem& p) {
+    const int64_t min_blocks = 4 * (int64_t)p.dev->sm_count;
+    if constexpr (KV == 1) {
+        if (p.M >= min_blocks * (kWarpBlock / 8)) return launch_packed_lpr<T, 1, 8>(p);
+    }
+    if constexpr (KV == 2) {
+        if (p.M >= min_blocks * (kWarpBlock / 16)) return launch_packed_lpr<T, 2, 16>(p);
+    }
+    return launch_packed_lpr<T, KV, 32>(p);
 }
 
 template <typename T, int VEC, int KV, bool MASKED>

@@ -250,6 +250,38 @@ def test_special_rows(dtype, N):
         assert g[6][-1] == 1.0 and np.all(g[6][:-1] == 0.0)
 
 
+# ---- many short rows: the WARP plan's shared-lane layouts ----
+
+# Rows of at most 64 vectors with rows enough for 4 blocks per SM are taken by
+# 8 lanes (<= 32 vectors) or 16 lanes (<= 64 vectors) each. The row counts are
+# ragged, so the last warp holds row groups past M, and the widths leave lanes
+# of a group without a vector. Special rows sit at both ends of the matrix.
+@pytest.mark.parametrize("dtype,M,N", [(synth.BF16, 20003, 256), (synth.F32, 20003, 128),
+                                       (synth.BF16, 20001, 40), (synth.F16, 9999, 512),
+                                       (synth.F32, 9731, 200), (synth.F16, 300, 512)],
+                         ids=lambda v: str(v))
+def test_short_rows_shared_lanes(dtype, M, N):
+    from tests import pins
+    w = synth.Workload("short", dtype, M, N, N, N, 21, synth.DIST_NORMAL, 0.0, 1.0)
+    x = w.generate()
+    sp = pins.encode_exact(special_rows(N, dtype), dtype)
+    k = sp.shape[0]
+    x[:k] = sp
+    x[M - k:] = sp
+    xd = gu.to_device(x, dtype)
+    for plan in (sr.SR_PLAN_AUTO, sr.SR_PLAN_WARP):
+        assert sr.softmax_rows_plan(xd, xd, M, N, N, N, dtype) == sr.SR_PLAN_WARP
+        st, y = run_plan(xd, M, N, N, N, dtype, plan)
+        assert st == sr.SR_OK
+        torch.cuda.synchronize()
+        out = gu.to_host(y, dtype)
+        gu.check_rows(out, x, N, N, dtype, "short rows %dx%d plan %s" % (M, N, sr.PLAN_NAMES[plan]))
+        g = synth.storage_to_float64(out, dtype)
+        assert np.isnan(g[0]).all() and np.isnan(g[M - k]).all()
+        assert g[k - 2][-1] == 1.0 and g[M - 2][-1] == 1.0
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
 # ---- in place, canaries, streams, empty and rejected calls ----
 
 @pytest.mark.parametrize("name", ["f32_4096x4096", "bf16_16384x1000_ld1024", "bf16_1024x131072",
