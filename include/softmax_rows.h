@@ -69,9 +69,11 @@ enum sr_status {
 };
 
 /*
- * Kernel plans. AUTO picks by row width, dtype and alignment: ROW for
- * aligned rows of 4 KiB to 32 KiB, WARP for shorter rows, WIDE for aligned
- * rows up to 512 KiB, ONLINE otherwise. Every plan computes the same
+ * Kernel plans. AUTO picks by row width, dtype and alignment. It takes ROW
+ * for rows of 256 16-byte vectors (4 KiB) up to 32 KiB (16-bit) or 64 KiB
+ * (FP32), WARP for shorter rows, WIDE for wider rows up to 512 KiB, and ONLINE
+ * otherwise. ROW and WIDE need rows that are aligned, or whose input and
+ * output share their offset from a 16-byte boundary. Every plan computes the same
  * function; forcing one (softmax_rows_ex) only changes the schedule:
  *   WARP    one warp per row, the row resident in registers; rows up to 2048 elements.
  *   CTA     one thread block per row, the row staged in shared memory by
@@ -85,12 +87,12 @@ enum sr_status {
  *           ring of shared-memory slots filled by bulk asynchronous copies;
  *           no block barrier at all; aligned rows up to 32 KiB.
  *   ROW     one thread block per row loaded straight into registers, one
- *           block per row in the grid; aligned rows up to 2048 vectors.
- *   WIDE    one thread-block cluster per row, each block holding a slice
- *           (staged in shared memory by a bulk asynchronous copy), warp
- *           (max, sum) pairs merged across the cluster, the exponential
- *           recomputed for the output; aligned rows up to 512 KiB. One HBM
- *           read per element.
+ *           block per row in the grid; rows up to 2048 vectors (16-bit) or
+ *           4096 vectors (FP32).
+ *   WIDE    one thread-block cluster per row, each block holding a slice of
+ *           the row in registers, warp (max, sum) pairs merged across the
+ *           cluster, the exponential recomputed for the output; rows up to
+ *           512 KiB. One HBM read per element.
  * All plans but ROW and WIDE run a persistent grid sized to the device's SM
  * count.
  */

@@ -47,7 +47,7 @@ def _stamp(extra_flags) -> str:
 
 # Sources each plan's kernel is built from (besides the shared headers).
 PLAN_SOURCES = {
-    "row": ["block_rows.cu"], "warp": ["warp_rows.cu", "packed.cuh"], "cta": ["tma_rows.cu"],
+    "row": ["block_rows.cu", "packed.cuh"], "warp": ["warp_rows.cu", "packed.cuh"], "cta": ["tma_rows.cu"],
     "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
     "split": ["split_rows.cu"], "wide": ["wide_rows.cu", "wide.h", "packed.cuh"],
     "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],

@@ -11,17 +11,28 @@
 // what sets the tail of a short kernel.
 #include "device.cuh"
 #include "internal.h"
+#include "packed.cuh"
 
 // Threads per row: the power of two that gives each thread about
-// SR_ROW_TARGET_KV 16-byte vectors, within [SR_ROW_MIN_THREADS, SR_ROW_MAX_THREADS].
+// SR_ROW_TARGET_KV 16-byte vectors, within [SR_ROW_MIN_THREADS, the dtype's
+// cap]. FP32 rows go up to 512 threads (64 KiB rows: on f32 4096 x 16384 this
+// ran at 79.9 µs against 86.0 µs for the WIDE plan); 16-bit rows stop at 256
+// threads (32 KiB), where WIDE is faster beyond.
 #ifndef SR_ROW_TARGET_KV
 #define SR_ROW_TARGET_KV 4
 #endif
 #ifndef SR_ROW_MIN_THREADS
 #define SR_ROW_MIN_THREADS 64
 #endif
-#ifndef SR_ROW_MAX_THREADS
-#define SR_ROW_MAX_THREADS 256
+#ifndef SR_ROW_MAX_THREADS_F32
+#define SR_ROW_MAX_THREADS_F32 512
+#endif
+#ifndef SR_ROW_MAX_THREADS_16
+#define SR_ROW_MAX_THREADS_16 256
+#endif
+// Resident blocks per SM the packed 16-bit kernel is compiled for.
+#ifndef SR_ROW_PACKED_MIN_BLOCKS
+#define SR_ROW_PACKED_MIN_BLOCKS 4
 #endif
 constexpr int kRowMaxKV = 8;
 
@@ -158,6 +169,79 @@ __global__ void __launch_bounds__(NT)
     }
 }
 
+// Packed variant for aligned, unmasked 16-bit rows of more than 1024
+// vectors (8 per thread at 256 threads). The unpacked kernel keeps 64 FP32
+// values per thread there and needs 119 registers (2 blocks/SM). This one
+// keeps the row as packed 16-byte vectors (4 registers per 8 elements), takes
+// the maximum in the storage format, and computes the exponential twice: once
+// for the sum and once for the output, with 1/S folded into the exponent
+// (y = 2^(x log2(e) - (m log2(e) + log2(S))), one FMA and one ex2). The result
+// is still rounded once, from FP32.
+template <typename T, int NT, int KV>
+__global__ void __launch_bounds__(NT, SR_ROW_PACKED_MIN_BLOCKS)
+    block_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                        int64_t ld_in, int64_t ld_out) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int NW = NT / 32;
+    static_assert(!Elem<T>::kAccurateExp, "16-bit data only");
+    __shared__ float red_m[NW], red_s[NW];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nvec = (int)(N / VEC);
+    for (int64_t r = blockIdx.x; r < M; r += gridDim.x) {
+        const T* rin = in + r * ld_in;
+        uint4 raw[KV];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + NT * k;
+            if (idx < nvec) raw[k] = ldg_stream(rin + (int64_t)idx * VEC);
+        }
+        VecMax<T> vm;
+#pragma unroll
+        for (int k = 0; k < KV; ++k)
+            if (tid + NT * k < nvec) vm.add(raw[k]);
+        const float mw = warp_max(vm.get());
+        if (lane == 0) red_m[warp] = mw;
+        __syncthreads();
+        float m = red_m[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) m = fmaxf(m, red_m[w]);
+        const float m_l2 = m * kLog2e;
+        float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            if (tid + NT * k < nvec) {
+                float f[VEC];
+                Elem<T>::unpack(raw[k], f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) {
+                    const float x = exp_shifted<T>(f[e], m, m_l2);
+                    if (e & 1) sb += x; else sa += x;
+                }
+            }
+        }
+        const float sw = warp_sum(sa + sb);
+        if (lane == 0) red_s[warp] = sw;
+        __syncthreads();
+        float s = red_s[0];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) s += red_s[w];
+        // An all -inf row gives -inf - -inf = NaN, as 0/0 does.
+        const float c = fmaf(m, kLog2e, lg2_approx(s));
+        T* rout = out + r * ld_out;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) {
+            const int idx = tid + NT * k;
+            if (idx < nvec) {
+                float f[VEC];
+                unpack_again<T>(raw[k], f);
+#pragma unroll
+                for (int e = 0; e < VEC; ++e) f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
+                stg_stream(rout + (int64_t)idx * VEC, Elem<T>::pack(f));
+            }
+        }
+    }
+}
+
 // One block per row, capped at the largest grid dimension; rows beyond it
 // are walked with a grid stride.
 template <typename T>
@@ -175,6 +259,14 @@ cudaError_t launch_nt_kv(const Problem& p) {
     if (p.mask.active()) return launch_grid(block_rows_kernel<T, NT, KV, true>, NT, p);
     if (!rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype))
         return launch_grid(block_rows_kernel<T, NT, KV, false, true>, NT, p);
+    if constexpr (!Elem<T>::kAccurateExp && KV == kRowMaxKV) {
+        auto kern = block_packed_kernel<T, NT, KV>;
+        const int64_t cap = 0x7fffffff;
+        const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
+        kern<<<grid, NT, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
+                                        p.N, p.ld_in, p.ld_out);
+        return cudaGetLastError();
+    }
     return launch_grid(block_rows_kernel<T, NT, KV, false>, NT, p);
 }
 
@@ -188,22 +280,33 @@ cudaError_t launch_nt(const Problem& p, int64_t nvec) {
     return cudaErrorInvalidValue;
 }
 
-inline int row_threads(int64_t nvec) {
+inline int row_max_threads(int dtype) {
+    return dtype == kF32 ? SR_ROW_MAX_THREADS_F32 : SR_ROW_MAX_THREADS_16;
+}
+
+// Up to 256 threads the block grows first (about SR_ROW_TARGET_KV vectors per
+// thread), then each thread takes up to kRowMaxKV vectors, and only rows
+// beyond 256 x kRowMaxKV vectors take 512 threads. On f32 8192-element rows,
+// 256 x 8 ran at 76.8 µs and 512 x 4 at 89.3 µs.
+inline int row_threads(int64_t nvec, int dtype) {
     int nt = SR_ROW_MIN_THREADS;
-    while (nt < SR_ROW_MAX_THREADS && (int64_t)nt * SR_ROW_TARGET_KV < nvec) nt *= 2;
+    while (nt < 256 && nt < row_max_threads(dtype) && (int64_t)nt * SR_ROW_TARGET_KV < nvec)
+        nt *= 2;
+    while (nt < row_max_threads(dtype) && (int64_t)nt * kRowMaxKV < nvec) nt *= 2;
     return nt;
 }
 
 template <typename T>
 cudaError_t launch_typed(const Problem& p) {
     constexpr int VEC = Elem<T>::kVec;
+    constexpr int kMaxNT = Elem<T>::kAccurateExp ? SR_ROW_MAX_THREADS_F32 : SR_ROW_MAX_THREADS_16;
     const int64_t nvec = p.N / VEC;
-    const int nt = row_threads(nvec);
+    const int nt = row_threads(nvec, p.dtype);
     if constexpr (SR_ROW_MIN_THREADS <= 32) if (nt == 32) return launch_nt<T, 32>(p, nvec);
     if constexpr (SR_ROW_MIN_THREADS <= 64) if (nt == 64) return launch_nt<T, 64>(p, nvec);
     if (nt == 128) return launch_nt<T, 128>(p, nvec);
-    if constexpr (SR_ROW_MAX_THREADS >= 256) if (nt == 256) return launch_nt<T, 256>(p, nvec);
-    if constexpr (SR_ROW_MAX_THREADS >= 512) if (nt == 512) return launch_nt<T, 512>(p, nvec);
+    if constexpr (kMaxNT >= 256) if (nt == 256) return launch_nt<T, 256>(p, nvec);
+    if constexpr (kMaxNT >= 512) if (nt == 512) return launch_nt<T, 512>(p, nvec);
     return cudaErrorInvalidValue;
 }
 
@@ -212,7 +315,7 @@ cudaError_t launch_typed(const Problem& p) {
 // Rows the ROW plan takes (aligned ones): at most kRowMaxKV vectors per thread.
 bool row_plan_fits(int64_t N, int dtype) {
     const int64_t nvec = N / (16 / elem_bytes(dtype));
-    return nvec <= (int64_t)kRowMaxKV * row_threads(nvec);
+    return nvec <= (int64_t)kRowMaxKV * row_threads(nvec, dtype);
 }
 
 cudaError_t launch_row(const Problem& p) {

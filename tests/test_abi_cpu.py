@@ -98,14 +98,17 @@ def test_plan_depends_on_alignment_and_width(lib):
     assert P(A, B, 10, 4096, 4097, 4096, 0) == sr.SR_PLAN_ONLINE       # odd pitch
     # Rows that share their offset from a 16-byte boundary (odd widths, equal
     # pitches, or bases equally misaligned) are read as shifted vectors: ROW up
-    # to 32 KiB, WIDE beyond.
+    # to 64 KiB (FP32) or 32 KiB (16-bit), WIDE beyond.
     assert P(A, B, 4, 32769, 32769, 32769, 2) == sr.SR_PLAN_WIDE
     assert P(A + 4, B + 4, 10, 4096, 4097, 4097, 0) == sr.SR_PLAN_ROW
     assert P(A, B, 10, 4097, 4097, 4097, 2) == sr.SR_PLAN_ROW
     assert P(A + 4, B + 4, 10, 40000, 40001, 40001, 0) == sr.SR_PLAN_WIDE
     assert P(A + 2, B + 4, 10, 4096, 4096, 4096, 2) == sr.SR_PLAN_ONLINE  # not congruent
     assert P(A, B, 10, 8192, 8192, 8192, 0) == sr.SR_PLAN_ROW          # 32 KiB rows
-    assert P(A, B, 10, 8196, 8196, 8196, 0) == sr.SR_PLAN_WIDE         # just over 32 KiB
+    assert P(A, B, 10, 16384, 16384, 16384, 0) == sr.SR_PLAN_ROW       # 64 KiB f32 rows
+    assert P(A, B, 10, 16388, 16388, 16388, 0) == sr.SR_PLAN_WIDE      # just over 64 KiB
+    assert P(A, B, 10, 16384, 16384, 16384, 2) == sr.SR_PLAN_ROW       # 32 KiB f16 rows
+    assert P(A, B, 10, 16392, 16392, 16392, 1) == sr.SR_PLAN_WIDE      # just over 32 KiB
     assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_WIDE   # 512 KiB bf16
     assert P(A, B, 10, 262152, 262152, 262152, 1) == sr.SR_PLAN_ONLINE  # wider than a cluster
     assert P(A, B, 10, 2048, 2048, 2048, 2) == sr.SR_PLAN_ROW
