@@ -221,7 +221,7 @@ def special_rows(N, dtype):
 
 
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
-@pytest.mark.parametrize("N", [5, 1000, 4096, 40000])
+@pytest.mark.parametrize("N", [5, 1000, 4096, 16384, 40000])
 def test_special_rows(dtype, N):
     from tests import pins
     vals = special_rows(N, dtype)
