@@ -10,6 +10,9 @@ namespace sr {
 
 // WIDE plan: clusters of `csize` blocks, `slice` 16-byte vectors per block,
 // `kv` vectors per thread. SR_WIDE_KV: the most vectors a thread holds.
+// Aligned rows too wide for the registers of a 16-block cluster are
+// `streamed`: each block reads its slice twice (the second time mostly
+// from L2) instead of holding it.
 #ifndef SR_WIDE_KV
 #define SR_WIDE_KV 8
 #endif
@@ -17,6 +20,7 @@ struct WideShape {
     int csize = 0;
     int kv = 0;
     int64_t slice = 0;
+    bool streamed = false;
 };
 bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out);
 bool wide_fits(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,

@@ -17,6 +17,9 @@
 // once, from FP32). The grid has one cluster per row, so the hardware starts
 // a new cluster as soon as one finishes.
 //
+// Aligned rows too wide for the cluster's registers (over 512 KiB) take a
+// streamed variant (wide_stream_kernel) that reads each slice twice instead.
+//
 // Failure: a wait that expires marks the block failed; it writes nothing
 // more, records the failure in the error word and, before leaving, waits once
 // more (bounded) so that a late peer's pair cannot land after it exits.
@@ -218,9 +221,204 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
     }
 }
 
-template <typename T, int KV, int MODE>
-cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
-    auto kern = wide_rows_kernel<T, KV, MODE>;
+// Streamed variant for aligned rows too wide for the registers of a 16-block
+// cluster (over 512 KiB): the looped plan of the same section (Wide rows),
+// spread over a cluster. Pass 1 walks the block's slice in steps of
+// kStreamChunk vectors per thread, keeping a per-thread online (max, sum):
+// the step's maximum is taken in the storage format, the sum is rescaled when
+// the maximum grows, and a thread whose values so far are all -inf shifts by 0
+// and keeps a zero sum. The lanes' pairs merge into one pair per warp with
+// the same rule, and the warp pairs are exchanged and merged exactly as in
+// wide_rows_kernel. Pass 2 reads the slice again and writes the output. The
+// resident clusters' rows were read moments before and fit in L2, so HBM sees
+// about one read per element.
+#ifndef SR_WIDE_STREAM_CHUNK
+#define SR_WIDE_STREAM_CHUNK 4
+#endif
+#ifndef SR_WIDE_STREAM_MIN_BLOCKS
+#define SR_WIDE_STREAM_MIN_BLOCKS 4
+#endif
+constexpr int kStreamChunk = SR_WIDE_STREAM_CHUNK;
+// 1: pass 1 marks the lines it reads for late eviction from L2 and pass 2
+// marks them for early eviction, so that the slices stay in L2 between the
+// two passes (L2 cache-policy hints of ld; no effect on results). Measured on
+// GB300, cold L2: bf16 128 x 524288 62.2 -> 54.7 µs, bf16 1024 x 262152
+// 249.6 -> 197.8 µs; rows of 4 MiB and more are too wide to stay in L2
+// either way.
+#ifndef SR_WIDE_STREAM_HINT
+#define SR_WIDE_STREAM_HINT 1
+#endif
+// Blocks per cluster of the streamed variant (8 or 16).
+#ifndef SR_WIDE_STREAM_CLUSTER
+#define SR_WIDE_STREAM_CLUSTER 8
+#endif
+
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+    uint64_t pol = 0;
+    if (SR_WIDE_STREAM_HINT) asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_drop() {
+    uint64_t pol = 0;
+    if (SR_WIDE_STREAM_HINT) asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// 16-byte load through the read-only path with an L2 cache policy.
+__device__ __forceinline__ uint4 ldg_policy(const void* p, uint64_t pol) {
+    uint4 v;
+    if (SR_WIDE_STREAM_HINT) {
+        asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+            : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+            : "l"(p), "l"(pol));
+    } else {
+        v = ldg_stream(p);
+    }
+    return v;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
+    wide_stream_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                       int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
+                       unsigned int* err, unsigned long long timeout_ns, int flags) {
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int NT = kWideThreads;
+    constexpr int NW = kWideWarps;
+    constexpr int CH = kStreamChunk;
+    __shared__ float2 pairs[2][kMaxCluster * NW];
+    __shared__ __align__(8) unsigned long long xbar[2];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = (int)cluster_ctarank();
+    const int64_t nclusters = gridDim.x / csize;
+    const int64_t nvec = N / VEC;
+    const int64_t u0 = (int64_t)rank * slice;
+    const int64_t u1 = (u0 + slice < nvec) ? u0 + slice : nvec;
+    const int npairs = csize * NW;
+    const bool send = !(flags & kFlagNoCopy);  // test hook: send nothing, every wait expires
+    const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
+
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+    bool started = false, failed = false;
+    uint32_t fail_bar = 0, fail_phase = 0;
+    int64_t it = 0;
+    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters, ++it) {
+        const int p = (int)(it & 1);
+        const uint32_t phase = (uint32_t)((it >> 1) & 1);
+        const T* rin = in + r * ld_in;
+        // Pass 1: per-thread online (m, s) over vectors u0 + tid + NT * j.
+        float m = neg_inf(), s = 0.0f;
+        for (int64_t j0 = u0 + tid; j0 < u1; j0 += (int64_t)NT * CH) {
+            const T* q = rin + j0 * VEC;
+            const int64_t rem = u1 - j0;  // vectors of this thread's step: k < rem / NT
+            uint4 raw[CH];
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+                if (NT * k < rem) raw[k] = ldg_policy(q + NT * k * VEC, keep);
+            VecMax<T> vm;
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+                if (NT * k < rem) vm.add(raw[k]);
+            const float mn = fmaxf(m, vm.get());
+            const float shift = (mn == neg_inf()) ? 0.0f : mn;
+            const float shift_l2 = shift * kLog2e;
+            float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                if (NT * k < rem) {
+                    float f[VEC];
+                    Elem<T>::unpack(raw[k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float x = exp_shifted<T>(f[e], shift, shift_l2);
+                        if (e & 1) sb += x; else sa += x;
+                    }
+                }
+            }
+            s = s * merge_scale(m, mn) + (sa + sb);
+            m = mn;
+        }
+        // One pair per warp (the merge is symmetric, so every lane ends with
+        // the same bits).
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            merge_ms(m, s, m2, s2);
+        }
+        if (!started) {
+            cluster_wait();
+            started = true;
+        }
+        const uint32_t xb = smem_addr(&xbar[p]);
+        if (tid == 0) mbar_expect_tx(xb, (uint32_t)npairs * 8u);
+        if (send && lane < csize)
+            st_async_f2(map_to_rank(smem_addr(&pairs[p][rank * NW + warp]), (uint32_t)lane), m, s,
+                        map_to_rank(xb, (uint32_t)lane));
+        if (!failed && !mbar_wait_bounded(xb, phase, timeout_ns)) {
+            failed = true;
+            fail_bar = xb;
+            fail_phase = phase;
+        }
+        if (failed) continue;  // no output; keep sending, so peers do not wait in vain
+        float mloc = neg_inf();
+        for (int i = lane; i < npairs; i += 32) mloc = fmaxf(mloc, pairs[p][i].x);
+        const float Mr = warp_max(mloc);
+        float sloc = 0.0f;
+        for (int i = lane; i < npairs; i += 32) {
+            const float2 q = pairs[p][i];
+            sloc += q.y * merge_scale(q.x, Mr);
+        }
+        const float Sr = warp_sum(sloc);
+        // Pass 2: the output, as in wide_rows_kernel.
+        T* rout = out + r * ld_out;
+        const float rs = Elem<T>::kAccurateExp ? final_rcp(Mr, Sr) : 0.0f;
+        const float c = Elem<T>::kAccurateExp ? 0.0f : fmaf(Mr, kLog2e, lg2_approx(Sr));
+        for (int64_t j0 = u0 + tid; j0 < u1; j0 += (int64_t)NT * CH) {
+            const T* q = rin + j0 * VEC;
+            T* o = rout + j0 * VEC;
+            const int64_t rem = u1 - j0;
+            uint4 raw[CH];
+#pragma unroll
+            for (int k = 0; k < CH; ++k)
+                if (NT * k < rem) raw[k] = ldg_policy(q + NT * k * VEC, drop);
+#pragma unroll
+            for (int k = 0; k < CH; ++k) {
+                if (NT * k < rem) {
+                    float f[VEC];
+                    Elem<T>::unpack(raw[k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        if constexpr (Elem<T>::kAccurateExp)
+                            f[e] = expf(f[e] - Mr) * rs;
+                        else
+                            f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
+                    }
+                    stg_stream(o + NT * k * VEC, Elem<T>::pack(f));
+                }
+            }
+        }
+    }
+    if (!started) cluster_wait();
+    if (failed) {
+        if (tid == 0) atomicOr(err, 1u);
+        mbar_wait_bounded(fail_bar, fail_phase, timeout_ns);
+    }
+}
+
+template <typename T>
+using WideKernel = void (*)(const T*, T*, int64_t, int64_t, int64_t, int64_t, int, int64_t,
+                            unsigned int*, unsigned long long, int);
+
+template <typename T>
+cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int64_t slice) {
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = ensure_smem_limit(fn, 0, csize > 8);
     if (e != cudaSuccess) return e;
@@ -255,9 +453,11 @@ cudaError_t launch_kv(const Problem& p, int csize, int64_t slice) {
 template <typename T, int KV>
 cudaError_t launch_mode(const Problem& p, const WideShape& sh, int mode) {
     switch (mode) {
-        case kAligned: return launch_kv<T, KV, kAligned>(p, sh.csize, sh.slice);
-        case kFull: return launch_kv<T, KV, kFull>(p, sh.csize, sh.slice);
-        case kShifted: return launch_kv<T, KV, kShifted>(p, sh.csize, sh.slice);
+        case kAligned: return launch_clusters<T>(wide_rows_kernel<T, KV, kAligned>, p, sh.csize,
+                                                 sh.slice);
+        case kFull: return launch_clusters<T>(wide_rows_kernel<T, KV, kFull>, p, sh.csize, sh.slice);
+        case kShifted: return launch_clusters<T>(wide_rows_kernel<T, KV, kShifted>, p, sh.csize,
+                                                 sh.slice);
     }
     return cudaErrorInvalidValue;
 }
@@ -265,8 +465,13 @@ cudaError_t launch_mode(const Problem& p, const WideShape& sh, int mode) {
 template <typename T>
 cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     const int64_t nvec = p.N / Elem<T>::kVec;
+    const bool aligned = rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype);
+    if (sh.streamed) {
+        if (!aligned) return cudaErrorInvalidValue;
+        return launch_clusters<T>(wide_stream_kernel<T>, p, sh.csize, sh.slice);
+    }
     int mode = kShifted;
-    if (rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype))
+    if (aligned)
         mode = (sh.slice == (int64_t)kWideThreads * sh.kv && nvec == sh.slice * sh.csize) ? kFull
                                                                                           : kAligned;
     switch (sh.kv) {
@@ -285,7 +490,9 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
 // vectors. While there are too few rows to give every SM two blocks, the
 // cluster doubles (up to 8: larger clusters are scheduled poorly) as long as
 // each thread keeps at least one vector. The vectors per thread are rounded
-// up to 1, 2, 4 or 8. Rows up to 16 x 256 x 8 vectors (512 KiB) fit.
+// up to 1, 2, 4 or 8. Rows up to 16 x 256 x 8 vectors (512 KiB) are held in
+// registers; wider rows are streamed by 8-block clusters (16 while the grid
+// would not fill one wave of resident blocks).
 bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
     const int64_t nvec = N * elem_bytes(dtype) / 16;
     for (int c = 2; c <= kMaxCluster; c *= 2) {
@@ -296,18 +503,27 @@ bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
         out->csize = c;
         out->slice = per;
         out->kv = kv <= 1 ? 1 : kv <= 2 ? 2 : kv <= 4 ? 4 : 8;
+        out->streamed = false;
         return true;
     }
-    return false;
+    int c = SR_WIDE_STREAM_CLUSTER;
+    while (c < kMaxCluster && M * c < (int64_t)SR_WIDE_STREAM_MIN_BLOCKS * sm_count) c *= 2;
+    out->csize = c;
+    out->slice = (nvec + c - 1) / c;
+    out->kv = 0;
+    out->streamed = true;
+    return true;
 }
 
-// Whether the WIDE plan takes these rows: aligned, or sharing their offset
-// from a 16-byte boundary (input and output), and at most 512 KiB.
+// Whether the WIDE plan takes these rows: aligned rows of any width, or rows
+// of at most 512 KiB whose input and output share their offset from a
+// 16-byte boundary.
 bool wide_fits(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
                int dtype) {
     WideShape sh;
     if (!wide_shape(1, N, dtype, 0, &sh)) return false;
     if (rows_vector_aligned(in, out, N, ld_in, ld_out, dtype)) return true;
+    if (sh.streamed) return false;
     const int64_t es = elem_bytes(dtype);
     const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
     return a % 16 == b % 16 && a % es == 0 && (ld_in * es) % 16 == (ld_out * es) % 16;

@@ -110,7 +110,9 @@ def test_plan_depends_on_alignment_and_width(lib):
     assert P(A, B, 10, 16384, 16384, 16384, 2) == sr.SR_PLAN_ROW       # 32 KiB f16 rows
     assert P(A, B, 10, 16392, 16392, 16392, 1) == sr.SR_PLAN_WIDE      # just over 32 KiB
     assert P(A, B, 10, 262144, 262144, 262144, 1) == sr.SR_PLAN_WIDE   # 512 KiB bf16
-    assert P(A, B, 10, 262152, 262152, 262152, 1) == sr.SR_PLAN_ONLINE  # wider than a cluster
+    assert P(A, B, 10, 262152, 262152, 262152, 1) == sr.SR_PLAN_WIDE   # streamed by a cluster
+    assert P(A, B, 10, 1 << 24, 1 << 24, 1 << 24, 0) == sr.SR_PLAN_WIDE  # 64 MiB rows
+    assert P(A + 2, B + 2, 10, 262152, 262153, 262153, 1) == sr.SR_PLAN_ONLINE  # shifted, too wide
     assert P(A, B, 10, 2048, 2048, 2048, 2) == sr.SR_PLAN_ROW
     assert P(A, B, 10, 2040, 2040, 2040, 2) == sr.SR_PLAN_WARP         # 255 vectors
     assert P(A + 2, B, 10, 2048, 2048, 2048, 2) == sr.SR_PLAN_WARP     # scalar warp variant
@@ -134,7 +136,8 @@ def test_forced_plan_checks(lib):
     assert C(A, B, 5, 8, 8, 8, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE
     assert C(A, B, 5, 131072, 131072, 131072, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE
     assert C(A, B, 5, 262144, 262144, 262144, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE  # 512 KiB
-    assert C(A, B, 5, 262152, 262152, 262152, 1, sr.SR_PLAN_WIDE) == -sr.SR_EPLAN
+    assert C(A, B, 5, 262152, 262152, 262152, 1, sr.SR_PLAN_WIDE) == sr.SR_PLAN_WIDE  # streamed
+    assert C(A + 2, B + 2, 5, 262152, 262153, 262153, 1, sr.SR_PLAN_WIDE) == -sr.SR_EPLAN
     assert C(A + 2, B, 5, 131072, 131072, 131072, 1, sr.SR_PLAN_WIDE) == -sr.SR_EPLAN
     assert C(A, B, 5, 4096, 4096, 4096, 0, sr.SR_PLAN_ROW) == sr.SR_PLAN_ROW
     assert C(A, B, 5, 16384, 16384, 16384, 1, sr.SR_PLAN_ROW) == sr.SR_PLAN_ROW

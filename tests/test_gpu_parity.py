@@ -250,6 +250,46 @@ def test_special_rows(dtype, N):
         assert g[6][-1] == 1.0 and np.all(g[6][:-1] == 0.0)
 
 
+# ---- rows too wide for a cluster's registers: the streamed WIDE kernel ----
+
+@pytest.mark.parametrize("dtype,M,N", [(synth.BF16, 3, 262152), (synth.F32, 2, 300000),
+                                       (synth.F16, 9, 600000), (synth.BF16, 40, 524288)],
+                         ids=lambda v: str(v))
+def test_streamed_wide_rows(dtype, M, N):
+    from tests import pins
+    x = synth.generate(M, N, dtype=dtype, seed=N + M, p1=3.0)
+    sp = pins.encode_exact(special_rows(N, dtype), dtype)
+    k = min(M, sp.shape[0])
+    x[:k] = sp[:k]  # all -inf, a NaN, a +inf, uniform, tied maxima, ... as rows allow
+    xd = gu.to_device(x, dtype)
+    assert sr.softmax_rows_plan(xd, xd, M, N, N, N, dtype) == sr.SR_PLAN_WIDE
+    st, y = run_plan(xd, M, N, N, N, dtype, sr.SR_PLAN_AUTO)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    out = gu.to_host(y, dtype)
+    gu.check_rows(out, x, N, N, dtype, "streamed %dx%d" % (M, N))
+    g = synth.storage_to_float64(out[:k], dtype)
+    assert np.isnan(g[0]).all()
+    if k > 2:
+        assert np.isnan(g[1]).all() and np.isnan(g[2]).all()
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
+def test_streamed_wide_wait_expiry():
+    M, N, dtype = 3, 262152, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=77, p1=2.0)
+    xd = gu.to_device(x, dtype)
+    y = nan_filled(M, N, dtype)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    sr.softmax_rows_test_expiry(xd, y, M, N, N, N, dtype, sr.SR_PLAN_WIDE, 2_000_000)
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert torch.isnan(y).all(), "an expired kernel wrote output"
+    sr.softmax_rows_ex(xd, y, M, N, N, N, dtype, sr.SR_PLAN_WIDE)
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "streamed after expiry")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
 # ---- many short rows: the WARP plan's shared-lane layouts ----
 
 # Rows of at most 64 vectors with rows enough for 4 blocks per SM are taken by
