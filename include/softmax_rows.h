@@ -71,9 +71,9 @@ enum sr_status {
 /*
  * Kernel plans. AUTO picks by row width, dtype and alignment. It takes ROW
  * for rows of 256 16-byte vectors (4 KiB) up to 32 KiB (16-bit) or 64 KiB
- * (FP32), WARP for shorter rows, WIDE for wider rows up to 512 KiB, and ONLINE
- * otherwise. ROW and WIDE need rows that are aligned, or whose input and
- * output share their offset from a 16-byte boundary. Every plan computes the same
+ * (FP32), WARP for shorter rows, WIDE for wider rows, and ONLINE otherwise.
+ * ROW and WIDE need rows that are aligned, or whose input and output share
+ * their offset from a 16-byte boundary (WIDE: aligned only beyond 512 KiB). Every plan computes the same
  * function; forcing one (softmax_rows_ex) only changes the schedule:
  *   WARP    one warp per row, the row resident in registers; rows up to 2048 elements.
  *   CTA     one thread block per row, the row staged in shared memory by
@@ -92,7 +92,8 @@ enum sr_status {
  *   WIDE    one thread-block cluster per row, each block holding a slice of
  *           the row in registers, warp (max, sum) pairs merged across the
  *           cluster, the exponential recomputed for the output; rows up to
- *           512 KiB. One HBM read per element.
+ *           512 KiB. Wider aligned rows are streamed: each block reads its
+ *           slice twice, the second time mostly from L2.
  * All plans but ROW and WIDE run a persistent grid sized to the device's SM
  * count.
  */
