@@ -27,6 +27,8 @@
 //           (distributed shared memory) and one hardware cluster barrier
 //           makes them visible; every block adds the C partials in rank order,
 //           so all blocks of a row use the same number.
+//           Aligned rows too wide for the cluster's registers are streamed:
+//           each block reads its slice to reduce it and again to write.
 //  ONLINE   one block per row reads the row to reduce it, then again to write.
 //
 // Units: with Mode::kAligned every row of all three matrices starts on a
@@ -287,8 +289,15 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_addr, float v, uint
 // wait is bounded, and a block whose wait expires writes nothing more,
 // records the failure in the error word and waits once more (bounded) before
 // it leaves, so that a late partial cannot land after it exits.
+// Resident blocks per SM the CLUSTER kernel is compiled for (at most 4 units
+// per thread). Without a bound the RMSNorm kernel for bf16 took 122 registers
+// (2 blocks/SM): at 4 blocks/SM bf16 2048 x 65536 went from 197 to 157 µs,
+// and the other shapes measured stayed within 2 %.
+#ifndef SR_PAIR_CLUSTER_MIN_BLOCKS
+#define SR_PAIR_CLUSTER_MIN_BLOCKS 4
+#endif
 template <class Op, typename T, Mode MODE, int KV>
-__global__ void __launch_bounds__(kClusterThreads)
+__global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN_BLOCKS : 2)
     cluster_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                    int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
                    int64_t slice, unsigned int* err, unsigned long long timeout_ns,
@@ -389,6 +398,138 @@ __global__ void __launch_bounds__(kClusterThreads)
             if (idx < u1) write_unit<Op, T, WIDE>(op, a[k], b[k], s, aux[k], rc + lay.unit_col(idx));
         }
         if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
+    }
+    if (!started) cluster_wait();
+    if (failed) {
+        if (tid == 0) atomicOr(err, 1u);
+        mbar_wait_bounded(fail_bar, fail_phase, timeout_ns);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Streamed CLUSTER plan, for aligned rows too wide for a cluster's registers:
+// each block reduces its slice in steps of kStreamUnroll units per thread,
+// exchanges the partial as cluster_kernel does, then reads the slice again to
+// write. Pass 1 reads with an L2 evict-last policy and pass 2 with
+// evict-first, so the resident clusters' slices stay in L2 between the passes
+// (cache hints only; the results do not depend on them).
+// ---------------------------------------------------------------------------
+constexpr int kStreamUnroll = 2;
+
+__device__ __forceinline__ uint64_t l2_policy(bool keep) {
+    uint64_t pol;
+    if (keep)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint4 ldg_policy(const void* p, uint64_t pol) {
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+template <class Op, typename T>
+__global__ void __launch_bounds__(kClusterThreads, kStreamMinBlocks)
+    stream_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
+                  int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
+                  int64_t slice, unsigned int* err, unsigned long long timeout_ns, int flags) {
+    using U = Unit<T, true>;
+    constexpr int VEC = U::kN;
+    using AuxV = typename Op::template Aux<VEC>;
+    constexpr int NT = kClusterThreads;
+    constexpr int NW = NT / 32;
+    constexpr int UR = kStreamUnroll;
+    __shared__ float red[2][NW];
+    __shared__ float part[2][kMaxCluster];
+    __shared__ __align__(8) unsigned long long xbar[2];
+    const int tid = threadIdx.x;
+    const int rank = (int)cluster_ctarank();
+    const int64_t nclusters = gridDim.x / csize;
+    const int64_t nv = N / VEC;
+    const int64_t u0 = (int64_t)rank * slice;
+    const int64_t u1 = (u0 + slice < nv) ? u0 + slice : nv;
+    const uint64_t keep = l2_policy(true), drop = l2_policy(false);
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+    bool started = false, failed = false;
+    uint32_t fail_bar = 0, fail_phase = 0;
+    int parity = 0;
+    int64_t it = 0;
+    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters, ++it) {
+        const T* ra = A + r * lda;
+        const T* rb = B + r * ldb;
+        float acc[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
+        for (int64_t j0 = u0 + tid; j0 < u1; j0 += (int64_t)NT * UR) {
+            const int64_t rem = u1 - j0;
+            U a[UR], b[UR];
+#pragma unroll
+            for (int j = 0; j < UR; ++j) {
+                if (NT * j < rem) {
+                    a[j].raw = ldg_policy(ra + (j0 + NT * j) * VEC, keep);
+                    b[j].raw = ldg_policy(rb + (j0 + NT * j) * VEC, keep);
+                } else {
+                    a[j].zero();
+                    b[j].zero();
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < UR; ++j) accumulate_unit<Op, T, true>(op, a[j], b[j], acc);
+        }
+        const float mine = team_sum<NW>(fold<VEC>(acc), red[parity], 0);
+        if (!started) {
+            cluster_wait();
+            started = true;
+        }
+        const uint32_t xb = smem_addr(&xbar[parity]);
+        const uint32_t phase = (uint32_t)((it >> 1) & 1);
+        if (tid == 0) mbar_expect_tx(xb, (uint32_t)csize * 4u);
+        if (tid < csize && !(flags & kFlagNoCopy))  // the test hook sends nothing
+            st_async_f32(map_to_rank(smem_addr(&part[parity][rank]), (uint32_t)tid), mine,
+                         map_to_rank(xb, (uint32_t)tid));
+        if (!failed && !mbar_wait_bounded(xb, phase, timeout_ns)) {
+            failed = true;
+            fail_bar = xb;
+            fail_phase = phase;
+        }
+        if (failed) {  // no output; keep sending, so peers do not wait in vain
+            parity ^= 1;
+            continue;
+        }
+        float total = part[parity][0];
+        for (int q = 1; q < csize; ++q) total += part[parity][q];
+        const float s = op.finish(total, N);
+        parity ^= 1;
+        T* rc = C + r * ldc;
+        for (int64_t j0 = u0 + tid; j0 < u1; j0 += (int64_t)NT * UR) {
+            const int64_t rem = u1 - j0;
+            U a[UR], b[UR];
+            AuxV aux[UR];
+#pragma unroll
+            for (int j = 0; j < UR; ++j) {
+                if (NT * j < rem) {
+                    const int64_t idx = j0 + NT * j;
+                    a[j].raw = ldg_policy(ra + idx * VEC, drop);
+                    b[j].raw = ldg_policy(rb + idx * VEC, drop);
+                    aux[j] = op.template load_aux<VEC>(idx * VEC);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < UR; ++j)
+                if (NT * j < rem)
+                    write_unit<Op, T, true>(op, a[j], b[j], s, aux[j], rc + (j0 + NT * j) * VEC);
+        }
     }
     if (!started) cluster_wait();
     if (failed) {
@@ -514,9 +655,13 @@ cudaError_t launch_team(const Op& op, const Args& p, const Shape& sh) {
     return cudaErrorInvalidValue;
 }
 
-template <class Op, typename T, Mode MODE, int KV>
-cudaError_t launch_cluster_kv(const Op& op, const Args& p, const Shape& sh) {
-    auto kern = cluster_kernel<Op, T, MODE, KV>;
+template <class Op, typename T>
+using ClusterKernel = void (*)(Op, const T*, const T*, T*, int64_t, int64_t, int64_t, int64_t,
+                               int64_t, int, int64_t, unsigned int*, unsigned long long, int);
+
+template <class Op, typename T>
+cudaError_t launch_clusters(ClusterKernel<Op, T> kern, const Op& op, const Args& p,
+                            const Shape& sh) {
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = ensure_smem_limit(fn, 0, sh.csize > 8);
     if (e != cudaSuccess) return e;
@@ -544,11 +689,18 @@ cudaError_t launch_cluster_kv(const Op& op, const Args& p, const Shape& sh) {
 template <class Op, typename T, Mode MODE>
 cudaError_t launch_cluster(const Op& op, const Args& p, const Shape& sh) {
     constexpr int KM = KvTarget<T, MODE>::kMax;
-    if (sh.kv == 1) return launch_cluster_kv<Op, T, MODE, 1>(op, p, sh);
-    if (sh.kv == 2) return launch_cluster_kv<Op, T, MODE, 2>(op, p, sh);
-    if (sh.kv == 4) return launch_cluster_kv<Op, T, MODE, 4>(op, p, sh);
-    if constexpr (KM >= 8) if (sh.kv == 8) return launch_cluster_kv<Op, T, MODE, 8>(op, p, sh);
-    if constexpr (KM >= 16) if (sh.kv == 16) return launch_cluster_kv<Op, T, MODE, 16>(op, p, sh);
+    if (sh.streamed) {
+        if constexpr (MODE == Mode::kAligned)
+            return launch_clusters<Op, T>(stream_kernel<Op, T>, op, p, sh);
+        return cudaErrorInvalidValue;
+    }
+    if (sh.kv == 1) return launch_clusters<Op, T>(cluster_kernel<Op, T, MODE, 1>, op, p, sh);
+    if (sh.kv == 2) return launch_clusters<Op, T>(cluster_kernel<Op, T, MODE, 2>, op, p, sh);
+    if (sh.kv == 4) return launch_clusters<Op, T>(cluster_kernel<Op, T, MODE, 4>, op, p, sh);
+    if constexpr (KM >= 8)
+        if (sh.kv == 8) return launch_clusters<Op, T>(cluster_kernel<Op, T, MODE, 8>, op, p, sh);
+    if constexpr (KM >= 16)
+        if (sh.kv == 16) return launch_clusters<Op, T>(cluster_kernel<Op, T, MODE, 16>, op, p, sh);
     return cudaErrorInvalidValue;
 }
 

@@ -226,11 +226,18 @@ def test_backward_plan_choice(lib):
     assert _bwd_plan(4, 32769, F16) == CL
     assert _bwd_plan(1024, 131072, BF16) == CL
     assert _bwd_plan(8, 4096, F32) == CL           # too few rows for one team each
-    assert _bwd_plan(64, 131080, F16) == ON
+    assert _bwd_plan(64, 131080, F16) == CL        # aligned: streamed by a cluster
+    assert _bwd_plan(64, 131080, F16, offset=2) == ON
+    # Rows that would need a 512-thread team run on CLUSTER.
+    assert _bwd_plan(4096, 16384, F16) == CL
+    assert _bwd_plan(1024, 16384, F32) == CL
+    assert _bwd_plan(16384, 8192, F32) == CL
+    assert _bwd_plan(16384, 4096, BF16) == ROW
     assert _bwd_plan(4, 65537, F16) == CL
     assert _bwd_plan(4, 65537, F16, offset=2) == ON
     assert _bwd_plan(4, 65536, F16, offset=2) == CL
-    assert _bwd_plan(64, 131080, F16, CL) == -sr.SR_EPLAN
+    assert _bwd_plan(64, 131080, F16, CL) == CL
+    assert _bwd_plan(64, 131080, F16, CL, offset=2) == -sr.SR_EPLAN
     # ONLINE takes anything.
     assert _bwd_plan(3, 1 << 22, F32, ON) == ON
     # A misaligned y base makes every row unaligned (element units).

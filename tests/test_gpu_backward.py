@@ -232,3 +232,36 @@ def test_cluster_wait_expiry(name):
     assert torch.isnan(dx).all(), "an expired kernel wrote output"
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
     check_case(y, dy, w.M, w.N, w.ld, w.ld, w.N, w.dtype, sr.SR_PLAN_CLUSTER, "after expiry")
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16],
+                         ids=lambda d: synth.DTYPE_NAMES[d])
+@pytest.mark.parametrize("M", [9, 80])
+def test_streamed_cluster_rows(dtype, M):
+    """Aligned rows too wide for a cluster's registers: the streamed CLUSTER
+    kernel (16-block clusters for 9 rows, 8-block clusters for 80)."""
+    N = 131080
+    for ld in (N, N + 8):
+        y = synth.generate(M, N, ld, dtype, seed=M + ld, dist=synth.DIST_UNIFORM, p0=0.0,
+                           p1=2.0 / N)
+        dy = synth.generate(M, N, ld, dtype, seed=M + ld + 1)
+        assert sr.softmax_rows_backward_plan(0x7F0000000000, 0x7F1000000000, 0x7F2000000000, M, N,
+                                             ld, ld, ld, dtype, sr.SR_PLAN_AUTO,
+                                             152) == sr.SR_PLAN_CLUSTER
+        for plan in (sr.SR_PLAN_AUTO, sr.SR_PLAN_CLUSTER):
+            assert check_case(y, dy, M, N, ld, ld, ld, dtype, plan,
+                              "streamed M=%d ld=%d/%s" % (M, ld, sr.PLAN_NAMES[plan]))
+
+
+def test_streamed_cluster_wait_expiry():
+    M, N, dtype = 3, 131080, synth.BF16
+    y = synth.generate(M, N, N, dtype, seed=5, dist=synth.DIST_UNIFORM, p0=0.0, p1=2.0 / N)
+    dy = synth.generate(M, N, N, dtype, seed=6)
+    yd, gd = gu.to_device(y, dtype), gu.to_device(dy, dtype)
+    dx = torch.full((M, N), float("nan"), dtype=gu.torch_dtype(dtype), device="cuda")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    sr.softmax_rows_backward_test_expiry(yd, gd, dx, M, N, N, N, N, dtype, 2_000_000)
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert torch.isnan(dx).all(), "an expired kernel wrote output"
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    check_case(y, dy, M, N, N, N, N, dtype, sr.SR_PLAN_CLUSTER, "streamed after expiry")

@@ -156,3 +156,19 @@ def test_full_size_sampled_rows(name):
                                          w.N, w.ld, w.ld, w.N, float(np.float32(w.eps)), w.dtype)
     dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :w.N]), w.dtype)
     rms_gate(dec(out), dec(ref), w.dtype, name)
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16],
+                         ids=lambda d: synth.DTYPE_NAMES[d])
+@pytest.mark.parametrize("M", [9, 80])
+def test_streamed_cluster_rows(dtype, M):
+    """Aligned rows too wide for a cluster's registers: the streamed CLUSTER
+    kernel reads x, the residual and the weights again in its second pass."""
+    N = 131080
+    x = synth.generate(M, N, N, dtype, seed=100 + M, p1=4.0)
+    r = synth.generate(M, N, N, dtype, seed=101 + M, p1=0.01)
+    w = synth.generate(1, N, N, dtype, seed=102 + M, dist=synth.DIST_UNIFORM, p0=-1.0,
+                       p1=2.0).reshape(-1)
+    for plan in (sr.SR_PLAN_AUTO, sr.SR_PLAN_CLUSTER):
+        assert run_case(x, r, w, M, N, N, N, N, 1e-6, dtype, plan,
+                        "streamed M=%d/%s" % (M, sr.PLAN_NAMES[plan]))
