@@ -14,6 +14,7 @@ namespace sr {
 namespace {
 
 struct BackwardOp {
+    static constexpr bool kBoundTeam = false;
     __device__ __forceinline__ void accumulate(float& acc, float y, float dy) const {
         acc = fmaf(y, dy, acc);
     }

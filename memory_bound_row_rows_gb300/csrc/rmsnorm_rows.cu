@@ -36,6 +36,7 @@ __device__ __forceinline__ float round_to<__half>(float v) {
 // one. They are read through the cache: every row uses the same N weights.
 template <typename T, bool WVEC>
 struct RmsNormOp {
+    static constexpr bool kBoundTeam = true;
     const T* w;
     float eps;
     template <int n>

@@ -16,6 +16,8 @@
 //     // out[e] = the result at the n columns the unit covers
 //     template <int n> __device__ void apply(const float* a, const float* b, float s,
 //                                            const Aux<n>& aux, float* out) const;
+//     // whether the ROW kernel is compiled for higher occupancy (see team_bounded)
+//     static constexpr bool kBoundTeam;
 //   };
 //
 // Three plans, each reading A and B once (ONLINE: twice) and writing C once:
@@ -40,6 +42,8 @@
 // loads single elements. A thread's columns are the same in every row in the
 // aligned mode, so its per-column data is loaded once, before the first row.
 #pragma once
+
+#include <type_traits>
 
 #include "device.cuh"
 #include "internal.h"
@@ -196,9 +200,9 @@ struct Extra {
 // ROW plan.
 // ---------------------------------------------------------------------------
 template <class Op, typename T, Mode MODE, int TPR, int KV>
-__global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
-    team_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
-                int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+__device__ __forceinline__ void team_body(Op op, const T* __restrict__ A, const T* __restrict__ B,
+                                          T* __restrict__ C, int64_t M, int64_t N, int64_t lda,
+                                          int64_t ldb, int64_t ldc) {
     constexpr bool WIDE = MODE != Mode::kScalar;
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;
@@ -260,6 +264,38 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
         }
         if constexpr (MODE == Mode::kShifted) ex.write(op, s, rc);
     }
+}
+
+// The ROW kernel, and the same kernel compiled for at least 24 resident warps
+// per SM (at most 85 registers at 256 threads), used for the operations whose
+// Op sets kBoundTeam on the element types SR_PAIR_TEAM_BOUND selects: 0 none,
+// 1 bf16, 2 both 16-bit types, 3 all. Unbounded, the bf16 RMSNorm kernels took
+// 92-96 registers (2 blocks of 256 threads per SM); bounded, bf16 8192 x 8192
+// went from 77.0 to 65.9 µs on GB300 (cold L2), while the f16 kernels and the
+// backward gained nothing.
+#ifndef SR_PAIR_TEAM_BOUND
+#define SR_PAIR_TEAM_BOUND 1
+#endif
+template <class Op, typename T>
+constexpr bool team_bounded() {
+    return Op::kBoundTeam &&
+           (SR_PAIR_TEAM_BOUND >= 3 || (SR_PAIR_TEAM_BOUND == 2 && sizeof(T) == 2) ||
+            (SR_PAIR_TEAM_BOUND == 1 && std::is_same<T, __nv_bfloat16>::value));
+}
+
+template <class Op, typename T, Mode MODE, int TPR, int KV>
+__global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
+    team_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
+                int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    team_body<Op, T, MODE, TPR, KV>(op, A, B, C, M, N, lda, ldb, ldc);
+}
+
+template <class Op, typename T, Mode MODE, int TPR, int KV>
+__global__ void __launch_bounds__(TPR < 128 ? 128 : TPR, 768 / (TPR < 128 ? 128 : TPR))
+    team_kernel_bounded(Op op, const T* __restrict__ A, const T* __restrict__ B,
+                        T* __restrict__ C, int64_t M, int64_t N, int64_t lda, int64_t ldb,
+                        int64_t ldc) {
+    team_body<Op, T, MODE, TPR, KV>(op, A, B, C, M, N, lda, ldb, ldc);
 }
 
 // ---------------------------------------------------------------------------
@@ -620,9 +656,16 @@ template <class Op, typename T, Mode MODE, int TPR, int KV>
 cudaError_t launch_team_kv(const Op& op, const Args& p) {
     constexpr int NT = TPR < 128 ? 128 : TPR;
     constexpr int RPB = NT / TPR;
-    team_kernel<Op, T, MODE, TPR, KV><<<grid_for((p.M + RPB - 1) / RPB, 1), NT, 0, p.stream>>>(
-        op, static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.c), p.M,
-        p.N, p.lda, p.ldb, p.ldc);
+    const unsigned grid = grid_for((p.M + RPB - 1) / RPB, 1);
+    const T* a = static_cast<const T*>(p.a);
+    const T* b = static_cast<const T*>(p.b);
+    T* c = static_cast<T*>(p.c);
+    if constexpr (team_bounded<Op, T>())
+        team_kernel_bounded<Op, T, MODE, TPR, KV><<<grid, NT, 0, p.stream>>>(op, a, b, c, p.M, p.N,
+                                                                             p.lda, p.ldb, p.ldc);
+    else
+        team_kernel<Op, T, MODE, TPR, KV><<<grid, NT, 0, p.stream>>>(op, a, b, c, p.M, p.N, p.lda,
+                                                                     p.ldb, p.ldc);
     return cudaGetLastError();
 }
 
