@@ -90,6 +90,40 @@ def test_backward_and_rmsnorm_in_a_graph(name, plan):
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
 
+def test_streamed_rows_in_a_graph():
+    """The streamed WIDE kernel and the streamed row-pair CLUSTER kernel, captured."""
+    M, N, dtype = 3, 262152, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=33, p1=2.0)
+    xd = gu.to_device(x, dtype)
+    y = torch.empty((M, N), dtype=gu.torch_dtype(dtype), device="cuda")
+    Mb, Nb = 4, 131080
+    yb = synth.generate(Mb, Nb, dtype=synth.F16, seed=34, dist=synth.DIST_UNIFORM, p0=0.0,
+                        p1=2.0 / Nb)
+    gb = synth.generate(Mb, Nb, dtype=synth.F16, seed=35)
+    ybd, gbd = gu.to_device(yb, synth.F16), gu.to_device(gb, synth.F16)
+    dx = torch.empty((Mb, Nb), dtype=torch.float16, device="cuda")
+
+    def calls():
+        sr.softmax_rows(xd, y, M, N, N, N, dtype)
+        sr.softmax_rows_backward(ybd, gbd, dx, Mb, Nb, Nb, Nb, Nb, synth.F16)
+
+    calls()
+    torch.cuda.synchronize()
+    y.fill_(float("nan"))
+    dx.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        calls()
+    g.replay()
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "streamed WIDE in a graph")
+    ref = oracle.load().softmax_backward(yb.reshape(-1), gb.reshape(-1), Mb, Nb, Nb, Nb, Nb,
+                                         synth.F16)
+    dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a), synth.F16)
+    assert np.allclose(dec(gu.to_host(dx, synth.F16)), dec(ref), rtol=2 ** -9, atol=1e-6)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
 def test_host_pipeline_in_a_graph():
     """softmax_rows_host forks onto its own streams and joins back: capturable too."""
     w = synth.WORKLOADS["f32_4096x4096"].with_rows(64)

@@ -275,6 +275,19 @@ def test_streamed_wide_rows(dtype, M, N):
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
 
+def test_streamed_wide_in_place():
+    """in == out: every block finishes its first pass over a row before any block
+    writes it (the pair exchange orders them), so the second pass still reads x."""
+    M, N, dtype = 5, 300000, synth.F32
+    x = synth.generate(M, N, dtype=dtype, seed=91, p1=3.0)
+    buf = gu.to_device(x, dtype)
+    st = sr.load().softmax_rows_ex(buf.data_ptr(), buf.data_ptr(), M, N, N, N, dtype,
+                                   sr.SR_PLAN_WIDE, torch.cuda.current_stream().cuda_stream)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(buf, dtype), x, N, N, dtype, "streamed in place")
+
+
 def test_streamed_wide_wait_expiry():
     M, N, dtype = 3, 262152, synth.BF16
     x = synth.generate(M, N, dtype=dtype, seed=77, p1=2.0)
