@@ -42,6 +42,21 @@ namespace {
 #endif
 
 constexpr int kWideThreads = 256;
+
+// exp(x - m) for FP32 data: the hardware ex2 of the difference (rounded once
+// in FP32) times log2(e), as in the ROW plan, instead of the library expf;
+// SR_WIDE_EX2 = 0 keeps expf. 16-bit data always takes one FMA and ex2.
+#ifndef SR_WIDE_EX2
+#define SR_WIDE_EX2 1
+#endif
+template <typename T>
+__device__ __forceinline__ float wide_exp(float x, float m, float m_l2) {
+    if constexpr (Elem<T>::kAccurateExp && SR_WIDE_EX2) {
+        return ex2_approx((x - m) * kLog2e);
+    } else {
+        return exp_shifted<T>(x, m, m_l2);
+    }
+}
 constexpr int kWideWarps = kWideThreads / 32;
 
 __device__ __forceinline__ void cluster_arrive_relaxed() {
@@ -144,12 +159,12 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
                 Elem<T>::unpack(raw[k], f);
 #pragma unroll
                 for (int e = 0; e < VEC; ++e) {
-                    const float x = exp_shifted<T>(f[e], shift, shift_l2);
+                    const float x = wide_exp<T>(f[e], shift, shift_l2);
                     if (e & 1) sb += x; else sa += x;
                 }
             }
         }
-        if (SHIFTED && ce >= 0) sa += exp_shifted<T>(xe, shift, shift_l2);
+        if (SHIFTED && ce >= 0) sa += wide_exp<T>(xe, shift, shift_l2);
         const float s_w = warp_sum(sa + sb);
         if (!started) {
             cluster_wait();
@@ -188,11 +203,11 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
                     float f[VEC];
                     unpack_again<T>(raw[k], f);
 #pragma unroll
-                    for (int e = 0; e < VEC; ++e) f[e] = expf(f[e] - Mr) * rs;
+                    for (int e = 0; e < VEC; ++e) f[e] = wide_exp<T>(f[e], Mr, 0.0f) * rs;
                     stg_stream(obody + idx * VEC, Elem<T>::pack(f));
                 }
             }
-            if (SHIFTED && ce >= 0) Elem<T>::store1(rout + ce, expf(xe - Mr) * rs);
+            if (SHIFTED && ce >= 0) Elem<T>::store1(rout + ce, wide_exp<T>(xe, Mr, 0.0f) * rs);
         } else {
             // 16-bit data: 1/S folded into the exponent,
             // y = 2^(x log2(e) - (M log2(e) + log2(S))), one FMA and one ex2 per
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
                     Elem<T>::unpack(raw[k], f);
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
-                        const float x = exp_shifted<T>(f[e], shift, shift_l2);
+                        const float x = wide_exp<T>(f[e], shift, shift_l2);
                         if (e & 1) sb += x; else sa += x;
                     }
                 }
@@ -397,7 +412,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) {
                         if constexpr (Elem<T>::kAccurateExp)
-                            f[e] = expf(f[e] - Mr) * rs;
+                            f[e] = wide_exp<T>(f[e], Mr, 0.0f) * rs;
                         else
                             f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
                     }
