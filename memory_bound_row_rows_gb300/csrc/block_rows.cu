@@ -18,8 +18,11 @@
 // cap]. FP32 rows go up to 512 threads (64 KiB rows: on f32 4096 x 16384 this
 // ran at 79.9 µs against 86.0 µs for the WIDE plan); 16-bit rows stop at 256
 // threads (32 KiB), where WIDE is faster beyond.
+// (8: f32 4096 x 4096 in 128-thread blocks ran at 20.3 against 20.6 µs with
+// 4 vectors in 256-thread blocks, bf16 8192 x 8192 at 39.4 against 41.5 µs;
+// GB300, cold L2.)
 #ifndef SR_ROW_TARGET_KV
-#define SR_ROW_TARGET_KV 4
+#define SR_ROW_TARGET_KV 8
 #endif
 #ifndef SR_ROW_MIN_THREADS
 #define SR_ROW_MIN_THREADS 64
