@@ -77,8 +77,20 @@ __device__ __forceinline__ void cluster_wait() {
 enum : int { kAligned = 0, kFull = 1, kShifted = 2 };
 
 // KV: 16-byte vectors per thread; `slice`: vectors per block (<= 256 * KV).
+// Slices of 5 or 6 vectors per thread (rows that would half fill 8) get
+// their own kernels, compiled for SR_WIDE_MIN_BLOCKS_MID blocks per SM, so
+// that more row bytes are resident per SM. Measured on GB300 (cold L2):
+// bf16 4096 x 16392 57.1 -> 51.2 µs, f32 3000 x 20000 86.2 -> 76.9 µs,
+// f16 2730 x 24576 46.8 -> 43.4 µs.
+#ifndef SR_WIDE_MID_KV
+#define SR_WIDE_MID_KV 1
+#endif
+#ifndef SR_WIDE_MIN_BLOCKS_MID
+#define SR_WIDE_MIN_BLOCKS_MID 5
+#endif
 template <typename T, int KV, int MODE>
-__global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
+__global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_MIN_BLOCKS_MID
+                                                                     : SR_WIDE_MIN_BLOCKS)
     wide_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
                      unsigned long long timeout_ns, int flags) {
@@ -494,6 +506,10 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
         case 2: return launch_mode<T, 2>(p, sh, mode);
         case 4: return launch_mode<T, 4>(p, sh, mode);
         case 8: return launch_mode<T, 8>(p, sh, mode);
+#if SR_WIDE_MID_KV
+        case 5: return launch_mode<T, 5>(p, sh, mode);
+        case 6: return launch_mode<T, 6>(p, sh, mode);
+#endif
     }
     return cudaErrorInvalidValue;
 }
@@ -517,7 +533,8 @@ bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
         const int64_t kv = (per + kWideThreads - 1) / kWideThreads;
         out->csize = c;
         out->slice = per;
-        out->kv = kv <= 1 ? 1 : kv <= 2 ? 2 : kv <= 4 ? 4 : 8;
+        out->kv = kv <= 1 ? 1 : kv <= 2 ? 2 : kv <= 4 ? 4
+                : (SR_WIDE_MID_KV && kv <= 5) ? 5 : (SR_WIDE_MID_KV && kv <= 6) ? 6 : 8;
         out->streamed = false;
         return true;
     }
