@@ -50,6 +50,18 @@ struct Shape {
 
 // Resident blocks per SM the streamed CLUSTER kernel is compiled for.
 constexpr int kStreamMinBlocks = 4;
+// Aligned rows of at least this many units are streamed even when a cluster
+// could hold them (never, by default: streaming rows of 8192 units helped the
+// RMSNorm and hurt the backward by as much).
+#ifndef SR_PAIR_STREAM_MIN_UNITS
+#define SR_PAIR_STREAM_MIN_UNITS (int64_t(1) << 62)
+#endif
+// Streamed clusters double (8 -> 16 blocks) only while the doubled grid still
+// fits one wave of resident blocks (backward f16 64 x 1048576: 102.2 -> 93.8 µs
+// against doubling whenever the grid is short of a wave).
+#ifndef SR_PAIR_STREAM_GROW_WAVE
+#define SR_PAIR_STREAM_GROW_WAVE 1
+#endif
 
 // The load mode the three matrices allow.
 inline int mode_for(const Args& p) {
@@ -87,9 +99,9 @@ inline int64_t pow2_at_least(int64_t v) {
 //    holds, in 16 blocks). While there are too few rows to give every SM two
 //    blocks, the cluster doubles (up to 16) as long as each block keeps at
 //    least one unit per thread; the units per thread follow the slice.
-//    Aligned rows too wide for that are streamed: 8-block clusters (16 while
-//    the grid would not fill one wave of resident blocks), each block reading
-//    its slice once to reduce it and again to write.
+//    Aligned rows too wide for that are streamed: 8-block clusters (16 when
+//    the doubled grid still fits one wave of resident blocks), each block
+//    reading its slice once to reduce it and again to write.
 inline bool shape_for(const Args& p, int plan, int sm_count, Shape* out) {
     Shape sh;
     sh.plan = plan;
@@ -115,11 +127,15 @@ inline bool shape_for(const Args& p, int plan, int sm_count, Shape* out) {
                     c = cc;
                     break;
                 }
-            if (c == 0) {
-                if ((int64_t)kMaxCluster * kClusterThreads * km < units) {
+            if (c == 0 || (sh.mode == (int)Mode::kAligned && units >= SR_PAIR_STREAM_MIN_UNITS)) {
+                if ((int64_t)kMaxCluster * kClusterThreads * km < units ||
+                    units >= SR_PAIR_STREAM_MIN_UNITS) {
                     if (sh.mode != (int)Mode::kAligned) return false;
                     c = 8;
-                    while (c < kMaxCluster && p.M * c < (int64_t)kStreamMinBlocks * sm_count)
+                    while (c < kMaxCluster &&
+                           (SR_PAIR_STREAM_GROW_WAVE
+                                ? p.M * c * 2 <= (int64_t)kStreamMinBlocks * sm_count
+                                : p.M * c < (int64_t)kStreamMinBlocks * sm_count))
                         c *= 2;
                     sh.csize = c;
                     sh.slice = (units + c - 1) / c;
