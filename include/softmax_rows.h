@@ -145,10 +145,17 @@ SR_API int softmax_rows_plan_check(const void* in, const void* out, int64_t M, i
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error
- * word, which a kernel sets when one of its bounded waits (for a bulk copy
- * into shared memory) expires. Returns SR_OK, SR_EDEVICE_TIMEOUT, or SR_ECUDA.
- * A kernel whose wait expired skips the rest of its rows and returns, so the
- * CUDA context stays usable; the output of that call is then incomplete.
+ * word, which a kernel sets when one of its bounded waits expires: a wait for
+ * a bulk copy into shared memory (CTA, CLUSTER, SMEM plans) or for the
+ * partial results of the other blocks of its cluster (WIDE, CLUSTER, and the
+ * CLUSTER plan of the backward and the RMSNorm). Returns SR_OK,
+ * SR_EDEVICE_TIMEOUT, or SR_ECUDA. A kernel whose wait expired skips the rest
+ * of its rows and returns, so the CUDA context stays usable; the output of
+ * that call is then incomplete. The word is one per device, shared by every
+ * stream, and the read and the clear are two steps: a kernel still running on
+ * another stream can set it in between, and its report is then lost. Call
+ * this when no other stream of the device has work of this library in flight,
+ * or read a set word as covering all of them.
  */
 SR_API int softmax_rows_last_device_error(sr_stream_t stream);
 
