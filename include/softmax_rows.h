@@ -314,10 +314,14 @@ SR_API int softmax_rows_backward(const void* y, const void* dy, void* dx, int64_
  * team of threads per row, the row held in registers; rows up to 16384
  * elements), SR_PLAN_CLUSTER (a thread-block cluster of 2..16 blocks per row,
  * partial dot products exchanged in distributed shared memory; rows up to
- * 131072 elements) or SR_PLAN_ONLINE (any row: y and dy are read twice).
- * Rows are read as 16-byte vectors when the three matrices' bases and pitches
- * agree modulo 16 bytes (an element-aligned head and tail are read singly);
- * otherwise element by element, and the limits halve (8192 and 65536).
+ * 131072 elements held in registers, and aligned rows of any width streamed:
+ * each block reads its slice once to reduce it and again to write) or
+ * SR_PLAN_ONLINE (any row: y and dy are read twice). Rows are read as 16-byte
+ * vectors when the three matrices' bases and pitches agree modulo 16 bytes
+ * (an element-aligned head and tail are read singly); otherwise element by
+ * element, and the limits halve (8192 and 65536). AUTO takes ROW for rows a
+ * team of at most 256 threads holds when there are rows enough for the GPU,
+ * CLUSTER for wider rows and for fewer rows than SMs, ONLINE otherwise.
  * SR_EPLAN when the plan cannot take the shape.
  */
 SR_API int softmax_rows_backward_ex(const void* y, const void* dy, void* dx, int64_t M,
