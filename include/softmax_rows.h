@@ -160,11 +160,12 @@ SR_API int softmax_rows_plan_check(const void* in, const void* out, int64_t M, i
 SR_API int softmax_rows_last_device_error(sr_stream_t stream);
 
 /*
- * Test hook for the bounded-wait path: runs `plan` (CTA, CLUSTER, SMEM or WIDE) on the
- * given arguments with its bulk copies switched off, so every wait for a copy
- * expires after `timeout_ns` nanoseconds; the kernel then records
- * SR_EDEVICE_TIMEOUT and returns without writing `out`. Nothing hangs and
- * nothing faults. Returns like softmax_rows_ex.
+ * Test hook for the bounded-wait path: runs `plan` (CTA, CLUSTER, SMEM or
+ * WIDE) on the given arguments with its bulk copies, or for WIDE its
+ * exchange of (max, sum) pairs, switched off, so every wait expires after
+ * `timeout_ns` nanoseconds; the kernel then records SR_EDEVICE_TIMEOUT and
+ * returns without writing `out`. Nothing hangs and nothing faults. Returns
+ * like softmax_rows_ex.
  */
 SR_API int softmax_rows_test_expiry(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                              int64_t ld_out, int dtype, int plan, uint64_t timeout_ns,
