@@ -552,7 +552,8 @@ int rmsnorm_residual_rows_ex(const void* x, const void* residual, const void* we
                              float eps, int dtype, int plan, sr_stream_t stream) {
     const int bad = sr::check_rms_args(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype);
     if (bad) return bad;
-    const sr::rp::Args a{x, residual, y, M, N, ld_x, ld_r, ld_y, dtype, (cudaStream_t)stream};
+    sr::rp::Args a{x, residual, y, M, N, ld_x, ld_r, ld_y, dtype, (cudaStream_t)stream};
+    a.stream_wide = true;
     return sr::run_pair(a, plan, [weight, eps](const sr::rp::Args& q, const sr::rp::Shape& sh) {
         return sr::launch_rmsnorm(q, sh, weight, eps);
     });
@@ -570,7 +571,8 @@ int rmsnorm_residual_rows_plan(const void* x, const void* residual, const void* 
                                int64_t ld_y, float eps, int dtype, int plan, int sm_count) {
     const int bad = sr::check_rms_args(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, eps, dtype);
     if (bad) return -bad;
-    const sr::rp::Args a{x, residual, const_cast<void*>(y), M, N, ld_x, ld_r, ld_y, dtype, nullptr};
+    sr::rp::Args a{x, residual, const_cast<void*>(y), M, N, ld_x, ld_r, ld_y, dtype, nullptr};
+    a.stream_wide = true;
     return sr::pair_plan_query(a, plan, sm_count);
 }
 

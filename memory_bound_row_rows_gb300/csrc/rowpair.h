@@ -35,6 +35,7 @@ struct Args {
     unsigned int* err = nullptr;            // device error word (CLUSTER plan's bounded waits)
     unsigned long long timeout_ns = 0;      // limit of one bounded wait
     int flags = 0;                          // kFlagNoCopy: the CLUSTER plan sends no partials
+    bool stream_wide = false;               // stream aligned rows of kStreamWideUnits and more
 };
 
 // How one plan runs one problem (host logic only, the same on every device).
@@ -50,6 +51,12 @@ struct Shape {
 
 // Resident blocks per SM the streamed CLUSTER kernel is compiled for.
 constexpr int kStreamMinBlocks = 4;
+// Aligned rows of at least this many units are streamed when the operation
+// asks for it (Args::stream_wide; the RMSNorm does): f16 64 x 131072 ran at
+// 15.5 against 16.8 µs and bf16 1024 x 131072 at 157.7 against 177.0 µs on
+// GB300 (cold L2). The backward holds such rows in registers: streaming them
+// cost it 10 %.
+constexpr int64_t kStreamWideUnits = 16384;
 // Aligned rows of at least this many units are streamed even when a cluster
 // could hold them (never, by default: streaming rows of 8192 units helped the
 // RMSNorm and hurt the backward by as much).
@@ -127,9 +134,11 @@ inline bool shape_for(const Args& p, int plan, int sm_count, Shape* out) {
                     c = cc;
                     break;
                 }
-            if (c == 0 || (sh.mode == (int)Mode::kAligned && units >= SR_PAIR_STREAM_MIN_UNITS)) {
-                if ((int64_t)kMaxCluster * kClusterThreads * km < units ||
-                    units >= SR_PAIR_STREAM_MIN_UNITS) {
+            const bool stream_anyway =
+                sh.mode == (int)Mode::kAligned &&
+                (units >= SR_PAIR_STREAM_MIN_UNITS || (p.stream_wide && units >= kStreamWideUnits));
+            if (c == 0 || stream_anyway) {
+                if ((int64_t)kMaxCluster * kClusterThreads * km < units || stream_anyway) {
                     if (sh.mode != (int)Mode::kAligned) return false;
                     c = 8;
                     while (c < kMaxCluster &&
