@@ -389,6 +389,19 @@ SR_API int rmsnorm_residual_rows_plan(const void* x, const void* residual, const
 SR_API const char* softmax_rows_strerror(int status);
 
 /* Library version as major*10000 + minor*100 + patch. */
+/*
+ * Host-only description of how the WIDE plan runs M rows of N elements (of
+ * the dtype, rows aligned or sharing their offset from a 16-byte boundary)
+ * on a device with sm_count SMs: blocks per cluster (`csize`), 16-byte
+ * vectors per block (`slice`), vectors each thread holds (`kv`; 0 for
+ * streamed rows), and whether the rows are streamed (`streamed`: each block
+ * reads its slice twice instead of holding it). Any output pointer may be
+ * NULL. Returns 0, or -SR_EDTYPE / -SR_EINVAL for a bad dtype or M < 0,
+ * N < 1, sm_count < 1. Makes no CUDA call.
+ */
+SR_API int softmax_rows_wide_shape(int64_t M, int64_t N, int dtype, int sm_count, int* csize,
+                                   int* kv, int64_t* slice, int* streamed);
+
 SR_API int softmax_rows_version(void);
 
 #ifdef __cplusplus

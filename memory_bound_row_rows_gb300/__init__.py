@@ -23,7 +23,7 @@ __all__ = [
     "softmax_rows_host_mapped",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
     "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
-    "rmsnorm_residual_rows_plan",
+    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape",
     "softmax", "softmax_backward", "rmsnorm_residual",
     "dtype_code",
 ]
@@ -89,6 +89,7 @@ def load():
         "rmsnorm_residual_rows_plan": [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, c_int, c_int,
                                        c_int],
         "softmax_rows_version": [],
+        "softmax_rows_wide_shape": [i64, i64, c_int, c_int, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -140,6 +141,20 @@ def softmax_rows_ex(in_, out, M, N, ld_in, ld_out, dtype, plan, stream=None) -> 
 def softmax_rows_plan(in_, out, M, N, ld_in, ld_out, dtype) -> int:
     """The plan softmax_rows would run (> 0), or a negative status."""
     return int(load().softmax_rows_plan(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype))
+
+
+def softmax_rows_wide_shape(M, N, dtype, sm_count) -> dict:
+    """How the WIDE plan runs M rows of N elements on `sm_count` SMs (host logic):
+    {"csize", "kv", "slice", "streamed"}; raises on bad arguments."""
+    csize, kv, streamed = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    slice_ = ctypes.c_int64()
+    st = load().softmax_rows_wide_shape(M, N, dtype, sm_count, ctypes.byref(csize),
+                                        ctypes.byref(kv), ctypes.byref(slice_),
+                                        ctypes.byref(streamed))
+    if st != 0:
+        raise SoftmaxRowsError(-st, "softmax_rows_wide_shape")
+    return {"csize": csize.value, "kv": kv.value, "slice": slice_.value,
+            "streamed": bool(streamed.value)}
 
 
 def softmax_rows_plan_check(in_, out, M, N, ld_in, ld_out, dtype, plan) -> int:

@@ -588,6 +588,19 @@ const char* softmax_rows_strerror(int status) {
     return "unknown status";
 }
 
+int softmax_rows_wide_shape(int64_t M, int64_t N, int dtype, int sm_count, int* csize, int* kv,
+                            int64_t* slice, int* streamed) {
+    if (dtype != SR_F32 && dtype != SR_BF16 && dtype != SR_F16) return -SR_EDTYPE;
+    if (M < 0 || N < 1 || sm_count < 1) return -SR_EINVAL;
+    sr::WideShape sh;
+    if (!sr::wide_shape(M, N, dtype, sm_count, &sh)) return -SR_EINVAL;
+    if (csize) *csize = sh.csize;
+    if (kv) *kv = sh.kv;
+    if (slice) *slice = sh.slice;
+    if (streamed) *streamed = sh.streamed ? 1 : 0;
+    return 0;
+}
+
 int softmax_rows_version(void) { return 100; }
 
 }  // extern "C"

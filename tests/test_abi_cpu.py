@@ -273,3 +273,26 @@ def test_host_mapped_refuses_without_a_device(lib):
     assert lib.softmax_rows_host_mapped(None, None, 0, 8, 8, 8, 0, None) == sr.SR_OK
     assert lib.softmax_rows_host_mapped(ALIGNED_IN, ALIGNED_OUT, 4, 8, 7, 8, 0, None) == \
         sr.SR_EINVAL
+
+
+def test_wide_shapes(lib):
+    """The WIDE plan's launch shape (host logic, 152 SMs)."""
+    S = lambda M, N, dt: sr.softmax_rows_wide_shape(M, N, dt, 152)
+    # bf16 1024 x 131072: 8-block clusters, 2048 vectors per block, 8 per thread.
+    assert S(1024, 131072, 1) == {"csize": 8, "kv": 8, "slice": 2048, "streamed": False}
+    # Few rows: clusters grow (up to 8) while each thread keeps a vector.
+    assert S(4, 32769, 2)["csize"] == 8
+    assert S(64, 131072, 2) == {"csize": 8, "kv": 8, "slice": 2048, "streamed": False}
+    # Slices that would half fill 8 vectors per thread take the 5- and 6-vector kernels.
+    assert S(4096, 16392, 1) == {"csize": 2, "kv": 5, "slice": 1025, "streamed": False}
+    assert S(2730, 24576, 2) == {"csize": 2, "kv": 6, "slice": 1536, "streamed": False}
+    assert S(2048, 16388, 0) == {"csize": 4, "kv": 5, "slice": 1025, "streamed": False}
+    # 512 KiB is the most 16 blocks hold; wider rows are streamed.
+    assert S(256, 262144, 1) == {"csize": 16, "kv": 8, "slice": 2048, "streamed": False}
+    assert S(128, 262152, 1)["streamed"]
+    assert S(128, 524288, 1) == {"csize": 8, "kv": 0, "slice": 8192, "streamed": True}
+    # Streamed rows too few for a wave of 8-block clusters double to 16.
+    assert S(32, 4194304, 0) == {"csize": 16, "kv": 0, "slice": 65536, "streamed": True}
+    for bad in ((4, 0, 1, 152), (-1, 8, 1, 152), (4, 8, 9, 152), (4, 8, 1, 0)):
+        with pytest.raises(sr.SoftmaxRowsError):
+            sr.softmax_rows_wide_shape(*bad)
