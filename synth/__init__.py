@@ -334,4 +334,5 @@ def storage_to_float64(a: np.ndarray, dtype: int) -> np.ndarray:
         return a.astype(np.float64)
     if dtype == BF16:
         return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    return a.view(np.float16).astype(np.float64)
+    with np.errstate(invalid="ignore"):  # NaN payloads warn on some platforms
+        return a.view(np.float16).astype(np.float64)
