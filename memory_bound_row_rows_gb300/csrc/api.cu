@@ -190,10 +190,13 @@ bool plan_fits(int plan, const void* in, const void* out, int64_t N, int64_t ld_
 }
 
 // Automatic plan (from plan sweeps on GB300, cold L2):
-//  - aligned rows of 256..2048 16-byte vectors: ROW (one block per row);
+//  - rows of 256 vectors up to the ROW plan's limit (2048 16-bit or 4096 FP32
+//    vectors), aligned or at a common offset from a 16-byte boundary: ROW
+//    (one block per row);
 //  - shorter rows (or unaligned rows up to 2048 elements): WARP;
-//  - aligned rows up to 512 KiB: WIDE (one register-resident cluster per row;
-//    faster than CLUSTER on every wide shape measured);
+//  - wider rows: WIDE (one cluster per row, the row in registers up to
+//    512 KiB, streamed beyond when aligned; faster than CLUSTER on every wide
+//    shape measured);
 //  - anything else: ONLINE.
 int choose_plan(const void* in, const void* out, int64_t N, int64_t ld_in, int64_t ld_out,
                 int dtype) {
