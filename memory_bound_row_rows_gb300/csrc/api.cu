@@ -11,8 +11,9 @@
 
 namespace sr {
 
-// Set (bit 0) by a kernel whose bounded wait for a bulk copy expired. One
-// word per device (each device holds its own copy of this module's globals).
+// Set (bit 0) by a kernel whose bounded wait (for a bulk copy, or for the
+// pairs or partials of its cluster peers) expired. One word per device (each
+// device holds its own copy of this module's globals).
 __device__ unsigned int g_error_word;
 
 namespace {
