@@ -296,3 +296,20 @@ def test_wide_shapes(lib):
     for bad in ((4, 0, 1, 152), (-1, 8, 1, 152), (4, 8, 9, 152), (4, 8, 1, 0)):
         with pytest.raises(sr.SoftmaxRowsError):
             sr.softmax_rows_wide_shape(*bad)
+
+
+def test_host_workspace_is_host_logic(lib):
+    """Workspace for full pipeline depth: 4 slots of up to 8 MiB of input rows
+    (rows padded to 16 bytes on the device), input and output per slot."""
+    W = sr.softmax_rows_host_workspace_bytes
+    # f32 4096 x 4096: 512 rows of 16 KiB make 8 MiB.
+    assert W(4096, 4096, 0) == 4 * 512 * 2 * 4096 * 4
+    # Fewer rows than a chunk: the chunk shrinks to the matrix.
+    assert W(10, 4096, 0) == 4 * 10 * 2 * 4096 * 4
+    # bf16 1000 columns pad to 1000 (2000 bytes is a multiple of 16); 1001 to 1008.
+    assert W(16384, 1000, 1) == 4 * ((8 << 20) // 2000) * 2 * 1000 * 2
+    assert W(16384, 1001, 1) == 4 * ((8 << 20) // 2016) * 2 * 1008 * 2
+    # A row larger than the chunk target still gets one row per slot.
+    assert W(4, 4 << 20, 0) == 4 * 1 * 2 * (4 << 20) * 4
+    assert W(4, 8, 9) == -sr.SR_EDTYPE
+    assert W(-1, 8, 0) == -sr.SR_EINVAL
