@@ -486,7 +486,7 @@ def bench_ours(args, w):
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic,
                      "traffic_note": (rec or {}).get("note") if traffic else
-                     "null: no ncu capture recorded for this build of the kernels"},
+                     "null: no ncu capture recorded for the current kernel sources"},
         "source_hash": src_hash,
     }
     if res["e2e"] is not None:
@@ -726,7 +726,7 @@ def bench_pair(args, lane):
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic,
                      "traffic_note": (rec or {}).get("note") if traffic else
-                     "null: no ncu capture recorded for this build of the kernels"},
+                     "null: no ncu capture recorded for the current kernel sources"},
         "source_hash": _build.source_hash(_build.PLAN_SOURCES[lane.api]),
     }
     if e2e is not None:
