@@ -226,7 +226,8 @@ SR_API int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype
  *            L_i = min(N, i mod causal_period + 1) entries (rows holding query
  *            positions i mod causal_period of causal attention over N keys).
  *            Neither given: no mask (same as softmax_rows_ex).
- * L_i = 0 leaves an all -inf row, which is NaN like any all -inf row.
+ * L_i = 0, or valid entries that are all -inf, leave an all -inf row, which
+ * is NaN everywhere like any all -inf row (its masked entries included).
  * plan: SR_PLAN_AUTO, SR_PLAN_WARP, SR_PLAN_ROW or SR_PLAN_ONLINE.
  * Other arguments and results as softmax_rows_ex; SR_EINVAL also for a
  * negative causal_period or for lengths and causal_period both given.

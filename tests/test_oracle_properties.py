@@ -96,3 +96,28 @@ def test_rmsnorm_oracle_matches_exact(case, eps):
     got = pins._rms(oracle.load(), x, r, w, eps, dtype)
     for i in range(M):
         assert pins.same(got[i], pins._rms_brute(x[i], r[i], w, eps, dtype)), (dtype, x[i], r[i])
+
+
+@hypothesis.settings(max_examples=100, deadline=None, derandomize=True)
+@hypothesis.given(rows(), st.data())
+def test_masked_oracle_matches_exact_prefix(case, data):
+    """Masked rows equal the exact softmax of the row with its masked entries set to
+    -inf, whatever the masked entries hold: exact zeros past L, and NaN everywhere
+    when no valid entry is finite (L = 0, or a valid prefix of -inf only; found by
+    this test: [-inf | 0] with L = 1 is [NaN, NaN])."""
+    dtype, vals = case
+    M, N = vals.shape
+    lens = np.array(data.draw(st.lists(st.integers(-2, N + 3), min_size=M, max_size=M)),
+                    dtype=np.int32)
+    poisoned = vals.copy()
+    for i, L in enumerate(lens):
+        poisoned[i, max(0, min(int(L), N)):] = math.nan  # never read
+    x = pins.encode_exact(poisoned, dtype)
+    got = pins.decode(oracle.load().softmax_rows_masked(x.reshape(-1), M, N, N, N, dtype,
+                                                        lens=lens), dtype)
+    for i, L in enumerate(lens):
+        L = max(0, min(int(L), N))
+        filled = vals[i].copy()
+        filled[L:] = -math.inf
+        want = brute.softmax_exact_cast(filled, dtype)
+        assert pins.same(got[i], want), (dtype, vals[i], L, got[i], want)
