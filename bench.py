@@ -1,28 +1,43 @@
 #!/usr/bin/env python3
 """Throughput of the fused row softmax on one GB300 (or N, as replicas).
 
-One step = one softmax_rows call (the whole hot path: plan, persistent
-schedule, row load, max, exp-sum, normalise-and-store) over the workload's
-M x N matrix, inputs resident in HBM. The headline workload is the FP32
-4096 x 4096 matrix with extreme rows (seed 1).
+One step = one softmax_rows call (the whole hot path: plan, schedule, row
+load, max, exp-sum, normalise-and-store) over the workload's M x N matrix,
+inputs resident in HBM. The default workload is the largest: the FP16 causal
+attention-score matrix, 524288 x 2048 (seed 4), 4.29 GB moved per call.
 
-Cold-L2 lane (default): before every step a 512 MiB (>= 4x L2) buffer is READ
-outside the event pair, evicting the L2 without leaving dirty lines that the
-timed kernel would have to write back. Each step is timed with CUDA events
-on the stream the kernel is launched on; value = algorithmic bytes
-(2*M*N*elem_bytes per step, one read and one write of every element) over the
-summed step time.
+Protocol (cold lane, the default):
+  1. The input is generated on the host and copied to the device. One call
+     runs and its output is checked against the CPU oracle on sampled rows
+     BEFORE any timing; a result outside the tolerance prints an error line
+     and exits non-zero.
+  2. Cold L2 by rotation: the steps cycle through R input/output sets that
+     together span at least 1 GiB (>= 4x the L2); R = 1 when one set alone
+     is that large. No flush runs between steps, so every step reads input
+     that left the L2 long before, and the write-back of earlier steps'
+     outputs falls inside the timed region (steady state).
+  3. Timing: CUDA events on the launching stream around batches of
+     consecutive launches (about 200 us of work per batch, at least five
+     batches), so the event timer's granularity is spread over the batch.
+     The step time is the median over batches of batch time / launches;
+     value = algorithmic bytes / that median (2*M*N*elem_bytes per step);
+     the mean step is reported beside it.
+  4. The output of the last timed call is checked against the oracle again.
+  5. copy_baseline: a device copy of the same M x N elements (torch copy_,
+     same sets, same batches), the practical ceiling at this size.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all]
-                  [--lane cold|warm] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all|wide]
+                  [--lane cold|warm] [--impl ours|reference] [--api ...]
 
 --impl reference times the CPU oracle (the plain FP64 C implementation) on the
-host cores, on the same workload and metric. Prints one JSON line (rank 0).
+host cores, on the same workload and metric. Prints one JSON line per
+workload (rank 0).
 """
 from __future__ import annotations
 
 import argparse
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -40,7 +55,13 @@ import synth  # noqa: E402
 
 NOMINAL_HBM_GBS = 8000.0  # the bar's denominator: ~8 TB/s HBM3e
 FALLBACK_HBM_GBS = 6800.0
-FLUSH_BYTES = 512 << 20
+# The cold lane cycles through input/output sets spanning at least this many
+# device bytes (>= 4x the L2 of a GB300, checked at run time against the
+# device's own L2 size).
+ROTATE_BYTES = 1 << 30
+# Work per pair of timing events, and the fewest batches a run is cut into.
+BATCH_TARGET_US = 200.0
+MIN_BATCHES = 5
 CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -67,9 +88,10 @@ def parse_args(argv=None):
     ap.add_argument("--lane", choices=("cold", "warm"), default="cold")
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--plan", type=int, default=0, help="forced plan (0 = automatic)")
-    ap.add_argument("--cpu-budget", type=float, default=6.0,
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for the CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-copy", action="store_true", help="skip the copy baseline")
     ap.add_argument("--burst", type=float, default=1.0, help="seconds of load before timing")
     ap.add_argument("--rows", type=int, default=0,
                     help="use only the first ROWS rows (small cases for profiling)")
@@ -179,13 +201,13 @@ def oracle_pass(w, x, nthreads):
     return time.perf_counter() - t0, y
 
 
-def cpu_baseline(w, x, budget_s: float):
+def cpu_baseline(w, x, budget_s: float) -> dict:
     """The oracle as it stands, on all host cores, repeated for about budget_s."""
     nthreads = synth.host_threads()
-    times, y = [], None
+    times = []
     t_start = time.perf_counter()
     while True:
-        dt, y = oracle_pass(w, x, nthreads)
+        dt, _y = oracle_pass(w, x, nthreads)
         times.append(dt)
         if time.perf_counter() - t_start >= budget_s:
             break
@@ -201,7 +223,111 @@ def cpu_baseline(w, x, budget_s: float):
                       % (w.name, w.M, w.N, len(times), nthreads),
             "rows_per_s": round(w.M * len(times) / sum(times), 1),
             "serial": {"value": round(2 * rows * w.N * w.elem_bytes / t1 / 1e9, 4), "unit": "GB/s",
-                       "cores": 1, "sample": "first %d rows, one pass" % rows}}, y
+                       "cores": 1, "sample": "first %d rows, one pass" % rows}}
+
+
+# ---- protocol (host logic, no GPU) ------------------------------------------------
+
+def rotation_count(set_bytes: int, lane: str, rotate_bytes: int = ROTATE_BYTES) -> int:
+    """Input/output sets the cold lane cycles through: the fewest whose bytes
+    together reach rotate_bytes (1 when one set alone does). The warm lane
+    reuses one set."""
+    if lane == "warm":
+        return 1
+    return max(1, -(-int(rotate_bytes) // max(1, int(set_bytes))))
+
+
+def batch_plan(steps: int, est_us: float, target_us: float = BATCH_TARGET_US,
+               min_batches: int = MIN_BATCHES) -> int:
+    """Launches per timed batch: enough for about target_us of work, but no
+    more than leaves min_batches batches (when there are that many steps)."""
+    b = max(1, int(math.ceil(target_us / max(float(est_us), 1e-3))))
+    if steps >= min_batches:
+        b = min(b, steps // min_batches)
+    return max(1, min(b, max(1, steps)))
+
+
+def batch_bounds(steps: int, b: int):
+    """[start, end) step ranges of consecutive batches of b launches (the last may be short)."""
+    return [(s, min(s + b, steps)) for s in range(0, steps, b)]
+
+
+def batch_stats(batch_ms, bounds) -> dict:
+    """Per-step statistics in µs from batch times: each batch contributes its
+    time / launches; the median and spread are over the full batches (every
+    batch when all are short), the mean over every step."""
+    per = np.asarray([ms * 1e3 / (e - s) for ms, (s, e) in zip(batch_ms, bounds)],
+                     dtype=np.float64)
+    full_len = bounds[0][1] - bounds[0][0]
+    full = np.asarray([p for p, (s, e) in zip(per, bounds) if e - s == full_len])
+    if full.size == 0:
+        full = per
+    steps = bounds[-1][1]
+    med = float(np.median(full))
+    return {"median_step_us": round(med, 3),
+            "mean_step_us": round(float(sum(batch_ms)) * 1e3 / steps, 3),
+            "p10_p90_step_us": [round(float(np.percentile(full, 10)), 3),
+                                round(float(np.percentile(full, 90)), 3)],
+            "mad_step_us": round(float(np.median(np.abs(full - med))), 3),
+            "min_max_step_us": [round(float(full.min()), 3), round(float(full.max()), 3)],
+            "batches": len(bounds), "launches_per_batch": full_len}
+
+
+def l2_protocol(set_bytes: int, lane: str) -> str:
+    """The config's statement of how the L2 is kept from serving a step's input."""
+    if lane == "warm":
+        return "warm: one input/output set, no flush (diagnostic; L2 may serve the input)"
+    r = rotation_count(set_bytes, lane)
+    if r == 1:
+        return ("inputs larger than L2: one input/output set of %.2f GB, no flush; the "
+                "write-back of the previous step's output falls inside the timed region"
+                % (set_bytes / 1e9))
+    return ("rotation: %d input/output sets of %.1f MB (%.2f GB in all, >= 4x L2), no flush; "
+            "each step's input was last touched %.2f GB of traffic earlier and the write-back "
+            "of earlier outputs falls inside the timed region"
+            % (r, set_bytes / 1e6, r * set_bytes / 1e9, (r - 1) * set_bytes / 1e9))
+
+
+def workload_config(w, lane: str, world: int) -> dict:
+    """The config object both arms print for a softmax workload."""
+    set_bytes = (w.M * w.ld_in + w.M * w.ld_out) * w.elem_bytes
+    return {"workload": w.name, "M": w.M, "N": w.N, "ld_in": w.ld_in, "ld_out": w.ld_out,
+            "l2": l2_protocol(set_bytes, lane),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def parity_rows(M: int, N: int, max_elements: int = 1 << 25, seed: int = 12345) -> np.ndarray:
+    """Rows the bench checks against the oracle: all of them when the matrix has at
+    most max_elements entries, else a seeded sample of about max_elements / N rows
+    (always with the first and the last)."""
+    if M * N <= max_elements:
+        return np.arange(M, dtype=np.int64)
+    k = max(2, min(M, max_elements // N))
+    rng = np.random.default_rng(seed)
+    rows = rng.choice(M, size=k - 2, replace=False).astype(np.int64)
+    return np.unique(np.concatenate([rows, [0, M - 1]]))
+
+
+def oracle_rows(w, x, rows) -> np.ndarray:
+    """The oracle's output for the selected rows of the input x (M x ld_in)."""
+    import oracle
+    xs = np.ascontiguousarray(x[rows])
+    return oracle.softmax_rows(xs.reshape(-1), len(rows), w.N, w.ld_in, w.ld_out, w.dtype,
+                               nthreads=synth.host_threads())
+
+
+def compare_rows(w, got, ref, rows) -> dict:
+    """The gate |got - ref| <= atol + rtol |ref| (NaN where the oracle is NaN)
+    at the tolerances of the workload's dtype, over the given rows."""
+    g = synth.storage_to_float64(np.ascontiguousarray(got[:, :w.N]), w.dtype)
+    r = synth.storage_to_float64(np.ascontiguousarray(ref[:, :w.N]), w.dtype)
+    atol = 1e-6 if w.dtype == synth.F32 else 4e-3
+    bad = ~(np.abs(g - r) <= atol + atol * np.abs(r))
+    bad &= ~(np.isnan(g) & np.isnan(r))
+    diff = np.abs(g - r)
+    return {"rows": int(len(rows)), "of_rows": w.M, "elements": int(g.size),
+            "outside_tolerance": int(bad.sum()), "atol": atol, "rtol": atol,
+            "max_abs_err": float(np.nanmax(diff)) if np.isfinite(diff).any() else 0.0}
 
 
 # ---- GPU leg ----------------------------------------------------------------------
@@ -216,110 +342,79 @@ def gpu_uuid(device_index: int):
         return None
 
 
-def step_stats(ms) -> dict:
-    """Per-step time statistics in µs: median, p10/p90, MAD, min, max."""
-    us = np.asarray(ms, dtype=np.float64) * 1e3
-    med = float(np.median(us))
-    return {"median_step_us": round(med, 3),
-            "p10_p90_step_us": [round(float(np.percentile(us, 10)), 3),
-                                round(float(np.percentile(us, 90)), 3)],
-            "mad_step_us": round(float(np.median(np.abs(us - med))), 3),
-            "min_max_step_us": [round(float(us.min()), 3), round(float(us.max()), 3)]}
-
-
-def timed_steps(args, step, flush_l2, stream, rank, local_rank, world):
-    """Warm-up, a burst of load, then exactly args.steps steps, each between a
-    pair of CUDA events on `stream` (the L2 flush, if any, outside the pair),
-    with nvidia-smi sampling the clocks throughout. Returns (ms list, clocks)."""
+def device_l2_bytes(dev) -> int:
     import torch
-    for _ in range(max(3, args.warmup)):
-        flush_l2()
-        step()
+    props = torch.cuda.get_device_properties(dev)
+    return int(getattr(props, "L2_cache_size", 0) or 0)
+
+
+def device_rows(t, rows) -> np.ndarray:
+    """Selected rows of a device matrix as host storage (uint16 bits for 16-bit types)."""
+    import torch
+    y = t[torch.from_numpy(np.asarray(rows, dtype=np.int64)).to(t.device)].detach().cpu()
+    if y.dtype in (torch.bfloat16, torch.float16):
+        return y.view(torch.int16).numpy().view(np.uint16)
+    return y.numpy()
+
+
+def timed_batches(args, launch, n_sets, stream, rank, local_rank, world):
+    """Warm-up, a burst of load, then exactly args.steps launches between CUDA
+    events on `stream`, recorded at batch boundaries; step k uses set
+    k mod n_sets (the counter runs on through warm-up, so rotation never
+    restarts). nvidia-smi samples the clocks during the burst and the timed
+    region. Returns (batch ms list, bounds, clocks, set of the last timed step)."""
+    import torch
+    k = 0
+
+    def run(count):
+        nonlocal k
+        for _ in range(count):
+            launch(k % n_sets)
+            k += 1
+
+    run(max(3, args.warmup))
     torch.cuda.synchronize()
+    # Estimate a step from a run of launches in one event pair.
+    n_est = max(4, min(n_sets, 64))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    run(n_est)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    est_us = e0.elapsed_time(e1) * 1e3 / n_est
+    b = batch_plan(args.steps, est_us)
+    bounds = batch_bounds(args.steps, b)
     clk = ClockSampler(gpu_uuid(local_rank) if rank == 0 else None)
     with clk:
         t_end = time.perf_counter() + args.burst
         while time.perf_counter() < t_end:
-            for _ in range(20):
-                flush_l2()
-                step()
+            run(max(1, min(64, int(20000 / max(est_us, 1.0)))))
             torch.cuda.synchronize()
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(bounds) + 1)]
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        for k in range(args.steps):
-            flush_l2()
-            starts[k].record(stream)
-            step()
-            ends[k].record(stream)
+        evs[0].record(stream)
+        for j, (s, e) in enumerate(bounds):
+            run(e - s)
+            evs[j + 1].record(stream)
         torch.cuda.synchronize()
         if world > 1:
             torch.distributed.barrier()
-    return [a.elapsed_time(b) for a, b in zip(starts, ends)], clk.summary()
+    batch_ms = [evs[j].elapsed_time(evs[j + 1]) for j in range(len(bounds))]
+    return batch_ms, bounds, clk.summary(), (k - 1) % n_sets
 
 
-def run_ours(args, w, rank, local_rank, world):
-    import torch
-
-    import memory_bound_row_rows_gb300 as sr
-
-    dev = torch.device("cuda", local_rank)
-    torch.cuda.set_device(dev)
-    lib = sr.load()
-    x = w.generate()
-    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[w.dtype]
-
-    def host_tensor(a):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return t if w.dtype == synth.F32 else t.view(torch.int16).view(tdt)
-
-    x_dev = host_tensor(x).to(dev)
-    y_dev = torch.empty((w.M, w.ld_out), dtype=tdt, device=dev)
-    ws, ws_bytes = None, 0
-    if args.api == "split":
-        ws_bytes = sr.softmax_rows_split_workspace_bytes(x_dev, y_dev, w.M, w.N, w.ld_in,
-                                                         w.ld_out, w.dtype)
-        ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
-    # float32 so the reduction reads the buffer directly (an int32 sum would
-    # first widen it to int64, writing 1 GiB and leaving dirty lines in L2).
-    flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    plan_used = sr.softmax_rows_plan(x_dev, y_dev, w.M, w.N, w.ld_in, w.ld_out, w.dtype) \
-        if args.plan == 0 else args.plan
-
-    def step():
-        if args.api == "split":
-            st = lib.softmax_rows_split(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
-                                        w.ld_out, w.dtype, ws.data_ptr(), ws_bytes, sh)
-        elif args.api == "masked":
-            st = lib.softmax_rows_masked(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
-                                         w.ld_out, w.dtype, None, w.causal_period, args.plan, sh)
-        else:
-            st = lib.softmax_rows_ex(x_dev.data_ptr(), y_dev.data_ptr(), w.M, w.N, w.ld_in,
-                                     w.ld_out, w.dtype, args.plan, sh)
-        if st != 0:
-            raise RuntimeError("softmax_rows failed: %s" % sr.softmax_rows_strerror(st))
-
-    def flush_l2():
-        if args.lane == "cold":
-            torch.sum(flush)  # reads 512 MiB: L2 now holds clean lines only
-
-    ms, clocks = timed_steps(args, step, flush_l2, stream, rank, local_rank, world)
-    assert sr.softmax_rows_last_device_error() == sr.SR_OK
-
-    e2e = None
-    if not args.no_e2e:
-        e2e = run_e2e(args, w, x, dev, lib, host_tensor, tdt)
-    if args.api == "split":
-        plan_used = "split"
-    elif args.api == "masked":
-        plan_used = "masked-" + sr.PLAN_NAMES.get(plan_used, str(plan_used))
-    return {"ms": ms, "clocks": clocks,
-            "plan": plan_used if isinstance(plan_used, str) else sr.PLAN_NAMES.get(plan_used, str(plan_used)),
-            "y_dev": y_dev, "e2e": e2e, "x": x}
+def kernel_record(sr) -> dict:
+    """Registers, local (spill) bytes and launch shape of the last kernel launched."""
+    try:
+        info = sr.softmax_rows_last_launch()
+    except Exception as exc:  # pragma: no cover - reported, not fatal
+        return {"error": str(exc)}
+    return {"name": info["name"], "registers": info["registers"],
+            "local_bytes": info["local_bytes"], "static_smem_bytes": info["static_smem_bytes"],
+            "dynamic_smem_bytes": info["dynamic_smem_bytes"], "grid": info["grid"],
+            "block": info["block"], "cluster": info["cluster"]}
 
 
 def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
@@ -379,30 +474,6 @@ def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
             "staged_gbs": round(w.fused_bytes / sec_s / 1e9, 2)}
 
 
-def parity_vs_oracle(w, y_dev, y_ref, max_elements: int = 1 << 25):
-    """Compare the GPU output with the CPU-baseline leg's oracle output.
-
-    Every row when the matrix has at most ``max_elements`` entries, otherwise
-    an evenly strided subset of rows (always including the first and last).
-    """
-    import torch
-    step = max(1, -(-w.M * w.N // max_elements))
-    rows = np.unique(np.concatenate([np.arange(0, w.M, step), [w.M - 1]]))
-    y = y_dev[torch.from_numpy(rows).to(y_dev.device)].detach().cpu()
-    if w.dtype != synth.F32:
-        y = y.view(torch.int16)
-    y = y.numpy()
-    if w.dtype != synth.F32:
-        y = y.view(np.uint16)
-    g = synth.storage_to_float64(y[:, :w.N], w.dtype)
-    r = synth.storage_to_float64(y_ref[rows, :w.N], w.dtype)
-    atol = 1e-6 if w.dtype == synth.F32 else 4e-3
-    bad = ~(np.abs(g - r) <= atol + atol * np.abs(r))
-    bad &= ~(np.isnan(g) & np.isnan(r))
-    return {"rows": int(rows.size), "of_rows": w.M, "elements": int(g.size),
-            "outside_tolerance": int(bad.sum()), "atol": atol, "rtol": atol,
-            "max_abs_err": float(np.nanmax(np.abs(g - r)))}
-
 
 def algorithmic_bytes(w, api: str) -> int:
     """Bytes one call must move: every element read once and written once; with
@@ -433,53 +504,175 @@ def replica_throughput(fused_bytes: int, steps: int, world: int, slowest_total_s
     return world * fused_bytes * steps / slowest_total_s / 1e9
 
 
+
+
+class ParityFailure(RuntimeError):
+    """The GPU output left the tolerance: no throughput is reported."""
+
+    def __init__(self, line):
+        super().__init__("parity gate failed")
+        self.line = line
+
+
+def torch_dtype(dtype):
+    import torch
+    return {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[dtype]
+
+
+def to_device(a, dtype, dev):
+    """Host storage (float32, or uint16 bits) -> device tensor of the dtype."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype != synth.F32:
+        t = t.view(torch.int16).view(torch_dtype(dtype))
+    return t.to(dev)
+
+
+def copy_baseline(args, launch_copy, n_sets, stream, rank, local_rank, world, nbytes):
+    """A device copy of the same elements under the same rotation and batches."""
+    batch_ms, bounds, _clk, _last = timed_batches(args, launch_copy, n_sets, stream, rank,
+                                                  local_rank, world)
+    st = batch_stats(batch_ms, bounds)
+    med_s = max_over_ranks(st["median_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
+    return {"value": round(world * nbytes / med_s / 1e9, 2), "unit": "GB/s",
+            "median_step_us": st["median_step_us"], "mean_step_us": st["mean_step_us"],
+            "kind": "torch copy_ of the same M x N elements (input pitch to output pitch), "
+                    "same sets and batches"}
+
+
 def bench_ours(args, w):
     import torch
+
+    import memory_bound_row_rows_gb300 as sr
+    from memory_bound_row_rows_gb300 import _build
     rank, local_rank, world = dist_env()
     if world > 1 and not torch.distributed.is_initialized():
         torch.distributed.init_process_group("nccl")
-    from memory_bound_row_rows_gb300 import _build
-    res = run_ours(args, w, rank, local_rank, world)
-    ms = res["ms"]
-    total_s = max_over_ranks(sum(ms) / 1e3, device="cuda" if world > 1 else "cpu")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    lib = sr.load()
+    x = w.generate()
+    tdt = torch_dtype(w.dtype)
+
+    # Input/output sets: every set's input holds the same matrix.
+    set_bytes = (w.M * w.ld_in + w.M * w.ld_out) * w.elem_bytes
+    n_sets = rotation_count(set_bytes, args.lane)
+    l2 = device_l2_bytes(dev)
+    while args.lane == "cold" and l2 and n_sets * set_bytes < 4 * l2:
+        n_sets += 1
+    x_sets = torch.empty((n_sets, w.M, w.ld_in), dtype=tdt, device=dev)
+    x_sets[0].copy_(to_device(x, w.dtype, dev))
+    for i in range(1, n_sets):
+        x_sets[i].copy_(x_sets[0])
+    y_sets = torch.full((n_sets, w.M, w.ld_out), float("nan"), dtype=tdt, device=dev)
+    ws, ws_bytes = None, 0
+    if args.api == "split":
+        ws_bytes = sr.softmax_rows_split_workspace_bytes(x_sets[0], y_sets[0], w.M, w.N, w.ld_in,
+                                                         w.ld_out, w.dtype)
+        ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    plan_used = sr.softmax_rows_plan(x_sets[0], y_sets[0], w.M, w.N, w.ld_in, w.ld_out,
+                                     w.dtype) if args.plan == 0 else args.plan
+    xp = [x_sets[i].data_ptr() for i in range(n_sets)]
+    yp = [y_sets[i].data_ptr() for i in range(n_sets)]
+
+    def launch(i):
+        if args.api == "split":
+            st = lib.softmax_rows_split(xp[i], yp[i], w.M, w.N, w.ld_in, w.ld_out, w.dtype,
+                                        ws.data_ptr(), ws_bytes, sh)
+        elif args.api == "masked":
+            st = lib.softmax_rows_masked(xp[i], yp[i], w.M, w.N, w.ld_in, w.ld_out, w.dtype,
+                                         None, w.causal_period, args.plan, sh)
+        else:
+            st = lib.softmax_rows_ex(xp[i], yp[i], w.M, w.N, w.ld_in, w.ld_out, w.dtype,
+                                     args.plan, sh)
+        if st != 0:
+            raise RuntimeError("softmax_rows failed: %s" % sr.softmax_rows_strerror(st))
+
+    if args.api == "split":
+        plan_used = "split"
+    elif args.api == "masked":
+        plan_used = "masked-" + sr.PLAN_NAMES.get(plan_used, str(plan_used))
+    else:
+        plan_used = sr.PLAN_NAMES.get(plan_used, str(plan_used))
+    config = workload_config(w, args.lane, world)
+    metric = (("cold-L2 softmax GB/s (2*M*N*bytes/time)" if args.lane == "cold"
+               else "warm-L2 softmax GB/s (2*M*N*bytes/time)") if args.api != "masked"
+              else "cold-L2 masked softmax GB/s ((valid reads + M*N writes)*bytes/time)")
+
+    # 1. Correctness before any timing: one call, sampled rows against the oracle.
+    rows = parity_rows(w.M, w.N)
+    ref = oracle_rows(w, x, rows)
+    launch(0)
+    torch.cuda.synchronize()
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    gate = compare_rows(w, device_rows(y_sets[0], rows), ref, rows)
+    if gate["outside_tolerance"]:
+        raise ParityFailure({"metric": metric, "error": "parity: output outside the tolerance "
+                             "before timing", "config": config, "plan": plan_used,
+                             "parity_before_timing": gate})
+
+    # 2-3. Timed steps over the rotating sets.
+    batch_ms, bounds, clocks, last = timed_batches(args, launch, n_sets, stream, rank,
+                                                   local_rank, world)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    kernel = kernel_record(sr)
+    stats = batch_stats(batch_ms, bounds)
+    med_s = max_over_ranks(stats["median_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
+    mean_s = max_over_ranks(stats["mean_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
+
+    # 4. The last timed call's output.
+    after = compare_rows(w, device_rows(y_sets[last], rows), ref, rows)
+
+    nbytes = algorithmic_bytes(w, args.api)
+    copy = None
+    if not args.no_copy:
+        def launch_copy(i):
+            y_sets[i][:, :w.N].copy_(x_sets[i][:, :w.N])
+        copy = copy_baseline(args, launch_copy, n_sets, stream, rank, local_rank, world,
+                             w.fused_bytes)
+    e2e = None
+    if not args.no_e2e:
+        del x_sets, y_sets
+        torch.cuda.empty_cache()
+        e2e = run_e2e(args, w, x, dev, lib, lambda a: to_device(a, w.dtype, "cpu"), tdt)
     if rank != 0:
         return None
-    steps = len(ms)
-    mean_s = total_s / steps
-    nbytes = algorithmic_bytes(w, args.api)
-    value = replica_throughput(nbytes, steps, world, total_s)
+    steps = bounds[-1][1]
+    value = world * nbytes / med_s / 1e9
     peaks = measured_peaks()
-    src_hash = _build.source_hash(_build.PLAN_SOURCES.get(res["plan"]))
-    traffic, rec = recorded_traffic(w.name, res["plan"])
-    achieved = nbytes / (sum(ms) / 1e3 / steps) / 1e9
+    src_hash = _build.source_hash(_build.PLAN_SOURCES.get(plan_used.replace("masked-", "")))
+    traffic, rec = recorded_traffic(w.name, plan_used)
+    achieved = nbytes / (stats["median_step_us"] / 1e6) / 1e9
     line = {
-        "metric": ("cold-L2 softmax GB/s (2*M*N*bytes/time)" if args.lane == "cold"
-                   else "warm-L2 softmax GB/s (2*M*N*bytes/time)") if args.api != "masked"
-        else "cold-L2 masked softmax GB/s ((valid reads + M*N writes)*bytes/time)",
+        "metric": metric,
         "value": round(value, 2),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": steps,
         "warmup": args.warmup,
-        "ms_per_step": round(mean_s * 1e3, 5),
+        "ms_per_step": round(med_s * 1e3, 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": synth.DTYPE_NAMES[w.dtype],
         "data": "synthetic: seeded SplitMix64/Box-Muller (seed %d), generated on the host" % w.seed,
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "ld_in": w.ld_in, "ld_out": w.ld_out,
-                   "plan": res["plan"], "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": ("flushed: a 512 MiB device buffer is read before every step, outside "
-                          "the event pair") if args.lane == "cold" else "warm (no flush)",
-                   "inputs_resident_in_hbm": True},
+        "config": config,
+        "plan": plan_used,
+        "statistic": "ms_per_step and value use the median step (over batches of consecutive "
+                     "launches); mean_step_us is the mean over all timed steps",
+        "mean_step_gbs": round(world * nbytes / mean_s / 1e9, 2),
         "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
-        "rows_per_s": round(world * w.M * steps / total_s, 1),
+        "rows_per_s": round(world * w.M / med_s, 1),
         "bytes_per_step": nbytes,
-        "dense_equivalent_gbs": round(world * w.fused_bytes * steps / total_s / 1e9, 2),
-        **step_stats(ms),
-        "gpu_launches": steps * (2 if res["plan"] == "split" else 1),
-        "clocks": res["clocks"],
+        "dense_equivalent_gbs": round(world * w.fused_bytes / med_s / 1e9, 2),
+        **stats,
+        "sets": n_sets,
+        "gpu_launches": steps * (2 if plan_used == "split" else 1),
+        "kernel": kernel,
+        "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2),
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -488,17 +681,22 @@ def bench_ours(args, w):
                      "traffic_note": (rec or {}).get("note") if traffic else
                      "null: no ncu capture recorded for the current kernel sources"},
         "source_hash": src_hash,
+        "parity_before_timing": gate,
+        "parity": after,
     }
-    if res["e2e"] is not None:
-        line["e2e"] = res["e2e"]
+    if copy is not None:
+        copy["ratio"] = round(value / world / (copy["value"] / world), 4)
+        line["copy_baseline"] = copy
+    if e2e is not None:
+        line["e2e"] = e2e
     if world == 1:
-        cpu, y_ref = cpu_baseline(w, res["x"], args.cpu_budget)
-        line["cpu_baseline"] = cpu
-        line["parity"] = parity_vs_oracle(w, res["y_dev"], y_ref)
+        line["cpu_baseline"] = cpu_baseline(w, x, args.cpu_budget)
+    if after["outside_tolerance"]:
+        line.pop("value")
+        line["error"] = "parity: the last timed output is outside the tolerance"
+        raise ParityFailure(line)
     return line
 
-
-# ---- row-pair lanes: softmax backward and residual RMSNorm ----------------------
 
 def _ulp(r, dtype):
     mant = {synth.F32: 23, synth.BF16: 7, synth.F16: 10}[dtype]
@@ -624,8 +822,29 @@ def pair_cpu_baseline(lane, budget_s: float):
                       % (rows.size, lane.w.M, lane.w.name, len(times), lane.label)}
 
 
+
+
+def pair_config(lane, lane_name: str, world: int) -> dict:
+    """The config object both arms print for a row-pair workload."""
+    w = lane.w
+    set_bytes = 3 * w.M * w.ld * w.elem_bytes
+    return {"workload": "%s %s" % (lane.api, w.name), "M": w.M, "N": w.N, "ld": w.ld,
+            "l2": l2_protocol(set_bytes, lane_name),
+            "parallelism": "replicas" if world > 1 else "single GPU"}
+
+
+def pair_parity(lane, out, rows) -> dict:
+    w = lane.w
+    g = device_rows(out, rows)
+    r = lane.oracle_rows(rows)
+    dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :w.N]), w.dtype)
+    return {"rows": int(rows.size), "of_rows": w.M,
+            "outside_tolerance": lane.outside_gate(dec(g), dec(r), rows), "gate": lane.gate}
+
+
 def bench_pair(args, lane):
-    """One row-pair call per step (softmax_rows_backward_ex or rmsnorm_residual_rows_ex)."""
+    """One row-pair call per step (softmax_rows_backward_ex or rmsnorm_residual_rows_ex),
+    under the softmax lane's protocol: parity first, rotating sets, batched events."""
     import torch
 
     import memory_bound_row_rows_gb300 as sr
@@ -637,45 +856,65 @@ def bench_pair(args, lane):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     lib = sr.load()
-    tdt = {synth.F32: torch.float32, synth.BF16: torch.bfloat16, synth.F16: torch.float16}[w.dtype]
-
-    def host_tensor(a):
-        t = torch.from_numpy(np.ascontiguousarray(a))
-        return t if w.dtype == synth.F32 else t.view(torch.int16).view(tdt)
-
-    dev_mats = [host_tensor(m).to(dev) for m in lane.mats]
-    dev_vecs = [host_tensor(v).to(dev) for v in lane.vecs]
-    out = torch.empty((w.M, w.N), dtype=tdt, device=dev)
-    flush = torch.zeros(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    tdt = torch_dtype(w.dtype)
+    set_bytes = 3 * w.M * w.ld * w.elem_bytes
+    n_sets = rotation_count(set_bytes, args.lane)
+    l2 = device_l2_bytes(dev)
+    while args.lane == "cold" and l2 and n_sets * set_bytes < 4 * l2:
+        n_sets += 1
+    sets = []
+    first = [to_device(m, w.dtype, dev) for m in lane.mats]
+    vecs = [to_device(v, w.dtype, dev) for v in lane.vecs]
+    for i in range(n_sets):
+        mats = first if i == 0 else [m.clone() for m in first]
+        sets.append((mats, torch.full((w.M, w.ld), float("nan"), dtype=tdt, device=dev)))
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    plan = lane.plan(sr, dev_mats, dev_vecs, out, args.plan)
+    plan = lane.plan(sr, sets[0][0], vecs, sets[0][1], args.plan)
     if plan < 0:
         raise RuntimeError("plan %d cannot take %s %s" % (args.plan, lane.api, w.name))
 
-    def step():
-        st = lane.call(lib, dev_mats, dev_vecs, out, args.plan, sh)
+    def launch(i):
+        mats, out = sets[i]
+        st = lane.call(lib, mats, vecs, out, args.plan, sh)
         if st != 0:
             raise RuntimeError("%s failed: %s" % (lane.api, sr.softmax_rows_strerror(st)))
 
-    def flush_l2():
-        if args.lane == "cold":
-            torch.sum(flush)
+    pname = "%s-%s" % (lane.api, sr.PLAN_NAMES[plan])
+    lanename = "cold-L2" if args.lane == "cold" else "warm-L2"
+    metric = "%s %s GB/s (%s/time)" % (lanename, lane.label, lane.model)
+    config = pair_config(lane, args.lane, world)
+    rows = np.unique(np.concatenate([np.linspace(0, w.M - 1, 64).astype(np.int64), [w.M - 1]]))
+    launch(0)
+    torch.cuda.synchronize()
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    gate = pair_parity(lane, sets[0][1], rows)
+    if gate["outside_tolerance"]:
+        raise ParityFailure({"metric": metric, "error": "parity: output outside the gate "
+                             "before timing", "config": config, "plan": pname,
+                             "parity_before_timing": gate})
 
-    ms, clocks = timed_steps(args, step, flush_l2, stream, rank, local_rank, world)
-    total_s = max_over_ranks(sum(ms) / 1e3, device="cuda" if world > 1 else "cpu")
+    batch_ms, bounds, clocks, last = timed_batches(args, launch, n_sets, stream, rank,
+                                                   local_rank, world)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    kernel = kernel_record(sr)
+    stats = batch_stats(batch_ms, bounds)
+    med_s = max_over_ranks(stats["median_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
+    mean_s = max_over_ranks(stats["mean_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
+    after = pair_parity(lane, sets[last][1], rows)
 
     e2e = None
     if not args.no_e2e:
         # Host buffers: the pinned inputs copied in, the call, the output copied back.
-        pins = [host_tensor(m).pin_memory() for m in lane.mats + lane.vecs]
-        out_pin = torch.empty((w.M, w.N), dtype=tdt).pin_memory()
-        targets = dev_mats + dev_vecs
+        pins = [to_device(m, w.dtype, "cpu").pin_memory() for m in lane.mats + lane.vecs]
+        mats0, out = sets[0]
+        out_pin = torch.empty((w.M, w.ld), dtype=tdt).pin_memory()
+        targets = mats0 + vecs
 
         def e2e_step():
             for d, h in zip(targets, pins):
                 d.copy_(h, non_blocking=True)
-            step()
+            launch(0)
             out_pin.copy_(out, non_blocking=True)
 
         for _ in range(3):
@@ -691,35 +930,35 @@ def bench_pair(args, lane):
         sec = t0.elapsed_time(t1) / 1e3 / k
         e2e = {"value": round(w.fused_bytes / sec / 1e9, 2), "unit": "GB/s",
                "h2d_bytes_per_step": sum(p.numel() * p.element_size() for p in pins),
-               "d2h_bytes_per_step": w.M * w.N * w.elem_bytes,
+               "d2h_bytes_per_step": w.M * w.ld * w.elem_bytes,
                "ms_per_step": round(sec * 1e3, 4), "steps": k,
                "path": "pinned host inputs -> device (copies), %s call, output -> pinned host, "
                        "in order on one stream" % lane.api}
     if rank != 0:
         return None
-    steps = len(ms)
-    value = replica_throughput(w.fused_bytes, steps, world, total_s)
-    achieved = w.fused_bytes / (sum(ms) / 1e3 / steps) / 1e9
+    steps = bounds[-1][1]
+    value = world * w.fused_bytes / med_s / 1e9
+    achieved = w.fused_bytes / (stats["median_step_us"] / 1e6) / 1e9
     peaks = measured_peaks()
-    pname = "%s-%s" % (lane.api, sr.PLAN_NAMES[plan])
     traffic, rec = recorded_traffic("%s:%s" % (lane.api, w.name), lane.api)
-    lanename = "cold-L2" if args.lane == "cold" else "warm-L2"
     line = {
-        "metric": "%s %s GB/s (%s/time)" % (lanename, lane.label, lane.model),
+        "metric": metric,
         "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": steps,
-        "warmup": args.warmup, "ms_per_step": round(total_s / steps * 1e3, 5),
+        "warmup": args.warmup, "ms_per_step": round(med_s * 1e3, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": synth.DTYPE_NAMES[w.dtype], "data": lane.data,
-        "config": {"workload": "%s %s" % (lane.api, w.name), "M": w.M, "N": w.N, "ld": w.ld,
-                   "plan": pname, "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": ("flushed: a 512 MiB device buffer is read before every step, outside "
-                          "the event pair") if args.lane == "cold" else "warm (no flush)",
-                   "inputs_resident_in_hbm": True},
+        "config": config,
+        "plan": pname,
+        "statistic": "ms_per_step and value use the median step (over batches of consecutive "
+                     "launches); mean_step_us is the mean over all timed steps",
+        "mean_step_gbs": round(world * w.fused_bytes / mean_s / 1e9, 2),
         "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "bytes_per_step": w.fused_bytes,
-        **step_stats(ms),
+        **stats,
+        "sets": n_sets,
         "gpu_launches": steps,
+        "kernel": kernel,
         "clocks": clocks,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peaks["hbm_gbs"],
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
@@ -728,20 +967,17 @@ def bench_pair(args, lane):
                      "traffic_note": (rec or {}).get("note") if traffic else
                      "null: no ncu capture recorded for the current kernel sources"},
         "source_hash": _build.source_hash(_build.PLAN_SOURCES[lane.api]),
+        "parity_before_timing": gate,
+        "parity": after,
     }
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1:
         line["cpu_baseline"] = pair_cpu_baseline(lane, args.cpu_budget)
-        rows = np.unique(np.concatenate([np.linspace(0, w.M - 1, 64).astype(np.int64),
-                                         [w.M - 1]]))
-        g = out[torch.from_numpy(rows).to(dev)].cpu()
-        g = g.numpy() if w.dtype == synth.F32 else g.view(torch.int16).numpy().view(np.uint16)
-        r = lane.oracle_rows(rows)
-        dec = lambda a: synth.storage_to_float64(np.ascontiguousarray(a[:, :w.N]), w.dtype)
-        line["parity"] = {"rows": int(rows.size), "of_rows": w.M,
-                          "outside_tolerance": lane.outside_gate(dec(g), dec(r), rows),
-                          "gate": lane.gate}
+    if after["outside_tolerance"]:
+        line.pop("value")
+        line["error"] = "parity: the last timed output is outside the gate"
+        raise ParityFailure(line)
     return line
 
 
@@ -758,17 +994,19 @@ def bench_reference(args, w):
     for _ in range(args.steps):
         dt, _y = oracle_pass(w, x, nthreads)
         times.append(dt)
-    total = sum(times)
-    value = w.fused_bytes * len(times) / total / 1e9
+    med = float(np.median(times))
+    value = w.fused_bytes / med / 1e9
     return {
         "impl": "reference",
         "metric": "cold-L2 softmax GB/s (2*M*N*bytes/time)",
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
-        "warmup": args.warmup, "ms_per_step": round(1e3 * total / len(times), 3),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * med, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": synth.DTYPE_NAMES[w.dtype],
-        "data": "synthetic: seeded SplitMix64/Box-Muller (seed %d)" % w.seed,
-        "config": {"workload": w.name, "M": w.M, "N": w.N, "ld_in": w.ld_in, "ld_out": w.ld_out},
+        "data": "synthetic: seeded SplitMix64/Box-Muller (seed %d), generated on the host" % w.seed,
+        "config": workload_config(w, args.lane, world),
+        "statistic": "ms_per_step and value use the median step; mean_step_us is the mean",
+        "mean_step_us": round(1e6 * sum(times) / len(times), 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthreads,
                          "kind": "oracle",
                          "sample": "whole %s matrix per step, FP64 C oracle, %d threads"
@@ -792,17 +1030,19 @@ def bench_reference_pair(args, lane):
         t0 = time.perf_counter()
         lane.oracle_rows(rows)
         times.append(time.perf_counter() - t0)
-    value = per_row * rows.size * len(times) / sum(times) / 1e9
+    med = float(np.median(times))
+    value = per_row * rows.size / med / 1e9
     sample = "first %d of %d rows of %s per step, FP64 C oracle's %s, 1 thread" % (
         rows.size, w.M, w.name, lane.label)
     return {
         "impl": "reference",
         "metric": "cold-L2 %s GB/s (%s/time)" % (lane.label, lane.model),
         "value": round(value, 4), "unit": "GB/s", "n_gpus": world, "steps": len(times),
-        "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 3),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * med, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": synth.DTYPE_NAMES[w.dtype], "data": lane.data,
-        "config": {"workload": "%s %s" % (lane.api, w.name), "M": w.M, "N": w.N, "ld": w.ld},
+        "config": pair_config(lane, args.lane, world),
+        "statistic": "ms_per_step and value use the median step",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -822,25 +1062,32 @@ def main(argv=None):
         wl = args.workload or synth.HEADLINE
         names = (list(synth.WORKLOADS) if wl == "all" else
                  list(synth.WIDE_FEW) if wl == "wide" else [wl])
+    failed = False
     for name in names:
         w = catalog[name]
         if args.rows:
             w = w.with_rows(min(args.rows, w.M))
-        if args.impl == "reference" and args.api in LANES:
-            line = bench_reference_pair(args, LANES[args.api](w))
-        elif args.impl == "reference":
-            line = bench_reference(args, w)
-        elif args.api in LANES:
-            line = bench_pair(args, LANES[args.api](w))
-        else:
-            line = bench_ours(args, w)
+        try:
+            if args.impl == "reference" and args.api in LANES:
+                line = bench_reference_pair(args, LANES[args.api](w))
+            elif args.impl == "reference":
+                line = bench_reference(args, w)
+            elif args.api in LANES:
+                line = bench_pair(args, LANES[args.api](w))
+            else:
+                line = bench_ours(args, w)
+        except ParityFailure as exc:
+            line, failed = exc.line, True
+            if dist_env()[0] != 0:
+                line = None
         if line is not None:
             print(json.dumps(line), flush=True)
     if args.impl == "ours":
         import torch
         if torch.distributed.is_initialized():
             torch.distributed.destroy_process_group()
+    return 1 if failed else 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

@@ -290,7 +290,6 @@ SR_API int softmax_rows_split_noalloc(const void* in, void* out, int64_t M, int6
                                       int64_t ld_in, int64_t ld_out, int dtype,
                                       sr_stream_t stream);
 
-/* A static, human-readable name for an sr_status value. */
 /*
  * Softmax backward ("Measured optimization case studies", Training: backward
  * kernels through autograd: the softmax keeps its output y and forms
@@ -387,9 +386,9 @@ SR_API int rmsnorm_residual_rows_plan(const void* x, const void* residual, const
                                       int64_t ld_r, int64_t ld_y, float eps, int dtype, int plan,
                                       int sm_count);
 
+/* A static, human-readable name for an sr_status value. */
 SR_API const char* softmax_rows_strerror(int status);
 
-/* Library version as major*10000 + minor*100 + patch. */
 /*
  * Host-only description of how the WIDE plan runs M rows of N elements (of
  * the dtype, rows aligned or sharing their offset from a 16-byte boundary)
@@ -403,6 +402,37 @@ SR_API const char* softmax_rows_strerror(int status);
 SR_API int softmax_rows_wide_shape(int64_t M, int64_t N, int dtype, int sm_count, int* csize,
                                    int* kv, int64_t* slice, int* streamed);
 
+/*
+ * What the calling host thread's last kernel launch through this library
+ * looked like, for result records and profiles (the pages tie kernel speed to
+ * register pressure: "Measured optimization case studies", Specialize). It
+ * describes the last kernel any entry point launched from this thread: for
+ * softmax_rows_split, the second of its two kernels. Fields:
+ *   registers            registers per thread of the kernel as compiled
+ *   local_bytes          local memory per thread (register spills and stack)
+ *   static_smem_bytes    statically declared shared memory per block
+ *   dynamic_smem_bytes   dynamic shared memory the launch requested per block
+ *   grid, block          blocks launched (x) and threads per block
+ *   cluster              blocks per thread-block cluster (1: no cluster)
+ *   name                 the kernel's symbol name, NUL-terminated (truncated)
+ * The attributes come from cudaFuncGetAttributes on the current device.
+ * Returns SR_OK; SR_EINVAL when info is NULL or this thread has launched no
+ * kernel yet; SR_ECUDA when the attribute query fails.
+ */
+typedef struct sr_launch_info {
+    int registers;
+    int local_bytes;
+    int static_smem_bytes;
+    int dynamic_smem_bytes;
+    int grid;
+    int block;
+    int cluster;
+    char name[256];
+} sr_launch_info;
+
+SR_API int softmax_rows_last_launch(sr_launch_info* info);
+
+/* Library version as major*10000 + minor*100 + patch. */
 SR_API int softmax_rows_version(void);
 
 #ifdef __cplusplus

@@ -23,7 +23,7 @@ __all__ = [
     "softmax_rows_host_mapped",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
     "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
-    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape",
+    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape", "softmax_rows_last_launch",
     "softmax", "softmax_backward", "rmsnorm_residual",
     "dtype_code",
 ]
@@ -90,6 +90,7 @@ def load():
                                        c_int],
         "softmax_rows_version": [],
         "softmax_rows_wide_shape": [i64, i64, c_int, c_int, vp, vp, vp, vp],
+        "softmax_rows_last_launch": [vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -283,6 +284,25 @@ def softmax_rows_strerror(status: int) -> str:
 
 def softmax_rows_version() -> int:
     return int(load().softmax_rows_version())
+
+
+class LaunchInfo(ctypes.Structure):
+    """Mirror of sr_launch_info."""
+    _fields_ = [("registers", ctypes.c_int), ("local_bytes", ctypes.c_int),
+                ("static_smem_bytes", ctypes.c_int), ("dynamic_smem_bytes", ctypes.c_int),
+                ("grid", ctypes.c_int), ("block", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("name", ctypes.c_char * 256)]
+
+
+def softmax_rows_last_launch() -> dict:
+    """The calling thread's last kernel launch through the library, as a dict
+    (registers, local_bytes, static_smem_bytes, dynamic_smem_bytes, grid, block,
+    cluster, name)."""
+    info = LaunchInfo()
+    _check(load().softmax_rows_last_launch(ctypes.byref(info)), "softmax_rows_last_launch")
+    d = {name: getattr(info, name) for name, _ in LaunchInfo._fields_}
+    d["name"] = info.name.decode(errors="replace")
+    return d
 
 
 def dtype_code(torch_dtype) -> int:

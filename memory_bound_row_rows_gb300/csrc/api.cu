@@ -87,6 +87,20 @@ const DeviceInfo* device_info(cudaError_t* err) {
 
 }  // namespace
 
+namespace {
+struct LaunchRecord {
+    const void* func = nullptr;
+    dim3 grid, block;
+    size_t smem = 0;
+    int cluster = 1;
+};
+thread_local LaunchRecord t_last_launch;
+}  // namespace
+
+void note_launch(const void* func, dim3 grid, dim3 block, size_t smem, int cluster) {
+    t_last_launch = LaunchRecord{func, grid, block, smem, cluster};
+}
+
 int blocks_per_sm(const void* func, int threads, size_t smem) {
     const OccKey key{current_device(), func, threads, smem, 0};
     {
@@ -605,6 +619,28 @@ int softmax_rows_wide_shape(int64_t M, int64_t N, int dtype, int sm_count, int* 
     return 0;
 }
 
-int softmax_rows_version(void) { return 100; }
+int softmax_rows_last_launch(sr_launch_info* info) {
+    const sr::LaunchRecord& r = sr::t_last_launch;
+    if (info == nullptr || r.func == nullptr) return SR_EINVAL;
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, r.func) != cudaSuccess) return SR_ECUDA;
+    info->registers = fa.numRegs;
+    info->local_bytes = (int)fa.localSizeBytes;
+    info->static_smem_bytes = (int)fa.sharedSizeBytes;
+    info->dynamic_smem_bytes = (int)r.smem;
+    info->grid = (int)r.grid.x;
+    info->block = (int)r.block.x;
+    info->cluster = r.cluster;
+    info->name[0] = '\0';
+    const char* name = nullptr;
+    if (cudaFuncGetName(&name, r.func) == cudaSuccess && name != nullptr) {
+        size_t k = 0;
+        for (; name[k] != '\0' && k + 1 < sizeof(info->name); ++k) info->name[k] = name[k];
+        info->name[k] = '\0';
+    }
+    return SR_OK;
+}
+
+int softmax_rows_version(void) { return 200; }
 
 }  // extern "C"

@@ -252,6 +252,7 @@ cudaError_t launch_grid(void (*kern)(const T*, T*, int64_t, int64_t, int64_t, in
                         int nt, const Problem& p) {
     const int64_t cap = 0x7fffffff;
     const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
+    note_launch(kern, grid, nt);
     kern<<<grid, nt, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
                                     p.N, p.ld_in, p.ld_out, p.mask);
     return cudaGetLastError();
@@ -266,6 +267,7 @@ cudaError_t launch_nt_kv(const Problem& p) {
         auto kern = block_packed_kernel<T, NT, KV>;
         const int64_t cap = 0x7fffffff;
         const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
+        note_launch(kern, grid, NT);
         kern<<<grid, NT, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
                                         p.N, p.ld_in, p.ld_out);
         return cudaGetLastError();

@@ -97,6 +97,14 @@ inline int cluster_size_for(int64_t N, int dtype, int min_cluster) {
     return 0;
 }
 
+// The calling host thread's record of the last kernel it launched through the
+// library (read back by softmax_rows_last_launch). Every launch site calls it.
+void note_launch(const void* func, dim3 grid, dim3 block, size_t smem, int cluster);
+template <typename F>
+inline void note_launch(F* func, dim3 grid, dim3 block, size_t smem = 0, int cluster = 1) {
+    note_launch(reinterpret_cast<const void*>(func), grid, block, smem, cluster);
+}
+
 // Resident blocks per SM for a kernel (cached per device).
 int blocks_per_sm(const void* func, int threads, size_t smem);
 // Resident clusters on the device for a cluster launch (cached per device).

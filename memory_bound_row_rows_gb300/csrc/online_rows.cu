@@ -81,6 +81,7 @@ cudaError_t launch_m(const Problem& p) {
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
     const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
+    note_launch(kern, grid, kOnlineThreads);
     kern<<<grid, kOnlineThreads, 0, p.stream>>>(static_cast<const T*>(p.in),
                                                 static_cast<T*>(p.out), p.M, p.N, p.ld_in,
                                                 p.ld_out, p.mask);

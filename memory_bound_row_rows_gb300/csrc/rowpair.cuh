@@ -660,12 +660,15 @@ cudaError_t launch_team_kv(const Op& op, const Args& p) {
     const T* a = static_cast<const T*>(p.a);
     const T* b = static_cast<const T*>(p.b);
     T* c = static_cast<T*>(p.c);
-    if constexpr (team_bounded<Op, T>())
+    if constexpr (team_bounded<Op, T>()) {
+        note_launch(team_kernel_bounded<Op, T, MODE, TPR, KV>, grid, NT);
         team_kernel_bounded<Op, T, MODE, TPR, KV><<<grid, NT, 0, p.stream>>>(op, a, b, c, p.M, p.N,
                                                                              p.lda, p.ldb, p.ldc);
-    else
+    } else {
+        note_launch(team_kernel<Op, T, MODE, TPR, KV>, grid, NT);
         team_kernel<Op, T, MODE, TPR, KV><<<grid, NT, 0, p.stream>>>(op, a, b, c, p.M, p.N, p.lda,
                                                                      p.ldb, p.ldc);
+    }
     return cudaGetLastError();
 }
 
@@ -722,6 +725,7 @@ cudaError_t launch_clusters(ClusterKernel<Op, T> kern, const Op& op, const Args&
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    note_launch(kern, cfg.gridDim, cfg.blockDim, 0, sh.csize);
     e = cudaLaunchKernelEx(&cfg, kern, op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
                            static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc, sh.csize,
                            sh.slice, p.err, p.timeout_ns, p.flags);
@@ -753,6 +757,7 @@ cudaError_t launch_mode(const Op& op, const Args& p, const Shape& sh) {
         case SR_PLAN_ROW: return launch_team<Op, T, MODE>(op, p, sh);
         case SR_PLAN_CLUSTER: return launch_cluster<Op, T, MODE>(op, p, sh);
         case SR_PLAN_ONLINE:
+            note_launch(loop_kernel<Op, T, MODE>, grid_for(p.M, 1), kLoopThreads);
             loop_kernel<Op, T, MODE><<<grid_for(p.M, 1), kLoopThreads, 0, p.stream>>>(
                 op, static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.c),
                 p.M, p.N, p.lda, p.ldb, p.ldc);

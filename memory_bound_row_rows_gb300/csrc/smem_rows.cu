@@ -235,6 +235,7 @@ cudaError_t launch_kv(const Problem& p, uint32_t slot_bytes) {
     const int64_t need = (p.M + nw - 1) / nw;
     const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
     const unsigned grid = (unsigned)(need < cap ? need : cap);
+    note_launch(kern, grid, nw * 32, smem);
     kern<<<grid, nw * 32, smem, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
                                             p.M, p.N, p.ld_in, p.ld_out, slots, slot_bytes,
                                             p.dev->err, p.timeout_ns, p.flags);

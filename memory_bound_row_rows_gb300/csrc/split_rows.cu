@@ -121,10 +121,12 @@ __global__ void __launch_bounds__(kSplitThreads)
 template <typename T, int VEC>
 cudaError_t launch_vec(const Problem& p, const SplitShape& sh, float2* ws) {
     const dim3 grid((unsigned)sh.chunks, (unsigned)p.M, 1);
+    note_launch(split_stats_kernel<T, VEC>, grid, kSplitThreads);
     split_stats_kernel<T, VEC><<<grid, kSplitThreads, 0, p.stream>>>(
         static_cast<const T*>(p.in), p.N, p.ld_in, sh.chunk_units, ws);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    note_launch(split_apply_kernel<T, VEC>, grid, kSplitThreads);
     split_apply_kernel<T, VEC><<<grid, kSplitThreads, 0, p.stream>>>(
         static_cast<const T*>(p.in), static_cast<T*>(p.out), p.N, p.ld_in, p.ld_out,
         sh.chunk_units, ws);

@@ -311,6 +311,7 @@ cudaError_t launch_kv(const Problem& p, int csize, SmemLayout L) {
         if (per_sm <= 0) return cudaErrorInvalidConfiguration;
         const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
         const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
+        note_launch(kern, grid, kTmaThreads, smem);
         kern<<<grid, kTmaThreads, smem, p.stream>>>(in, out, p.M, p.N, p.ld_in, p.ld_out, 1, L,
                                                     p.dev->err, p.timeout_ns, p.flags);
         return cudaGetLastError();
@@ -330,6 +331,7 @@ cudaError_t launch_kv(const Problem& p, int csize, SmemLayout L) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
+        note_launch(kern, cfg.gridDim, cfg.blockDim, smem, csize);
         e = cudaLaunchKernelEx(&cfg, kern, in, out, p.M, p.N, p.ld_in, p.ld_out, csize, L,
                                p.dev->err, p.timeout_ns, p.flags);
         if (e != cudaSuccess) return e;

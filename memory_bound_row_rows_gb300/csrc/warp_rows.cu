@@ -253,6 +253,7 @@ cudaError_t launch_packed_lpr(const Problem& p) {
     const int64_t need = (p.M + rows_per_block - 1) / rows_per_block;
     const int64_t cap = 0x7fffffff;
     const unsigned grid = (unsigned)(need < cap ? need : cap);
+    note_launch(kern, grid, kPackedBlock);
     kern<<<grid, kPackedBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
                                             p.M, (int)p.N, p.ld_in, p.ld_out);
     return cudaGetLastError();
@@ -289,6 +290,7 @@ cudaError_t launch_one_m(const Problem& p) {
         cap = (int64_t)per_sm * p.dev->sm_count;
     }
     const unsigned grid = (unsigned)(need < cap ? need : cap);
+    note_launch(kern, grid, kWarpBlock);
     kern<<<grid, kWarpBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
                                             p.M, (int)p.N, p.ld_in, p.ld_out, p.mask);
     return cudaGetLastError();

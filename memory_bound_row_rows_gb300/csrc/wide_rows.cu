@@ -470,6 +470,7 @@ cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int
     attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
     attr[1].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)SR_WIDE_POLICY;
     cfg.numAttrs = 2;
+    note_launch(kern, cfg.gridDim, cfg.blockDim, 0, csize);
     e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
                            p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
                            p.flags);

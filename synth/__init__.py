@@ -324,8 +324,9 @@ RMSNORM = {
 }
 RMSNORM_HEADLINE = "f16_16384x4096"
 
-# The workload the headline throughput is quoted on (square FP32 matrix, 4096 x 4096).
-HEADLINE = "f32_4096x4096"
+# The workload the headline throughput is quoted on: the largest, the FP16
+# causal attention-score matrix (524288 x 2048, 4.29 GB moved per call).
+HEADLINE = "f16_causal_524288x2048"
 
 
 def storage_to_float64(a: np.ndarray, dtype: int) -> np.ndarray:

@@ -313,3 +313,15 @@ def test_host_workspace_is_host_logic(lib):
     assert W(4, 4 << 20, 0) == 4 * 1 * 2 * (4 << 20) * 4
     assert W(4, 8, 9) == -sr.SR_EDTYPE
     assert W(-1, 8, 0) == -sr.SR_EINVAL
+
+
+def test_last_launch_without_a_launch(lib):
+    # No kernel has been launched from a fresh host thread: nothing to describe.
+    import threading
+    got = []
+    th = threading.Thread(target=lambda: got.append(
+        lib.softmax_rows_last_launch(ctypes.byref(sr.LaunchInfo()))))
+    th.start()
+    th.join()
+    assert got == [sr.SR_EINVAL]
+    assert lib.softmax_rows_last_launch(None) == sr.SR_EINVAL
