@@ -528,16 +528,28 @@ def to_device(a, dtype, dev):
     return t.to(dev)
 
 
-def copy_baseline(args, launch_copy, n_sets, stream, rank, local_rank, world, nbytes):
-    """A device copy of the same elements under the same rotation and batches."""
+def timed_copy(args, launch_copy, n_sets, stream, rank, local_rank, world, nbytes):
+    """GB/s and step statistics of a copy under the same rotation and batches."""
     batch_ms, bounds, _clk, _last = timed_batches(args, launch_copy, n_sets, stream, rank,
                                                   local_rank, world)
     st = batch_stats(batch_ms, bounds)
     med_s = max_over_ranks(st["median_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
-    return {"value": round(world * nbytes / med_s / 1e9, 2), "unit": "GB/s",
-            "median_step_us": st["median_step_us"], "mean_step_us": st["mean_step_us"],
-            "kind": "torch copy_ of the same M x N elements (input pitch to output pitch), "
-                    "same sets and batches"}
+    return round(world * nbytes / med_s / 1e9, 2), st
+
+
+def copy_baseline(args, launch_rows, launch_torch, n_sets, stream, rank, local_rank, world,
+                  nbytes):
+    """The copy ceiling: the library's row copy (softmax_rows_copy_ceiling: the same
+    bytes at the same pitches, the same 16-byte streaming accesses, no arithmetic),
+    with torch's copy_ of the same elements beside it, both under the bench protocol."""
+    gbs, st = timed_copy(args, launch_rows, n_sets, stream, rank, local_rank, world, nbytes)
+    tgbs, tst = timed_copy(args, launch_torch, n_sets, stream, rank, local_rank, world, nbytes)
+    return {"value": gbs, "unit": "GB/s", "median_step_us": st["median_step_us"],
+            "mean_step_us": st["mean_step_us"],
+            "kind": "softmax_rows_copy_ceiling: the same M x N elements from the input pitch to "
+                    "the output pitch with the softmax's 16-byte streaming loads and stores, "
+                    "same sets and batches",
+            "torch_copy_gbs": tgbs, "torch_copy_median_step_us": tst["median_step_us"]}
 
 
 def bench_ours(args, w):
@@ -628,10 +640,18 @@ def bench_ours(args, w):
     nbytes = algorithmic_bytes(w, args.api)
     copy = None
     if not args.no_copy:
-        def launch_copy(i):
+        eb = w.elem_bytes
+
+        def launch_rows(i):
+            st = lib.softmax_rows_copy_ceiling(xp[i], yp[i], w.M, w.N * eb, w.ld_in * eb,
+                                               w.ld_out * eb, sh)
+            if st != 0:
+                raise RuntimeError("softmax_rows_copy_ceiling: %s" % sr.softmax_rows_strerror(st))
+
+        def launch_torch(i):
             y_sets[i][:, :w.N].copy_(x_sets[i][:, :w.N])
-        copy = copy_baseline(args, launch_copy, n_sets, stream, rank, local_rank, world,
-                             w.fused_bytes)
+        copy = copy_baseline(args, launch_rows, launch_torch, n_sets, stream, rank, local_rank,
+                             world, w.fused_bytes)
     e2e = None
     if not args.no_e2e:
         del x_sets, y_sets

@@ -65,7 +65,9 @@ enum sr_status {
     SR_EDTYPE = 2,          /* unknown dtype */
     SR_ECUDA = 3,           /* a CUDA runtime call or launch failed */
     SR_EDEVICE_TIMEOUT = 4, /* a kernel's bounded wait expired (see softmax_rows_last_device_error) */
-    SR_EPLAN = 5            /* the forced plan cannot handle this shape or alignment */
+    SR_EPLAN = 5,           /* the forced plan cannot handle this shape or alignment */
+    SR_EBOUNDS = 6          /* bounds-checking build: a device access fell outside the call's
+                               matrices (see softmax_rows_last_device_error) */
 };
 
 /*
@@ -149,7 +151,9 @@ SR_API int softmax_rows_plan_check(const void* in, const void* out, int64_t M, i
  * a bulk copy into shared memory (CTA, CLUSTER, SMEM plans) or for the
  * partial results of the other blocks of its cluster (WIDE, CLUSTER, and the
  * CLUSTER plan of the backward and the RMSNorm). Returns SR_OK,
- * SR_EDEVICE_TIMEOUT, or SR_ECUDA. A kernel whose wait expired skips the rest
+ * SR_EDEVICE_TIMEOUT, SR_EBOUNDS (bounds-checking build only: an access was
+ * refused; it takes precedence when both were recorded), or SR_ECUDA. A
+ * kernel whose wait expired skips the rest
  * of its rows and returns, so the CUDA context stays usable; the output of
  * that call is then incomplete. The word is one per device, shared by every
  * stream, and the read and the clear are two steps: a kernel still running on
@@ -431,6 +435,52 @@ typedef struct sr_launch_info {
 } sr_launch_info;
 
 SR_API int softmax_rows_last_launch(sr_launch_info* info);
+
+/*
+ * The copy ceiling: copies M rows of row_bytes bytes from `in` (row pitch
+ * ld_in_bytes) to `out` (row pitch ld_out_bytes), both DEVICE, caller-owned,
+ * not overlapping. It moves exactly the bytes a row softmax of the same shape
+ * moves, with the same 16-byte streaming loads and stores (byte by byte when
+ * a base, a pitch or the row length is not a multiple of 16) and no
+ * arithmetic: the measured device copy that the "Warpline" README (Ceilings)
+ * takes as the roofline's bandwidth denominator, on the softmax's own shapes
+ * and layouts. A measurement tool; no softmax entry point uses it. Bytes
+ * [row_bytes, pitch) of each output row are not written. Asynchronous on
+ * `stream`. Returns SR_OK, SR_EINVAL (M < 0, row_bytes < 1, a pitch below
+ * row_bytes, a null pointer with M > 0, or a last byte beyond INT64_MAX;
+ * nothing launched) or SR_ECUDA.
+ */
+SR_API int softmax_rows_copy_ceiling(const void* in, void* out, int64_t M, int64_t row_bytes,
+                                     int64_t ld_in_bytes, int64_t ld_out_bytes,
+                                     sr_stream_t stream);
+
+/*
+ * Bounds-checking build. The library can also be built with every kernel
+ * checking its own global accesses (libsoftmax_rows_check.so: the same entry
+ * points, compiled with SR_BOUNDS_CHECK=1; a debug build for tests, never the
+ * product). It stands in for the memory and race checkers that the "Measured
+ * optimization case studies" page (CUDA reduction) runs before trusting a
+ * kernel. Each kernel records the matrices of its call (inputs readable, the
+ * output writable, each as rows of N valid elements at its pitch; masks,
+ * weights and workspaces as runs of bytes). Every load, store and bulk copy
+ * must fall inside the valid columns of one row of a matrix that allows it;
+ * one that does not is skipped instead of executed (a skipped bulk copy makes
+ * its bounded wait expire), and softmax_rows_last_device_error then returns
+ * SR_EBOUNDS. Nothing traps.
+ *
+ * softmax_rows_build_flags: SR_BUILD_BOUNDS_CHECK when this is that build, else 0.
+ * softmax_rows_bounds_address: the first address a check refused since the
+ *   last query (then cleared); 0 when none, or in the product build.
+ * softmax_rows_test_bounds_shrink: test hook of the checking build: every
+ *   later kernel treats the last `bytes` bytes of each row of its writable
+ *   matrices as outside, so a correct kernel's last stores must be refused
+ *   (the checker's positive control; the memory itself is valid). 0 restores
+ *   the exact extents. SR_EINVAL in the product build or for bytes < 0.
+ */
+#define SR_BUILD_BOUNDS_CHECK 1
+SR_API int softmax_rows_build_flags(void);
+SR_API uint64_t softmax_rows_bounds_address(void);
+SR_API int softmax_rows_test_bounds_shrink(int64_t bytes);
 
 /* Library version as major*10000 + minor*100 + patch. */
 SR_API int softmax_rows_version(void);

@@ -13,9 +13,9 @@ import os
 
 __all__ = [
     "SR_F32", "SR_BF16", "SR_F16", "SR_OK", "SR_EINVAL", "SR_EDTYPE", "SR_ECUDA",
-    "SR_EDEVICE_TIMEOUT", "SR_EPLAN", "SR_PLAN_AUTO", "SR_PLAN_WARP", "SR_PLAN_CTA",
+    "SR_EDEVICE_TIMEOUT", "SR_EPLAN", "SR_EBOUNDS", "SR_BUILD_BOUNDS_CHECK", "SR_PLAN_AUTO", "SR_PLAN_WARP", "SR_PLAN_CTA",
     "SR_PLAN_CLUSTER", "SR_PLAN_ONLINE", "SR_PLAN_SMEM", "SR_PLAN_ROW", "SR_PLAN_WIDE",
-    "PLAN_NAMES", "SoftmaxRowsError", "load", "lib_path",
+    "PLAN_NAMES", "SoftmaxRowsError", "load", "lib_path", "open_library",
     "softmax_rows", "softmax_rows_ex", "softmax_rows_plan", "softmax_rows_plan_check",
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
@@ -23,13 +23,15 @@ __all__ = [
     "softmax_rows_host_mapped",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
     "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
-    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape", "softmax_rows_last_launch",
+    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape", "softmax_rows_last_launch", "softmax_rows_copy_ceiling",
     "softmax", "softmax_backward", "rmsnorm_residual",
     "dtype_code",
 ]
 
 SR_F32, SR_BF16, SR_F16 = 0, 1, 2
 SR_OK, SR_EINVAL, SR_EDTYPE, SR_ECUDA, SR_EDEVICE_TIMEOUT, SR_EPLAN = 0, 1, 2, 3, 4, 5
+SR_EBOUNDS = 6
+SR_BUILD_BOUNDS_CHECK = 1
 SR_PLAN_AUTO, SR_PLAN_WARP, SR_PLAN_CTA, SR_PLAN_CLUSTER, SR_PLAN_ONLINE = 0, 1, 2, 3, 4
 SR_PLAN_SMEM, SR_PLAN_ROW, SR_PLAN_WIDE = 5, 6, 7
 PLAN_NAMES = {SR_PLAN_AUTO: "auto", SR_PLAN_WARP: "warp", SR_PLAN_CTA: "cta",
@@ -54,9 +56,14 @@ def lib_path() -> str:
 def load():
     """The loaded CUDA library; raises if it has not been built."""
     global _lib
-    if _lib is not None:
-        return _lib
-    path = lib_path()
+    if _lib is None:
+        _lib = open_library(lib_path())
+    return _lib
+
+
+def open_library(path: str):
+    """A ctypes handle on a build of the library at ``path`` with every entry
+    point's signature declared (the product build, or the bounds-checking one)."""
     if not os.path.exists(path):
         raise RuntimeError(
             "softmax_rows CUDA library not found at %s; build it with "
@@ -91,14 +98,18 @@ def load():
         "softmax_rows_version": [],
         "softmax_rows_wide_shape": [i64, i64, c_int, c_int, vp, vp, vp, vp],
         "softmax_rows_last_launch": [vp],
+        "softmax_rows_build_flags": [],
+        "softmax_rows_copy_ceiling": [vp, vp, i64, i64, i64, i64, vp],
+        "softmax_rows_bounds_address": [],
+        "softmax_rows_test_bounds_shrink": [i64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = {"softmax_rows_strerror": ctypes.c_char_p,
                       "softmax_rows_host_workspace_bytes": i64,
-                      "softmax_rows_split_workspace_bytes": i64}.get(name, c_int)
-    _lib = lib
+                      "softmax_rows_split_workspace_bytes": i64,
+                      "softmax_rows_bounds_address": u64}.get(name, c_int)
     return lib
 
 
@@ -280,6 +291,13 @@ def softmax_rows_strerror(status: int) -> str:
         return load().softmax_rows_strerror(status).decode()
     except RuntimeError:
         return "status %d" % status
+
+
+def softmax_rows_copy_ceiling(in_, out, M, row_bytes, ld_in_bytes, ld_out_bytes,
+                              stream=None) -> int:
+    return _check(load().softmax_rows_copy_ceiling(_ptr(in_), _ptr(out), M, row_bytes,
+                                                   ld_in_bytes, ld_out_bytes, _stream(stream)),
+                  "softmax_rows_copy_ceiling")
 
 
 def softmax_rows_version() -> int:

@@ -17,11 +17,16 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libsoftmax_rows.so")
+# The bounds-checking debug build: every kernel checks its global accesses
+# against the call's matrices (SR_BOUNDS_CHECK); relocatable device code lets
+# the checks in every translation unit reach the one device error word.
+CHECK_LIB = os.path.join(LIBDIR, "libsoftmax_rows_check.so")
+CHECK_FLAGS = ["-DSR_BOUNDS_CHECK=1", "-rdc=true"]
 HEADER = os.path.join(ROOT, "include", "softmax_rows.h")
 
 UNITS = ["api.cu", "warp_rows.cu", "tma_rows.cu", "online_rows.cu", "smem_rows.cu",
          "block_rows.cu", "host_stream.cu",
-         "split_rows.cu", "backward_rows.cu", "rmsnorm_rows.cu", "wide_rows.cu"]
+         "split_rows.cu", "backward_rows.cu", "rmsnorm_rows.cu", "wide_rows.cu", "copy_rows.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-fvisibility=hidden", "-Xptxas", "-v"]
@@ -52,6 +57,7 @@ PLAN_SOURCES = {
     "split": ["split_rows.cu"], "wide": ["wide_rows.cu", "wide.h", "packed.cuh"],
     "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],
     "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h"],
+    "copy": ["copy_rows.cu"],
 }
 SHARED_SOURCES = ["device.cuh", "internal.h"]
 
@@ -72,7 +78,8 @@ def source_hash(files=None) -> str:
     return h.hexdigest()[:16]
 
 
-def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: bool = False) -> str:
+def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: bool = False,
+          jobs: int | None = None) -> str:
     out = out or LIB
     os.makedirs(os.path.dirname(out), exist_ok=True)
     stamp_path = out + ".stamp"
@@ -96,10 +103,11 @@ def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: 
             f.write(r.stderr)
         return obj
 
-    with cf.ThreadPoolExecutor(max_workers=len(UNITS)) as ex:
+    with cf.ThreadPoolExecutor(max_workers=jobs or len(UNITS)) as ex:
         objs = list(ex.map(compile_unit, UNITS))
     tmp = out + ".tmp%d" % os.getpid()
-    cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
+    link_flags = [f for f in extra_flags if f.startswith("-rdc")]
+    cmd = [cc, *ARCH, *link_flags, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("nvcc link failed:\n%s\n%s" % (r.stdout, r.stderr))
@@ -109,6 +117,11 @@ def build(force: bool = False, extra_flags=(), out: str | None = None, verbose: 
     if verbose:
         print("built", out)
     return out
+
+
+def build_checked(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
+    """The bounds-checking debug build (same entry points, lib/libsoftmax_rows_check.so)."""
+    return build(force=force, extra_flags=CHECK_FLAGS, out=CHECK_LIB, verbose=verbose, jobs=jobs)
 
 
 if __name__ == "__main__":

@@ -11,10 +11,18 @@
 
 namespace sr {
 
-// Set (bit 0) by a kernel whose bounded wait (for a bulk copy, or for the
-// pairs or partials of its cluster peers) expired. One word per device (each
-// device holds its own copy of this module's globals).
+// Set (bit 0, kErrTimeout) by a kernel whose bounded wait (for a bulk copy,
+// or for the pairs or partials of its cluster peers) expired; in the
+// bounds-checking build also (bit 1, kErrBounds) by an access outside the
+// call's matrices. One word per device (each device holds its own copy of
+// this module's globals).
 __device__ unsigned int g_error_word;
+#if SR_BOUNDS_CHECK
+// First address a checked access refused, and the test hook's shrink of the
+// writable extents (bounds-checking build only).
+__device__ unsigned long long g_bounds_addr;
+__device__ long long g_bounds_shrink;
+#endif
 
 namespace {
 
@@ -416,7 +424,7 @@ int softmax_rows_last_device_error(sr_stream_t stream) {
         const unsigned int zero = 0;
         if (cudaMemcpyToSymbol(sr::g_error_word, &zero, sizeof(zero)) != cudaSuccess)
             return SR_ECUDA;
-        return SR_EDEVICE_TIMEOUT;
+        return (word & sr::kErrBounds) ? SR_EBOUNDS : SR_EDEVICE_TIMEOUT;
     }
     return SR_OK;
 }
@@ -602,6 +610,7 @@ const char* softmax_rows_strerror(int status) {
         case SR_ECUDA: return "CUDA runtime error";
         case SR_EDEVICE_TIMEOUT: return "a bounded device wait expired";
         case SR_EPLAN: return "plan cannot handle this shape or alignment";
+        case SR_EBOUNDS: return "a device access fell outside the call's matrices (bounds check)";
     }
     return "unknown status";
 }
@@ -639,6 +648,51 @@ int softmax_rows_last_launch(sr_launch_info* info) {
         info->name[k] = '\0';
     }
     return SR_OK;
+}
+
+int softmax_rows_copy_ceiling(const void* in, void* out, int64_t M, int64_t row_bytes,
+                              int64_t ld_in_bytes, int64_t ld_out_bytes, sr_stream_t stream) {
+    if (M < 0 || row_bytes < 1 || ld_in_bytes < row_bytes || ld_out_bytes < row_bytes)
+        return SR_EINVAL;
+    if (M > 0 && (in == nullptr || out == nullptr)) return SR_EINVAL;
+    if (M > 0) {
+        const __int128 ld = ld_in_bytes > ld_out_bytes ? ld_in_bytes : ld_out_bytes;
+        if ((__int128)(M - 1) * ld + row_bytes > (__int128)INT64_MAX) return SR_EINVAL;
+    }
+    if (M == 0) return SR_OK;
+    cudaError_t e;
+    const sr::DeviceInfo* dev = sr::device_info(&e);
+    if (!dev) return SR_ECUDA;
+    return sr::launch_copy_rows(in, out, M, row_bytes, ld_in_bytes, ld_out_bytes,
+                                (cudaStream_t)stream, dev->sm_count) == cudaSuccess
+               ? SR_OK
+               : SR_ECUDA;
+}
+
+int softmax_rows_build_flags(void) { return SR_BOUNDS_CHECK ? SR_BUILD_BOUNDS_CHECK : 0; }
+
+uint64_t softmax_rows_bounds_address(void) {
+#if SR_BOUNDS_CHECK
+    unsigned long long a = 0;
+    if (cudaMemcpyFromSymbol(&a, sr::g_bounds_addr, sizeof(a)) != cudaSuccess) return 0;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyToSymbol(sr::g_bounds_addr, &zero, sizeof(zero)) != cudaSuccess) return 0;
+    return (uint64_t)a;
+#else
+    return 0;
+#endif
+}
+
+int softmax_rows_test_bounds_shrink(int64_t bytes) {
+#if SR_BOUNDS_CHECK
+    if (bytes < 0) return SR_EINVAL;
+    const long long v = (long long)bytes;
+    return cudaMemcpyToSymbol(sr::g_bounds_shrink, &v, sizeof(v)) == cudaSuccess ? SR_OK
+                                                                                 : SR_ECUDA;
+#else
+    (void)bytes;
+    return SR_EINVAL;
+#endif
 }
 
 int softmax_rows_version(void) { return 200; }

@@ -15,6 +15,8 @@ namespace {
 
 struct BackwardOp {
     static constexpr bool kBoundTeam = false;
+    // Per-column data the op reads beside the two matrices: none.
+    __device__ __forceinline__ const void* aux_base() const { return nullptr; }
     __device__ __forceinline__ void accumulate(float& acc, float y, float dy) const {
         acc = fmaf(y, dy, acc);
     }

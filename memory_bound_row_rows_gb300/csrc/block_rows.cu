@@ -69,6 +69,8 @@ template <typename T, int NT, int KV, bool MASKED, bool SHIFTED = false>
 __global__ void __launch_bounds__(NT)
     block_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                       int64_t ld_in, int64_t ld_out, RowMask mask) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
+                    SR_SPAN_IN(mask.lens, M * 4));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NW = NT / 32;
     __shared__ float red_m[NW], red_s[NW];
@@ -184,6 +186,7 @@ template <typename T, int NT, int KV>
 __global__ void __launch_bounds__(NT, SR_ROW_PACKED_MIN_BLOCKS)
     block_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                         int64_t ld_in, int64_t ld_out) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NW = NT / 32;
     static_assert(!Elem<T>::kAccurateExp, "16-bit data only");

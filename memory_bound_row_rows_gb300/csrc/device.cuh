@@ -17,6 +17,104 @@ namespace sr {
 
 constexpr float kLog2e = 1.4426950408889634074f;
 
+// ---------------------------------------------------------------------------
+// Bounds-checking build (compiled with -DSR_BOUNDS_CHECK=1 and relocatable
+// device code; never in the product library). Every kernel first records the
+// extents of the matrices of its call in a per-block table: each matrix as
+// rows of `row_bytes` valid bytes at a pitch of `ld_bytes`, readable or
+// writable. Every global load, store and bulk copy then checks that all of
+// its bytes lie inside the valid columns of one row of a matrix that allows
+// the access. An access that does not is skipped (a load returns NaN bits),
+// bit 1 of the device error word is set and the first offending address is
+// kept, so that softmax_rows_last_device_error reports SR_EBOUNDS: the
+// checks record, they never trap.
+// ---------------------------------------------------------------------------
+#ifndef SR_BOUNDS_CHECK
+#define SR_BOUNDS_CHECK 0
+#endif
+constexpr unsigned int kErrTimeout = 1u;
+constexpr unsigned int kErrBounds = 2u;
+
+#if SR_BOUNDS_CHECK
+extern __device__ unsigned int g_error_word;
+extern __device__ unsigned long long g_bounds_addr;
+// Test hook: bytes taken off the end of every writable region's rows, so that
+// a correct kernel's last stores fall outside and must be refused.
+extern __device__ long long g_bounds_shrink;
+
+namespace bounds {
+
+struct Region {
+    const char* base;
+    int64_t rows, ld_bytes, row_bytes;
+    int writable;
+};
+constexpr int kMaxRegions = 4;
+struct Table {
+    int n;
+    Region r[kMaxRegions];
+};
+static __shared__ Table s_table;
+
+// A matrix of `rows` rows of n elements of `es` bytes at a pitch of ld elements.
+__device__ __forceinline__ Region matrix(const void* base, int64_t rows, int64_t ld, int64_t n,
+                                         int es, bool writable) {
+    return Region{static_cast<const char*>(base), base ? rows : 0, ld * es, n * es,
+                  writable ? 1 : 0};
+}
+// A contiguous run of `bytes` bytes (a vector or a workspace).
+__device__ __forceinline__ Region span(const void* base, int64_t bytes, bool writable) {
+    return Region{static_cast<const char*>(base), base ? 1 : 0, bytes, bytes, writable ? 1 : 0};
+}
+
+template <typename... R>
+__device__ __forceinline__ void begin(R... regions) {
+    static_assert(sizeof...(R) <= kMaxRegions, "too many regions");
+    if (threadIdx.x == 0) {
+        const Region list[] = {regions...};
+        s_table.n = (int)sizeof...(R);
+        for (int i = 0; i < (int)sizeof...(R); ++i) {
+            s_table.r[i] = list[i];
+            if (list[i].writable) s_table.r[i].row_bytes -= g_bounds_shrink;
+        }
+    }
+    __syncthreads();
+}
+
+static __device__ __noinline__ bool inside(const void* p, int64_t bytes, bool write) {
+    const char* a = static_cast<const char*>(p);
+    for (int i = 0; i < s_table.n; ++i) {
+        const Region& g = s_table.r[i];
+        if ((write && !g.writable) || g.rows <= 0 || a < g.base) continue;
+        const int64_t off = a - g.base;
+        if (off >= g.rows * g.ld_bytes) continue;
+        const int64_t row = off / g.ld_bytes;
+        if (off - row * g.ld_bytes + bytes <= g.row_bytes) return true;
+    }
+    atomicOr(&g_error_word, kErrBounds);
+    atomicCAS(&g_bounds_addr, 0ull, (unsigned long long)(uintptr_t)p);
+    return false;
+}
+
+}  // namespace bounds
+
+#define SR_BOUNDS_BEGIN(...) ::sr::bounds::begin(__VA_ARGS__)
+#define SR_READ_OK(p, bytes) ::sr::bounds::inside((p), (bytes), false)
+#define SR_WRITE_OK(p, bytes) ::sr::bounds::inside((p), (bytes), true)
+#else
+#define SR_BOUNDS_BEGIN(...) ((void)0)
+#define SR_READ_OK(p, bytes) true
+#define SR_WRITE_OK(p, bytes) true
+#endif
+// Regions for SR_BOUNDS_BEGIN: a matrix read or written by the call (rows of
+// n elements of *p's type at a pitch of ld), and a contiguous run of bytes.
+#define SR_MAT_IN(p, rows, ld, n) \
+    ::sr::bounds::matrix((p), (rows), (ld), (n), (int)sizeof(*(p)), false)
+#define SR_MAT_OUT(p, rows, ld, n) \
+    ::sr::bounds::matrix((p), (rows), (ld), (n), (int)sizeof(*(p)), true)
+#define SR_SPAN_IN(p, bytes) ::sr::bounds::span((p), (bytes), false)
+#define SR_SPAN_OUT(p, bytes) ::sr::bounds::span((p), (bytes), true)
+
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000u); }
 
 // ---------------------------------------------------------------------------
@@ -40,8 +138,13 @@ struct Elem<float> {
         return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
                           __float_as_uint(f[3]));
     }
-    __device__ __forceinline__ static float load1(const float* p) { return __ldg(p); }
-    __device__ __forceinline__ static void store1(float* p, float v) { __stcs(p, v); }
+    __device__ __forceinline__ static float load1(const float* p) {
+        if (!SR_READ_OK(p, 4)) return __int_as_float(0x7fc00000);
+        return __ldg(p);
+    }
+    __device__ __forceinline__ static void store1(float* p, float v) {
+        if (SR_WRITE_OK(p, 4)) __stcs(p, v);
+    }
 };
 
 template <>
@@ -67,11 +170,12 @@ struct Elem<__nv_bfloat16> {
                           pack2(f[6], f[7]));
     }
     __device__ __forceinline__ static float load1(const __nv_bfloat16* p) {
+        if (!SR_READ_OK(p, 2)) return __int_as_float(0x7fc00000);
         unsigned short s = __ldg(reinterpret_cast<const unsigned short*>(p));
         return __uint_as_float(((uint32_t)s) << 16);
     }
     __device__ __forceinline__ static void store1(__nv_bfloat16* p, float v) {
-        *p = __float2bfloat16_rn(v);
+        if (SR_WRITE_OK(p, 2)) *p = __float2bfloat16_rn(v);
     }
 };
 
@@ -100,10 +204,13 @@ struct Elem<__half> {
                           pack2(f[6], f[7]));
     }
     __device__ __forceinline__ static float load1(const __half* p) {
+        if (!SR_READ_OK(p, 2)) return __int_as_float(0x7fc00000);
         unsigned short s = __ldg(reinterpret_cast<const unsigned short*>(p));
         return __half2float(*reinterpret_cast<__half*>(&s));
     }
-    __device__ __forceinline__ static void store1(__half* p, float v) { *p = __float2half_rn(v); }
+    __device__ __forceinline__ static void store1(__half* p, float v) {
+        if (SR_WRITE_OK(p, 2)) *p = __float2half_rn(v);
+    }
 };
 
 // ---------------------------------------------------------------------------
@@ -169,6 +276,7 @@ __device__ __forceinline__ float final_rcp(float M, float S) {
 // and streaming store.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    if (!SR_READ_OK(p, 16)) return make_uint4(0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u);
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -177,6 +285,7 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
 }
 
 __device__ __forceinline__ void stg_stream(void* p, const uint4& v) {
+    if (!SR_WRITE_OK(p, 16)) return;
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
                  : "memory");
@@ -220,6 +329,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 // on the mbarrier as transaction bytes.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {
+    // A refused copy never completes: the bounded wait for it expires.
+    if (!SR_READ_OK(src, bytes)) return;
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(dst),

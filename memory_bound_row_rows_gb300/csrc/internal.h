@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "device.cuh"
+
 namespace sr {
 
 enum : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
@@ -46,7 +48,7 @@ struct RowMask {
     __device__ __forceinline__ int64_t valid(int64_t r, int64_t N) const {
         int64_t v = N;
         if (lens) {
-            v = lens[r];
+            v = SR_READ_OK(lens + r, 4) ? lens[r] : 0;
         } else if (period > 0) {
             // 32-bit division when both fit: a 64-bit one costs as much as the
             // rest of a short row's work.
@@ -117,6 +119,9 @@ cudaError_t launch_tma(const Problem& p, int cluster);
 cudaError_t launch_online(const Problem& p);
 cudaError_t launch_smem(const Problem& p);
 cudaError_t launch_row(const Problem& p);
+// The copy ceiling: M rows of row_bytes from pitch ld_in to pitch ld_out (bytes).
+cudaError_t launch_copy_rows(const void* in, void* out, int64_t M, int64_t row_bytes,
+                             int64_t ld_in, int64_t ld_out, cudaStream_t stream, int sm_count);
 bool row_plan_fits(int64_t N, int dtype);
 int64_t host_workspace_bytes(int64_t M, int64_t N, int dtype);
 

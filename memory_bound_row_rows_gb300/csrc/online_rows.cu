@@ -21,6 +21,8 @@ template <typename T, bool MASKED>
 __global__ void __launch_bounds__(kOnlineThreads)
     online_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, RowMask mask) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
+                    SR_SPAN_IN(mask.lens, M * 4));
     constexpr int NW = kOnlineThreads / 32;
     __shared__ float2 red[NW];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;

@@ -39,6 +39,8 @@ struct RmsNormOp {
     static constexpr bool kBoundTeam = true;
     const T* w;
     float eps;
+    // Per-column data the op reads beside the two matrices: the N weights.
+    __device__ __forceinline__ const T* aux_base() const { return w; }
     template <int n>
     struct Aux {
         uint4 raw;  // n == kVec: n weights packed as stored
@@ -49,7 +51,7 @@ struct RmsNormOp {
         if constexpr (n == 1) {
             a.raw.x = __float_as_uint(Elem<T>::load1(w + col));
         } else if constexpr (WVEC) {
-            a.raw = __ldg(reinterpret_cast<const uint4*>(w + col));
+            if (SR_READ_OK(w + col, 16)) a.raw = __ldg(reinterpret_cast<const uint4*>(w + col));
         } else {
             float f[n];
 #pragma unroll

@@ -287,6 +287,8 @@ template <class Op, typename T, Mode MODE, int TPR, int KV>
 __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
     team_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                 int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
+                    SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     team_body<Op, T, MODE, TPR, KV>(op, A, B, C, M, N, lda, ldb, ldc);
 }
 
@@ -295,6 +297,8 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR, 768 / (TPR < 128 ? 128 
     team_kernel_bounded(Op op, const T* __restrict__ A, const T* __restrict__ B,
                         T* __restrict__ C, int64_t M, int64_t N, int64_t lda, int64_t ldb,
                         int64_t ldc) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
+                    SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     team_body<Op, T, MODE, TPR, KV>(op, A, B, C, M, N, lda, ldb, ldc);
 }
 
@@ -338,6 +342,8 @@ __global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN
                    int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
                    int64_t slice, unsigned int* err, unsigned long long timeout_ns,
                    int flags) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
+                    SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     constexpr bool WIDE = MODE != Mode::kScalar;
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;
@@ -462,6 +468,7 @@ __device__ __forceinline__ uint64_t l2_policy(bool keep) {
 }
 
 __device__ __forceinline__ uint4 ldg_policy(const void* p, uint64_t pol) {
+    if (!SR_READ_OK(p, 16)) return make_uint4(0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u);
     uint4 v;
     asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
         : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -474,6 +481,8 @@ __global__ void __launch_bounds__(kClusterThreads, kStreamMinBlocks)
     stream_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                   int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
                   int64_t slice, unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
+                    SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     using U = Unit<T, true>;
     constexpr int VEC = U::kN;
     using AuxV = typename Op::template Aux<VEC>;
@@ -581,6 +590,8 @@ template <class Op, typename T, Mode MODE>
 __global__ void __launch_bounds__(kLoopThreads)
     loop_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                 int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
+                    SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     constexpr bool WIDE = MODE != Mode::kScalar;
     using U = Unit<T, WIDE>;
     using L = Layout<T, MODE>;

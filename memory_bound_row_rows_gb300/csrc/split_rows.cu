@@ -59,6 +59,8 @@ template <typename T, int VEC>
 __global__ void __launch_bounds__(kSplitThreads)
     split_stats_kernel(const T* __restrict__ in, int64_t N, int64_t ld_in, int64_t chunk_units,
                        float2* __restrict__ ws) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, (int64_t)gridDim.y, ld_in, N),
+                    SR_SPAN_OUT(ws, (int64_t)gridDim.x * gridDim.y * 8));
     __shared__ float2 red[kSplitNW];
     const int64_t r = blockIdx.y, c = blockIdx.x, C = gridDim.x;
     const int64_t units = N / VEC;  // VEC divides N when VEC > 1
@@ -81,19 +83,23 @@ __global__ void __launch_bounds__(kSplitThreads)
         m = mn;
     }
     block_merge(m, s, red);
-    if (threadIdx.x == 0) ws[r * C + c] = make_float2(m, s);
+    if (threadIdx.x == 0 && SR_WRITE_OK(ws + r * C + c, 8)) ws[r * C + c] = make_float2(m, s);
 }
 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kSplitThreads)
     split_apply_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t N, int64_t ld_in,
                        int64_t ld_out, int64_t chunk_units, const float2* __restrict__ ws) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, (int64_t)gridDim.y, ld_in, N),
+                    SR_MAT_OUT(out, (int64_t)gridDim.y, ld_out, N),
+                    SR_SPAN_IN(ws, (int64_t)gridDim.x * gridDim.y * 8));
     __shared__ float2 red[kSplitNW];
     const int64_t r = blockIdx.y, c = blockIdx.x, C = gridDim.x;
     // The row's (M, S) from all of its chunks' pairs.
     float m = neg_inf(), s = 0.0f;
     for (int64_t k = threadIdx.x; k < C; k += kSplitThreads) {
-        const float2 q = ws[r * C + k];
+        const float2 q = SR_READ_OK(ws + r * C + k, 8) ? ws[r * C + k]
+                                                       : make_float2(__int_as_float(0x7fc00000), 0.0f);
         merge_ms(m, s, q.x, q.y);
     }
     block_merge(m, s, red);

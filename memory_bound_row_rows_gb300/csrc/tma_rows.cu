@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
     tma_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                     int64_t ld_in, int64_t ld_out, int csize, SmemLayout L, unsigned int* err,
                     unsigned long long timeout_ns, int flags) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NW = NT / 32;
     static_assert(NW <= 8 || !CLUSTER, "cluster exchange slots hold 8 warps per block");

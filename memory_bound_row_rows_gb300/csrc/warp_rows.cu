@@ -44,6 +44,8 @@ template <typename T, int VEC, int KV, bool MASKED>
 __global__ void __launch_bounds__(kWarpBlock)
     warp_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
                      int64_t ld_in, int64_t ld_out, RowMask mask) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
+                    SR_SPAN_IN(mask.lens, M * 4));
     const int lane = threadIdx.x & 31;
     const int64_t first = ((int64_t)blockIdx.x * kWarpBlock + threadIdx.x) >> 5;
     const int64_t stride = ((int64_t)gridDim.x * kWarpBlock) >> 5;
@@ -175,6 +177,7 @@ __global__ void __launch_bounds__(kPackedBlock,
                                                             : 2))
     warp_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
                        int64_t ld_in, int64_t ld_out) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int RPW = 32 / LPR;  // rows per warp
     const int lane = threadIdx.x & 31;

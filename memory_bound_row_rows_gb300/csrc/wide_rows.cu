@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
     wide_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
                      unsigned long long timeout_ns, int flags) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NT = kWideThreads;
     constexpr int NW = kWideWarps;
@@ -294,6 +295,7 @@ __device__ __forceinline__ uint64_t l2_policy_drop() {
 
 // 16-byte load through the read-only path with an L2 cache policy.
 __device__ __forceinline__ uint4 ldg_policy(const void* p, uint64_t pol) {
+    if (!SR_READ_OK(p, 16)) return make_uint4(0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u);
     uint4 v;
     if (SR_WIDE_STREAM_HINT) {
         asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
@@ -310,6 +312,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
     wide_stream_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
                        unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NT = kWideThreads;
     constexpr int NW = kWideWarps;

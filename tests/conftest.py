@@ -27,3 +27,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _no_refused_access(request):
+    """Under the bounds-checking build (SOFTMAX_ROWS_LIB pointing at
+    libsoftmax_rows_check.so) every GPU test must end with no access refused."""
+    yield
+    if "gpu" not in request.keywords or not _has_gpu():
+        return
+    import memory_bound_row_rows_gb300 as sr
+    lib = sr._lib
+    if lib is None or lib.softmax_rows_build_flags() != sr.SR_BUILD_BOUNDS_CHECK:
+        return
+    st = lib.softmax_rows_last_device_error(None)
+    addr = lib.softmax_rows_bounds_address()
+    assert st != sr.SR_EBOUNDS, "an access was refused (first address 0x%x)" % addr

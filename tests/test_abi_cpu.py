@@ -43,7 +43,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_version_and_strerror(lib):
     assert sr.softmax_rows_version() >= 100
-    for st in range(6):
+    for st in range(7):
         assert sr.softmax_rows_strerror(st)
     assert sr.softmax_rows_strerror(99) == "unknown status"
 
@@ -325,3 +325,21 @@ def test_last_launch_without_a_launch(lib):
     th.join()
     assert got == [sr.SR_EINVAL]
     assert lib.softmax_rows_last_launch(None) == sr.SR_EINVAL
+
+
+def test_product_build_flags(lib):
+    # The product library is not the bounds-checking build; its hooks refuse.
+    assert lib.softmax_rows_build_flags() == 0
+    assert lib.softmax_rows_test_bounds_shrink(8) == sr.SR_EINVAL
+    assert sr.softmax_rows_strerror(sr.SR_EBOUNDS).startswith("a device access")
+
+
+def test_copy_ceiling_rejects_before_any_device_call(lib):
+    C = lib.softmax_rows_copy_ceiling
+    assert C(None, None, 0, 16, 16, 16, None) == sr.SR_OK
+    assert C(ALIGNED_IN, ALIGNED_OUT, -1, 16, 16, 16, None) == sr.SR_EINVAL
+    assert C(ALIGNED_IN, ALIGNED_OUT, 4, 0, 16, 16, None) == sr.SR_EINVAL
+    assert C(ALIGNED_IN, ALIGNED_OUT, 4, 32, 16, 32, None) == sr.SR_EINVAL
+    assert C(ALIGNED_IN, ALIGNED_OUT, 4, 32, 32, 31, None) == sr.SR_EINVAL
+    assert C(None, ALIGNED_OUT, 4, 32, 32, 32, None) == sr.SR_EINVAL
+    assert C(ALIGNED_IN, ALIGNED_OUT, 2, 16, 2**63 - 8, 16, None) == sr.SR_EINVAL
