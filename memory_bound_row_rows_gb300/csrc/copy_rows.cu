@@ -7,11 +7,12 @@
 // kernels and no arithmetic, so "as fast as a copy" can be checked on the
 // same shapes and layouts. It is a measurement tool; no softmax path calls it.
 //
-// Work split: rows are cut into chunks of 32 lanes x kCopyUnroll 16-byte
-// vectors; warps of a grid sized to fill every SM take chunks in turn, each
-// lane issuing its kCopyUnroll loads before any store. Rows that are not
-// 16-byte aligned (either pitch, either base, or the row length) are copied
-// byte by byte in the same chunks.
+// Work split: the rows' 16-byte vectors are numbered row by row and cut into
+// tiles of kCopyThreads x kCopyUnroll vectors, one tile per block of a grid
+// with a block per tile (the hardware starts a new block as one retires, as
+// in the ROW softmax); each thread issues its kCopyUnroll loads before any
+// store. Rows that are not 16-byte aligned (either pitch, either base, or the
+// row length) are copied byte by byte in the same tiles.
 #include "../../include/softmax_rows.h"
 #include "device.cuh"
 #include "internal.h"
@@ -19,84 +20,94 @@
 namespace sr {
 namespace {
 
-constexpr int kCopyThreads = 256;
+constexpr int kCopyThreads = 64;
 constexpr int kCopyUnroll = 4;
-constexpr int64_t kChunk = 32 * kCopyUnroll;  // units per warp chunk
+constexpr int64_t kTile = (int64_t)kCopyThreads * kCopyUnroll;  // units per block
 
-template <bool VEC>
+// Unit u of the numbering -> (row, unit within the row); 32-bit division when
+// the numbering fits in 31 bits.
+template <typename I>
+__device__ __forceinline__ void split_unit(I u, I per_row, int64_t& r, int64_t& c) {
+    const I q = u / per_row;
+    r = (int64_t)q;
+    c = (int64_t)(u - q * per_row);
+}
+
+template <bool VEC, typename I>
 __global__ void __launch_bounds__(kCopyThreads)
     copy_rows_kernel(const char* __restrict__ in, char* __restrict__ out, int64_t M,
                      int64_t row_bytes, int64_t ld_in, int64_t ld_out) {
     SR_BOUNDS_BEGIN(::sr::bounds::matrix(in, M, ld_in, row_bytes, 1, false),
                     ::sr::bounds::matrix(out, M, ld_out, row_bytes, 1, true));
-    const int lane = threadIdx.x & 31;
-    const int64_t units = VEC ? row_bytes / 16 : row_bytes;
-    const int64_t chunks = (units + kChunk - 1) / kChunk;
-    const int64_t items = M * chunks;
-    const int64_t warps = (int64_t)gridDim.x * (kCopyThreads / 32);
-    for (int64_t it = ((int64_t)blockIdx.x * kCopyThreads + threadIdx.x) >> 5; it < items;
-         it += warps) {
-        const int64_t r = it / chunks;
-        const int64_t c0 = (it - r * chunks) * kChunk + lane;
-        const char* src = in + r * ld_in;
-        char* dst = out + r * ld_out;
+    const I per_row = (I)(VEC ? row_bytes / 16 : row_bytes);
+    const I total = (I)M * per_row;
+    for (int64_t b = blockIdx.x; b * kTile < (int64_t)total; b += gridDim.x) {
+        const I base = (I)(b * kTile) + (I)threadIdx.x;
         if constexpr (VEC) {
             uint4 v[kCopyUnroll];
+            int64_t r[kCopyUnroll], c[kCopyUnroll];
 #pragma unroll
             for (int k = 0; k < kCopyUnroll; ++k) {
-                const int64_t c = c0 + 32 * k;
-                if (c < units) v[k] = ldg_stream(src + c * 16);
+                const I u = base + (I)(kCopyThreads * k);
+                split_unit<I>(u, per_row, r[k], c[k]);
+                if (u < total) v[k] = ldg_stream(in + r[k] * ld_in + c[k] * 16);
             }
 #pragma unroll
             for (int k = 0; k < kCopyUnroll; ++k) {
-                const int64_t c = c0 + 32 * k;
-                if (c < units) stg_stream(dst + c * 16, v[k]);
+                const I u = base + (I)(kCopyThreads * k);
+                if (u < total) stg_stream(out + r[k] * ld_out + c[k] * 16, v[k]);
             }
         } else {
-            unsigned char b[kCopyUnroll];
+            unsigned char v[kCopyUnroll];
+            int64_t r[kCopyUnroll], c[kCopyUnroll];
 #pragma unroll
             for (int k = 0; k < kCopyUnroll; ++k) {
-                const int64_t c = c0 + 32 * k;
-                if (c < units && SR_READ_OK(src + c, 1))
-                    b[k] = (unsigned char)__ldg(reinterpret_cast<const unsigned char*>(src + c));
+                const I u = base + (I)(kCopyThreads * k);
+                split_unit<I>(u, per_row, r[k], c[k]);
+                const char* p = in + r[k] * ld_in + c[k];
+                if (u < total && SR_READ_OK(p, 1))
+                    v[k] = (unsigned char)__ldg(reinterpret_cast<const unsigned char*>(p));
             }
 #pragma unroll
             for (int k = 0; k < kCopyUnroll; ++k) {
-                const int64_t c = c0 + 32 * k;
-                if (c < units && SR_WRITE_OK(dst + c, 1)) dst[c] = (char)b[k];
+                const I u = base + (I)(kCopyThreads * k);
+                char* p = out + r[k] * ld_out + c[k];
+                if (u < total && SR_WRITE_OK(p, 1)) *p = (char)v[k];
             }
         }
     }
+}
+
+template <bool VEC, typename I>
+cudaError_t launch_copy(const char* in, char* out, int64_t M, int64_t row_bytes, int64_t ld_in,
+                        int64_t ld_out, cudaStream_t stream) {
+    const int64_t units = M * (VEC ? row_bytes / 16 : row_bytes);
+    const int64_t need = (units + kTile - 1) / kTile;
+    const unsigned grid = (unsigned)(need < 0x7fffffff ? need : 0x7fffffff);
+    note_launch(copy_rows_kernel<VEC, I>, grid, kCopyThreads);
+    copy_rows_kernel<VEC, I><<<grid, kCopyThreads, 0, stream>>>(in, out, M, row_bytes, ld_in,
+                                                                ld_out);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_copy_rows(const void* in, void* out, int64_t M, int64_t row_bytes,
                              int64_t ld_in, int64_t ld_out, cudaStream_t stream, int sm_count) {
+    (void)sm_count;
     const bool vec = reinterpret_cast<uintptr_t>(in) % 16 == 0 &&
                      reinterpret_cast<uintptr_t>(out) % 16 == 0 && row_bytes % 16 == 0 &&
                      ld_in % 16 == 0 && ld_out % 16 == 0;
-    const void* fn = vec ? reinterpret_cast<const void*>(copy_rows_kernel<true>)
-                         : reinterpret_cast<const void*>(copy_rows_kernel<false>);
-    const int per_sm = blocks_per_sm(fn, kCopyThreads, 0);
-    if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-    const int64_t units = vec ? row_bytes / 16 : row_bytes;
-    const int64_t items = M * ((units + kChunk - 1) / kChunk);
-    const int64_t need = (items + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-    const int64_t cap = (int64_t)per_sm * sm_count;
-    const unsigned grid = (unsigned)(need < cap ? need : cap);
     const char* src = static_cast<const char*>(in);
     char* dst = static_cast<char*>(out);
-    if (vec) {
-        note_launch(copy_rows_kernel<true>, grid, kCopyThreads);
-        copy_rows_kernel<true><<<grid, kCopyThreads, 0, stream>>>(src, dst, M, row_bytes, ld_in,
-                                                                   ld_out);
-    } else {
-        note_launch(copy_rows_kernel<false>, grid, kCopyThreads);
-        copy_rows_kernel<false><<<grid, kCopyThreads, 0, stream>>>(src, dst, M, row_bytes, ld_in,
-                                                                    ld_out);
-    }
-    return cudaGetLastError();
+    // 32-bit unit numbers while the last unit of the last tile fits.
+    const int64_t units = M * (vec ? row_bytes / 16 : row_bytes);
+    const bool narrow = units + kTile < 0x7fffffff;
+    if (vec)
+        return narrow ? launch_copy<true, int32_t>(src, dst, M, row_bytes, ld_in, ld_out, stream)
+                      : launch_copy<true, int64_t>(src, dst, M, row_bytes, ld_in, ld_out, stream);
+    return narrow ? launch_copy<false, int32_t>(src, dst, M, row_bytes, ld_in, ld_out, stream)
+                  : launch_copy<false, int64_t>(src, dst, M, row_bytes, ld_in, ld_out, stream);
 }
 
 }  // namespace sr
