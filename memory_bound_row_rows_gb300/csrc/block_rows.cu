@@ -69,6 +69,7 @@ template <typename T, int NT, int KV, bool MASKED, bool SHIFTED = false>
 __global__ void __launch_bounds__(NT)
     block_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                       int64_t ld_in, int64_t ld_out, RowMask mask) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
                     SR_SPAN_IN(mask.lens, M * 4));
     constexpr int VEC = Elem<T>::kVec;
@@ -186,6 +187,7 @@ template <typename T, int NT, int KV>
 __global__ void __launch_bounds__(NT, SR_ROW_PACKED_MIN_BLOCKS)
     block_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                         int64_t ld_in, int64_t ld_out) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NW = NT / 32;
@@ -255,10 +257,9 @@ cudaError_t launch_grid(void (*kern)(const T*, T*, int64_t, int64_t, int64_t, in
                         int nt, const Problem& p) {
     const int64_t cap = 0x7fffffff;
     const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
-    note_launch(kern, grid, nt);
-    kern<<<grid, nt, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
-                                    p.N, p.ld_in, p.ld_out, p.mask);
-    return cudaGetLastError();
+    return launch_kernel(kern, LaunchShape{dim3(grid), dim3(nt)}, p.stream,
+                         static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, p.N, p.ld_in,
+                         p.ld_out, p.mask);
 }
 
 template <typename T, int NT, int KV>
@@ -270,10 +271,9 @@ cudaError_t launch_nt_kv(const Problem& p) {
         auto kern = block_packed_kernel<T, NT, KV>;
         const int64_t cap = 0x7fffffff;
         const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
-        note_launch(kern, grid, NT);
-        kern<<<grid, NT, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
-                                        p.N, p.ld_in, p.ld_out);
-        return cudaGetLastError();
+        return launch_kernel(kern, LaunchShape{dim3(grid), dim3(NT)}, p.stream,
+                             static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, p.N,
+                             p.ld_in, p.ld_out);
     }
     return launch_grid(block_rows_kernel<T, NT, KV, false>, NT, p);
 }

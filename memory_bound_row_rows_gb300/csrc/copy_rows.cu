@@ -37,6 +37,7 @@ template <bool VEC, typename I>
 __global__ void __launch_bounds__(kCopyThreads)
     copy_rows_kernel(const char* __restrict__ in, char* __restrict__ out, int64_t M,
                      int64_t row_bytes, int64_t ld_in, int64_t ld_out) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(::sr::bounds::matrix(in, M, ld_in, row_bytes, 1, false),
                     ::sr::bounds::matrix(out, M, ld_out, row_bytes, 1, true));
     const I per_row = (I)(VEC ? row_bytes / 16 : row_bytes);
@@ -84,10 +85,8 @@ cudaError_t launch_copy(const char* in, char* out, int64_t M, int64_t row_bytes,
     const int64_t units = M * (VEC ? row_bytes / 16 : row_bytes);
     const int64_t need = (units + kTile - 1) / kTile;
     const unsigned grid = (unsigned)(need < 0x7fffffff ? need : 0x7fffffff);
-    note_launch(copy_rows_kernel<VEC, I>, grid, kCopyThreads);
-    copy_rows_kernel<VEC, I><<<grid, kCopyThreads, 0, stream>>>(in, out, M, row_bytes, ld_in,
-                                                                ld_out);
-    return cudaGetLastError();
+    return launch_kernel(copy_rows_kernel<VEC, I>, LaunchShape{dim3(grid), dim3(kCopyThreads)},
+                         stream, in, out, M, row_bytes, ld_in, ld_out);
 }
 
 }  // namespace

@@ -35,6 +35,24 @@ constexpr float kLog2e = 1.4426950408889634074f;
 constexpr unsigned int kErrTimeout = 1u;
 constexpr unsigned int kErrBounds = 2u;
 
+// Programmatic dependent launch (see launch_kernel in internal.h): the first
+// statement of every kernel. It lets the next kernel on the stream be
+// scheduled once every block of this one has started, then waits until the
+// previous kernel on the stream has completed and its memory is visible; no
+// global memory is touched before it.
+#ifndef SR_PDL
+#define SR_PDL 1
+#endif
+#if SR_PDL
+#define SR_GRID_DEPENDENCY()                                          \
+    do {                                                              \
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); \
+        asm volatile("griddepcontrol.wait;" ::: "memory");            \
+    } while (0)
+#else
+#define SR_GRID_DEPENDENCY() ((void)0)
+#endif
+
 #if SR_BOUNDS_CHECK
 extern __device__ unsigned int g_error_word;
 extern __device__ unsigned long long g_bounds_addr;

@@ -100,11 +100,63 @@ inline int cluster_size_for(int64_t N, int dtype, int min_cluster) {
 }
 
 // The calling host thread's record of the last kernel it launched through the
-// library (read back by softmax_rows_last_launch). Every launch site calls it.
+// library (read back by softmax_rows_last_launch). launch_kernel calls it.
 void note_launch(const void* func, dim3 grid, dim3 block, size_t smem, int cluster);
 template <typename F>
 inline void note_launch(F* func, dim3 grid, dim3 block, size_t smem = 0, int cluster = 1) {
     note_launch(reinterpret_cast<const void*>(func), grid, block, smem, cluster);
+}
+
+// How a kernel is launched: grid and block, dynamic shared memory, blocks per
+// cluster (1: no cluster) and the cluster scheduling policy (-1: default).
+struct LaunchShape {
+    dim3 grid;
+    dim3 block;
+    size_t smem = 0;
+    int cluster = 1;
+    int policy = -1;
+};
+
+// Every kernel of the library is launched here. With SR_PDL the launch allows
+// programmatic stream serialisation: the kernel may be scheduled while the
+// previous kernel on the stream drains, and (SR_GRID_DEPENDENCY, the first
+// statement of every kernel) waits for that kernel to complete and its
+// memory to be visible before any global access of its own, so stream order
+// holds exactly as without it; only the launch and the block dispatch
+// overlap the previous kernel's tail.
+template <typename... P, typename... A>
+cudaError_t launch_kernel(void (*kern)(P...), const LaunchShape& ls, cudaStream_t stream,
+                          A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = ls.grid;
+    cfg.blockDim = ls.block;
+    cfg.dynamicSmemBytes = ls.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[3];
+    int n = 0;
+    if (ls.cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)ls.cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (ls.policy >= 0) {
+        attr[n].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
+        attr[n].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)ls.policy;
+        ++n;
+    }
+    if (SR_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = (unsigned)n;
+    note_launch(kern, ls.grid, ls.block, ls.smem, ls.cluster);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 // Resident blocks per SM for a kernel (cached per device).

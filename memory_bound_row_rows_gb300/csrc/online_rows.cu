@@ -21,6 +21,7 @@ template <typename T, bool MASKED>
 __global__ void __launch_bounds__(kOnlineThreads)
     online_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, RowMask mask) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
                     SR_SPAN_IN(mask.lens, M * 4));
     constexpr int NW = kOnlineThreads / 32;
@@ -83,11 +84,9 @@ cudaError_t launch_m(const Problem& p) {
     if (per_sm <= 0) return cudaErrorInvalidConfiguration;
     const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
     const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
-    note_launch(kern, grid, kOnlineThreads);
-    kern<<<grid, kOnlineThreads, 0, p.stream>>>(static_cast<const T*>(p.in),
-                                                static_cast<T*>(p.out), p.M, p.N, p.ld_in,
-                                                p.ld_out, p.mask);
-    return cudaGetLastError();
+    return launch_kernel(kern, LaunchShape{dim3(grid), dim3(kOnlineThreads)}, p.stream,
+                         static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, p.N, p.ld_in,
+                         p.ld_out, p.mask);
 }
 
 template <typename T>

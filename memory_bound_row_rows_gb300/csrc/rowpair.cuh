@@ -287,6 +287,7 @@ template <class Op, typename T, Mode MODE, int TPR, int KV>
 __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR)
     team_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                 int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     team_body<Op, T, MODE, TPR, KV>(op, A, B, C, M, N, lda, ldb, ldc);
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(TPR < 128 ? 128 : TPR, 768 / (TPR < 128 ? 128 
     team_kernel_bounded(Op op, const T* __restrict__ A, const T* __restrict__ B,
                         T* __restrict__ C, int64_t M, int64_t N, int64_t lda, int64_t ldb,
                         int64_t ldc) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     team_body<Op, T, MODE, TPR, KV>(op, A, B, C, M, N, lda, ldb, ldc);
@@ -342,6 +344,7 @@ __global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN
                    int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
                    int64_t slice, unsigned int* err, unsigned long long timeout_ns,
                    int flags) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     constexpr bool WIDE = MODE != Mode::kScalar;
@@ -456,7 +459,10 @@ __global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN
 // evict-first, so the resident clusters' slices stay in L2 between the passes
 // (cache hints only; the results do not depend on them).
 // ---------------------------------------------------------------------------
-constexpr int kStreamUnroll = 2;
+#ifndef SR_PAIR_STREAM_UNROLL
+#define SR_PAIR_STREAM_UNROLL 2
+#endif
+constexpr int kStreamUnroll = SR_PAIR_STREAM_UNROLL;
 
 __device__ __forceinline__ uint64_t l2_policy(bool keep) {
     uint64_t pol;
@@ -481,6 +487,7 @@ __global__ void __launch_bounds__(kClusterThreads, kStreamMinBlocks)
     stream_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                   int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
                   int64_t slice, unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     using U = Unit<T, true>;
@@ -590,6 +597,7 @@ template <class Op, typename T, Mode MODE>
 __global__ void __launch_bounds__(kLoopThreads)
     loop_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                 int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
     constexpr bool WIDE = MODE != Mode::kScalar;
@@ -671,16 +679,13 @@ cudaError_t launch_team_kv(const Op& op, const Args& p) {
     const T* a = static_cast<const T*>(p.a);
     const T* b = static_cast<const T*>(p.b);
     T* c = static_cast<T*>(p.c);
-    if constexpr (team_bounded<Op, T>()) {
-        note_launch(team_kernel_bounded<Op, T, MODE, TPR, KV>, grid, NT);
-        team_kernel_bounded<Op, T, MODE, TPR, KV><<<grid, NT, 0, p.stream>>>(op, a, b, c, p.M, p.N,
-                                                                             p.lda, p.ldb, p.ldc);
-    } else {
-        note_launch(team_kernel<Op, T, MODE, TPR, KV>, grid, NT);
-        team_kernel<Op, T, MODE, TPR, KV><<<grid, NT, 0, p.stream>>>(op, a, b, c, p.M, p.N, p.lda,
-                                                                     p.ldb, p.ldc);
-    }
-    return cudaGetLastError();
+    const LaunchShape ls{dim3(grid), dim3(NT)};
+    if constexpr (team_bounded<Op, T>())
+        return launch_kernel(team_kernel_bounded<Op, T, MODE, TPR, KV>, ls, p.stream, op, a, b, c,
+                             p.M, p.N, p.lda, p.ldb, p.ldc);
+    else
+        return launch_kernel(team_kernel<Op, T, MODE, TPR, KV>, ls, p.stream, op, a, b, c, p.M,
+                             p.N, p.lda, p.ldb, p.ldc);
 }
 
 template <class Op, typename T, Mode MODE, int TPR>
@@ -724,24 +729,12 @@ cudaError_t launch_clusters(ClusterKernel<Op, T> kern, const Op& op, const Args&
     if (e != cudaSuccess) return e;
     if (max_active_clusters(fn, kClusterThreads, 0, sh.csize) <= 0)
         return cudaErrorInvalidConfiguration;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid_for(p.M, sh.csize), 1, 1);
-    cfg.blockDim = dim3(kClusterThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = p.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)sh.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    note_launch(kern, cfg.gridDim, cfg.blockDim, 0, sh.csize);
-    e = cudaLaunchKernelEx(&cfg, kern, op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
-                           static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc, sh.csize,
-                           sh.slice, p.err, p.timeout_ns, p.flags);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
+    return launch_kernel(kern,
+                         LaunchShape{dim3(grid_for(p.M, sh.csize)), dim3(kClusterThreads), 0,
+                                     sh.csize},
+                         p.stream, op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
+                         static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc, sh.csize, sh.slice,
+                         p.err, p.timeout_ns, p.flags);
 }
 
 template <class Op, typename T, Mode MODE>
@@ -768,11 +761,10 @@ cudaError_t launch_mode(const Op& op, const Args& p, const Shape& sh) {
         case SR_PLAN_ROW: return launch_team<Op, T, MODE>(op, p, sh);
         case SR_PLAN_CLUSTER: return launch_cluster<Op, T, MODE>(op, p, sh);
         case SR_PLAN_ONLINE:
-            note_launch(loop_kernel<Op, T, MODE>, grid_for(p.M, 1), kLoopThreads);
-            loop_kernel<Op, T, MODE><<<grid_for(p.M, 1), kLoopThreads, 0, p.stream>>>(
-                op, static_cast<const T*>(p.a), static_cast<const T*>(p.b), static_cast<T*>(p.c),
-                p.M, p.N, p.lda, p.ldb, p.ldc);
-            return cudaGetLastError();
+            return launch_kernel(loop_kernel<Op, T, MODE>,
+                                 LaunchShape{dim3(grid_for(p.M, 1)), dim3(kLoopThreads)}, p.stream,
+                                 op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
+                                 static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc);
     }
     return cudaErrorInvalidValue;
 }

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(256)
     smem_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int slots, uint32_t slot_bytes,
                      unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -236,11 +237,9 @@ cudaError_t launch_kv(const Problem& p, uint32_t slot_bytes) {
     const int64_t need = (p.M + nw - 1) / nw;
     const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
     const unsigned grid = (unsigned)(need < cap ? need : cap);
-    note_launch(kern, grid, nw * 32, smem);
-    kern<<<grid, nw * 32, smem, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
-                                            p.M, p.N, p.ld_in, p.ld_out, slots, slot_bytes,
-                                            p.dev->err, p.timeout_ns, p.flags);
-    return cudaGetLastError();
+    return launch_kernel(kern, LaunchShape{dim3(grid), dim3(nw * 32), smem}, p.stream,
+                         static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, p.N, p.ld_in,
+                         p.ld_out, slots, slot_bytes, p.dev->err, p.timeout_ns, p.flags);
 }
 
 template <typename T>

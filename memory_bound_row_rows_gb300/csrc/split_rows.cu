@@ -59,6 +59,7 @@ template <typename T, int VEC>
 __global__ void __launch_bounds__(kSplitThreads)
     split_stats_kernel(const T* __restrict__ in, int64_t N, int64_t ld_in, int64_t chunk_units,
                        float2* __restrict__ ws) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, (int64_t)gridDim.y, ld_in, N),
                     SR_SPAN_OUT(ws, (int64_t)gridDim.x * gridDim.y * 8));
     __shared__ float2 red[kSplitNW];
@@ -90,6 +91,7 @@ template <typename T, int VEC>
 __global__ void __launch_bounds__(kSplitThreads)
     split_apply_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t N, int64_t ld_in,
                        int64_t ld_out, int64_t chunk_units, const float2* __restrict__ ws) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, (int64_t)gridDim.y, ld_in, N),
                     SR_MAT_OUT(out, (int64_t)gridDim.y, ld_out, N),
                     SR_SPAN_IN(ws, (int64_t)gridDim.x * gridDim.y * 8));
@@ -127,16 +129,14 @@ __global__ void __launch_bounds__(kSplitThreads)
 template <typename T, int VEC>
 cudaError_t launch_vec(const Problem& p, const SplitShape& sh, float2* ws) {
     const dim3 grid((unsigned)sh.chunks, (unsigned)p.M, 1);
-    note_launch(split_stats_kernel<T, VEC>, grid, kSplitThreads);
-    split_stats_kernel<T, VEC><<<grid, kSplitThreads, 0, p.stream>>>(
-        static_cast<const T*>(p.in), p.N, p.ld_in, sh.chunk_units, ws);
-    cudaError_t e = cudaGetLastError();
+    const LaunchShape ls{grid, dim3(kSplitThreads)};
+    const cudaError_t e = launch_kernel(split_stats_kernel<T, VEC>, ls, p.stream,
+                                        static_cast<const T*>(p.in), p.N, p.ld_in, sh.chunk_units,
+                                        ws);
     if (e != cudaSuccess) return e;
-    note_launch(split_apply_kernel<T, VEC>, grid, kSplitThreads);
-    split_apply_kernel<T, VEC><<<grid, kSplitThreads, 0, p.stream>>>(
-        static_cast<const T*>(p.in), static_cast<T*>(p.out), p.N, p.ld_in, p.ld_out,
-        sh.chunk_units, ws);
-    return cudaGetLastError();
+    return launch_kernel(split_apply_kernel<T, VEC>, ls, p.stream, static_cast<const T*>(p.in),
+                         static_cast<T*>(p.out), p.N, p.ld_in, p.ld_out, sh.chunk_units,
+                         static_cast<const float2*>(ws));
 }
 
 template <typename T>

@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(NT, !CLUSTER ? 1
     tma_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                     int64_t ld_in, int64_t ld_out, int csize, SmemLayout L, unsigned int* err,
                     unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NW = NT / 32;
@@ -312,31 +313,17 @@ cudaError_t launch_kv(const Problem& p, int csize, SmemLayout L) {
         if (per_sm <= 0) return cudaErrorInvalidConfiguration;
         const int64_t cap = (int64_t)per_sm * p.dev->sm_count;
         const unsigned grid = (unsigned)(p.M < cap ? p.M : cap);
-        note_launch(kern, grid, kTmaThreads, smem);
-        kern<<<grid, kTmaThreads, smem, p.stream>>>(in, out, p.M, p.N, p.ld_in, p.ld_out, 1, L,
-                                                    p.dev->err, p.timeout_ns, p.flags);
-        return cudaGetLastError();
+        return launch_kernel(kern, LaunchShape{dim3(grid), dim3(kTmaThreads), smem}, p.stream, in,
+                             out, p.M, p.N, p.ld_in, p.ld_out, 1, L, p.dev->err, p.timeout_ns,
+                             p.flags);
     } else {
         const int nclusters = max_active_clusters(fn, kTmaThreads, smem, csize);
         if (nclusters <= 0) return cudaErrorInvalidConfiguration;
         const int64_t units = p.M < nclusters ? p.M : nclusters;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(units * csize), 1, 1);
-        cfg.blockDim = dim3(kTmaThreads, 1, 1);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = p.stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)csize;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        note_launch(kern, cfg.gridDim, cfg.blockDim, smem, csize);
-        e = cudaLaunchKernelEx(&cfg, kern, in, out, p.M, p.N, p.ld_in, p.ld_out, csize, L,
-                               p.dev->err, p.timeout_ns, p.flags);
-        if (e != cudaSuccess) return e;
-        return cudaGetLastError();
+        return launch_kernel(
+            kern, LaunchShape{dim3((unsigned)(units * csize)), dim3(kTmaThreads), smem, csize},
+            p.stream, in, out, p.M, p.N, p.ld_in, p.ld_out, csize, L, p.dev->err, p.timeout_ns,
+            p.flags);
     }
 }
 

@@ -44,6 +44,7 @@ template <typename T, int VEC, int KV, bool MASKED>
 __global__ void __launch_bounds__(kWarpBlock)
     warp_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
                      int64_t ld_in, int64_t ld_out, RowMask mask) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
                     SR_SPAN_IN(mask.lens, M * 4));
     const int lane = threadIdx.x & 31;
@@ -177,6 +178,7 @@ __global__ void __launch_bounds__(kPackedBlock,
                                                             : 2))
     warp_packed_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int N,
                        int64_t ld_in, int64_t ld_out) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int RPW = 32 / LPR;  // rows per warp
@@ -256,10 +258,9 @@ cudaError_t launch_packed_lpr(const Problem& p) {
     const int64_t need = (p.M + rows_per_block - 1) / rows_per_block;
     const int64_t cap = 0x7fffffff;
     const unsigned grid = (unsigned)(need < cap ? need : cap);
-    note_launch(kern, grid, kPackedBlock);
-    kern<<<grid, kPackedBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
-                                            p.M, (int)p.N, p.ld_in, p.ld_out);
-    return cudaGetLastError();
+    return launch_kernel(kern, LaunchShape{dim3(grid), dim3(kPackedBlock)}, p.stream,
+                         static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, (int)p.N,
+                         p.ld_in, p.ld_out);
 }
 
 // No row loop: the hardware hands out rows as blocks retire (measured faster
@@ -293,10 +294,9 @@ cudaError_t launch_one_m(const Problem& p) {
         cap = (int64_t)per_sm * p.dev->sm_count;
     }
     const unsigned grid = (unsigned)(need < cap ? need : cap);
-    note_launch(kern, grid, kWarpBlock);
-    kern<<<grid, kWarpBlock, 0, p.stream>>>(static_cast<const T*>(p.in), static_cast<T*>(p.out),
-                                            p.M, (int)p.N, p.ld_in, p.ld_out, p.mask);
-    return cudaGetLastError();
+    return launch_kernel(kern, LaunchShape{dim3(grid), dim3(kWarpBlock)}, p.stream,
+                         static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, (int)p.N,
+                         p.ld_in, p.ld_out, p.mask);
 }
 
 template <typename T, int VEC, int KV>

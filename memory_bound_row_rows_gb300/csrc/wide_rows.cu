@@ -41,12 +41,6 @@ namespace {
 #define SR_WIDE_MIN_BLOCKS 4
 #endif
 
-// 1: evenly split aligned rows with several rows per resident cluster run the
-// prefetching persistent variant (wide_prefetch_kernel).
-#ifndef SR_WIDE_PREFETCH
-#define SR_WIDE_PREFETCH 1
-#endif
-
 constexpr int kWideThreads = 256;
 
 // exp(x - m) for FP32 data: the hardware ex2 of the difference (rounded once
@@ -100,6 +94,7 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
     wide_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
                      unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NT = kWideThreads;
@@ -255,163 +250,6 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
     }
 }
 
-// Prefetching variant for evenly split aligned rows (every block's slice is
-// exactly 256 x KV vectors), when each cluster has several rows to do: a
-// persistent grid of as many clusters as are resident, each walking rows
-// r, r + clusters, ... Besides the slice held in registers, every block
-// stages its slice of the NEXT row in shared memory by one 1-D bulk copy
-// (cp.async.bulk, completing on an mbarrier), issued as soon as the current
-// row has been moved from shared memory into registers. So while a row's
-// (max, sum) pairs are exchanged and its output written from registers, the
-// next row is already on its way: every SM keeps reads in flight during its
-// write phase instead of alternating between the two. The arithmetic, the
-// exchange are those of wide_rows_kernel. Failure: a block whose copy or pair
-// wait expires writes nothing more, keeps sending (placeholder) pairs so that
-// its peers' waits end, waits (bounded) for a copy still in flight into its
-// shared memory, and leaves after one cluster barrier, which every block
-// reaches because every wait is bounded.
-template <typename T, int KV>
-__global__ void __launch_bounds__(kWideThreads, SR_WIDE_MIN_BLOCKS)
-    wide_prefetch_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
-                         int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
-                         unsigned int* err, unsigned long long timeout_ns, int flags) {
-    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
-    constexpr int VEC = Elem<T>::kVec;
-    constexpr int NT = kWideThreads;
-    constexpr int NW = kWideWarps;
-    extern __shared__ __align__(128) unsigned char stage_buf[];
-    __shared__ float2 pairs[2][kMaxCluster * NW];
-    __shared__ __align__(8) unsigned long long xbar[2];
-    __shared__ __align__(8) unsigned long long lbar;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rank = (int)cluster_ctarank();
-    const int64_t nclusters = gridDim.x / csize;
-    const int64_t u0 = (int64_t)rank * slice;
-    const int npairs = csize * NW;
-    const bool live = !(flags & kFlagNoCopy);  // test hook: no copies, no sends
-    const uint32_t stage = smem_addr(stage_buf);
-    const uint32_t lb = smem_addr(&lbar);
-    const uint32_t bytes = (uint32_t)(slice * 16);
-
-    if (tid == 0) {
-        mbar_init(smem_addr(&xbar[0]), 1);
-        mbar_init(smem_addr(&xbar[1]), 1);
-        mbar_init(lb, 1);
-        fence_mbar_init();
-    }
-    __syncthreads();
-    cluster_arrive_relaxed();
-    const int64_t r0 = blockIdx.x / csize;
-    int64_t issued = 0, confirmed = 0;  // thread 0's copies issued / seen complete
-    if (tid == 0 && live && r0 < M) {
-        mbar_expect_tx(lb, bytes);
-        bulk_g2s(stage, in + r0 * ld_in + u0 * VEC, bytes, lb);
-        issued = 1;
-    }
-    bool started = false, failed = false;
-    int64_t it = 0;
-    for (int64_t r = r0; r < M; r += nclusters, ++it) {
-        const int p = (int)(it & 1);
-        const uint32_t phase = (uint32_t)((it >> 1) & 1);
-        bool ok = !failed;
-        if (ok) {
-            ok = mbar_wait_bounded(lb, (uint32_t)(it & 1), timeout_ns);
-            if (ok && tid == 0) confirmed = it + 1;
-        }
-        uint4 raw[KV];
-#pragma unroll
-        for (int k = 0; k < KV; ++k)
-            raw[k] = ok ? lds128(stage + 16u * (uint32_t)(tid + NT * k))
-                        : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-        // Every thread has its values: the stage takes the next row, unless a
-        // wait failed anywhere in the block.
-        if (__syncthreads_or(!ok)) failed = true;
-        if (tid == 0 && !failed && live && r + nclusters < M) {
-            fence_proxy_async_smem();
-            mbar_expect_tx(lb, bytes);
-            bulk_g2s(stage, in + (r + nclusters) * ld_in + u0 * VEC, bytes, lb);
-            ++issued;
-        }
-        VecMax<T> vm;
-#pragma unroll
-        for (int k = 0; k < KV; ++k) vm.add(raw[k]);
-        float m_w = warp_max(vm.get());
-        if (failed) m_w = neg_inf();  // placeholder pair (-inf, 0): peers' waits still end
-        const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
-        const float shift_l2 = shift * kLog2e;
-        float sa = 0.0f, sb = 0.0f;
-        if (!failed) {
-#pragma unroll
-            for (int k = 0; k < KV; ++k) {
-                float f[VEC];
-                Elem<T>::unpack(raw[k], f);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) {
-                    const float x = wide_exp<T>(f[e], shift, shift_l2);
-                    if (e & 1) sb += x; else sa += x;
-                }
-            }
-        }
-        const float s_w = warp_sum(sa + sb);
-        if (!started) {
-            cluster_wait();
-            started = true;
-        }
-        const uint32_t xb = smem_addr(&xbar[p]);
-        // A failed block no longer waits, so it no longer arms its barriers,
-        // but it still sends (placeholder) pairs.
-        if (tid == 0 && !failed) mbar_expect_tx(xb, (uint32_t)npairs * 8u);
-        if (live && lane < csize)
-            st_async_f2(map_to_rank(smem_addr(&pairs[p][rank * NW + warp]), (uint32_t)lane), m_w,
-                        s_w, map_to_rank(xb, (uint32_t)lane));
-        if (!failed && !mbar_wait_bounded(xb, phase, timeout_ns)) failed = true;
-        if (failed) continue;
-        float mloc = neg_inf();
-        for (int i = lane; i < npairs; i += 32) mloc = fmaxf(mloc, pairs[p][i].x);
-        const float Mr = warp_max(mloc);
-        float sloc = 0.0f;
-        for (int i = lane; i < npairs; i += 32) {
-            const float2 q = pairs[p][i];
-            sloc += q.y * merge_scale(q.x, Mr);
-        }
-        const float Sr = warp_sum(sloc);
-        T* obody = out + r * ld_out;
-        if constexpr (Elem<T>::kAccurateExp) {
-            const float rs = final_rcp(Mr, Sr);
-#pragma unroll
-            for (int k = 0; k < KV; ++k) {
-                const int64_t idx = u0 + tid + NT * k;
-                float f[VEC];
-                unpack_again<T>(raw[k], f);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = wide_exp<T>(f[e], Mr, 0.0f) * rs;
-                stg_stream(obody + idx * VEC, Elem<T>::pack(f));
-            }
-        } else {
-            const float c = fmaf(Mr, kLog2e, lg2_approx(Sr));
-#pragma unroll
-            for (int k = 0; k < KV; ++k) {
-                const int64_t idx = u0 + tid + NT * k;
-                float f[VEC];
-                unpack_again<T>(raw[k], f);
-#pragma unroll
-                for (int e = 0; e < VEC; ++e) f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
-                stg_stream(obody + idx * VEC, Elem<T>::pack(f));
-            }
-        }
-    }
-    if (!started) cluster_wait();
-    if (failed && tid == 0) atomicOr(err, 1u);
-    // A copy issued before a failure may still be landing in this block's
-    // shared memory: wait for it (bounded) before the block leaves.
-    if (tid == 0 && issued > confirmed)
-        mbar_wait_bounded(lb, (uint32_t)((issued - 1) & 1), timeout_ns);
-    // Every block of the cluster walks the same rows and every wait above is
-    // bounded, so all of them arrive here; none leaves while a peer may still
-    // send it a pair.
-    cluster_sync_all();
-}
-
 // Streamed variant for aligned rows too wide for the registers of a 16-block
 // cluster (over 512 KiB): the looped plan of the same section (Wide rows),
 // spread over a cluster. Pass 1 walks the block's slice in steps of
@@ -475,6 +313,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
     wide_stream_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
                        unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
     constexpr int NT = kWideThreads;
@@ -619,75 +458,20 @@ cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int
     // One cluster per row up to the largest grid; beyond it rows are walked
     // with a stride.
     const int64_t cap = 0x7fffffff / csize;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((p.M < cap ? p.M : cap) * csize), 1, 1);
-    cfg.blockDim = dim3(kWideThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = p.stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    // Let the hardware balance a cluster's blocks over the SMs of a GPC
-    // (measured: 1.5 % faster than the default policy on 1024 x 131072 bf16).
-    attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
-    attr[1].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)SR_WIDE_POLICY;
-    cfg.numAttrs = 2;
-    note_launch(kern, cfg.gridDim, cfg.blockDim, 0, csize);
-    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
-                           p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
-                           p.flags);
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
-// Persistent launch of the prefetching variant: as many clusters as are
-// resident with the staging buffer, each walking rows with that stride. Returns
-// cudaErrorNotSupported when the rows give no cluster a second row (the
-// one-cluster-per-row kernel then runs).
-template <typename T, int KV>
-cudaError_t launch_prefetch(const Problem& p, const WideShape& sh) {
-    auto kern = wide_prefetch_kernel<T, KV>;
-    const void* fn = reinterpret_cast<const void*>(kern);
-    const size_t smem = (size_t)sh.slice * 16;
-    cudaError_t e = ensure_smem_limit(fn, smem, sh.csize > 8);
-    if (e != cudaSuccess) return e;
-    const int resident = max_active_clusters(fn, kWideThreads, smem, sh.csize);
-    if (resident <= 0) return cudaErrorInvalidConfiguration;
-    if (p.M <= resident) return cudaErrorNotSupported;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(resident * sh.csize), 1, 1);
-    cfg.blockDim = dim3(kWideThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = p.stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)sh.csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
-    attr[1].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)SR_WIDE_POLICY;
-    cfg.attrs = attr;
-    cfg.numAttrs = 2;
-    note_launch(kern, cfg.gridDim, cfg.blockDim, smem, sh.csize);
-    e = cudaLaunchKernelEx(&cfg, kern, static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M,
-                           p.N, p.ld_in, p.ld_out, sh.csize, sh.slice, p.dev->err, p.timeout_ns,
-                           p.flags);
+    // The cluster scheduling policy lets the hardware balance a cluster's
+    // blocks over the SMs of a GPC (measured: 1.5 % faster than the default
+    // policy on 1024 x 131072 bf16).
+    const LaunchShape ls{dim3((unsigned)((p.M < cap ? p.M : cap) * csize)), dim3(kWideThreads), 0,
+                         csize, SR_WIDE_POLICY};
+    e = launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in), static_cast<T*>(p.out),
+                      p.M, p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
+                      p.flags);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 template <typename T, int KV>
 cudaError_t launch_mode(const Problem& p, const WideShape& sh, int mode) {
-    if constexpr (SR_WIDE_PREFETCH && KV == 8) {
-        if (mode == kFull) {
-            const cudaError_t e = launch_prefetch<T, KV>(p, sh);
-            if (e != cudaErrorNotSupported) return e;
-        }
-    }
     switch (mode) {
         case kAligned: return launch_clusters<T>(wide_rows_kernel<T, KV, kAligned>, p, sh.csize,
                                                  sh.slice);

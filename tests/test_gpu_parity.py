@@ -399,41 +399,6 @@ def test_side_stream_and_empty_calls():
     assert torch.isnan(y2).all()
 
 
-# ---- evenly split wide rows with more rows than resident clusters: the
-# persistent WIDE variant that stages the next row by bulk copy ----
-
-@pytest.mark.parametrize("dtype,M,N", [(synth.BF16, 200, 131072), (synth.F16, 301, 131072),
-                                       (synth.F32, 157, 65536)],
-                         ids=["bf16-200", "f16-301", "f32-157"])
-def test_wide_prefetch_rows(dtype, M, N):
-    x = synth.generate(M, N, dtype=dtype, seed=900 + M, p1=1.5)
-    xd = gu.to_device(x, dtype)
-    st, y = run_plan(xd, M, N, N, N, dtype, sr.SR_PLAN_AUTO)
-    assert st == sr.SR_OK
-    torch.cuda.synchronize()
-    assert "wide_prefetch_kernel" in sr.softmax_rows_last_launch()["name"]
-    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "prefetching WIDE")
-    assert sr.softmax_rows_last_device_error() == sr.SR_OK
-
-
-def test_wide_prefetch_wait_expiry():
-    """No copies and no pair sends: every wait of the persistent variant expires."""
-    M, N, dtype = 200, 131072, synth.BF16
-    x = synth.generate(M, N, dtype=dtype, seed=31)
-    xd = gu.to_device(x, dtype)
-    y = nan_filled(M, N, dtype)
-    assert sr.softmax_rows_last_device_error() == sr.SR_OK
-    sr.softmax_rows_test_expiry(xd, y, M, N, N, N, dtype, sr.SR_PLAN_WIDE, 2_000_000)
-    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
-    assert "wide_prefetch_kernel" in sr.softmax_rows_last_launch()["name"]
-    assert torch.isnan(y).all(), "an expired kernel wrote output"
-    st, y = run_plan(xd, M, N, N, N, dtype, sr.SR_PLAN_WIDE)
-    assert st == sr.SR_OK
-    torch.cuda.synchronize()
-    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "after expiry")
-    assert sr.softmax_rows_last_device_error() == sr.SR_OK
-
-
 # ---- the bounded wait: an expiring wait reports an error, the context survives ----
 
 @pytest.mark.parametrize("name,plan", [("f32_4096x4096", sr.SR_PLAN_CTA),
