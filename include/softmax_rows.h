@@ -30,6 +30,12 @@
  *     the legacy default stream) on the current device. Nothing blocks the
  *     host and nothing is allocated per call. The first call on a device
  *     queries and caches its properties.
+ *   - Kernels are launched with programmatic stream serialisation: a call's
+ *     kernel may be scheduled while the previous kernel on `stream` drains,
+ *     but it waits for that kernel to complete, with its memory visible,
+ *     before reading or writing any global memory. Stream order is exactly
+ *     as without it; back-to-back calls overlap only their launch and block
+ *     dispatch with the previous kernel's tail.
  *   - Arguments are checked before anything is launched; a rejected call
  *     launches nothing and leaves `out` untouched.
  *   - Misaligned pointers or pitches are not an error: they select plans

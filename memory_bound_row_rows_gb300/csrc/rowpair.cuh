@@ -47,7 +47,6 @@
 
 #include "device.cuh"
 #include "internal.h"
-#include "prefetch.cuh"
 #include "rowpair.h"
 
 namespace sr {
@@ -463,10 +462,6 @@ __global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN
 #ifndef SR_PAIR_STREAM_UNROLL
 #define SR_PAIR_STREAM_UNROLL 2
 #endif
-// Steps of pass 1 prefetched into L2 ahead of the loads (0: none).
-#ifndef SR_PAIR_STREAM_PREFETCH
-#define SR_PAIR_STREAM_PREFETCH 4
-#endif
 constexpr int kStreamUnroll = SR_PAIR_STREAM_UNROLL;
 
 __device__ __forceinline__ uint64_t l2_policy(bool keep) {
@@ -525,23 +520,10 @@ __global__ void __launch_bounds__(kClusterThreads, kStreamMinBlocks)
     for (int64_t r = blockIdx.x / csize; r < M; r += nclusters, ++it) {
         const T* ra = A + r * lda;
         const T* rb = B + r * ldb;
-        // Thread 0 has the bulk-copy engine prefetch both matrices' slice
-        // SR_PAIR_STREAM_PREFETCH steps ahead of the loads into L2.
-        constexpr int PD = SR_PAIR_STREAM_PREFETCH;
-        auto prefetch = [&](int64_t v) {  // the step starting at vector v (thread 0 only)
-            if (v < u1) {
-                const int64_t n = (u1 - v < (int64_t)NT * UR) ? u1 - v : (int64_t)NT * UR;
-                bulk_prefetch_l2(ra + v * VEC, (uint32_t)(n * 16), keep);
-                bulk_prefetch_l2(rb + v * VEC, (uint32_t)(n * 16), keep);
-            }
-        };
-        if (PD > 0 && tid == 0)
-            for (int d = 0; d < PD; ++d) prefetch(u0 + (int64_t)d * NT * UR);
         float acc[VEC];
 #pragma unroll
         for (int e = 0; e < VEC; ++e) acc[e] = 0.0f;
         for (int64_t j0 = u0 + tid; j0 < u1; j0 += (int64_t)NT * UR) {
-            if (PD > 0 && tid == 0) prefetch(j0 + (int64_t)PD * NT * UR);
             const int64_t rem = u1 - j0;
             U a[UR], b[UR];
 #pragma unroll

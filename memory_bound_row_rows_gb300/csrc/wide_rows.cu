@@ -26,7 +26,6 @@
 #include "device.cuh"
 #include "internal.h"
 #include "packed.cuh"
-#include "prefetch.cuh"
 #include "wide.h"
 
 namespace sr {
@@ -282,10 +281,6 @@ constexpr int kStreamChunk = SR_WIDE_STREAM_CHUNK;
 #ifndef SR_WIDE_STREAM_CLUSTER
 #define SR_WIDE_STREAM_CLUSTER 8
 #endif
-// Steps of pass 1 prefetched into L2 ahead of the loads (0: none).
-#ifndef SR_WIDE_STREAM_PREFETCH
-#define SR_WIDE_STREAM_PREFETCH 4
-#endif
 
 __device__ __forceinline__ uint64_t l2_policy_keep() {
     uint64_t pol = 0;
@@ -350,23 +345,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
         const int p = (int)(it & 1);
         const uint32_t phase = (uint32_t)((it >> 1) & 1);
         const T* rin = in + r * ld_in;
-        // The block's slice is read in steps of NT * CH vectors; thread 0 has
-        // the bulk-copy engine prefetch step j + SR_WIDE_STREAM_PREFETCH into L2
-        // while the block loads step j, so that more bytes are on their way
-        // than the threads' registers hold.
-        constexpr int PD = SR_WIDE_STREAM_PREFETCH;
-        auto prefetch = [&](int64_t v) {  // the step starting at vector v (thread 0 only)
-            if (v < u1) {
-                const int64_t n = (u1 - v < (int64_t)NT * CH) ? u1 - v : (int64_t)NT * CH;
-                bulk_prefetch_l2(rin + v * VEC, (uint32_t)(n * 16), keep);
-            }
-        };
-        if (PD > 0 && tid == 0)
-            for (int d = 0; d < PD; ++d) prefetch(u0 + (int64_t)d * NT * CH);
         // Pass 1: per-thread online (m, s) over vectors u0 + tid + NT * j.
         float m = neg_inf(), s = 0.0f;
         for (int64_t j0 = u0 + tid; j0 < u1; j0 += (int64_t)NT * CH) {
-            if (PD > 0 && tid == 0) prefetch(j0 + (int64_t)PD * NT * CH);
             const T* q = rin + j0 * VEC;
             const int64_t rem = u1 - j0;  // vectors of this thread's step: k < rem / NT
             uint4 raw[CH];

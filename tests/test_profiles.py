@@ -39,8 +39,11 @@ def test_records_are_consistent():
         # Every input byte is read from DRAM about once (two of the three
         # matrices of a row-pair operation are inputs, one of the two of the
         # softmax): far above would be a re-read, below the capture is wrong.
+        # Streamed kernels read their slices twice by design, the second time
+        # mostly from L2: at most twice from DRAM.
         inputs = r["algorithmic_bytes"] * (2 / 3 if ":" in key else 1 / 2)
-        assert 0.95 <= r["dram_read"] / inputs <= 1.10, key
+        top = 2.0 if "stream" in r["kernel"] else 1.10
+        assert 0.95 <= r["dram_read"] / inputs <= top, key
         summary = os.path.join(ROOT, r["summary"])
         assert os.path.exists(summary), key
         with open(summary) as f:
