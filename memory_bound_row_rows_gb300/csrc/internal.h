@@ -108,12 +108,15 @@ inline void note_launch(F* func, dim3 grid, dim3 block, size_t smem = 0, int clu
 }
 
 // How a kernel is launched: grid and block, dynamic shared memory, blocks per
-// cluster (1: no cluster) and the cluster scheduling policy (-1: default).
+// cluster and the cluster scheduling policy (-1: default). `cluster` is 0 for
+// a kernel that uses no cluster features; a kernel that does (cluster
+// barriers, distributed shared memory, st.async) passes its cluster size,
+// 1 included, and is always launched with that cluster dimension.
 struct LaunchShape {
     dim3 grid;
     dim3 block;
     size_t smem = 0;
-    int cluster = 1;
+    int cluster = 0;
     int policy = -1;
 };
 
@@ -134,14 +137,14 @@ cudaError_t launch_kernel(void (*kern)(P...), const LaunchShape& ls, cudaStream_
     cfg.stream = stream;
     cudaLaunchAttribute attr[3];
     int n = 0;
-    if (ls.cluster > 1) {
+    if (ls.cluster > 0) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
         attr[n].val.clusterDim.x = (unsigned)ls.cluster;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
-    if (ls.policy >= 0) {
+    if (ls.cluster > 0 && ls.policy >= 0) {
         attr[n].id = cudaLaunchAttributeClusterSchedulingPolicyPreference;
         attr[n].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)ls.policy;
         ++n;
@@ -153,7 +156,7 @@ cudaError_t launch_kernel(void (*kern)(P...), const LaunchShape& ls, cudaStream_
     }
     cfg.attrs = attr;
     cfg.numAttrs = (unsigned)n;
-    note_launch(kern, ls.grid, ls.block, ls.smem, ls.cluster);
+    note_launch(kern, ls.grid, ls.block, ls.smem, ls.cluster > 0 ? ls.cluster : 1);
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<A&&>(args)...);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

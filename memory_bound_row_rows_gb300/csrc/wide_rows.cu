@@ -43,6 +43,20 @@ namespace {
 
 constexpr int kWideThreads = 256;
 
+// 1: every cluster of the register-resident kernel prefetches into L2 the
+// slice of the row that starts about one wave of resident clusters later.
+#ifndef SR_WIDE_L2_AHEAD
+#define SR_WIDE_L2_AHEAD 1
+#endif
+
+// Bulk prefetch of `bytes` of global memory into L2 (multiple of 16, start
+// 16-byte aligned) by the bulk-copy engine: no registers, no shared memory,
+// nothing to wait for; later loads of those bytes hit L2.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
+    if (!SR_READ_OK(p, bytes)) return;
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // exp(x - m) for FP32 data: the hardware ex2 of the difference (rounded once
 // in FP32) times log2(e), as in the ROW plan, instead of the library expf;
 // SR_WIDE_EX2 = 0 keeps expf. 16-bit data always takes one FMA and ex2.
@@ -93,7 +107,7 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
                                                                      : SR_WIDE_MIN_BLOCKS)
     wide_rows_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
-                     unsigned long long timeout_ns, int flags) {
+                     unsigned long long timeout_ns, int flags, int64_t ahead) {
     SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
@@ -143,6 +157,14 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
         }
         const T* rbody = rin + head;
         const int64_t u1 = (u0 + slice < nvb) ? u0 + slice : nvb;
+        // The row `ahead` rows on (the one a cluster starts about one wave of
+        // resident clusters later) is prefetched into L2 by the bulk-copy
+        // engine, so that its blocks load from L2 and hold their registers
+        // for less time; DRAM streams it in the background meanwhile.
+        if constexpr (!SHIFTED) {
+            if (SR_WIDE_L2_AHEAD && tid == 0 && ahead > 0 && r + ahead < M && u1 > u0)
+                bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)((u1 - u0) * 16));
+        }
         uint4 raw[KV];
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
@@ -312,7 +334,8 @@ template <typename T>
 __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
     wide_stream_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
-                       unsigned int* err, unsigned long long timeout_ns, int flags) {
+                       unsigned int* err, unsigned long long timeout_ns, int flags,
+                       int64_t /* ahead: unused */) {
     SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
     constexpr int VEC = Elem<T>::kVec;
@@ -447,14 +470,15 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
 
 template <typename T>
 using WideKernel = void (*)(const T*, T*, int64_t, int64_t, int64_t, int64_t, int, int64_t,
-                            unsigned int*, unsigned long long, int);
+                            unsigned int*, unsigned long long, int, int64_t);
 
 template <typename T>
 cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int64_t slice) {
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = ensure_smem_limit(fn, 0, csize > 8);
     if (e != cudaSuccess) return e;
-    if (max_active_clusters(fn, kWideThreads, 0, csize) <= 0) return cudaErrorInvalidConfiguration;
+    const int resident = max_active_clusters(fn, kWideThreads, 0, csize);
+    if (resident <= 0) return cudaErrorInvalidConfiguration;
     // One cluster per row up to the largest grid; beyond it rows are walked
     // with a stride.
     const int64_t cap = 0x7fffffff / csize;
@@ -465,7 +489,7 @@ cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int
                          csize, SR_WIDE_POLICY};
     e = launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                       p.M, p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
-                      p.flags);
+                      p.flags, (int64_t)resident);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
