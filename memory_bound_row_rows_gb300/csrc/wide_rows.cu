@@ -25,6 +25,7 @@
 // more (bounded) so that a late peer's pair cannot land after it exits.
 #include "device.cuh"
 #include "internal.h"
+#include "l2prefetch.cuh"
 #include "packed.cuh"
 #include "wide.h"
 
@@ -43,19 +44,6 @@ namespace {
 
 constexpr int kWideThreads = 256;
 
-// 1: every cluster of the register-resident kernel prefetches into L2 the
-// slice of the row that starts about one wave of resident clusters later.
-#ifndef SR_WIDE_L2_AHEAD
-#define SR_WIDE_L2_AHEAD 1
-#endif
-
-// Bulk prefetch of `bytes` of global memory into L2 (multiple of 16, start
-// 16-byte aligned) by the bulk-copy engine: no registers, no shared memory,
-// nothing to wait for; later loads of those bytes hit L2.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) {
-    if (!SR_READ_OK(p, bytes)) return;
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // exp(x - m) for FP32 data: the hardware ex2 of the difference (rounded once
 // in FP32) times log2(e), as in the ROW plan, instead of the library expf;
@@ -162,7 +150,7 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
         // engine, so that its blocks load from L2 and hold their registers
         // for less time; DRAM streams it in the background meanwhile.
         if constexpr (!SHIFTED) {
-            if (SR_WIDE_L2_AHEAD && tid == 0 && ahead > 0 && r + ahead < M && u1 > u0)
+            if (tid == 0 && ahead > 0 && r + ahead < M && u1 > u0)
                 bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)((u1 - u0) * 16));
         }
         uint4 raw[KV];
@@ -489,7 +477,7 @@ cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int
                          csize, SR_WIDE_POLICY};
     e = launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                       p.M, p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
-                      p.flags, (int64_t)resident);
+                      p.flags, (int64_t)(csize >= kAheadMinCluster ? resident : 0));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
