@@ -55,8 +55,8 @@ PLAN_SOURCES = {
     "row": ["block_rows.cu", "packed.cuh"], "warp": ["warp_rows.cu", "packed.cuh"], "cta": ["tma_rows.cu"],
     "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
     "split": ["split_rows.cu"], "wide": ["wide_rows.cu", "wide.h", "packed.cuh", "l2prefetch.cuh"],
-    "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h", "l2prefetch.cuh"],
-    "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h", "l2prefetch.cuh"],
+    "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],
+    "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h"],
     "copy": ["copy_rows.cu"],
 }
 SHARED_SOURCES = ["device.cuh", "internal.h"]

@@ -1,5 +1,6 @@
-// L2 prefetch by the bulk-copy engine, for the cluster kernels that prefetch
-// the row a cluster will start about one wave of resident clusters later.
+// L2 prefetch by the bulk-copy engine, for the WIDE kernel, whose clusters
+// prefetch the row a cluster will start about one wave of resident clusters
+// later.
 #pragma once
 
 #include "device.cuh"
@@ -15,9 +16,11 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
 }
 
 // Clusters of at least this many blocks prefetch one wave ahead (measured on
-// GB300, cold L2: with 8-block clusters bf16 1024 x 131072 84.5 -> 82.6 µs,
-// with 16-block clusters f32 512 x 131072 88.2 -> 83.4 µs; 4-block clusters
-// unchanged, 2-block clusters 0.5 % slower).
+// GB300, cold L2: with 8-block clusters bf16 1024 x 131072 84.5 -> 82.6 µs and
+// 82.5 -> 81.9 µs on two machines, with 16-block clusters f32 512 x 131072
+// 88.2 -> 83.4 µs; 4-block clusters unchanged, 2-block clusters 0.5 % slower).
+// The row-pair CLUSTER kernel does not prefetch: on the backward of f16
+// 64 x 131072 (1.7 waves of 16-block clusters) it cost 5 %.
 #ifndef SR_AHEAD_MIN_CLUSTER
 #define SR_AHEAD_MIN_CLUSTER 4
 #endif

@@ -47,7 +47,6 @@
 
 #include "device.cuh"
 #include "internal.h"
-#include "l2prefetch.cuh"
 #include "rowpair.h"
 
 namespace sr {
@@ -344,7 +343,7 @@ __global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN
     cluster_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                    int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
                    int64_t slice, unsigned int* err, unsigned long long timeout_ns,
-                   int flags, int64_t ahead) {
+                   int flags) {
     SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
@@ -390,14 +389,6 @@ __global__ void __launch_bounds__(kClusterThreads, KV <= 4 ? SR_PAIR_CLUSTER_MIN
         const T* rb = B + r * ldb;
         const L lay(ra, N);
         const int64_t u1 = (u0 + slice < lay.nv) ? u0 + slice : lay.nv;
-        // Both inputs' slices of the row `ahead` rows on (the one a cluster
-        // starts about one wave of resident clusters later) go to L2 now.
-        if constexpr (MODE == Mode::kAligned) {
-            if (tid == 0 && ahead > 0 && r + ahead < M && u1 > u0) {
-                bulk_prefetch_l2(A + (r + ahead) * lda + u0 * VEC, (uint32_t)((u1 - u0) * 16));
-                bulk_prefetch_l2(B + (r + ahead) * ldb + u0 * VEC, (uint32_t)((u1 - u0) * 16));
-            }
-        }
         U a[KV], b[KV];
 #pragma unroll
         for (int k = 0; k < KV; ++k) {
@@ -495,8 +486,7 @@ template <class Op, typename T>
 __global__ void __launch_bounds__(kClusterThreads, kStreamMinBlocks)
     stream_kernel(Op op, const T* __restrict__ A, const T* __restrict__ B, T* __restrict__ C,
                   int64_t M, int64_t N, int64_t lda, int64_t ldb, int64_t ldc, int csize,
-                  int64_t slice, unsigned int* err, unsigned long long timeout_ns, int flags,
-                  int64_t /* ahead: unused */) {
+                  int64_t slice, unsigned int* err, unsigned long long timeout_ns, int flags) {
     SR_GRID_DEPENDENCY();
     SR_BOUNDS_BEGIN(SR_MAT_IN(A, M, lda, N), SR_MAT_IN(B, M, ldb, N), SR_MAT_OUT(C, M, ldc, N),
                     SR_SPAN_IN(op.aux_base(), N * (int64_t)sizeof(T)));
@@ -729,8 +719,7 @@ cudaError_t launch_team(const Op& op, const Args& p, const Shape& sh) {
 
 template <class Op, typename T>
 using ClusterKernel = void (*)(Op, const T*, const T*, T*, int64_t, int64_t, int64_t, int64_t,
-                               int64_t, int, int64_t, unsigned int*, unsigned long long, int,
-                               int64_t);
+                               int64_t, int, int64_t, unsigned int*, unsigned long long, int);
 
 template <class Op, typename T>
 cudaError_t launch_clusters(ClusterKernel<Op, T> kern, const Op& op, const Args& p,
@@ -738,15 +727,14 @@ cudaError_t launch_clusters(ClusterKernel<Op, T> kern, const Op& op, const Args&
     const void* fn = reinterpret_cast<const void*>(kern);
     cudaError_t e = ensure_smem_limit(fn, 0, sh.csize > 8);
     if (e != cudaSuccess) return e;
-    const int resident = max_active_clusters(fn, kClusterThreads, 0, sh.csize);
-    if (resident <= 0) return cudaErrorInvalidConfiguration;
+    if (max_active_clusters(fn, kClusterThreads, 0, sh.csize) <= 0)
+        return cudaErrorInvalidConfiguration;
     return launch_kernel(kern,
                          LaunchShape{dim3(grid_for(p.M, sh.csize)), dim3(kClusterThreads), 0,
                                      sh.csize},
                          p.stream, op, static_cast<const T*>(p.a), static_cast<const T*>(p.b),
                          static_cast<T*>(p.c), p.M, p.N, p.lda, p.ldb, p.ldc, sh.csize, sh.slice,
-                         p.err, p.timeout_ns, p.flags,
-                         (int64_t)(sh.csize >= kAheadMinCluster ? resident : 0));
+                         p.err, p.timeout_ns, p.flags);
 }
 
 template <class Op, typename T, Mode MODE>
