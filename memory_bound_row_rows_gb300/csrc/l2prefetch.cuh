@@ -25,5 +25,9 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void* p, uint32_t bytes) 
 #define SR_AHEAD_MIN_CLUSTER 4
 #endif
 constexpr int kAheadMinCluster = SR_AHEAD_MIN_CLUSTER;
+// How far ahead, in half waves of resident clusters.
+#ifndef SR_WIDE_AHEAD_HALVES
+#define SR_WIDE_AHEAD_HALVES 2
+#endif
 
 }  // namespace sr

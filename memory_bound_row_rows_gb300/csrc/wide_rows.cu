@@ -477,7 +477,8 @@ cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int
                          csize, SR_WIDE_POLICY};
     e = launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                       p.M, p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
-                      p.flags, (int64_t)(csize >= kAheadMinCluster ? resident : 0));
+                      p.flags,
+                      (int64_t)(csize >= kAheadMinCluster ? resident * SR_WIDE_AHEAD_HALVES / 2 : 0));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
