@@ -42,6 +42,12 @@ namespace {
 #define SR_WIDE_MIN_BLOCKS 4
 #endif
 
+// 1: evenly split aligned rows of 2..16 slices of 4096 vectors run the staged
+// variant (half of each slice in shared memory; wide_staged_kernel).
+#ifndef SR_WIDE_STAGED
+#define SR_WIDE_STAGED 1
+#endif
+
 constexpr int kWideThreads = 256;
 
 
@@ -260,6 +266,150 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
     }
 }
 
+// Staged variant for evenly split aligned rows: each thread holds 8 vectors
+// of its block's slice in registers and 8 more in shared memory, brought in
+// by 16-byte cp.async copies that occupy no registers while in flight (each
+// thread reads back only its own slots, so no block barrier is needed). A
+// block thus holds 64 KiB of the row instead of 32, and a row needs half as
+// many blocks, i.e. half as many SMs waiting for each other's (max, sum)
+// pairs; 1 MiB rows fit on chip in 16-block clusters. Arithmetic, exchange,
+// prefetch and failure path as in wide_rows_kernel (kFull).
+constexpr int kStagedKV = 8;
+constexpr int kStagedKS = 8;
+constexpr int64_t kStagedSlice = (int64_t)kWideThreads * (kStagedKV + kStagedKS);
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    if (!SR_READ_OK(src, 16)) return;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+#ifndef SR_WIDE_STAGED_MIN_BLOCKS
+#define SR_WIDE_STAGED_MIN_BLOCKS 3
+#endif
+template <typename T>
+__global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
+    wide_staged_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                       int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
+                       unsigned int* err, unsigned long long timeout_ns, int flags,
+                       int64_t ahead) {
+    SR_GRID_DEPENDENCY();
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int NT = kWideThreads;
+    constexpr int NW = kWideWarps;
+    constexpr int KV = kStagedKV;
+    constexpr int KS = kStagedKS;
+    extern __shared__ __align__(128) unsigned char stage_buf[];  // slot k*NT + tid: 16 bytes
+    __shared__ float2 pairs[2][kMaxCluster * NW];
+    __shared__ __align__(8) unsigned long long xbar[2];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = (int)cluster_ctarank();
+    const int64_t nclusters = gridDim.x / csize;
+    const int64_t u0 = (int64_t)rank * slice;
+    const int npairs = csize * NW;
+    const bool send = !(flags & kFlagNoCopy);
+    const uint32_t stage = smem_addr(stage_buf) + 16u * (uint32_t)tid;
+
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+    bool started = false, failed = false;
+    uint32_t fail_bar = 0, fail_phase = 0;
+    int64_t it = 0;
+    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters, ++it) {
+        const int p = (int)(it & 1);
+        const uint32_t phase = (uint32_t)((it >> 1) & 1);
+        const T* rin = in + r * ld_in + u0 * VEC;
+        if (tid == 0 && ahead > 0 && r + ahead < M)
+            bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)(slice * 16));
+        // Vectors NT*KV + tid + NT*k of the slice go to this thread's staging
+        // slots, vectors tid + NT*k to its registers.
+#pragma unroll
+        for (int k = 0; k < KS; ++k)
+            cp_async16(stage + 16u * (uint32_t)(NT * k), rin + (int64_t)(NT * KV + tid + NT * k) * VEC);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        uint4 raw[KV];
+#pragma unroll
+        for (int k = 0; k < KV; ++k) raw[k] = ldg_stream(rin + (int64_t)(tid + NT * k) * VEC);
+        VecMax<T> vm;
+#pragma unroll
+        for (int k = 0; k < KV; ++k) vm.add(raw[k]);
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+#pragma unroll
+        for (int k = 0; k < KS; ++k) vm.add(lds128(stage + 16u * (uint32_t)(NT * k)));
+        const float m_w = warp_max(vm.get());
+        const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
+        const float shift_l2 = shift * kLog2e;
+        float sa = 0.0f, sb = 0.0f;
+        auto add_exp = [&](const uint4& u) {
+            float f[VEC];
+            Elem<T>::unpack(u, f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                const float x = wide_exp<T>(f[e], shift, shift_l2);
+                if (e & 1) sb += x; else sa += x;
+            }
+        };
+#pragma unroll
+        for (int k = 0; k < KV; ++k) add_exp(raw[k]);
+#pragma unroll
+        for (int k = 0; k < KS; ++k) add_exp(lds128(stage + 16u * (uint32_t)(NT * k)));
+        const float s_w = warp_sum(sa + sb);
+        if (!started) {
+            cluster_wait();
+            started = true;
+        }
+        const uint32_t xb = smem_addr(&xbar[p]);
+        if (tid == 0) mbar_expect_tx(xb, (uint32_t)npairs * 8u);
+        if (send && lane < csize)
+            st_async_f2(map_to_rank(smem_addr(&pairs[p][rank * NW + warp]), (uint32_t)lane), m_w,
+                        s_w, map_to_rank(xb, (uint32_t)lane));
+        if (!failed && !mbar_wait_bounded(xb, phase, timeout_ns)) {
+            failed = true;
+            fail_bar = xb;
+            fail_phase = phase;
+        }
+        if (failed) continue;
+        float mloc = neg_inf();
+        for (int i = lane; i < npairs; i += 32) mloc = fmaxf(mloc, pairs[p][i].x);
+        const float Mr = warp_max(mloc);
+        float sloc = 0.0f;
+        for (int i = lane; i < npairs; i += 32) {
+            const float2 q = pairs[p][i];
+            sloc += q.y * merge_scale(q.x, Mr);
+        }
+        const float Sr = warp_sum(sloc);
+        T* rout = out + r * ld_out + u0 * VEC;
+        const float rs = Elem<T>::kAccurateExp ? final_rcp(Mr, Sr) : 0.0f;
+        const float c = Elem<T>::kAccurateExp ? 0.0f : fmaf(Mr, kLog2e, lg2_approx(Sr));
+        auto put = [&](const uint4& u, int64_t idx) {
+            float f[VEC];
+            unpack_again<T>(u, f);
+#pragma unroll
+            for (int e = 0; e < VEC; ++e) {
+                if constexpr (Elem<T>::kAccurateExp)
+                    f[e] = wide_exp<T>(f[e], Mr, 0.0f) * rs;
+                else
+                    f[e] = ex2_approx(fmaf(f[e], kLog2e, -c));
+            }
+            stg_stream(rout + idx * VEC, Elem<T>::pack(f));
+        };
+#pragma unroll
+        for (int k = 0; k < KV; ++k) put(raw[k], tid + NT * k);
+#pragma unroll
+        for (int k = 0; k < KS; ++k) put(lds128(stage + 16u * (uint32_t)(NT * k)), NT * KV + tid + NT * k);
+    }
+    if (!started) cluster_wait();
+    if (failed) {
+        if (tid == 0) atomicOr(err, 1u);
+        mbar_wait_bounded(fail_bar, fail_phase, timeout_ns);
+    }
+}
+
 // Streamed variant for aligned rows too wide for the registers of a 16-block
 // cluster (over 512 KiB): the looped plan of the same section (Wide rows),
 // spread over a cluster. Pass 1 walks the block's slice in steps of
@@ -456,6 +606,14 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
     }
 }
 
+// Cluster size of the staged variant for aligned rows of nvec vectors: rows
+// that split evenly into 2..16 slices of kStagedSlice vectors; 0 otherwise.
+inline int staged_cluster(int64_t nvec) {
+    if (nvec % kStagedSlice != 0) return 0;
+    const int64_t c = nvec / kStagedSlice;
+    return (c == 2 || c == 4 || c == 8 || c == 16) ? (int)c : 0;
+}
+
 template <typename T>
 using WideKernel = void (*)(const T*, T*, int64_t, int64_t, int64_t, int64_t, int, int64_t,
                             unsigned int*, unsigned long long, int, int64_t);
@@ -478,7 +636,7 @@ cudaError_t launch_clusters(WideKernel<T> kern, const Problem& p, int csize, int
     e = launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in), static_cast<T*>(p.out),
                       p.M, p.N, p.ld_in, p.ld_out, csize, slice, p.dev->err, p.timeout_ns,
                       p.flags,
-                      (int64_t)(csize >= kAheadMinCluster ? resident * SR_WIDE_AHEAD_HALVES / 2 : 0));
+                      (int64_t)(csize >= kAheadMinCluster ? resident * SR_WIDE_AHEAD_QUARTERS / 4 : 0));
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -499,6 +657,26 @@ template <typename T>
 cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     const int64_t nvec = p.N / Elem<T>::kVec;
     const bool aligned = rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype);
+    if (SR_WIDE_STAGED && aligned) {
+        const int c = staged_cluster(nvec);
+        if (c > 0) {
+            auto kern = wide_staged_kernel<T>;
+            const size_t smem = (size_t)kWideThreads * kStagedKS * 16;
+            const void* fn = reinterpret_cast<const void*>(kern);
+            cudaError_t e = ensure_smem_limit(fn, smem, c > 8);
+            if (e != cudaSuccess) return e;
+            const int resident = max_active_clusters(fn, kWideThreads, smem, c);
+            if (resident <= 0) return cudaErrorInvalidConfiguration;
+            const int64_t cap = 0x7fffffff / c;
+            const LaunchShape ls{dim3((unsigned)((p.M < cap ? p.M : cap) * c)), dim3(kWideThreads),
+                                 smem, c, SR_WIDE_POLICY};
+            return launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in),
+                                 static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, c,
+                                 kStagedSlice, p.dev->err, p.timeout_ns, p.flags,
+                                 (int64_t)(c >= kAheadMinCluster ? resident * SR_WIDE_AHEAD_QUARTERS / 4
+                                                                 : 0));
+        }
+    }
     if (sh.streamed) {
         if (!aligned) return cudaErrorInvalidValue;
         return launch_clusters<T>(wide_stream_kernel<T>, p, sh.csize, sh.slice);

@@ -399,6 +399,43 @@ def test_side_stream_and_empty_calls():
     assert torch.isnan(y2).all()
 
 
+# ---- evenly split aligned wide rows: the staged WIDE variant (half of each
+# block's slice in shared memory, 2..16-block clusters, 1 MiB rows on chip) ----
+
+@pytest.mark.parametrize("dtype,M,N,csize", [(synth.BF16, 130, 524288, 16),
+                                             (synth.F32, 77, 131072, 8),
+                                             (synth.F16, 301, 131072, 4),
+                                             (synth.BF16, 40, 65536, 2)],
+                         ids=["bf16-1MiB-16", "f32-512KiB-8", "f16-256KiB-4", "bf16-128KiB-2"])
+def test_wide_staged_rows(dtype, M, N, csize):
+    x = synth.generate(M, N, dtype=dtype, seed=700 + M, p1=2.0)
+    xd = gu.to_device(x, dtype)
+    st, y = run_plan(xd, M, N, N, N, dtype, sr.SR_PLAN_AUTO)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    info = sr.softmax_rows_last_launch()
+    assert "wide_staged_kernel" in info["name"] and info["cluster"] == csize
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "staged WIDE")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
+def test_wide_staged_wait_expiry():
+    M, N, dtype = 8, 131072, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=32)
+    xd = gu.to_device(x, dtype)
+    y = nan_filled(M, N, dtype)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    sr.softmax_rows_test_expiry(xd, y, M, N, N, N, dtype, sr.SR_PLAN_WIDE, 2_000_000)
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert "wide_staged_kernel" in sr.softmax_rows_last_launch()["name"]
+    assert torch.isnan(y).all(), "an expired kernel wrote output"
+    st, y = run_plan(xd, M, N, N, N, dtype, sr.SR_PLAN_WIDE)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "after expiry")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
 # ---- the bounded wait: an expiring wait reports an error, the context survives ----
 
 @pytest.mark.parametrize("name,plan", [("f32_4096x4096", sr.SR_PLAN_CTA),
