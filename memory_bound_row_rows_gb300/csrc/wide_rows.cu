@@ -42,8 +42,11 @@ namespace {
 #define SR_WIDE_MIN_BLOCKS 4
 #endif
 
-// 1: evenly split aligned rows of 2..16 slices of 4096 vectors run the staged
-// variant (half of each slice in shared memory; wide_staged_kernel).
+// 1: aligned rows over 512 KiB and up to 1 MiB run the staged variant (up to
+// half of each slice in shared memory; wide_staged_kernel) instead of being
+// streamed: bf16 128 x 524288 48.5 against 56.6 µs on GB300 (cold L2). On
+// rows the registers hold it gained nothing (within 1 %), so it is not used
+// there.
 #ifndef SR_WIDE_STAGED
 #define SR_WIDE_STAGED 1
 #endif
@@ -266,17 +269,16 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
     }
 }
 
-// Staged variant for evenly split aligned rows: each thread holds 8 vectors
-// of its block's slice in registers and 8 more in shared memory, brought in
-// by 16-byte cp.async copies that occupy no registers while in flight (each
-// thread reads back only its own slots, so no block barrier is needed). A
-// block thus holds 64 KiB of the row instead of 32, and a row needs half as
-// many blocks, i.e. half as many SMs waiting for each other's (max, sum)
-// pairs; 1 MiB rows fit on chip in 16-block clusters. Arithmetic, exchange,
-// prefetch and failure path as in wide_rows_kernel (kFull).
+// Staged variant for aligned rows too wide for a 16-block cluster's registers
+// (over 512 KiB, up to 1 MiB): each thread holds 8 vectors of its block's
+// slice in registers and up to 8 more in shared memory, brought in by 16-byte
+// cp.async copies that occupy no registers while in flight (each thread reads
+// back only its own slots, so no block barrier is needed). A block holds up to
+// 64 KiB of the row, so such rows stay on chip and are read from DRAM once
+// instead of being streamed twice. Arithmetic, exchange, prefetch and failure
+// path as in wide_rows_kernel (kAligned).
 constexpr int kStagedKV = 8;
 constexpr int kStagedKS = 8;
-constexpr int64_t kStagedSlice = (int64_t)kWideThreads * (kStagedKV + kStagedKS);
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     if (!SR_READ_OK(src, 16)) return;
@@ -306,6 +308,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
     const int rank = (int)cluster_ctarank();
     const int64_t nclusters = gridDim.x / csize;
     const int64_t u0 = (int64_t)rank * slice;
+    const int64_t nvec = N / VEC;
+    // Vectors of this block's slice (the last blocks' slices may be short).
+    const int64_t n = u0 >= nvec ? 0 : (nvec - u0 < slice ? nvec - u0 : slice);
     const int npairs = csize * NW;
     const bool send = !(flags & kFlagNoCopy);
     const uint32_t stage = smem_addr(stage_buf) + 16u * (uint32_t)tid;
@@ -324,23 +329,28 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
         const int p = (int)(it & 1);
         const uint32_t phase = (uint32_t)((it >> 1) & 1);
         const T* rin = in + r * ld_in + u0 * VEC;
-        if (tid == 0 && ahead > 0 && r + ahead < M)
-            bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)(slice * 16));
-        // Vectors NT*KV + tid + NT*k of the slice go to this thread's staging
-        // slots, vectors tid + NT*k to its registers.
+        if (tid == 0 && ahead > 0 && r + ahead < M && n > 0)
+            bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)(n * 16));
+        // Vectors NT*KV + tid + NT*k of the slice (those below n) go to this
+        // thread's staging slots, vectors tid + NT*k to its registers.
 #pragma unroll
         for (int k = 0; k < KS; ++k)
-            cp_async16(stage + 16u * (uint32_t)(NT * k), rin + (int64_t)(NT * KV + tid + NT * k) * VEC);
+            if (NT * KV + tid + NT * k < n)
+                cp_async16(stage + 16u * (uint32_t)(NT * k),
+                           rin + (int64_t)(NT * KV + tid + NT * k) * VEC);
         asm volatile("cp.async.commit_group;" ::: "memory");
         uint4 raw[KV];
 #pragma unroll
-        for (int k = 0; k < KV; ++k) raw[k] = ldg_stream(rin + (int64_t)(tid + NT * k) * VEC);
+        for (int k = 0; k < KV; ++k)
+            if (tid + NT * k < n) raw[k] = ldg_stream(rin + (int64_t)(tid + NT * k) * VEC);
         VecMax<T> vm;
 #pragma unroll
-        for (int k = 0; k < KV; ++k) vm.add(raw[k]);
+        for (int k = 0; k < KV; ++k)
+            if (tid + NT * k < n) vm.add(raw[k]);
         asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
-        for (int k = 0; k < KS; ++k) vm.add(lds128(stage + 16u * (uint32_t)(NT * k)));
+        for (int k = 0; k < KS; ++k)
+            if (NT * KV + tid + NT * k < n) vm.add(lds128(stage + 16u * (uint32_t)(NT * k)));
         const float m_w = warp_max(vm.get());
         const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
         const float shift_l2 = shift * kLog2e;
@@ -355,9 +365,11 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
             }
         };
 #pragma unroll
-        for (int k = 0; k < KV; ++k) add_exp(raw[k]);
+        for (int k = 0; k < KV; ++k)
+            if (tid + NT * k < n) add_exp(raw[k]);
 #pragma unroll
-        for (int k = 0; k < KS; ++k) add_exp(lds128(stage + 16u * (uint32_t)(NT * k)));
+        for (int k = 0; k < KS; ++k)
+            if (NT * KV + tid + NT * k < n) add_exp(lds128(stage + 16u * (uint32_t)(NT * k)));
         const float s_w = warp_sum(sa + sb);
         if (!started) {
             cluster_wait();
@@ -399,9 +411,12 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
             stg_stream(rout + idx * VEC, Elem<T>::pack(f));
         };
 #pragma unroll
-        for (int k = 0; k < KV; ++k) put(raw[k], tid + NT * k);
+        for (int k = 0; k < KV; ++k)
+            if (tid + NT * k < n) put(raw[k], tid + NT * k);
 #pragma unroll
-        for (int k = 0; k < KS; ++k) put(lds128(stage + 16u * (uint32_t)(NT * k)), NT * KV + tid + NT * k);
+        for (int k = 0; k < KS; ++k)
+            if (NT * KV + tid + NT * k < n)
+                put(lds128(stage + 16u * (uint32_t)(NT * k)), NT * KV + tid + NT * k);
     }
     if (!started) cluster_wait();
     if (failed) {
@@ -606,14 +621,6 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
     }
 }
 
-// Cluster size of the staged variant for aligned rows of nvec vectors: rows
-// that split evenly into 2..16 slices of kStagedSlice vectors; 0 otherwise.
-inline int staged_cluster(int64_t nvec) {
-    if (nvec % kStagedSlice != 0) return 0;
-    const int64_t c = nvec / kStagedSlice;
-    return (c == 2 || c == 4 || c == 8 || c == 16) ? (int)c : 0;
-}
-
 template <typename T>
 using WideKernel = void (*)(const T*, T*, int64_t, int64_t, int64_t, int64_t, int, int64_t,
                             unsigned int*, unsigned long long, int, int64_t);
@@ -657,25 +664,24 @@ template <typename T>
 cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     const int64_t nvec = p.N / Elem<T>::kVec;
     const bool aligned = rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype);
-    if (SR_WIDE_STAGED && aligned) {
-        const int c = staged_cluster(nvec);
-        if (c > 0) {
-            auto kern = wide_staged_kernel<T>;
-            const size_t smem = (size_t)kWideThreads * kStagedKS * 16;
-            const void* fn = reinterpret_cast<const void*>(kern);
-            cudaError_t e = ensure_smem_limit(fn, smem, c > 8);
-            if (e != cudaSuccess) return e;
-            const int resident = max_active_clusters(fn, kWideThreads, smem, c);
-            if (resident <= 0) return cudaErrorInvalidConfiguration;
-            const int64_t cap = 0x7fffffff / c;
-            const LaunchShape ls{dim3((unsigned)((p.M < cap ? p.M : cap) * c)), dim3(kWideThreads),
-                                 smem, c, SR_WIDE_POLICY};
-            return launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in),
-                                 static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, c,
-                                 kStagedSlice, p.dev->err, p.timeout_ns, p.flags,
-                                 (int64_t)(c >= kAheadMinCluster ? resident * SR_WIDE_AHEAD_QUARTERS / 4
-                                                                 : 0));
-        }
+    if (sh.staged) {
+        if (!aligned) return cudaErrorInvalidValue;
+        auto kern = wide_staged_kernel<T>;
+        const int c = sh.csize;
+        const size_t smem = (size_t)kWideThreads * kStagedKS * 16;
+        const void* fn = reinterpret_cast<const void*>(kern);
+        cudaError_t e = ensure_smem_limit(fn, smem, c > 8);
+        if (e != cudaSuccess) return e;
+        const int resident = max_active_clusters(fn, kWideThreads, smem, c);
+        if (resident <= 0) return cudaErrorInvalidConfiguration;
+        const int64_t cap = 0x7fffffff / c;
+        const LaunchShape ls{dim3((unsigned)((p.M < cap ? p.M : cap) * c)), dim3(kWideThreads),
+                             smem, c, SR_WIDE_POLICY};
+        return launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in),
+                             static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, c, sh.slice,
+                             p.dev->err, p.timeout_ns, p.flags,
+                             (int64_t)(c >= kAheadMinCluster ? resident * SR_WIDE_AHEAD_QUARTERS / 4
+                                                             : 0));
     }
     if (sh.streamed) {
         if (!aligned) return cudaErrorInvalidValue;
@@ -706,8 +712,10 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
 // cluster doubles (up to 8: larger clusters are scheduled poorly) as long as
 // each thread keeps at least one vector. The vectors per thread are rounded
 // up to 1, 2, 4 or 8. Rows up to 16 x 256 x 8 vectors (512 KiB) are held in
-// registers; wider rows are streamed by 8-block clusters (16 while the grid
-// would not fill one wave of resident blocks).
+// registers; rows up to twice that are staged (16-block clusters, 8 vectors
+// per thread in registers and up to 8 in shared memory); wider rows are
+// streamed by 8-block clusters (16 while the grid would not fill one wave of
+// resident blocks).
 bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
     const int64_t nvec = N * elem_bytes(dtype) / 16;
     for (int c = 2; c <= kMaxCluster; c *= 2) {
@@ -720,6 +728,15 @@ bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
         out->kv = kv <= 1 ? 1 : kv <= 2 ? 2 : kv <= 4 ? 4
                 : (SR_WIDE_MID_KV && kv <= 5) ? 5 : (SR_WIDE_MID_KV && kv <= 6) ? 6 : 8;
         out->streamed = false;
+        return true;
+    }
+    if (SR_WIDE_STAGED &&
+        nvec <= (int64_t)kMaxCluster * kWideThreads * (kStagedKV + kStagedKS)) {
+        out->csize = kMaxCluster;
+        out->slice = (nvec + kMaxCluster - 1) / kMaxCluster;
+        out->kv = kStagedKV + kStagedKS;
+        out->streamed = false;
+        out->staged = true;
         return true;
     }
     int c = SR_WIDE_STREAM_CLUSTER;
@@ -739,7 +756,7 @@ bool wide_fits(const void* in, const void* out, int64_t N, int64_t ld_in, int64_
     WideShape sh;
     if (!wide_shape(1, N, dtype, 0, &sh)) return false;
     if (rows_vector_aligned(in, out, N, ld_in, ld_out, dtype)) return true;
-    if (sh.streamed) return false;
+    if (sh.streamed || sh.staged) return false;
     const int64_t es = elem_bytes(dtype);
     const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
     return a % 16 == b % 16 && a % es == 0 && (ld_in * es) % 16 == (ld_out * es) % 16;

@@ -252,8 +252,8 @@ def test_special_rows(dtype, N):
 
 # ---- rows too wide for a cluster's registers: the streamed WIDE kernel ----
 
-@pytest.mark.parametrize("dtype,M,N", [(synth.BF16, 3, 262152), (synth.F32, 2, 300000),
-                                       (synth.F16, 9, 600000), (synth.BF16, 40, 524288)],
+@pytest.mark.parametrize("dtype,M,N", [(synth.BF16, 3, 600008), (synth.F32, 2, 300000),
+                                       (synth.F16, 9, 600000), (synth.BF16, 20, 1048576)],
                          ids=lambda v: str(v))
 def test_streamed_wide_rows(dtype, M, N):
     from tests import pins
@@ -289,7 +289,7 @@ def test_streamed_wide_in_place():
 
 
 def test_streamed_wide_wait_expiry():
-    M, N, dtype = 3, 262152, synth.BF16
+    M, N, dtype = 3, 600008, synth.BF16
     x = synth.generate(M, N, dtype=dtype, seed=77, p1=2.0)
     xd = gu.to_device(x, dtype)
     y = nan_filled(M, N, dtype)
@@ -399,14 +399,14 @@ def test_side_stream_and_empty_calls():
     assert torch.isnan(y2).all()
 
 
-# ---- evenly split aligned wide rows: the staged WIDE variant (half of each
-# block's slice in shared memory, 2..16-block clusters, 1 MiB rows on chip) ----
+# ---- aligned rows over 512 KiB and up to 1 MiB: the staged WIDE variant (16-block
+# clusters, up to half of each block's slice in shared memory) ----
 
 @pytest.mark.parametrize("dtype,M,N,csize", [(synth.BF16, 130, 524288, 16),
-                                             (synth.F32, 77, 131072, 8),
-                                             (synth.F16, 301, 131072, 4),
-                                             (synth.BF16, 40, 65536, 2)],
-                         ids=["bf16-1MiB-16", "f32-512KiB-8", "f16-256KiB-4", "bf16-128KiB-2"])
+                                             (synth.F32, 77, 262144, 16),
+                                             (synth.F16, 50, 262152, 16),
+                                             (synth.BF16, 33, 400008, 16)],
+                         ids=["bf16-1MiB", "f32-1MiB", "f16-just-over-512KiB", "bf16-uneven"])
 def test_wide_staged_rows(dtype, M, N, csize):
     x = synth.generate(M, N, dtype=dtype, seed=700 + M, p1=2.0)
     xd = gu.to_device(x, dtype)
@@ -419,8 +419,22 @@ def test_wide_staged_rows(dtype, M, N, csize):
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
 
+def test_wide_staged_in_place():
+    """in == out: each block reads its whole slice (registers and shared memory)
+    before the exchange and writes only its own slice after it."""
+    M, N, dtype = 6, 400008, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=93, p1=2.0)
+    buf = gu.to_device(x, dtype)
+    st = sr.load().softmax_rows_ex(buf.data_ptr(), buf.data_ptr(), M, N, N, N, dtype,
+                                   sr.SR_PLAN_AUTO, torch.cuda.current_stream().cuda_stream)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    assert "wide_staged_kernel" in sr.softmax_rows_last_launch()["name"]
+    gu.check_rows(gu.to_host(buf, dtype), x, N, N, dtype, "staged WIDE in place")
+
+
 def test_wide_staged_wait_expiry():
-    M, N, dtype = 8, 131072, synth.BF16
+    M, N, dtype = 8, 524288, synth.BF16
     x = synth.generate(M, N, dtype=dtype, seed=32)
     xd = gu.to_device(x, dtype)
     y = nan_filled(M, N, dtype)
