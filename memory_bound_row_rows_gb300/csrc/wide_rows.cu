@@ -288,7 +288,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 #ifndef SR_WIDE_STAGED_MIN_BLOCKS
 #define SR_WIDE_STAGED_MIN_BLOCKS 3
 #endif
-template <typename T>
+template <typename T, bool EVEN>
 __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
     wide_staged_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
@@ -310,7 +310,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
     const int64_t u0 = (int64_t)rank * slice;
     const int64_t nvec = N / VEC;
     // Vectors of this block's slice (the last blocks' slices may be short).
-    const int64_t n = u0 >= nvec ? 0 : (nvec - u0 < slice ? nvec - u0 : slice);
+    // EVEN: every slice is exactly NT * (KV + KS) vectors (no guard needed).
+    const int64_t n = EVEN ? (int64_t)NT * (KV + KS)
+                           : (u0 >= nvec ? 0 : (nvec - u0 < slice ? nvec - u0 : slice));
     const int npairs = csize * NW;
     const bool send = !(flags & kFlagNoCopy);
     const uint32_t stage = smem_addr(stage_buf) + 16u * (uint32_t)tid;
@@ -666,8 +668,10 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     const bool aligned = rows_vector_aligned(p.in, p.out, p.N, p.ld_in, p.ld_out, p.dtype);
     if (sh.staged) {
         if (!aligned) return cudaErrorInvalidValue;
-        auto kern = wide_staged_kernel<T>;
         const int c = sh.csize;
+        const bool even = sh.slice == (int64_t)kWideThreads * (kStagedKV + kStagedKS) &&
+                          nvec == sh.slice * c;
+        auto kern = even ? wide_staged_kernel<T, true> : wide_staged_kernel<T, false>;
         const size_t smem = (size_t)kWideThreads * kStagedKS * 16;
         const void* fn = reinterpret_cast<const void*>(kern);
         cudaError_t e = ensure_smem_limit(fn, smem, c > 8);
