@@ -100,9 +100,9 @@ enum sr_status {
  *   WIDE    one thread-block cluster per row, each block holding a slice of
  *           the row in registers, warp (max, sum) pairs merged across the
  *           cluster, the exponential recomputed for the output; rows up to
- *           512 KiB, and aligned rows up to 1 MiB with half of each slice
- *           in shared memory. Wider aligned rows are streamed: each block
- *           reads its slice twice, the second time mostly from L2.
+ *           512 KiB, and aligned rows of exactly 1 MiB with half of each
+ *           slice in shared memory. Other wider aligned rows are streamed:
+ *           each block reads its slice twice, the second time mostly from L2.
  * All plans but ROW and WIDE run a persistent grid sized to the device's SM
  * count.
  */
@@ -405,8 +405,8 @@ SR_API const char* softmax_rows_strerror(int status);
  * the dtype, rows aligned or sharing their offset from a 16-byte boundary)
  * on a device with sm_count SMs: blocks per cluster (`csize`), 16-byte
  * vectors per block (`slice`), vectors each thread holds (`kv`; 0 for
- * streamed rows; 16 for aligned rows over 512 KiB and up to 1 MiB, of which
- * up to 8 are held in shared memory), and whether the rows are streamed
+ * streamed rows; 16 for aligned rows of exactly 1 MiB, of which 8 are held
+ * in shared memory), and whether the rows are streamed
  * (`streamed`: each block reads its slice twice instead of holding it).
  * Any output pointer may be
  * NULL. Returns 0, or -SR_EDTYPE / -SR_EINVAL for a bad dtype or M < 0,

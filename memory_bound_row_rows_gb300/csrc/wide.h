@@ -10,9 +10,9 @@ namespace sr {
 
 // WIDE plan: clusters of `csize` blocks, `slice` 16-byte vectors per block,
 // `kv` vectors per thread. SR_WIDE_KV: the most vectors a thread holds in
-// registers. Aligned rows too wide for the registers of a 16-block cluster
-// but at most twice that are `staged`: each thread holds 8 vectors in
-// registers and up to 8 more in shared memory (kv = 16). Wider aligned rows
+// registers. Aligned rows of exactly twice what the registers of a 16-block
+// cluster hold (1 MiB) are `staged`: each thread holds 8 vectors in
+// registers and 8 more in shared memory (kv = 16). Other wider aligned rows
 // are `streamed`: each block reads its slice twice (the second time mostly
 // from L2) instead of holding it.
 #ifndef SR_WIDE_KV

@@ -42,11 +42,14 @@ namespace {
 #define SR_WIDE_MIN_BLOCKS 4
 #endif
 
-// 1: aligned rows over 512 KiB and up to 1 MiB run the staged variant (up to
-// half of each slice in shared memory; wide_staged_kernel) instead of being
-// streamed: bf16 128 x 524288 48.5 against 56.6 µs on GB300 (cold L2). On
-// rows the registers hold it gained nothing (within 1 %), so it is not used
-// there.
+// 1: aligned rows of exactly 1 MiB (65536 vectors) run the staged variant
+// (half of each slice in shared memory; wide_staged_kernel) instead of being
+// streamed. Measured on GB300 (cold L2), µs, staged against streamed: bf16
+// 128 x 524288 48.3 / 56.7, 256 x 524288 86.0 / 113.7, f32 256 x 262144
+// 85.4 / 115.7, 64 x 262144 28.3 / 31.0. Rows between 512 KiB and 1 MiB,
+// whose slices do not split evenly, were slower staged (bf16 512 x 400008
+// 170.9 / 157.0 streamed), and on rows the registers hold it gained nothing
+// (within 1 %).
 #ifndef SR_WIDE_STAGED
 #define SR_WIDE_STAGED 1
 #endif
@@ -269,14 +272,14 @@ __global__ void __launch_bounds__(kWideThreads, (KV == 5 || KV == 6) ? SR_WIDE_M
     }
 }
 
-// Staged variant for aligned rows too wide for a 16-block cluster's registers
-// (over 512 KiB, up to 1 MiB): each thread holds 8 vectors of its block's
-// slice in registers and up to 8 more in shared memory, brought in by 16-byte
-// cp.async copies that occupy no registers while in flight (each thread reads
-// back only its own slots, so no block barrier is needed). A block holds up to
-// 64 KiB of the row, so such rows stay on chip and are read from DRAM once
-// instead of being streamed twice. Arithmetic, exchange, prefetch and failure
-// path as in wide_rows_kernel (kAligned).
+// Staged variant for aligned 1 MiB rows (16 slices of 4096 vectors), twice
+// what a 16-block cluster's registers hold: each thread holds 8 vectors of its
+// block's slice in registers and 8 more in shared memory, brought in by
+// 16-byte cp.async copies that occupy no registers while in flight (each
+// thread reads back only its own slots, so no block barrier is needed). Such
+// rows stay on chip and are read from DRAM once instead of being streamed
+// twice. Arithmetic, exchange, prefetch and failure path as in
+// wide_rows_kernel (kFull).
 constexpr int kStagedKV = 8;
 constexpr int kStagedKS = 8;
 
@@ -288,7 +291,7 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
 #ifndef SR_WIDE_STAGED_MIN_BLOCKS
 #define SR_WIDE_STAGED_MIN_BLOCKS 3
 #endif
-template <typename T, bool EVEN>
+template <typename T>
 __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
     wide_staged_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                        int64_t ld_in, int64_t ld_out, int csize, int64_t slice,
@@ -308,11 +311,6 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
     const int rank = (int)cluster_ctarank();
     const int64_t nclusters = gridDim.x / csize;
     const int64_t u0 = (int64_t)rank * slice;
-    const int64_t nvec = N / VEC;
-    // Vectors of this block's slice (the last blocks' slices may be short).
-    // EVEN: every slice is exactly NT * (KV + KS) vectors (no guard needed).
-    const int64_t n = EVEN ? (int64_t)NT * (KV + KS)
-                           : (u0 >= nvec ? 0 : (nvec - u0 < slice ? nvec - u0 : slice));
     const int npairs = csize * NW;
     const bool send = !(flags & kFlagNoCopy);
     const uint32_t stage = smem_addr(stage_buf) + 16u * (uint32_t)tid;
@@ -331,28 +329,23 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
         const int p = (int)(it & 1);
         const uint32_t phase = (uint32_t)((it >> 1) & 1);
         const T* rin = in + r * ld_in + u0 * VEC;
-        if (tid == 0 && ahead > 0 && r + ahead < M && n > 0)
-            bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)(n * 16));
-        // Vectors NT*KV + tid + NT*k of the slice (those below n) go to this
-        // thread's staging slots, vectors tid + NT*k to its registers.
+        if (tid == 0 && ahead > 0 && r + ahead < M)
+            bulk_prefetch_l2(in + (r + ahead) * ld_in + u0 * VEC, (uint32_t)(slice * 16));
+        // Vectors NT*KV + tid + NT*k of the slice go to this thread's staging
+        // slots, vectors tid + NT*k to its registers.
 #pragma unroll
         for (int k = 0; k < KS; ++k)
-            if (NT * KV + tid + NT * k < n)
-                cp_async16(stage + 16u * (uint32_t)(NT * k),
-                           rin + (int64_t)(NT * KV + tid + NT * k) * VEC);
+            cp_async16(stage + 16u * (uint32_t)(NT * k), rin + (int64_t)(NT * KV + tid + NT * k) * VEC);
         asm volatile("cp.async.commit_group;" ::: "memory");
         uint4 raw[KV];
 #pragma unroll
-        for (int k = 0; k < KV; ++k)
-            if (tid + NT * k < n) raw[k] = ldg_stream(rin + (int64_t)(tid + NT * k) * VEC);
+        for (int k = 0; k < KV; ++k) raw[k] = ldg_stream(rin + (int64_t)(tid + NT * k) * VEC);
         VecMax<T> vm;
 #pragma unroll
-        for (int k = 0; k < KV; ++k)
-            if (tid + NT * k < n) vm.add(raw[k]);
+        for (int k = 0; k < KV; ++k) vm.add(raw[k]);
         asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
-        for (int k = 0; k < KS; ++k)
-            if (NT * KV + tid + NT * k < n) vm.add(lds128(stage + 16u * (uint32_t)(NT * k)));
+        for (int k = 0; k < KS; ++k) vm.add(lds128(stage + 16u * (uint32_t)(NT * k)));
         const float m_w = warp_max(vm.get());
         const float shift = (m_w == neg_inf()) ? 0.0f : m_w;
         const float shift_l2 = shift * kLog2e;
@@ -367,11 +360,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
             }
         };
 #pragma unroll
-        for (int k = 0; k < KV; ++k)
-            if (tid + NT * k < n) add_exp(raw[k]);
+        for (int k = 0; k < KV; ++k) add_exp(raw[k]);
 #pragma unroll
-        for (int k = 0; k < KS; ++k)
-            if (NT * KV + tid + NT * k < n) add_exp(lds128(stage + 16u * (uint32_t)(NT * k)));
+        for (int k = 0; k < KS; ++k) add_exp(lds128(stage + 16u * (uint32_t)(NT * k)));
         const float s_w = warp_sum(sa + sb);
         if (!started) {
             cluster_wait();
@@ -413,12 +404,9 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STAGED_MIN_BLOCKS)
             stg_stream(rout + idx * VEC, Elem<T>::pack(f));
         };
 #pragma unroll
-        for (int k = 0; k < KV; ++k)
-            if (tid + NT * k < n) put(raw[k], tid + NT * k);
+        for (int k = 0; k < KV; ++k) put(raw[k], tid + NT * k);
 #pragma unroll
-        for (int k = 0; k < KS; ++k)
-            if (NT * KV + tid + NT * k < n)
-                put(lds128(stage + 16u * (uint32_t)(NT * k)), NT * KV + tid + NT * k);
+        for (int k = 0; k < KS; ++k) put(lds128(stage + 16u * (uint32_t)(NT * k)), NT * KV + tid + NT * k);
     }
     if (!started) cluster_wait();
     if (failed) {
@@ -669,9 +657,9 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     if (sh.staged) {
         if (!aligned) return cudaErrorInvalidValue;
         const int c = sh.csize;
-        const bool even = sh.slice == (int64_t)kWideThreads * (kStagedKV + kStagedKS) &&
-                          nvec == sh.slice * c;
-        auto kern = even ? wide_staged_kernel<T, true> : wide_staged_kernel<T, false>;
+        if (sh.slice != (int64_t)kWideThreads * (kStagedKV + kStagedKS) || nvec != sh.slice * c)
+            return cudaErrorInvalidValue;
+        auto kern = wide_staged_kernel<T>;
         const size_t smem = (size_t)kWideThreads * kStagedKS * 16;
         const void* fn = reinterpret_cast<const void*>(kern);
         cudaError_t e = ensure_smem_limit(fn, smem, c > 8);
@@ -716,10 +704,10 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
 // cluster doubles (up to 8: larger clusters are scheduled poorly) as long as
 // each thread keeps at least one vector. The vectors per thread are rounded
 // up to 1, 2, 4 or 8. Rows up to 16 x 256 x 8 vectors (512 KiB) are held in
-// registers; rows up to twice that are staged (16-block clusters, 8 vectors
-// per thread in registers and up to 8 in shared memory); wider rows are
-// streamed by 8-block clusters (16 while the grid would not fill one wave of
-// resident blocks).
+// registers; aligned rows of exactly twice that (1 MiB) are staged (16-block
+// clusters, 8 vectors per thread in registers and 8 in shared memory); other
+// wider rows are streamed by 8-block clusters (16 while the grid would not
+// fill one wave of resident blocks).
 bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
     const int64_t nvec = N * elem_bytes(dtype) / 16;
     for (int c = 2; c <= kMaxCluster; c *= 2) {
@@ -734,8 +722,7 @@ bool wide_shape(int64_t M, int64_t N, int dtype, int sm_count, WideShape* out) {
         out->streamed = false;
         return true;
     }
-    if (SR_WIDE_STAGED &&
-        nvec <= (int64_t)kMaxCluster * kWideThreads * (kStagedKV + kStagedKS)) {
+    if (SR_WIDE_STAGED && nvec == (int64_t)kMaxCluster * kWideThreads * (kStagedKV + kStagedKS)) {
         out->csize = kMaxCluster;
         out->slice = (nvec + kMaxCluster - 1) / kMaxCluster;
         out->kv = kStagedKV + kStagedKS;

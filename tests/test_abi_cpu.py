@@ -287,13 +287,13 @@ def test_wide_shapes(lib):
     assert S(4096, 16392, 1) == {"csize": 2, "kv": 5, "slice": 1025, "streamed": False}
     assert S(2730, 24576, 2) == {"csize": 2, "kv": 6, "slice": 1536, "streamed": False}
     assert S(2048, 16388, 0) == {"csize": 4, "kv": 5, "slice": 1025, "streamed": False}
-    # 512 KiB is the most 16 blocks hold in registers; rows up to twice that
-    # are staged (kv 16: 8 vectors per thread in registers, up to 8 in shared
-    # memory), wider rows are streamed.
+    # 512 KiB is the most 16 blocks hold in registers; rows of exactly 1 MiB
+    # are staged (kv 16: 8 vectors per thread in registers, 8 in shared
+    # memory), other wider rows are streamed.
     assert S(256, 262144, 1) == {"csize": 16, "kv": 8, "slice": 2048, "streamed": False}
-    assert S(128, 262152, 1) == {"csize": 16, "kv": 16, "slice": 2049, "streamed": False}
     assert S(128, 524288, 1) == {"csize": 16, "kv": 16, "slice": 4096, "streamed": False}
     assert S(128, 262144, 0) == {"csize": 16, "kv": 16, "slice": 4096, "streamed": False}
+    assert S(128, 262152, 1) == {"csize": 8, "kv": 0, "slice": 4097, "streamed": True}
     assert S(128, 524296, 1) == {"csize": 8, "kv": 0, "slice": 8193, "streamed": True}
     # Streamed rows too few for a wave of 8-block clusters double to 16.
     assert S(32, 4194304, 0) == {"csize": 16, "kv": 0, "slice": 65536, "streamed": True}

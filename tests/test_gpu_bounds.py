@@ -83,7 +83,7 @@ def test_misaligned_and_special_inside(checked, dtype, N):
 def test_wide_streamed_in_place_guards_inside(checked):
     tp.test_wide_shifted_rows(synth.BF16, 32769, 4)
     tp.test_streamed_wide_rows(synth.BF16, 3, 600008)
-    tp.test_wide_staged_rows(synth.BF16, 33, 400008, 16)
+    tp.test_wide_staged_rows(synth.F16, 3, 524288, 16)
     tp.test_wide_staged_in_place()
     tp.test_in_place("bf16_16384x1000_ld1024")
     tp.test_guard_regions_untouched()

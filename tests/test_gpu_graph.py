@@ -141,3 +141,22 @@ def test_host_pipeline_in_a_graph():
     g.replay()
     torch.cuda.synchronize()
     gu.check_rows(y_pin.numpy(), x, w.N, w.ld_in, w.dtype, "host pipeline in a graph")
+
+
+def test_staged_rows_in_a_graph():
+    """The staged WIDE kernel (1 MiB rows, half of each slice in shared memory), captured."""
+    M, N, dtype = 4, 524288, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=36, p1=2.0)
+    xd = gu.to_device(x, dtype)
+    y = torch.empty((M, N), dtype=gu.torch_dtype(dtype), device="cuda")
+    sr.softmax_rows(xd, y, M, N, N, N, dtype)
+    torch.cuda.synchronize()
+    assert "wide_staged_kernel" in sr.softmax_rows_last_launch()["name"]
+    y.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        sr.softmax_rows(xd, y, M, N, N, N, dtype)
+    g.replay()
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "staged WIDE in a graph")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
