@@ -500,7 +500,8 @@ def max_over_ranks(value: float, device="cpu") -> float:
 
 def replica_throughput(fused_bytes: int, steps: int, world: int, slowest_total_s: float) -> float:
     """Whole-job GB/s when every rank runs the full workload (weak scaling):
-    all ranks' bytes over the slowest rank's time."""
+    all ranks' bytes over the slowest rank's time (for `steps` steps; the bench
+    passes one step and the slowest rank's median step time)."""
     return world * fused_bytes * steps / slowest_total_s / 1e9
 
 
@@ -534,7 +535,7 @@ def timed_copy(args, launch_copy, n_sets, stream, rank, local_rank, world, nbyte
                                                   local_rank, world)
     st = batch_stats(batch_ms, bounds)
     med_s = max_over_ranks(st["median_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
-    return round(world * nbytes / med_s / 1e9, 2), st
+    return round(replica_throughput(nbytes, 1, world, med_s), 2), st
 
 
 def copy_baseline(args, launch_rows, launch_torch, n_sets, stream, rank, local_rank, world,
@@ -660,7 +661,7 @@ def bench_ours(args, w):
     if rank != 0:
         return None
     steps = bounds[-1][1]
-    value = world * nbytes / med_s / 1e9
+    value = replica_throughput(nbytes, 1, world, med_s)  # the slowest rank's median step
     peaks = measured_peaks()
     src_hash = _build.source_hash(_build.PLAN_SOURCES.get(plan_used.replace("masked-", "")))
     traffic, rec = recorded_traffic(w.name, plan_used)
@@ -682,7 +683,7 @@ def bench_ours(args, w):
         "plan": plan_used,
         "statistic": "ms_per_step and value use the median step (over batches of consecutive "
                      "launches); mean_step_us is the mean over all timed steps",
-        "mean_step_gbs": round(world * nbytes / mean_s / 1e9, 2),
+        "mean_step_gbs": round(replica_throughput(nbytes, 1, world, mean_s), 2),
         "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "rows_per_s": round(world * w.M / med_s, 1),
@@ -957,7 +958,7 @@ def bench_pair(args, lane):
     if rank != 0:
         return None
     steps = bounds[-1][1]
-    value = world * w.fused_bytes / med_s / 1e9
+    value = replica_throughput(w.fused_bytes, 1, world, med_s)  # the slowest rank's median step
     achieved = w.fused_bytes / (stats["median_step_us"] / 1e6) / 1e9
     peaks = measured_peaks()
     traffic, rec = recorded_traffic("%s:%s" % (lane.api, w.name), lane.api)
@@ -971,7 +972,7 @@ def bench_pair(args, lane):
         "plan": pname,
         "statistic": "ms_per_step and value use the median step (over batches of consecutive "
                      "launches); mean_step_us is the mean over all timed steps",
-        "mean_step_gbs": round(world * w.fused_bytes / mean_s / 1e9, 2),
+        "mean_step_gbs": round(replica_throughput(w.fused_bytes, 1, world, mean_s), 2),
         "pct_of_8000_gbs": round(100 * value / world / NOMINAL_HBM_GBS, 2),
         "pct_of_measured_hbm": round(100 * value / world / peaks["hbm_gbs"], 2),
         "bytes_per_step": w.fused_bytes,
