@@ -248,32 +248,73 @@ SR_API int softmax_rows_masked(const void* in, void* out, int64_t M, int64_t N, 
                                int64_t causal_period, int plan, sr_stream_t stream);
 
 /*
- * The split plan for few, wide rows ("Measured optimization case studies",
- * Wide rows: split across programs when there are fewer rows than SMs).
- * Every row is cut into chunks handled by separate thread blocks; a first
- * kernel writes each chunk's online (max, sum) pair into `workspace`, a second
- * kernel has every chunk merge its row's pairs (with the all -inf guard) and
- * write exp(x - M) / S for its chunk, rereading the input. Same arguments and
- * layout rules as softmax_rows, plus a caller-owned DEVICE workspace of at
- * least softmax_rows_split_workspace_bytes(...) bytes, 16-byte aligned, whose
- * contents on entry do not matter. In-place use (in == out) is rejected
- * (SR_EINVAL): the second kernel rereads the input. Calls that share a
- * workspace must not overlap on the GPU. Returns like softmax_rows, or
- * SR_EINVAL for a missing, misaligned or too small workspace.
+ * The split plan for wide rows ("Measured optimization case studies", Wide
+ * rows: a row split across programs, each reducing its chunk to an online
+ * (max, sum) pair, the pairs merged with the guard for all -inf chunks).
+ * One cooperative kernel: its blocks form groups, each group takes one row
+ * at a time, each block of a group always the same part of the row; a block
+ * reduces its part and stores the pair, tagged with the step, in `workspace`;
+ * two rows later it waits, bounded, for the tagged pairs of the rest of the
+ * group, merges them into the row's (M, S) and reads its part again, from
+ * L2, to write exp(x - M) / S. A row may span any number of SMs, so rows
+ * wider than a thread-block cluster holds are read from DRAM once. Before the
+ * kernel the call zeroes the slots it uses (one cudaMemsetAsync on
+ * `stream`).
+ * Same arguments and layout rules as softmax_rows, plus a caller-owned
+ * DEVICE workspace of at least softmax_rows_split_workspace_bytes(...) bytes
+ * (a fixed size), 16-byte aligned, whose contents on entry do not matter.
+ * In-place use (in == out) is rejected (SR_EINVAL): the second pass rereads
+ * the input. Calls that share a workspace must not overlap on the GPU.
+ * Returns like softmax_rows, or SR_EINVAL for a missing, misaligned or too
+ * small workspace; an expired wait is reported by
+ * softmax_rows_last_device_error (SR_EDEVICE_TIMEOUT).
  */
 SR_API int softmax_rows_split(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                               int64_t ld_out, int dtype, void* workspace, int64_t workspace_bytes,
                               sr_stream_t stream);
 
 /*
- * Workspace bytes softmax_rows_split needs for these arguments (M * chunks
- * pairs of floats; the chunking depends only on the arguments, not on the
- * device), or a negative sr_status. Pure host logic; pointers are read only
- * for alignment.
+ * Workspace bytes softmax_rows_split needs: 262144 for every valid problem (a
+ * ring of four steps of tagged (max, sum) pairs, 16 bytes each, for up to 4096
+ * blocks), or a negative sr_status for invalid arguments. Pure host logic;
+ * pointers are read only for alignment.
  */
 SR_API int64_t softmax_rows_split_workspace_bytes(const void* in, const void* out, int64_t M,
                                                   int64_t N, int64_t ld_in, int64_t ld_out,
                                                   int dtype);
+
+/* How softmax_rows_split cuts a problem (softmax_rows_split_shape). */
+typedef struct sr_split_shape {
+    int lanes;          /* groups of blocks, each taking one row at a time */
+    int parts;          /* blocks per group = parts per row */
+    int64_t part_units; /* units per part (the last part may be shorter) */
+    int unit_elems;     /* elements per unit: 16 / element size for 16-byte
+                           aligned rows, else 1 */
+} sr_split_shape;
+
+/*
+ * Host query: the groups and parts softmax_rows_split would use. max_blocks:
+ * how many blocks of its kernel the device holds at once; l2_bytes: the
+ * device's L2 size. Either <= 0 reads it from the current device (the only
+ * case that touches CUDA). Groups: as many as rows and blocks allow while
+ * three rows per group fit in half the L2; parts: the blocks left per group,
+ * none shorter than 256 units. Returns SR_OK and fills *shape, or an
+ * sr_status (SR_EINVAL also for a null shape).
+ */
+SR_API int softmax_rows_split_shape(const void* in, const void* out, int64_t M, int64_t N,
+                                    int64_t ld_in, int64_t ld_out, int dtype, int max_blocks,
+                                    int64_t l2_bytes, sr_split_shape* shape);
+
+/*
+ * Test hook: softmax_rows_split with no block counting itself in, so that
+ * every wait expires after `timeout_ns`; the call must then leave the output
+ * unwritten and softmax_rows_last_device_error must report
+ * SR_EDEVICE_TIMEOUT, with the context still usable.
+ */
+SR_API int softmax_rows_split_test_expiry(const void* in, void* out, int64_t M, int64_t N,
+                                          int64_t ld_in, int64_t ld_out, int dtype,
+                                          void* workspace, int64_t workspace_bytes,
+                                          uint64_t timeout_ns, sr_stream_t stream);
 
 /*
  * The split plan without a caller workspace, for callers that cannot
@@ -285,17 +326,15 @@ SR_API int64_t softmax_rows_split_workspace_bytes(const void* in, const void* ou
  * changes where the split plan keeps its statistics.
  *
  * Same arguments, results and layout rules as softmax_rows_split, without
- * the workspace: the statistics live in a 512 KiB array built into the
- * library's device image (every GPU that loads the library holds it until
- * the process exits). This call allocates nothing and calls no allocating
- * routine. Limit: softmax_rows_split_workspace_bytes(...) for the same
- * arguments must be at most 524288 (65536 pairs, i.e. M * chunks); larger
- * problems are rejected with SR_EINVAL, launching nothing. The first call
- * on a device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.
- * Every call on a device shares the one array and leaves its statistics in
- * it; nothing in it needs to start at zero. Calls whose kernels overlap on
- * the GPU (other streams, other host threads) race on the array: order them.
+ * the workspace: the split plan's workspace (its fixed size, every problem
+ * fits) lives in an array built into the library's device image (every GPU
+ * that loads the library holds it until the process exits). This call
+ * allocates nothing and calls no allocating routine. The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * Every call on a device shares the one array; nothing in it needs to start
+ * at zero. Calls whose kernels overlap on the GPU (other streams, other host
+ * threads) race on the array: order them.
  */
 SR_API int softmax_rows_split_noalloc(const void* in, void* out, int64_t M, int64_t N,
                                       int64_t ld_in, int64_t ld_out, int dtype,
@@ -419,8 +458,7 @@ SR_API int softmax_rows_wide_shape(int64_t M, int64_t N, int dtype, int sm_count
  * What the calling host thread's last kernel launch through this library
  * looked like, for result records and profiles (the pages tie kernel speed to
  * register pressure: "Measured optimization case studies", Specialize). It
- * describes the last kernel any entry point launched from this thread: for
- * softmax_rows_split, the second of its two kernels. Fields:
+ * describes the last kernel any entry point launched from this thread. Fields:
  *   registers            registers per thread of the kernel as compiled
  *   local_bytes          local memory per thread (register spills and stack)
  *   static_smem_bytes    statically declared shared memory per block

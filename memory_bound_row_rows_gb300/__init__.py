@@ -20,6 +20,7 @@ __all__ = [
     "softmax_rows_last_device_error", "softmax_rows_test_expiry", "softmax_rows_strerror",
     "softmax_rows_version", "softmax_rows_host", "softmax_rows_host_workspace_bytes",
     "softmax_rows_split", "softmax_rows_split_workspace_bytes", "softmax_rows_split_noalloc",
+    "softmax_rows_split_shape", "softmax_rows_split_test_expiry",
     "softmax_rows_host_mapped",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
     "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
@@ -85,6 +86,8 @@ def open_library(path: str):
         "softmax_rows_split": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, vp],
         "softmax_rows_split_workspace_bytes": [vp, vp, i64, i64, i64, i64, c_int],
         "softmax_rows_split_noalloc": [vp, vp, i64, i64, i64, i64, c_int, vp],
+        "softmax_rows_split_shape": [vp, vp, i64, i64, i64, i64, c_int, c_int, i64, vp],
+        "softmax_rows_split_test_expiry": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, u64, vp],
         "softmax_rows_masked": [vp, vp, i64, i64, i64, i64, c_int, vp, i64, c_int, vp],
         "softmax_rows_backward": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, vp],
         "softmax_rows_backward_ex": [vp, vp, vp, i64, i64, i64, i64, i64, c_int, c_int, vp],
@@ -262,9 +265,34 @@ def rmsnorm_residual_rows_plan(x, residual, weight, y, M, N, ld_x, ld_r, ld_y, e
                                                  sm_count))
 
 
+class _SplitShape(ctypes.Structure):
+    _fields_ = [("lanes", ctypes.c_int), ("parts", ctypes.c_int),
+                ("part_units", ctypes.c_int64), ("unit_elems", ctypes.c_int)]
+
+
+def softmax_rows_split_shape(in_, out, M, N, ld_in, ld_out, dtype, max_blocks=0,
+                             l2_bytes=0) -> dict:
+    """How the split plan cuts a problem (host logic when max_blocks and l2_bytes
+    are given): {"lanes", "parts", "part_units", "unit_elems"}; raises on bad
+    arguments."""
+    sh = _SplitShape()
+    _check(load().softmax_rows_split_shape(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
+                                           max_blocks, l2_bytes, ctypes.byref(sh)),
+           "softmax_rows_split_shape")
+    return {"lanes": sh.lanes, "parts": sh.parts, "part_units": sh.part_units,
+            "unit_elems": sh.unit_elems}
+
+
+def softmax_rows_split_test_expiry(in_, out, M, N, ld_in, ld_out, dtype, workspace,
+                                   workspace_bytes, timeout_ns, stream=None) -> int:
+    return int(load().softmax_rows_split_test_expiry(_ptr(in_), _ptr(out), M, N, ld_in, ld_out,
+                                                     dtype, _ptr(workspace), workspace_bytes,
+                                                     timeout_ns, _stream(stream)))
+
+
 def softmax_rows_split(in_, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,
                        stream=None) -> int:
-    """Split plan for few, wide rows; `workspace` is a device buffer."""
+    """Split plan for wide rows (one cooperative kernel); `workspace` is a device buffer."""
     return _check(load().softmax_rows_split(_ptr(in_), _ptr(out), M, N, ld_in, ld_out, dtype,
                                             _ptr(workspace), workspace_bytes, _stream(stream)),
                   "softmax_rows_split")

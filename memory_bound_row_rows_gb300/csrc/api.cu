@@ -8,6 +8,7 @@
 #include "rowpair.h"
 #include "wide.h"
 #include "internal.h"
+#include "split.h"
 
 namespace sr {
 
@@ -473,27 +474,83 @@ int64_t softmax_rows_split_workspace_bytes(const void* in, const void* out, int6
                                            int64_t ld_in, int64_t ld_out, int dtype) {
     const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
     if (bad) return -bad;
-    const sr::SplitShape sh = sr::split_shape(M, N, ld_in, ld_out, dtype, in, out);
-    return M * sh.chunks * (int64_t)sizeof(float2);
+    return sr::kSplitWorkspaceBytes;
 }
+
+namespace sr {
+namespace {
+
+// Blocks of the SPLIT kernel the current device holds at once.
+int split_max_blocks(const DeviceInfo* dev, int dtype, int vec) {
+    const int per_sm = blocks_per_sm(split_kernel(dtype, vec), kSplitThreadsPerBlock, 0);
+    if (per_sm <= 0) return -1;
+    const int64_t n = (int64_t)per_sm * dev->sm_count;
+    return n > kSplitMaxBlocks ? kSplitMaxBlocks : (int)n;
+}
+
+int run_split(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
+              int dtype, void* workspace, int64_t workspace_bytes, cudaStream_t stream,
+              unsigned long long timeout_ns, int flags) {
+    const int bad = check_args(in, out, M, N, ld_in, ld_out, dtype);
+    if (bad) return bad;
+    if (M == 0) return SR_OK;
+    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 16 != 0 ||
+        workspace_bytes < kSplitWorkspaceBytes)
+        return SR_EINVAL;
+    if (in == out) return SR_EINVAL;  // the second pass rereads the input
+    cudaError_t e;
+    const DeviceInfo* dev = device_info(&e);
+    if (!dev) return SR_ECUDA;
+    const bool vec = rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
+    const int max_blocks = split_max_blocks(dev, dtype, vec ? 2 : 1);
+    if (max_blocks <= 0) return SR_ECUDA;
+    const SplitShape sh = split_shape(M, N, ld_in, ld_out, dtype, in, out, max_blocks,
+                                      dev->l2_bytes);
+    Problem p{in, out, M, N, ld_in, ld_out, dtype, stream, dev, timeout_ns, flags};
+    return launch_split(p, sh, workspace) == cudaSuccess ? SR_OK : SR_ECUDA;
+}
+
+}  // namespace
+}  // namespace sr
 
 int softmax_rows_split(const void* in, void* out, int64_t M, int64_t N, int64_t ld_in,
                        int64_t ld_out, int dtype, void* workspace, int64_t workspace_bytes,
                        sr_stream_t stream) {
+    return sr::run_split(in, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,
+                         (cudaStream_t)stream, sr::kDefaultTimeoutNs, 0);
+}
+
+int softmax_rows_split_test_expiry(const void* in, void* out, int64_t M, int64_t N,
+                                   int64_t ld_in, int64_t ld_out, int dtype, void* workspace,
+                                   int64_t workspace_bytes, uint64_t timeout_ns,
+                                   sr_stream_t stream) {
+    return sr::run_split(in, out, M, N, ld_in, ld_out, dtype, workspace, workspace_bytes,
+                         (cudaStream_t)stream, (unsigned long long)timeout_ns,
+                         sr::kFlagNoArrive);
+}
+
+int softmax_rows_split_shape(const void* in, const void* out, int64_t M, int64_t N,
+                             int64_t ld_in, int64_t ld_out, int dtype, int max_blocks,
+                             int64_t l2_bytes, sr_split_shape* shape) {
     const int bad = sr::check_args(in, out, M, N, ld_in, ld_out, dtype);
     if (bad) return bad;
-    if (M == 0) return SR_OK;
-    const sr::SplitShape sh = sr::split_shape(M, N, ld_in, ld_out, dtype, in, out);
-    if (workspace == nullptr || reinterpret_cast<uintptr_t>(workspace) % 16 != 0 ||
-        workspace_bytes < M * sh.chunks * (int64_t)sizeof(float2))
-        return SR_EINVAL;
-    if (in == out) return SR_EINVAL;  // the second pass rereads the input
-    cudaError_t e;
-    const sr::DeviceInfo* dev = sr::device_info(&e);
-    if (!dev) return SR_ECUDA;
-    sr::Problem p{in, out, M, N, ld_in, ld_out, dtype, (cudaStream_t)stream, dev,
-                  sr::kDefaultTimeoutNs, 0};
-    return sr::launch_split(p, sh, workspace) == cudaSuccess ? SR_OK : SR_ECUDA;
+    if (shape == nullptr) return SR_EINVAL;
+    if (max_blocks <= 0 || l2_bytes <= 0) {
+        cudaError_t e;
+        const sr::DeviceInfo* dev = sr::device_info(&e);
+        if (!dev) return SR_ECUDA;
+        const bool vec = sr::rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
+        if (max_blocks <= 0) max_blocks = sr::split_max_blocks(dev, dtype, vec ? 2 : 1);
+        if (max_blocks <= 0) return SR_ECUDA;
+        if (l2_bytes <= 0) l2_bytes = dev->l2_bytes;
+    }
+    const sr::SplitShape sh =
+        sr::split_shape(M, N, ld_in, ld_out, dtype, in, out, max_blocks, l2_bytes);
+    shape->lanes = sh.lanes;
+    shape->parts = sh.parts;
+    shape->part_units = sh.part_units;
+    shape->unit_elems = sh.vec;
+    return SR_OK;
 }
 
 int64_t softmax_rows_host_workspace_bytes(int64_t M, int64_t N, int dtype) {
@@ -695,6 +752,6 @@ int softmax_rows_test_bounds_shrink(int64_t bytes) {
 #endif
 }
 
-int softmax_rows_version(void) { return 200; }
+int softmax_rows_version(void) { return 210; }
 
 }  // extern "C"

@@ -10,8 +10,10 @@ namespace sr {
 
 enum : int { kF32 = 0, kBF16 = 1, kF16 = 2 };
 
-// Debug flag for the bounded-wait test hook: issue no bulk copies.
+// Debug flags for the bounded-wait test hooks: issue no bulk copies; (SPLIT
+// plan, split.h) count no block in.
 constexpr int kFlagNoCopy = 1;
+constexpr int kFlagNoArrive = 2;
 
 // Rows up to this many elements run one warp per row (64 values per lane).
 constexpr int64_t kWarpMaxN = 2048;
@@ -112,12 +114,16 @@ inline void note_launch(F* func, dim3 grid, dim3 block, size_t smem = 0, int clu
 // a kernel that uses no cluster features; a kernel that does (cluster
 // barriers, distributed shared memory, st.async) passes its cluster size,
 // 1 included, and is always launched with that cluster dimension.
+// `cooperative`: every block of the grid must be resident at once (its
+// blocks wait on one another); the launch fails instead of starting a grid
+// the device cannot hold.
 struct LaunchShape {
     dim3 grid;
     dim3 block;
     size_t smem = 0;
     int cluster = 0;
     int policy = -1;
+    bool cooperative = false;
 };
 
 // Every kernel of the library is launched here. With SR_PDL the launch allows
@@ -126,7 +132,8 @@ struct LaunchShape {
 // statement of every kernel) waits for that kernel to complete and its
 // memory to be visible before any global access of its own, so stream order
 // holds exactly as without it; only the launch and the block dispatch
-// overlap the previous kernel's tail.
+// overlap the previous kernel's tail. A cooperative launch goes without it:
+// it starts once the previous kernel has completed.
 template <typename... P, typename... A>
 cudaError_t launch_kernel(void (*kern)(P...), const LaunchShape& ls, cudaStream_t stream,
                           A&&... args) {
@@ -149,7 +156,11 @@ cudaError_t launch_kernel(void (*kern)(P...), const LaunchShape& ls, cudaStream_
         attr[n].val.clusterSchedulingPolicyPreference = (cudaClusterSchedulingPolicy)ls.policy;
         ++n;
     }
-    if (SR_PDL) {
+    if (ls.cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    } else if (SR_PDL) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
@@ -180,20 +191,6 @@ cudaError_t launch_copy_rows(const void* in, void* out, int64_t M, int64_t row_b
 bool row_plan_fits(int64_t N, int dtype);
 int64_t host_workspace_bytes(int64_t M, int64_t N, int dtype);
 
-// SPLIT plan: chunks per row and chunk length (in 16-byte vectors when vec > 1,
-// else in elements); the workspace holds M * chunks (max, sum) pairs.
-constexpr int64_t kSplitTargetBlocks = 640;
-constexpr int64_t kSplitMinUnits = 256;
-constexpr int64_t kSplitMaxChunks = 4096;
-constexpr int64_t kSplitMaxGridRows = 65535;
-struct SplitShape {
-    int64_t chunks = 1;
-    int64_t chunk_units = 1;
-    int vec = 1;
-};
-SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int dtype,
-                       const void* in, const void* out);
-cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws);
 int run_host(const void* h_in, void* h_out, int64_t M, int64_t N, int64_t ld_in, int64_t ld_out,
              int dtype, void* d_work, int64_t work_bytes, cudaStream_t stream,
              int (*launch)(const void*, void*, int64_t, int64_t, int64_t, int64_t, int,

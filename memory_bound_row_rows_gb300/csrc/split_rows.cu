@@ -1,44 +1,144 @@
-// SPLIT plan: rows cut into chunks across many blocks, statistics through a
-// workspace, two launches.
+// SPLIT plan: every row cut into parts held by different thread blocks of one
+// grid whose blocks are all resident together (a cooperative launch); the
+// parts' statistics meet in a small caller-owned workspace. One launch.
 //
 // The split plan of "Measured optimization case studies" (Wide rows): when
-// there are fewer rows than SMs, one program per row cannot fill the GPU, so
-// every row is split into chunks; the first kernel writes each chunk's
-// statistics, and in the second every chunk merges its row's statistics
-// itself and writes its part of the output. The statistics are online
-// (max, sum) pairs merged with the same section's rule and its guard for
-// chunks that are entirely -inf.
+// one program cannot take a whole row, the row is split across programs,
+// each reduces its chunk to an online (max, sum) pair, and the pairs are
+// merged with the same section's rule and its guard for chunks that are
+// entirely -inf. Here a row may span any number of SMs, beyond the 16 blocks
+// of a thread-block cluster, because the pairs travel through global memory.
 //
-// stats_kernel: block (row r, chunk c) reduces its chunk to (m, s) with
-//   s = sum exp(x - m) and stores it at ws[r * C + c].
-// apply_kernel: block (row r, chunk c) merges ws[r * C .. r * C + C) into
-//   the row's (M, S), rereads its chunk (from L2 for the few-row shapes this
-//   plan is for) and writes exp(x - M) / S.
-// The grid is (C, M): block x = chunk, y = row. Chunks are whole 16-byte
-// vectors when rows are 16-byte aligned (VEC = 16 / sizeof(T)), else
-// elements (VEC = 1).
+// Schedule. The B = lanes x parts blocks form `lanes` groups of `parts`
+// blocks; group g takes rows g, g + lanes, g + 2 lanes, ... in turn (its
+// steps), block p of the group always the same part of the row. For step t a
+// block
+//   1. reads its part and reduces it to a pair (pass 1, loads marked to stay
+//      in L2);
+//   2. stores the pair, tagged with the step, in the workspace;
+//   3. kLag steps later, merges the group's tagged pairs of step t (waiting,
+//      bounded, for any not there yet) into the row's (M, S), and reads its
+//      part again to write exp(x - M) / S (pass 2, loads marked for early
+//      eviction).
+// Pass 1 of step t + kLag and pass 2 of step t run in one sweep over the
+// part, each step of the sweep issuing both rows' loads first, so that DRAM
+// reads and writes overlap; kLag - 1 sweeps lie between storing a pair and
+// needing the group's, which hides the exchange. The pass-2 read comes from
+// L2: a group reads kLag more rows between a part's two reads, and the host
+// picks `lanes` so that kLag + 1 rows per group fit in half of the L2. DRAM
+// then sees each element read once and written once, whatever the row width.
+//
+// Workspace: slots[kRing][B], 16 bytes each; slot (t mod kRing, block) holds
+// the block's pair of step t as two 8-byte words (max bits, t + 1) and (sum
+// bits, t + 1), each stored and loaded as one relaxed 64-bit access, so a
+// reader that finds its tag in both words holds that step's pair: no fence,
+// no counter. The host zeroes the slots before the launch (tags start at 1).
+// A block stores its pair for step t only after it has merged the pairs of
+// step t - kLag, which every block of its group stored only after it had
+// merged those of step t - 2 kLag: with kRing = 2 kLag slots no pair is
+// overwritten while it may still be read.
+//
+// Failure: a wait that expires sets the timeout bit of the error word; the
+// block's threads leave together after the next barrier, writing nothing
+// more, and the other blocks of the group then expire in turn. No block waits
+// on shared memory of another block.
 #include <mutex>
+#include <type_traits>
 
 #include "../../include/softmax_rows.h"
 #include "device.cuh"
 #include "internal.h"
+#include "l2prefetch.cuh"
+#include "split.h"
 
 namespace sr {
+
+static_assert(kSplitLag != 2 || kSplitWorkspaceBytes == 262144, "the header documents this size");
+
 namespace {
 
-constexpr int kSplitThreads = 256;
+constexpr int kSplitThreads = kSplitThreadsPerBlock;
 constexpr int kSplitNW = kSplitThreads / 32;
+constexpr int kRing = kSplitRing;
+constexpr int kLag = kSplitLag;  // pass 2 of step t runs kLag steps after its pass 1
 
-template <typename T, int VEC>
-__device__ __forceinline__ void load_vec(const T* p, float* f) {
-    if constexpr (VEC == 1) {
-        f[0] = Elem<T>::load1(p);
+// Units per thread and row in one step of a sweep (loads in flight).
+#ifndef SR_SPLIT_UNROLL
+#define SR_SPLIT_UNROLL 4
+#endif
+constexpr int kSplitUnroll = SR_SPLIT_UNROLL;
+
+// Steps ahead that a block has the bulk-copy engine prefetch its part of a
+// row into L2 (aligned rows; 0: none).
+#ifndef SR_SPLIT_AHEAD
+#define SR_SPLIT_AHEAD 1
+#endif
+
+// Resident blocks per SM the kernel is compiled for (bounds its registers).
+// Measured on GB300 (cold L2, µs, 2 / 3 / 4 blocks per SM with 4 / 4 / 2
+// units per step): f32 32 x 4194304 272 / 327 / 300, bf16 128 x 524288
+// 83 / 86 / 85, bf16 512 x 400008 251 / 249 / 236, f16 64 x 131072
+// 38 / 46 / 48; 2 blocks per SM with 8 units per step 367 / 101 / 332 / 50.
+#ifndef SR_SPLIT_MIN_BLOCKS
+#define SR_SPLIT_MIN_BLOCKS 2
+#endif
+
+__device__ __forceinline__ uint64_t l2_keep() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ uint64_t l2_drop() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// Loads through the read-only path with an L2 cache policy: one 16-byte
+// vector, or one element.
+__device__ __forceinline__ uint4 ld_vec(const void* p, uint64_t pol) {
+    if (!SR_READ_OK(p, 16)) return make_uint4(0x7fc00000u, 0x7fc00000u, 0x7fc00000u, 0x7fc00000u);
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p), "l"(pol));
+    return v;
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_one(const T* p, uint64_t pol) {
+    if (!SR_READ_OK(p, sizeof(T))) return __int_as_float(0x7fc00000);
+    if constexpr (sizeof(T) == 4) {
+        float v;
+        asm("ld.global.nc.L1::no_allocate.L2::cache_hint.f32 %0, [%1], %2;"
+            : "=f"(v)
+            : "l"(p), "l"(pol));
+        return v;
     } else {
-        Elem<T>::unpack(ldg_stream(p), f);
+        unsigned short h;
+        asm("ld.global.nc.L1::no_allocate.L2::cache_hint.b16 %0, [%1], %2;"
+            : "=h"(h)
+            : "l"(p), "l"(pol));
+        if constexpr (std::is_same<T, __half>::value) return __half2float(__ushort_as_half(h));
+        else return __uint_as_float(((uint32_t)h) << 16);
     }
 }
 
-// Block-wide online (max, sum) merge; every thread returns the result.
+// exp(x - m): for FP32 data the hardware ex2 of the FP32 difference times
+// log2(e), for 16-bit data one FMA and ex2 (m_l2 = m * log2(e)), as in the
+// ROW and WIDE plans.
+template <typename T>
+__device__ __forceinline__ float split_exp(float x, float m, float m_l2) {
+    if constexpr (Elem<T>::kAccurateExp) {
+        return ex2_approx((x - m) * kLog2e);
+    } else {
+        return exp_shifted<T>(x, m, m_l2);
+    }
+}
+
+// Block-wide online (max, sum) merge; every thread returns the result. Ends
+// with a barrier, so `red` may be reused at once.
 __device__ __forceinline__ void block_merge(float& m, float& s, float2* red) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -53,138 +153,307 @@ __device__ __forceinline__ void block_merge(float& m, float& s, float2* red) {
     s = red[0].y;
 #pragma unroll
     for (int w = 1; w < kSplitNW; ++w) merge_ms(m, s, red[w].x, red[w].y);
+    __syncthreads();
 }
 
+// The units one thread holds in one step of a sweep: kSplitUnroll 16-byte
+// vectors (VEC > 1, kept packed until used) or elements (VEC == 1).
 template <typename T, int VEC>
-__global__ void __launch_bounds__(kSplitThreads)
-    split_stats_kernel(const T* __restrict__ in, int64_t N, int64_t ld_in, int64_t chunk_units,
-                       float2* __restrict__ ws) {
-    SR_GRID_DEPENDENCY();
-    SR_BOUNDS_BEGIN(SR_MAT_IN(in, (int64_t)gridDim.y, ld_in, N),
-                    SR_SPAN_OUT(ws, (int64_t)gridDim.x * gridDim.y * 8));
-    __shared__ float2 red[kSplitNW];
-    const int64_t r = blockIdx.y, c = blockIdx.x, C = gridDim.x;
-    const int64_t units = N / VEC;  // VEC divides N when VEC > 1
-    const int64_t u0 = c * chunk_units;
-    const int64_t u1 = (u0 + chunk_units < units) ? u0 + chunk_units : units;
-    const T* rin = in + r * ld_in;
-    float m = neg_inf(), s = 0.0f;
-    for (int64_t u = u0 + threadIdx.x; u < u1; u += kSplitThreads) {
-        float f[VEC];
-        load_vec<T, VEC>(rin + u * VEC, f);
-        float cm = f[0];
+struct Units {
+    uint4 v[kSplitUnroll];
+    __device__ __forceinline__ void load(const T* p, int left, uint64_t pol) {
 #pragma unroll
-        for (int e = 1; e < VEC; ++e) cm = fmaxf(cm, f[e]);
-        const float mn = fmaxf(m, cm);
-        const float shift = (mn == neg_inf()) ? 0.0f : mn;
-        float cs = 0.0f;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) cs += expf(f[e] - shift);
-        s = s * merge_scale(m, mn) + cs;
-        m = mn;
+        for (int k = 0; k < kSplitUnroll; ++k)
+            if (k < left) v[k] = ld_vec(p + (int64_t)k * kSplitThreads * VEC, pol);
     }
-    block_merge(m, s, red);
-    if (threadIdx.x == 0 && SR_WRITE_OK(ws + r * C + c, 8)) ws[r * C + c] = make_float2(m, s);
-}
+    __device__ __forceinline__ void get(int k, float* f) const { Elem<T>::unpack(v[k], f); }
+};
 
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kSplitThreads)
-    split_apply_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t N, int64_t ld_in,
-                       int64_t ld_out, int64_t chunk_units, const float2* __restrict__ ws) {
-    SR_GRID_DEPENDENCY();
-    SR_BOUNDS_BEGIN(SR_MAT_IN(in, (int64_t)gridDim.y, ld_in, N),
-                    SR_MAT_OUT(out, (int64_t)gridDim.y, ld_out, N),
-                    SR_SPAN_IN(ws, (int64_t)gridDim.x * gridDim.y * 8));
-    __shared__ float2 red[kSplitNW];
-    const int64_t r = blockIdx.y, c = blockIdx.x, C = gridDim.x;
-    // The row's (M, S) from all of its chunks' pairs.
-    float m = neg_inf(), s = 0.0f;
-    for (int64_t k = threadIdx.x; k < C; k += kSplitThreads) {
-        const float2 q = SR_READ_OK(ws + r * C + k, 8) ? ws[r * C + k]
-                                                       : make_float2(__int_as_float(0x7fc00000), 0.0f);
-        merge_ms(m, s, q.x, q.y);
-    }
-    block_merge(m, s, red);
-    const float rs = final_rcp(m, s);
-    const float m_l2 = m * kLog2e;
-
-    const int64_t units = N / VEC;
-    const int64_t u0 = c * chunk_units;
-    const int64_t u1 = (u0 + chunk_units < units) ? u0 + chunk_units : units;
-    const T* rin = in + r * ld_in;
-    T* rout = out + r * ld_out;
-    for (int64_t u = u0 + threadIdx.x; u < u1; u += kSplitThreads) {
-        float f[VEC];
-        load_vec<T, VEC>(rin + u * VEC, f);
+template <typename T>
+struct Units<T, 1> {
+    float v[kSplitUnroll];
+    __device__ __forceinline__ void load(const T* p, int left, uint64_t pol) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) f[e] = exp_shifted<T>(f[e], m, m_l2) * rs;
-        if constexpr (VEC == 1) {
-            Elem<T>::store1(rout + u, f[0]);
-        } else {
-            stg_stream(rout + u * VEC, Elem<T>::pack(f));
+        for (int k = 0; k < kSplitUnroll; ++k)
+            if (k < left) v[k] = ld_one<T>(p + (int64_t)k * kSplitThreads, pol);
+    }
+    __device__ __forceinline__ void get(int k, float* f) const { f[0] = v[k]; }
+};
+
+// One sweep over a block's part in two rows at once: pass 1 of row `a`
+// (STATS: its (m, s), returned in every thread) and pass 2 of row `b`
+// (APPLY: y = exp(x - M) / S written to `bo`). The pointers address this
+// thread's first unit of the part (16-byte vectors when VEC > 1, elements
+// when VEC == 1); its units follow at a stride of kSplitThreads, `n` of them.
+// Each step of the sweep issues both rows' loads before using either; pass 1
+// takes one max over the step's units, one rescale, then the exponentials.
+template <typename T, int VEC, bool STATS, bool APPLY>
+__device__ __forceinline__ float2 sweep(const T* a, const T* b, T* bo, int n, uint64_t keep,
+                                        uint64_t drop, float M, float S, float2* red) {
+    float m = neg_inf(), s = 0.0f;
+    const float rs = final_rcp(M, S);
+    const float m_l2 = M * kLog2e;
+    constexpr int U = kSplitUnroll;
+    constexpr int64_t kStep = (int64_t)U * kSplitThreads * VEC;  // elements per sweep step
+#pragma unroll 1
+    for (int k0 = 0; k0 < n; k0 += U, a += kStep, b += kStep, bo += kStep) {
+        const int left = n - k0;
+        Units<T, VEC> ua, ub;
+        if (STATS) ua.load(a, left, keep);
+        if (APPLY) ub.load(b, left, drop);
+        if (STATS) {
+            float cm = neg_inf();
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (k < left) {
+                    float f[VEC];
+                    ua.get(k, f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) cm = fmaxf(cm, f[e]);
+                }
+            }
+            const float mn = fmaxf(m, cm);
+            const float shift = (mn == neg_inf()) ? 0.0f : mn;
+            const float shift_l2 = shift * kLog2e;
+            float cs = 0.0f;
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (k < left) {
+                    float f[VEC];
+                    ua.get(k, f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) cs += split_exp<T>(f[e], shift, shift_l2);
+                }
+            }
+            s = s * merge_scale(m, mn) + cs;
+            m = mn;
+        }
+        if (APPLY) {
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                if (k < left) {
+                    float f[VEC];
+                    ub.get(k, f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) f[e] = split_exp<T>(f[e], M, m_l2) * rs;
+                    if constexpr (VEC == 1) {
+                        Elem<T>::store1(bo + (int64_t)k * kSplitThreads, f[0]);
+                    } else {
+                        stg_stream(bo + (int64_t)k * kSplitThreads * VEC, Elem<T>::pack(f));
+                    }
+                }
+            }
         }
     }
+    if (STATS) block_merge(m, s, red);
+    return make_float2(m, s);
+}
+
+// A block's (max, sum) for a step, tagged with the step, as two 8-byte words.
+__device__ __forceinline__ void st_tagged(void* p, float m, float s, unsigned int tag) {
+    asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p),
+                 "l"(((unsigned long long)tag << 32) | __float_as_uint(m)),
+                 "l"(((unsigned long long)tag << 32) | __float_as_uint(s))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool ld_tagged(const void* p, unsigned int tag, float& m, float& s) {
+    unsigned long long a, b;
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+    m = __uint_as_float((unsigned int)a);
+    s = __uint_as_float((unsigned int)b);
+    return (unsigned int)(a >> 32) == tag && (unsigned int)(b >> 32) == tag;
+}
+
+// The exchange of one group: slots[kRing][B] of 16 bytes in the workspace.
+struct Exchange {
+    unsigned char* slots;
+    int parts, B, g, b;
+    __device__ Exchange(void* ws, int B_, int parts_, int g_, int b_)
+        : slots(static_cast<unsigned char*>(ws)), parts(parts_), B(B_), g(g_), b(b_) {}
+
+    // Thread 0 stores the block's pair for step t (tag t + 1).
+    __device__ __forceinline__ void publish(int64_t t, float m, float s, int flags_) {
+        if (threadIdx.x != 0 || (flags_ & kFlagNoArrive)) return;
+        unsigned char* slot = slots + ((int64_t)(t % kRing) * B + b) * 16;
+        if (SR_WRITE_OK(slot, 16)) st_tagged(slot, m, s, (unsigned int)(t + 1));
+    }
+
+    // The row's (M, S) of step q from the group's `parts` pairs, each thread
+    // merging (after waiting, bounded, for them) pairs tid, tid + threads, ...;
+    // false in every thread when a wait expired (the timeout bit is then set).
+    // Block-wide.
+    __device__ __forceinline__ bool merge_row(int64_t q, float& M, float& S, float2* red,
+                                              int* s_fail, unsigned int* err,
+                                              unsigned long long timeout_ns) {
+        const unsigned int tag = (unsigned int)(q + 1);
+        const unsigned char* grp = slots + ((int64_t)(q % kRing) * B + (int64_t)g * parts) * 16;
+        float m = neg_inf(), s = 0.0f;
+        bool ok = true;
+        for (int k = threadIdx.x; k < parts && ok; k += kSplitThreads) {
+            const unsigned char* slot = grp + (int64_t)k * 16;
+            if (!SR_READ_OK(slot, 16)) {
+                ok = false;
+                break;
+            }
+            float pm, ps;
+            if (!ld_tagged(slot, tag, pm, ps)) {
+                const uint64_t t0 = global_timer_ns();
+                while (!ld_tagged(slot, tag, pm, ps)) {
+                    if (global_timer_ns() - t0 > timeout_ns) {
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(64);
+                }
+            }
+            if (ok) merge_ms(m, s, pm, ps);
+        }
+        if (!ok) {
+            *s_fail = 1;
+            atomicOr(err, kErrTimeout);
+        }
+        __syncthreads();
+        if (*s_fail) return false;
+        block_merge(m, s, red);
+        M = m;
+        S = s;
+        return true;
+    }
+};
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kSplitThreads, SR_SPLIT_MIN_BLOCKS)
+    split_grid_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                      int64_t ld_in, int64_t ld_out, int lanes, int parts, int64_t part_units,
+                      void* ws, unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
+                    SR_SPAN_OUT(ws, kSplitWorkspaceBytes));
+    __shared__ float2 red[kSplitNW];
+    __shared__ int s_fail;
+    const int tid = threadIdx.x;
+    if (tid == 0) s_fail = 0;
+    const int b_idx = blockIdx.x;
+    const int g = b_idx / parts, p = b_idx - g * parts;
+    Exchange x(ws, (int)gridDim.x, parts, g, b_idx);
+    const int64_t units = N / VEC;  // VEC divides N when VEC > 1
+    const int64_t u0 = (p * part_units < units) ? p * part_units : units;
+    const int64_t u1 = (u0 + part_units < units) ? u0 + part_units : units;
+    const int64_t steps = (M > g) ? (M - g + lanes - 1) / lanes : 0;
+    // This thread's units of the part: u0 + tid + k * threads, k < n.
+    const int n = (u1 - u0 > tid) ? (int)((u1 - u0 - tid + kSplitThreads - 1) / kSplitThreads) : 0;
+    const int64_t first = (u0 + tid) * VEC;  // element offset of the first one in a row
+    const uint64_t keep = l2_keep(), drop = l2_drop();
+
+    // Iteration t: merge step t - kLag's pairs, then one sweep that runs pass 1
+    // of step t and pass 2 of step t - kLag, then store step t's pair.
+#pragma unroll 1
+    for (int64_t t = 0; t < steps + kLag; ++t) {
+        const bool stats = t < steps, apply = t >= kLag;
+        if (VEC > 1 && SR_SPLIT_AHEAD > 0 && tid == 0 && u1 > u0) {
+            for (int64_t k = (t == 0 ? 1 : SR_SPLIT_AHEAD); k <= SR_SPLIT_AHEAD; ++k) {
+                if (t + k < steps)
+                    bulk_prefetch_l2(in + (g + (t + k) * lanes) * ld_in + u0 * VEC,
+                                     (uint32_t)((u1 - u0) * 16));
+            }
+        }
+        if (!stats && !apply) continue;  // a group with fewer rows than kLag (block-uniform)
+        float rm = neg_inf(), rsum = 0.0f;  // the row's (M, S) for pass 2
+        if (apply && !x.merge_row(t - kLag, rm, rsum, red, &s_fail, err, timeout_ns)) return;
+        const T* a = stats ? in + (g + t * lanes) * ld_in + first : nullptr;
+        const T* b = apply ? in + (g + (t - kLag) * lanes) * ld_in + first : nullptr;
+        T* bo = apply ? out + (g + (t - kLag) * lanes) * ld_out + first : nullptr;
+        float2 ms;
+        if (stats && apply) {
+            ms = sweep<T, VEC, true, true>(a, b, bo, n, keep, drop, rm, rsum, red);
+        } else if (stats) {
+            ms = sweep<T, VEC, true, false>(a, b, bo, n, keep, drop, rm, rsum, red);
+        } else {
+            ms = sweep<T, VEC, false, true>(a, b, bo, n, keep, drop, rm, rsum, red);
+        }
+        if (stats) x.publish(t, ms.x, ms.y, flags);
+    }
 }
 
 template <typename T, int VEC>
-cudaError_t launch_vec(const Problem& p, const SplitShape& sh, float2* ws) {
-    const dim3 grid((unsigned)sh.chunks, (unsigned)p.M, 1);
-    const LaunchShape ls{grid, dim3(kSplitThreads)};
-    const cudaError_t e = launch_kernel(split_stats_kernel<T, VEC>, ls, p.stream,
-                                        static_cast<const T*>(p.in), p.N, p.ld_in, sh.chunk_units,
-                                        ws);
+cudaError_t launch_vec(const Problem& p, const SplitShape& sh, void* ws) {
+    // Zero the slots the launch uses (slots[kRing][B], 16 bytes each).
+    const int B = sh.lanes * sh.parts;
+    cudaError_t e = cudaMemsetAsync(ws, 0, (size_t)kRing * B * 16, p.stream);
     if (e != cudaSuccess) return e;
-    return launch_kernel(split_apply_kernel<T, VEC>, ls, p.stream, static_cast<const T*>(p.in),
-                         static_cast<T*>(p.out), p.N, p.ld_in, p.ld_out, sh.chunk_units,
-                         static_cast<const float2*>(ws));
+    LaunchShape ls{dim3((unsigned)B), dim3(kSplitThreads)};
+    ls.cooperative = true;
+    return launch_kernel(split_grid_kernel<T, VEC>, ls, p.stream, static_cast<const T*>(p.in),
+                         static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, sh.lanes, sh.parts,
+                         sh.part_units, ws, p.dev->err, p.timeout_ns, p.flags);
 }
 
 template <typename T>
-cudaError_t launch_typed(const Problem& p, const SplitShape& sh, float2* ws) {
+cudaError_t launch_typed(const Problem& p, const SplitShape& sh, void* ws) {
     if (sh.vec > 1) return launch_vec<T, 16 / sizeof(T)>(p, sh, ws);
     return launch_vec<T, 1>(p, sh, ws);
 }
 
+template <typename T>
+const void* typed_kernel(int vec) {
+    return vec > 1 ? reinterpret_cast<const void*>(split_grid_kernel<T, 16 / sizeof(T)>)
+                   : reinterpret_cast<const void*>(split_grid_kernel<T, 1>);
+}
+
 }  // namespace
 
-// Chunking (host logic, the same on every device): about kSplitTargetBlocks
-// blocks in total, chunks of at least kSplitMinUnits vectors (or elements),
-// at most kSplitMaxChunks chunks per row.
+const void* split_kernel(int dtype, int vec) {
+    switch (dtype) {
+        case kF32: return typed_kernel<float>(vec);
+        case kBF16: return typed_kernel<__nv_bfloat16>(vec);
+        case kF16: return typed_kernel<__half>(vec);
+    }
+    return nullptr;
+}
+
+// Lanes and parts (host logic). `max_blocks` is how many blocks of the
+// kernel the device holds at once (at most kSplitMaxBlocks), `l2_bytes` its
+// L2. Lanes: as many groups as half the L2 allows at three rows per group
+// (a row's parts wait for their second read while the group reads two more),
+// but no more than leave each group kSplitMinSteps rows (the first two
+// sweeps of a group only read and the last two only write, so a group needs
+// a few steps to overlap them), nor more than the rows or the blocks. Parts:
+// the blocks left per group, but no part under kSplitMinUnits units; the
+// parts are then evened out so that none is empty.
 SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int dtype,
-                       const void* in, const void* out) {
+                       const void* in, const void* out, int max_blocks, int64_t l2_bytes) {
     SplitShape sh;
     const bool vec = rows_vector_aligned(in, out, N, ld_in, ld_out, dtype);
     sh.vec = vec ? 16 / elem_bytes(dtype) : 1;
     const int64_t units = N / sh.vec;
-    const int64_t target_blocks = kSplitTargetBlocks;
-    int64_t chunks = M > 0 ? (target_blocks + M - 1) / M : 1;
-    const int64_t max_chunks = (units + kSplitMinUnits - 1) / kSplitMinUnits;
-    if (chunks > max_chunks) chunks = max_chunks;
-    if (chunks > kSplitMaxChunks) chunks = kSplitMaxChunks;
-    if (chunks < 1) chunks = 1;
-    sh.chunk_units = (units + chunks - 1) / chunks;
-    sh.chunks = (units + sh.chunk_units - 1) / sh.chunk_units;
+    const int64_t row_bytes = N * elem_bytes(dtype);
+    if (max_blocks > kSplitMaxBlocks) max_blocks = kSplitMaxBlocks;
+    if (max_blocks < 1) max_blocks = 1;
+    int64_t lanes = (l2_bytes / 2) / ((kLag + 1) * (row_bytes > 0 ? row_bytes : 1));
+    if (lanes > M / kSplitMinSteps) lanes = M / kSplitMinSteps;
+    if (lanes > M) lanes = M;
+    if (lanes > max_blocks) lanes = max_blocks;
+    if (lanes < 1) lanes = 1;
+    int64_t parts = max_blocks / lanes;
+    const int64_t most = (units + kSplitMinUnits - 1) / kSplitMinUnits;
+    if (parts > most) parts = most;
+    if (parts < 1) parts = 1;
+    sh.part_units = (units + parts - 1) / parts;
+    if (sh.part_units < 1) sh.part_units = 1;
+    sh.parts = (int)((units + sh.part_units - 1) / sh.part_units);
+    if (sh.parts < 1) sh.parts = 1;
+    sh.lanes = (int)lanes;
     return sh;
 }
 
-// Rows go in batches of at most kSplitMaxGridRows (the grid's y dimension).
 cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws) {
-    const int64_t es = elem_bytes(p.dtype);
-    for (int64_t r0 = 0; r0 < p.M; r0 += kSplitMaxGridRows) {
-        Problem q = p;
-        q.M = (p.M - r0 < kSplitMaxGridRows) ? p.M - r0 : kSplitMaxGridRows;
-        q.in = static_cast<const char*>(p.in) + r0 * p.ld_in * es;
-        q.out = static_cast<char*>(p.out) + r0 * p.ld_out * es;
-        float2* w = static_cast<float2*>(ws) + r0 * sh.chunks;
-        cudaError_t e = cudaErrorInvalidValue;
-        switch (p.dtype) {
-            case kF32: e = launch_typed<float>(q, sh, w); break;
-            case kBF16: e = launch_typed<__nv_bfloat16>(q, sh, w); break;
-            case kF16: e = launch_typed<__half>(q, sh, w); break;
-        }
-        if (e != cudaSuccess) return e;
+    switch (p.dtype) {
+        case kF32: return launch_typed<float>(p, sh, ws);
+        case kBF16: return launch_typed<__nv_bfloat16>(p, sh, ws);
+        case kF16: return launch_typed<__half>(p, sh, ws);
     }
-    return cudaSuccess;
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace sr
@@ -204,9 +473,8 @@ cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws) {
 namespace sr {
 namespace {
 
-// Room for this many (max, sum) pairs: M * chunks of a call must fit.
-constexpr int64_t kNoAllocPairs = 65536;  // 512 KiB
-static __device__ __align__(256) float2 g_noalloc_scratch[kNoAllocPairs];
+// The split plan's workspace, whatever the problem.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kSplitWorkspaceBytes];
 
 std::mutex g_noalloc_mu;
 void* g_noalloc_addr[64];  // the array's device address, per device, once set up
@@ -237,11 +505,9 @@ extern "C" int softmax_rows_split_noalloc(const void* in, void* out, int64_t M, 
     const int64_t need = softmax_rows_split_workspace_bytes(in, out, M, N, ld_in, ld_out, dtype);
     if (need < 0) return (int)-need;
     if (M == 0) return SR_OK;
-    if (need > sr::kNoAllocPairs * (int64_t)sizeof(float2)) return SR_EINVAL;  // too big
+    if (need > sr::kSplitWorkspaceBytes) return SR_EINVAL;
     void* scratch = nullptr;
     const int st = sr::noalloc_scratch(&scratch);
     if (st != SR_OK) return st;
-    // Nothing in the scratch has to start at zero: the first kernel writes
-    // every pair the second one reads.
     return softmax_rows_split(in, out, M, N, ld_in, ld_out, dtype, scratch, need, stream);
 }

@@ -187,7 +187,9 @@ WIDE_FEW = {
         Workload("f16_64x131072", F16, 64, 131072, 131072, 131072, 6, DIST_NORMAL, 0.0, 1.0),
         Workload("f16_128x32769", F16, 128, 32769, 32769, 32769, 7, DIST_NORMAL, 0.0, 1.0),
         Workload("f16_1024x16384", F16, 1024, 16384, 16384, 16384, 8, DIST_NORMAL, 0.0, 1.0),
-        # Rows wider than a 16-block cluster's registers (1 MiB and 16 MiB).
+        # Rows wider than a 16-block cluster's registers (800 KB, 1 MiB and 16 MiB).
+        Workload("bf16_512x400008", BF16, 512, 400008, 400008, 400008, 11, DIST_NORMAL, 0.0,
+                 1.0),
         Workload("bf16_128x524288", BF16, 128, 524288, 524288, 524288, 9, DIST_NORMAL, 0.0, 1.0),
         Workload("f32_32x4194304", F32, 32, 4194304, 4194304, 4194304, 10, DIST_NORMAL, 0.0,
                  1.0),

@@ -156,17 +156,60 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
 def test_split_workspace_is_host_logic(lib):
     A, B = ALIGNED_IN, ALIGNED_OUT
     W = sr.softmax_rows_split_workspace_bytes
-    # 4 rows x 32769 f16 (unaligned: chunks of elements): 129 chunks of 255 elements.
-    assert W(A, B, 4, 32769, 32769, 32769, 2) == 4 * 129 * 8
-    # 64 rows x 131072 f16 (aligned): 10 chunks per row.
-    assert W(A, B, 64, 131072, 131072, 131072, 2) == 64 * 10 * 8
-    # Many short rows: one chunk per row.
-    assert W(A, B, 100000, 64, 64, 64, 1) == 100000 * 8
+    # A fixed size: four steps of tagged 16-byte pairs for up to 4096 blocks.
+    for args in [(4, 32769, 32769, 32769, 2), (64, 131072, 131072, 131072, 2),
+                 (100000, 64, 64, 64, 1), (32, 1 << 22, 1 << 22, 1 << 22, 0)]:
+        assert W(A, B, *args) == 4 * 4096 * 16 == 262144
     assert W(A, B, 4, 0, 8, 8, 0) == -sr.SR_EINVAL
     assert W(A, B, 4, 8, 8, 8, 9) == -sr.SR_EDTYPE
     L = lib
     assert L.softmax_rows_split(A, B, 0, 8, 8, 8, 0, None, 0, None) == sr.SR_OK
     assert L.softmax_rows_split(A, B, 4, 8, 8, 8, 0, None, 1024, None) == sr.SR_EINVAL
+    assert L.softmax_rows_split(A, B, 4, 8, 8, 8, 0, A + 4096, 262144 - 16, None) == sr.SR_EINVAL
+
+
+# A device holding 608 blocks of the split kernel, with a 126.5 MiB L2 (half:
+# 66322432 bytes).
+SPLIT_BLOCKS, SPLIT_L2 = 608, 132644864
+
+
+@pytest.mark.parametrize("M,N,dtype,aligned,expect", [
+    # 16 MiB rows: three of them exceed half the L2 -> one group of all 608 blocks;
+    # 1048576 vectors in parts of ceil(1048576 / 608) = 1725.
+    (32, 1 << 22, 0, True, (1, 608, 1725, 4)),
+    # 1 MiB rows: the L2 allows 66322432 // (3 * 1048576) = 21 groups, eight rows
+    # per group allow 128 // 8 = 16; 608 // 16 = 38 blocks; 65536 vectors -> 1725 x 38.
+    (128, 1 << 19, 1, True, (16, 38, 1725, 8)),
+    # 64 rows of 256 KiB: 8 groups of 76 blocks, but no part under 256 vectors -> 64.
+    (64, 131072, 2, True, (8, 64, 256, 8)),
+    # Four unaligned rows of 32769 f16: one group; no part under 256 elements
+    # -> 129 parts of 255 elements.
+    (4, 32769, 2, False, (1, 129, 255, 1)),
+    # Many short rows: a group per block, one part per row.
+    (100000, 64, 0, True, (608, 1, 16, 4)),
+    # Three rows of 250 vectors: one group, one part.
+    (3, 1000, 0, True, (1, 1, 250, 4)),
+])
+def test_split_shape_is_host_logic(lib, M, N, dtype, aligned, expect):
+    A, B = ALIGNED_IN, ALIGNED_OUT
+    if not aligned:
+        B += 2
+    sh = sr.softmax_rows_split_shape(A, B, M, N, N, N, dtype, SPLIT_BLOCKS, SPLIT_L2)
+    assert (sh["lanes"], sh["parts"], sh["part_units"], sh["unit_elems"]) == expect
+    # Every part non-empty, the parts cover the row, and the grid fits the device.
+    units = N // sh["unit_elems"]
+    assert (sh["parts"] - 1) * sh["part_units"] < units <= sh["parts"] * sh["part_units"]
+    assert sh["lanes"] * sh["parts"] <= SPLIT_BLOCKS and sh["lanes"] <= M
+
+
+def test_split_shape_caps_and_errors(lib):
+    A, B = ALIGNED_IN, ALIGNED_OUT
+    sh = sr.softmax_rows_split_shape(A, B, 8, 1 << 22, 1 << 22, 1 << 22, 0, 100000, SPLIT_L2)
+    assert sh["lanes"] * sh["parts"] <= 4096  # the workspace's block limit
+    with pytest.raises(sr.SoftmaxRowsError):
+        sr.softmax_rows_split_shape(A, B, 8, 0, 8, 8, 0, SPLIT_BLOCKS, SPLIT_L2)
+    assert lib.softmax_rows_split_shape(A, B, 8, 64, 64, 64, 0, SPLIT_BLOCKS, SPLIT_L2,
+                                        None) == sr.SR_EINVAL
 
 
 ALIGNED_DY = 0x7F0200000000

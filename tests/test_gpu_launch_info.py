@@ -40,7 +40,7 @@ def test_warp_plan_launch_record():
     assert "warp" in info["name"] and info["cluster"] == 1
 
 
-def test_split_records_its_second_kernel():
+def test_split_records_its_kernel():
     w = synth.WIDE_FEW["f16_4x32769"]
     xd = gu.to_device(w.generate(), w.dtype)
     y = torch.empty((w.M, w.ld_out), dtype=xd.dtype, device="cuda")
@@ -48,4 +48,6 @@ def test_split_records_its_second_kernel():
     ws = torch.empty(need, dtype=torch.uint8, device="cuda")
     sr.softmax_rows_split(xd, y, w.M, w.N, w.ld_in, w.ld_out, w.dtype, ws, need)
     torch.cuda.synchronize()
-    assert "split_apply" in sr.softmax_rows_last_launch()["name"]
+    info = sr.softmax_rows_last_launch()
+    sh = sr.softmax_rows_split_shape(xd, y, w.M, w.N, w.ld_in, w.ld_out, w.dtype)
+    assert "split_grid_kernel" in info["name"] and info["grid"] == sh["lanes"] * sh["parts"]

@@ -1,4 +1,5 @@
-"""softmax_rows_split (few, wide rows; statistics through a workspace) against the oracle."""
+"""softmax_rows_split (wide rows across any number of blocks of one cooperative
+grid; statistics through a workspace) against the oracle."""
 import math
 
 import numpy as np
@@ -24,9 +25,14 @@ def run_split(x, M, N, ld_in, ld_out, dtype, ws_extra=0):
 
 
 # The few-row, wide shapes of "Measured optimization case studies" (Wide rows),
-# plus single huge rows and padded pitches.
+# plus single huge rows and padded pitches; and rows wide enough that a group
+# of blocks takes several rows in turn, so that the four-step ring of pairs and
+# counters wraps: 1 MiB rows of bf16 / f16 (about 21 groups, 7 steps), 4 MiB
+# f32 rows at a padded pitch (5 groups, 5 steps) and 16 MiB f32 rows (one
+# group of every block, 9 steps).
 SHAPES = [(4, 32769, 32769), (64, 131072, 131072), (128, 32769, 32776), (1, 1 << 20, 1 << 20),
-          (3, 1000, 1000), (37, 12345, 12350), (2, 524288 + 8, 524288 + 8)]
+          (3, 1000, 1000), (37, 12345, 12350), (2, 524288 + 8, 524288 + 8),
+          (130, 1 << 19, 1 << 19), (23, 1 << 20, (1 << 20) + 8), (9, 1 << 22, 1 << 22)]
 
 
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16, synth.F16], ids=["f32", "bf16", "f16"])
@@ -74,3 +80,39 @@ def test_split_rejects_bad_workspace_and_in_place():
                                 need, st) == sr.SR_OK
     torch.cuda.synchronize()
     assert torch.allclose(y, torch.softmax(x, dim=1), atol=1e-6, rtol=1e-5)
+
+
+def test_split_launch_shape_matches_host_query():
+    M, N, dtype = 130, 1 << 19, synth.BF16
+    x = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty_like(x)
+    sh = sr.softmax_rows_split_shape(x, y, M, N, N, N, dtype)
+    assert sh["lanes"] > 1 and -(-M // sh["lanes"]) > 4, sh  # the ring wraps
+    ws = torch.empty(sr.softmax_rows_split_workspace_bytes(x, y, M, N, N, N, dtype),
+                     dtype=torch.uint8, device="cuda")
+    sr.softmax_rows_split(x, y, M, N, N, N, dtype, ws, ws.numel())
+    torch.cuda.synchronize()
+    info = sr.softmax_rows_last_launch()
+    assert "split_grid_kernel" in info["name"]
+    assert info["grid"] == sh["lanes"] * sh["parts"] and info["block"] == 256
+    if sr.load().softmax_rows_build_flags() == 0:  # the product build spills nothing
+        assert info["local_bytes"] == 0
+    assert torch.allclose(y.float(), torch.full_like(y.float(), 1.0 / N))
+
+
+def test_split_wait_expiry():
+    M, N, dtype = 6, 1 << 20, synth.F16
+    x = synth.generate(M, N, dtype=dtype, seed=91, p1=2.0)
+    xd = gu.to_device(x, dtype)
+    y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    need = sr.softmax_rows_split_workspace_bytes(xd, y, M, N, N, N, dtype)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    st = sr.softmax_rows_split_test_expiry(xd, y, M, N, N, N, dtype, ws, need, 2_000_000)
+    assert st == sr.SR_OK
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert torch.isnan(y).all(), "an expired kernel wrote output"
+    sr.softmax_rows_split(xd, y, M, N, N, N, dtype, ws, need)
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "split after expiry")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK

@@ -8,9 +8,11 @@ calls in a row on different data (the built-in scratch keeps the previous
 call's contents) and compares its output with the CPU oracle at the parity
 tolerance (and the 1-ulp diagnostic of the 16-bit types), and with the
 workspace entry point (softmax_rows_split) on the same input: the two run the
-same kernels on the same chunking, so their outputs agree bit for bit. This file is
-collected last so that a run stopping at its first failure has already run
-every other test; it also passes on its own in a fresh process.
+same kernel on the same cut of the rows, so their outputs agree bit for bit.
+The split plan's workspace has a fixed size, so the built-in scratch takes
+every problem. This file is collected last so that a run stopping at its
+first failure has already run every other test; it also passes on its own in
+a fresh process.
 """
 import numpy as np
 import pytest
@@ -21,10 +23,6 @@ from tests import gpu_util as gu
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
-
-# Largest statistics the built-in scratch holds, in bytes (65536 pairs).
-NOALLOC_LIMIT = 65536 * 8
-
 
 def _with_workspace(xd, M, N, ld_in, ld_out, dtype):
     y = torch.full((M, ld_out), float("nan"), dtype=xd.dtype, device="cuda")
@@ -58,14 +56,16 @@ def test_no_alloc_matches_workspace_entry_point_twice(dtype):
         assert torch.isnan(got[:, N:]).all() if ld_out > N else True
 
 
-def test_no_alloc_rejects_problems_beyond_its_scratch():
-    M, N = 70000, 64  # one chunk per row: 70000 pairs, more than the scratch holds
-    x = torch.randn(M, N, device="cuda", dtype=torch.float16)
-    y = torch.full_like(x, float("nan"))
-    need = sr.softmax_rows_split_workspace_bytes(x, y, M, N, N, N, synth.F16)
-    assert need > NOALLOC_LIMIT
-    st = sr.load().softmax_rows_split_noalloc(x.data_ptr(), y.data_ptr(), M, N, N, N,
-                                              synth.F16, torch.cuda.current_stream().cuda_stream)
-    assert st == sr.SR_EINVAL
-    torch.cuda.synchronize()
-    assert torch.isnan(y).all(), "a rejected call wrote output"
+def test_no_alloc_takes_many_rows_and_wide_rows():
+    # 70000 short rows (one group per block, many rows per group) and 16 MiB
+    # rows (one group of every block): the fixed scratch serves both.
+    for M, N, dtype, seed in [(70000, 64, synth.F16, 5), (3, 1 << 22, synth.F32, 6)]:
+        x = synth.generate(M, N, dtype=dtype, seed=seed, p1=2.0)
+        xd = gu.to_device(x, dtype)
+        assert sr.softmax_rows_split_workspace_bytes(xd, xd, M, N, N, N, dtype) == 262144
+        ref = _with_workspace(xd, M, N, N, N, dtype)
+        got = _no_alloc(xd, M, N, N, N, dtype)
+        torch.cuda.synchronize()
+        got_h = gu.to_host(got, dtype)
+        gu.check_rows(got_h, x, N, N, dtype, "no-alloc %dx%d" % (M, N))
+        assert np.array_equal(got_h, gu.to_host(ref, dtype)), "output differs from softmax_rows_split"
