@@ -17,6 +17,12 @@ torch = pytest.importorskip("torch")
     (3, 262144, 262144, 262160, 0, 16),
     (37, 4097 * 2, 4097 * 2, 4100 * 2, 2, 6),  # unaligned: the byte path
     (5, 1, 3, 7, 1, 5),
+    # Co-aligned (equal base offsets and pitches modulo 16): head, vectors, tail.
+    (128, 32769 * 2, 32769 * 2, 32769 * 2, 0, 0),  # the f16 128 x 32769 rows
+    (7, 100, 130, 146, 3, 3),
+    (4, 10, 18, 34, 5, 5),                          # rows shorter than their head
+    (3, 40, 40, 56, 9, 9),
+    (9, 333, 338, 354, 14, 14),
 ])
 def test_copies_rows_exactly(M, row_bytes, ld_in, ld_out, off_in, off_out):
     g = torch.Generator().manual_seed(M * 7 + row_bytes)
