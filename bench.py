@@ -666,7 +666,7 @@ def bench_ours(args, w):
     value = replica_throughput(nbytes, 1, world, med_s)  # the slowest rank's median step
     peaks = measured_peaks()
     src_hash = _build.source_hash(_build.PLAN_SOURCES.get(plan_used.replace("masked-", "")))
-    traffic, rec = recorded_traffic(w.name, plan_used)
+    traffic, rec = recorded_traffic(("split:" if args.api == "split" else "") + w.name, plan_used)
     achieved = nbytes / (stats["median_step_us"] / 1e6) / 1e9
     line = {
         "metric": metric,
@@ -930,6 +930,26 @@ def bench_pair(args, lane):
     mean_s = max_over_ranks(stats["mean_step_us"] / 1e6, device="cuda" if world > 1 else "cpu")
     after = pair_parity(lane, sets[last][1], rows)
 
+    copy = None
+    if not args.no_copy:
+        eb = w.elem_bytes
+
+        def launch_rows(i):
+            (a, b), out = sets[i]
+            st = lib.softmax_rows_copy_ceiling2(a.data_ptr(), b.data_ptr(), out.data_ptr(), w.M,
+                                                w.N * eb, w.ld * eb, w.ld * eb, w.ld * eb, sh)
+            if st != 0:
+                raise RuntimeError("softmax_rows_copy_ceiling2: %s" % sr.softmax_rows_strerror(st))
+
+        def launch_torch(i):
+            (a, b), out = sets[i]
+            torch.add(a[:, :w.N], b[:, :w.N], out=out[:, :w.N])
+        copy = copy_baseline(args, launch_rows, launch_torch, n_sets, stream, rank, local_rank,
+                             world, 3 * w.M * w.N * w.elem_bytes)
+        copy["kind"] = ("softmax_rows_copy_ceiling2: out = a XOR b over the same two input and "
+                        "one output matrices (3*M*N*bytes; the weight vector aside), with the "
+                        "same 16-byte streaming loads and stores, same sets and batches; "
+                        "torch_copy_* is torch.add of the same matrices")
     e2e = None
     if not args.no_e2e:
         # Host buffers: the pinned inputs copied in, the call, the output copied back.
@@ -997,6 +1017,10 @@ def bench_pair(args, lane):
         "parity_before_timing": gate,
         "parity": after,
     }
+    if copy is not None:
+        copy["ratio"] = round((3 * w.M * w.N * w.elem_bytes / (stats["median_step_us"] / 1e6) / 1e9)
+                              / (copy["value"] / world), 4)
+        line["copy_baseline"] = copy
     if e2e is not None:
         line["e2e"] = e2e
     if world == 1:

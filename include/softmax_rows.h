@@ -488,10 +488,13 @@ SR_API int softmax_rows_last_launch(sr_launch_info* info);
  * ld_in_bytes) to `out` (row pitch ld_out_bytes), both DEVICE, caller-owned,
  * not overlapping. It moves exactly the bytes a row softmax of the same shape
  * moves, with the same 16-byte streaming loads and stores (byte by byte when
- * a base, a pitch or the row length is not a multiple of 16) and no
+ * a base, a pitch or the row length is not a multiple of 16, unless the rows
+ * are co-aligned as below) and no
  * arithmetic: the measured device copy that the "Warpline" README (Ceilings)
  * takes as the roofline's bandwidth denominator, on the softmax's own shapes
- * and layouts. A measurement tool; no softmax entry point uses it. Bytes
+ * and layouts. Rows at the same offset from a 16-byte boundary in both
+ * matrices (equal base offsets and pitches modulo 16) are copied as a head,
+ * 16-byte vectors and a tail. A measurement tool; no softmax entry point uses it. Bytes
  * [row_bytes, pitch) of each output row are not written. Asynchronous on
  * `stream`. Returns SR_OK, SR_EINVAL (M < 0, row_bytes < 1, a pitch below
  * row_bytes, a null pointer with M > 0, or a last byte beyond INT64_MAX;
@@ -500,6 +503,23 @@ SR_API int softmax_rows_last_launch(sr_launch_info* info);
 SR_API int softmax_rows_copy_ceiling(const void* in, void* out, int64_t M, int64_t row_bytes,
                                      int64_t ld_in_bytes, int64_t ld_out_bytes,
                                      sr_stream_t stream);
+
+/*
+ * The two-input copy ceiling of the row-pair operations (softmax backward,
+ * residual RMSNorm: two matrices read, one written): for M rows,
+ * out[r][i] = a[r][i] XOR b[r][i] over row_bytes bytes, with a, b and out at
+ * their own pitches (bytes), all DEVICE, caller-owned, out overlapping
+ * neither input. The same bytes those operations move (their weight vector
+ * aside), with 16-byte streaming loads and stores (bytes when a base, a pitch
+ * or the row length is not a multiple of 16) and one XOR. A measurement tool.
+ * Bytes [row_bytes, pitch) of each output row are not written. Asynchronous
+ * on `stream`. Returns SR_OK, SR_EINVAL (M < 0, row_bytes < 1, a pitch below
+ * row_bytes, a null pointer with M > 0, or a last byte beyond INT64_MAX;
+ * nothing launched) or SR_ECUDA.
+ */
+SR_API int softmax_rows_copy_ceiling2(const void* a, const void* b, void* out, int64_t M,
+                                      int64_t row_bytes, int64_t ld_a_bytes, int64_t ld_b_bytes,
+                                      int64_t ld_out_bytes, sr_stream_t stream);
 
 /*
  * Bounds-checking build. The library can also be built with every kernel

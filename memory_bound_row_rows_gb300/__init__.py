@@ -24,7 +24,7 @@ __all__ = [
     "softmax_rows_host_mapped",
     "softmax_rows_masked", "softmax_rows_backward", "softmax_rows_backward_ex",
     "softmax_rows_backward_plan", "softmax_rows_backward_test_expiry", "rmsnorm_residual_rows", "rmsnorm_residual_rows_ex",
-    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape", "softmax_rows_last_launch", "softmax_rows_copy_ceiling",
+    "rmsnorm_residual_rows_plan", "softmax_rows_wide_shape", "softmax_rows_last_launch", "softmax_rows_copy_ceiling", "softmax_rows_copy_ceiling2",
     "softmax", "softmax_backward", "rmsnorm_residual",
     "dtype_code",
 ]
@@ -103,6 +103,7 @@ def open_library(path: str):
         "softmax_rows_last_launch": [vp],
         "softmax_rows_build_flags": [],
         "softmax_rows_copy_ceiling": [vp, vp, i64, i64, i64, i64, vp],
+        "softmax_rows_copy_ceiling2": [vp, vp, vp, i64, i64, i64, i64, i64, vp],
         "softmax_rows_bounds_address": [],
         "softmax_rows_test_bounds_shrink": [i64],
     }
@@ -319,6 +320,14 @@ def softmax_rows_strerror(status: int) -> str:
         return load().softmax_rows_strerror(status).decode()
     except RuntimeError:
         return "status %d" % status
+
+
+def softmax_rows_copy_ceiling2(a, b, out, M, row_bytes, ld_a_bytes, ld_b_bytes, ld_out_bytes,
+                               stream=None) -> int:
+    return _check(load().softmax_rows_copy_ceiling2(_ptr(a), _ptr(b), _ptr(out), M, row_bytes,
+                                                    ld_a_bytes, ld_b_bytes, ld_out_bytes,
+                                                    _stream(stream)),
+                  "softmax_rows_copy_ceiling2")
 
 
 def softmax_rows_copy_ceiling(in_, out, M, row_bytes, ld_in_bytes, ld_out_bytes,

@@ -707,6 +707,28 @@ int softmax_rows_last_launch(sr_launch_info* info) {
     return SR_OK;
 }
 
+int softmax_rows_copy_ceiling2(const void* a, const void* b, void* out, int64_t M,
+                               int64_t row_bytes, int64_t ld_a_bytes, int64_t ld_b_bytes,
+                               int64_t ld_out_bytes, sr_stream_t stream) {
+    if (M < 0 || row_bytes < 1 || ld_a_bytes < row_bytes || ld_b_bytes < row_bytes ||
+        ld_out_bytes < row_bytes)
+        return SR_EINVAL;
+    if (M > 0 && (a == nullptr || b == nullptr || out == nullptr)) return SR_EINVAL;
+    if (M > 0) {
+        __int128 ld = ld_a_bytes > ld_b_bytes ? ld_a_bytes : ld_b_bytes;
+        if (ld_out_bytes > ld) ld = ld_out_bytes;
+        if ((__int128)(M - 1) * ld + row_bytes > (__int128)INT64_MAX) return SR_EINVAL;
+    }
+    if (M == 0) return SR_OK;
+    cudaError_t e;
+    const sr::DeviceInfo* dev = sr::device_info(&e);
+    if (!dev) return SR_ECUDA;
+    return sr::launch_copy_pair(a, b, out, M, row_bytes, ld_a_bytes, ld_b_bytes, ld_out_bytes,
+                                (cudaStream_t)stream) == cudaSuccess
+               ? SR_OK
+               : SR_ECUDA;
+}
+
 int softmax_rows_copy_ceiling(const void* in, void* out, int64_t M, int64_t row_bytes,
                               int64_t ld_in_bytes, int64_t ld_out_bytes, sr_stream_t stream) {
     if (M < 0 || row_bytes < 1 || ld_in_bytes < row_bytes || ld_out_bytes < row_bytes)

@@ -123,6 +123,67 @@ __global__ void __launch_bounds__(kCopyThreads)
     }
 }
 
+// The two-input ceiling of the row-pair operations (two matrices read, one
+// written): out = a XOR b, byte for byte, in the same tiles; 16-byte vectors
+// when every base and pitch and the row length are multiples of 16, else bytes.
+template <bool VEC, typename I>
+__global__ void __launch_bounds__(kCopyThreads)
+    copy_pair_kernel(const char* __restrict__ a, const char* __restrict__ b, char* __restrict__ out,
+                     int64_t M, int64_t row_bytes, int64_t ld_a, int64_t ld_b, int64_t ld_out) {
+    SR_GRID_DEPENDENCY();
+    SR_BOUNDS_BEGIN(::sr::bounds::matrix(a, M, ld_a, row_bytes, 1, false),
+                    ::sr::bounds::matrix(b, M, ld_b, row_bytes, 1, false),
+                    ::sr::bounds::matrix(out, M, ld_out, row_bytes, 1, true));
+    const I per_row = (I)(VEC ? row_bytes / 16 : row_bytes);
+    const I total = (I)M * per_row;
+    for (int64_t blk = blockIdx.x; blk * kTile < (int64_t)total; blk += gridDim.x) {
+        const I base = (I)(blk * kTile) + (I)threadIdx.x;
+        int64_t r[kCopyUnroll], c[kCopyUnroll];
+        if constexpr (VEC) {
+            uint4 va[kCopyUnroll], vb[kCopyUnroll];
+#pragma unroll
+            for (int k = 0; k < kCopyUnroll; ++k) {
+                const I u = base + (I)(kCopyThreads * k);
+                split_unit<I>(u, per_row, r[k], c[k]);
+                if (u < total) {
+                    va[k] = ldg_stream(a + r[k] * ld_a + c[k] * 16);
+                    vb[k] = ldg_stream(b + r[k] * ld_b + c[k] * 16);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kCopyUnroll; ++k) {
+                const I u = base + (I)(kCopyThreads * k);
+                if (u < total)
+                    stg_stream(out + r[k] * ld_out + c[k] * 16,
+                               make_uint4(va[k].x ^ vb[k].x, va[k].y ^ vb[k].y, va[k].z ^ vb[k].z,
+                                          va[k].w ^ vb[k].w));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kCopyUnroll; ++k) {
+                const I u = base + (I)(kCopyThreads * k);
+                split_unit<I>(u, per_row, r[k], c[k]);
+                const char* pa = a + r[k] * ld_a + c[k];
+                const char* pb = b + r[k] * ld_b + c[k];
+                char* po = out + r[k] * ld_out + c[k];
+                if (u < total && SR_READ_OK(pa, 1) && SR_READ_OK(pb, 1) && SR_WRITE_OK(po, 1))
+                    *po = (char)(__ldg(reinterpret_cast<const unsigned char*>(pa)) ^
+                                 __ldg(reinterpret_cast<const unsigned char*>(pb)));
+            }
+        }
+    }
+}
+
+template <bool VEC, typename I>
+cudaError_t launch_pair(const char* a, const char* b, char* out, int64_t M, int64_t row_bytes,
+                        int64_t ld_a, int64_t ld_b, int64_t ld_out, cudaStream_t stream) {
+    const int64_t units = M * (VEC ? row_bytes / 16 : row_bytes);
+    const int64_t need = (units + kTile - 1) / kTile;
+    const unsigned grid = (unsigned)(need < 0x7fffffff ? need : 0x7fffffff);
+    return launch_kernel(copy_pair_kernel<VEC, I>, LaunchShape{dim3(grid), dim3(kCopyThreads)},
+                         stream, a, b, out, M, row_bytes, ld_a, ld_b, ld_out);
+}
+
 template <int MODE, typename I>
 cudaError_t launch_copy(const char* in, char* out, int64_t M, int64_t row_bytes, int64_t ld_in,
                         int64_t ld_out, cudaStream_t stream) {
@@ -158,6 +219,25 @@ cudaError_t launch_copy_rows(const void* in, void* out, int64_t M, int64_t row_b
     if (coaligned)
         return launch_mode<kCopyCoaligned>(src, dst, M, row_bytes, ld_in, ld_out, stream);
     return launch_mode<kCopyBytes>(src, dst, M, row_bytes, ld_in, ld_out, stream);
+}
+
+cudaError_t launch_copy_pair(const void* a, const void* b, void* out, int64_t M,
+                             int64_t row_bytes, int64_t ld_a, int64_t ld_b, int64_t ld_out,
+                             cudaStream_t stream) {
+    const bool vec = reinterpret_cast<uintptr_t>(a) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(b) % 16 == 0 &&
+                     reinterpret_cast<uintptr_t>(out) % 16 == 0 && row_bytes % 16 == 0 &&
+                     ld_a % 16 == 0 && ld_b % 16 == 0 && ld_out % 16 == 0;
+    const char* pa = static_cast<const char*>(a);
+    const char* pb = static_cast<const char*>(b);
+    char* po = static_cast<char*>(out);
+    const int64_t units = M * (vec ? row_bytes / 16 : row_bytes);
+    const bool narrow = units + kTile < 0x7fffffff;
+    if (vec)
+        return narrow ? launch_pair<true, int32_t>(pa, pb, po, M, row_bytes, ld_a, ld_b, ld_out, stream)
+                      : launch_pair<true, int64_t>(pa, pb, po, M, row_bytes, ld_a, ld_b, ld_out, stream);
+    return narrow ? launch_pair<false, int32_t>(pa, pb, po, M, row_bytes, ld_a, ld_b, ld_out, stream)
+                  : launch_pair<false, int64_t>(pa, pb, po, M, row_bytes, ld_a, ld_b, ld_out, stream);
 }
 
 }  // namespace sr

@@ -188,6 +188,10 @@ cudaError_t launch_row(const Problem& p);
 // The copy ceiling: M rows of row_bytes from pitch ld_in to pitch ld_out (bytes).
 cudaError_t launch_copy_rows(const void* in, void* out, int64_t M, int64_t row_bytes,
                              int64_t ld_in, int64_t ld_out, cudaStream_t stream, int sm_count);
+// The two-input ceiling: out = a XOR b over M rows of row_bytes (pitches in bytes).
+cudaError_t launch_copy_pair(const void* a, const void* b, void* out, int64_t M,
+                             int64_t row_bytes, int64_t ld_a, int64_t ld_b, int64_t ld_out,
+                             cudaStream_t stream);
 bool row_plan_fits(int64_t N, int dtype);
 int64_t host_workspace_bytes(int64_t M, int64_t N, int dtype);
 

@@ -390,3 +390,17 @@ def test_copy_ceiling_rejects_before_any_device_call(lib):
     assert C(ALIGNED_IN, ALIGNED_OUT, 4, 32, 32, 31, None) == sr.SR_EINVAL
     assert C(None, ALIGNED_OUT, 4, 32, 32, 32, None) == sr.SR_EINVAL
     assert C(ALIGNED_IN, ALIGNED_OUT, 2, 16, 2**63 - 8, 16, None) == sr.SR_EINVAL
+
+
+def test_copy_ceiling2_rejects_before_any_device_call(lib):
+    C = lib.softmax_rows_copy_ceiling2
+    A, B, O = ALIGNED_IN, ALIGNED_OUT, ALIGNED_DY
+    assert C(None, None, None, 0, 16, 16, 16, 16, None) == sr.SR_OK
+    assert C(A, B, O, -1, 16, 16, 16, 16, None) == sr.SR_EINVAL
+    assert C(A, B, O, 4, 0, 16, 16, 16, None) == sr.SR_EINVAL
+    assert C(A, B, O, 4, 32, 16, 32, 32, None) == sr.SR_EINVAL
+    assert C(A, B, O, 4, 32, 32, 31, 32, None) == sr.SR_EINVAL
+    assert C(A, B, O, 4, 32, 32, 32, 31, None) == sr.SR_EINVAL
+    assert C(A, None, O, 4, 32, 32, 32, 32, None) == sr.SR_EINVAL
+    assert C(A, B, None, 4, 32, 32, 32, 32, None) == sr.SR_EINVAL
+    assert C(A, B, O, 2, 16, 16, 2**63 - 8, 16, None) == sr.SR_EINVAL

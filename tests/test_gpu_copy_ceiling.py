@@ -38,3 +38,25 @@ def test_copies_rows_exactly(M, row_bytes, ld_in, ld_out, off_in, off_out):
     assert (body[:, row_bytes:] == 0xA5).all()
     assert (d[:off_out] == 0xA5).all() and (d[off_out + M * ld_out:] == 0xA5).all()
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
+@pytest.mark.parametrize("M,row_bytes,ld_a,ld_b,ld_out,off", [
+    (64, 262144, 262144, 262144, 262144, 0),    # the backward's few wide rows, f16
+    (100, 8192, 8208, 8192, 8224, 0),
+    (9, 333, 340, 350, 360, 3),                 # unaligned: the byte path
+])
+def test_pair_ceiling_xors_rows_exactly(M, row_bytes, ld_a, ld_b, ld_out, off):
+    g = torch.Generator().manual_seed(M + row_bytes)
+    a = torch.randint(0, 256, (off + M * ld_a,), dtype=torch.uint8, generator=g).cuda()
+    b = torch.randint(0, 256, (off + M * ld_b,), dtype=torch.uint8, generator=g).cuda()
+    o = torch.full((off + M * ld_out + 64,), 0xA5, dtype=torch.uint8, device="cuda")
+    sr.softmax_rows_copy_ceiling2(a.data_ptr() + off, b.data_ptr() + off, o.data_ptr() + off, M,
+                                  row_bytes, ld_a, ld_b, ld_out)
+    torch.cuda.synchronize()
+    ah = a.cpu().numpy()[off:].reshape(M, ld_a)[:, :row_bytes]
+    bh = b.cpu().numpy()[off:].reshape(M, ld_b)[:, :row_bytes]
+    oh = o.cpu().numpy()
+    body = oh[off:off + M * ld_out].reshape(M, ld_out)
+    assert np.array_equal(body[:, :row_bytes], ah ^ bh)
+    assert (body[:, row_bytes:] == 0xA5).all() and (oh[off + M * ld_out:] == 0xA5).all()
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
