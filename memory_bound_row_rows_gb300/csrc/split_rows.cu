@@ -414,11 +414,13 @@ const void* split_kernel(int dtype, int vec) {
 
 // Lanes and parts (host logic). `max_blocks` is how many blocks of the
 // kernel the device holds at once (at most kSplitMaxBlocks), `l2_bytes` its
-// L2. Lanes: as many groups as half the L2 allows at three rows per group
-// (a row's parts wait for their second read while the group reads two more),
-// but no more than leave each group kSplitMinSteps rows (the first two
-// sweeps of a group only read and the last two only write, so a group needs
-// a few steps to overlap them), nor more than the rows or the blocks. Parts:
+// L2. Lanes: when the whole input fits in half the L2, a group per row (as
+// many as there are blocks); else as many groups as half the L2 allows at
+// kLag + 1 rows per group (a row's parts wait for their second read while the
+// group reads kLag more), but no more than leave each group kSplitMinSteps
+// rows (the first kLag sweeps of a group only read and the last kLag only
+// write, so a group needs a few steps to overlap them); never more than the
+// rows or the blocks. Parts:
 // the blocks left per group, but no part under kSplitMinUnits units; the
 // parts are then evened out so that none is empty.
 SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int dtype,
@@ -431,7 +433,11 @@ SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int 
     if (max_blocks > kSplitMaxBlocks) max_blocks = kSplitMaxBlocks;
     if (max_blocks < 1) max_blocks = 1;
     int64_t lanes = (l2_bytes / 2) / ((kLag + 1) * (row_bytes > 0 ? row_bytes : 1));
-    if (lanes > M / kSplitMinSteps) lanes = M / kSplitMinSteps;
+    if (M * row_bytes <= l2_bytes / 2) {
+        lanes = M;  // the whole input stays in L2 between the passes: all rows at once
+    } else if (lanes > M / kSplitMinSteps) {
+        lanes = M / kSplitMinSteps;
+    }
     if (lanes > M) lanes = M;
     if (lanes > max_blocks) lanes = max_blocks;
     if (lanes < 1) lanes = 1;

@@ -180,15 +180,16 @@ SPLIT_BLOCKS, SPLIT_L2 = 608, 132644864
     # 1 MiB rows: the L2 allows 66322432 // (3 * 1048576) = 21 groups, eight rows
     # per group allow 128 // 8 = 16; 608 // 16 = 38 blocks; 65536 vectors -> 1725 x 38.
     (128, 1 << 19, 1, True, (16, 38, 1725, 8)),
-    # 64 rows of 256 KiB: 8 groups of 76 blocks, but no part under 256 vectors -> 64.
-    (64, 131072, 2, True, (8, 64, 256, 8)),
-    # Four unaligned rows of 32769 f16: one group; no part under 256 elements
-    # -> 129 parts of 255 elements.
-    (4, 32769, 2, False, (1, 129, 255, 1)),
-    # Many short rows: a group per block, one part per row.
+    # 64 rows of 256 KiB (16 MiB: fits in half the L2): a group per row, 608 // 64 = 9
+    # blocks each; 16384 vectors -> 1821 x 9.
+    (64, 131072, 2, True, (64, 9, 1821, 8)),
+    # Four unaligned rows of 32769 f16: a group per row of 152 blocks, but no part
+    # under 256 elements -> 129 parts of 255 elements.
+    (4, 32769, 2, False, (4, 129, 255, 1)),
+    # Many short rows (25.6 MB): a group per block, one part per row.
     (100000, 64, 0, True, (608, 1, 16, 4)),
-    # Three rows of 250 vectors: one group, one part.
-    (3, 1000, 0, True, (1, 1, 250, 4)),
+    # Three rows of 250 vectors: a group per row, one part.
+    (3, 1000, 0, True, (3, 1, 250, 4)),
 ])
 def test_split_shape_is_host_logic(lib, M, N, dtype, aligned, expect):
     A, B = ALIGNED_IN, ALIGNED_OUT
