@@ -54,7 +54,7 @@ def _stamp(extra_flags) -> str:
 PLAN_SOURCES = {
     "row": ["block_rows.cu", "packed.cuh"], "warp": ["warp_rows.cu", "packed.cuh"], "cta": ["tma_rows.cu"],
     "cluster": ["tma_rows.cu"], "smem": ["smem_rows.cu"], "online": ["online_rows.cu"],
-    "split": ["split_rows.cu", "split.h", "l2prefetch.cuh"], "wide": ["wide_rows.cu", "wide.h", "packed.cuh", "l2prefetch.cuh"],
+    "split": ["split_rows.cu", "split.h"], "wide": ["wide_rows.cu", "wide.h", "packed.cuh", "l2prefetch.cuh"],
     "backward": ["backward_rows.cu", "rowpair.cuh", "rowpair.h"],
     "rmsnorm": ["rmsnorm_rows.cu", "rowpair.cuh", "rowpair.h"],
     "copy": ["copy_rows.cu"],

@@ -482,7 +482,10 @@ namespace {
 
 // Blocks of the SPLIT kernel the current device holds at once.
 int split_max_blocks(const DeviceInfo* dev, int dtype, int vec) {
-    const int per_sm = blocks_per_sm(split_kernel(dtype, vec), kSplitThreadsPerBlock, 0);
+    const void* func = split_kernel(dtype, vec);
+    const size_t smem = split_smem(vec);
+    if (smem > 0 && ensure_smem_limit(func, smem, false) != cudaSuccess) return -1;
+    const int per_sm = blocks_per_sm(func, split_threads(vec), smem);
     if (per_sm <= 0) return -1;
     const int64_t n = (int64_t)per_sm * dev->sm_count;
     return n > kSplitMaxBlocks ? kSplitMaxBlocks : (int)n;

@@ -33,8 +33,11 @@ struct SplitShape {
 };
 SplitShape split_shape(int64_t M, int64_t N, int64_t ld_in, int64_t ld_out, int dtype,
                        const void* in, const void* out, int max_blocks, int64_t l2_bytes);
-// The SPLIT kernel for a dtype and vector width (for occupancy queries).
+// The SPLIT kernel for a dtype and vector width, its dynamic shared memory
+// and its threads per block (for occupancy queries).
 const void* split_kernel(int dtype, int vec);
+size_t split_smem(int vec);
+int split_threads(int vec);
 cudaError_t launch_split(const Problem& p, const SplitShape& sh, void* ws);
 
 }  // namespace sr

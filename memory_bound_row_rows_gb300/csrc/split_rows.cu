@@ -38,6 +38,12 @@
 // merged those of step t - 2 kLag: with kRing = 2 kLag slots no pair is
 // overwritten while it may still be read.
 //
+// Two kernels run this schedule: the register sweep below for rows that are
+// not 16-byte aligned (each thread's loads for a step of the sweep in
+// registers), and for aligned rows a variant whose loads are 1-D bulk copies
+// into a ring of shared memory fed by a producer warp (split_bulk_kernel),
+// which keeps more bytes in flight than the registers can.
+//
 // Failure: a wait that expires sets the timeout bit of the error word; the
 // block's threads leave together after the next barrier, writing nothing
 // more, and the other blocks of the group then expire in turn. No block waits
@@ -48,7 +54,6 @@
 #include "../../include/softmax_rows.h"
 #include "device.cuh"
 #include "internal.h"
-#include "l2prefetch.cuh"
 #include "split.h"
 
 namespace sr {
@@ -67,12 +72,6 @@ constexpr int kLag = kSplitLag;  // pass 2 of step t runs kLag steps after its p
 #define SR_SPLIT_UNROLL 4
 #endif
 constexpr int kSplitUnroll = SR_SPLIT_UNROLL;
-
-// Steps ahead that a block has the bulk-copy engine prefetch its part of a
-// row into L2 (aligned rows; 0: none).
-#ifndef SR_SPLIT_AHEAD
-#define SR_SPLIT_AHEAD 1
-#endif
 
 // Resident blocks per SM the kernel is compiled for (bounds its registers).
 // Measured on GB300 (cold L2, µs, 2 / 3 / 4 blocks per SM with 4 / 4 / 2
@@ -137,8 +136,18 @@ __device__ __forceinline__ float split_exp(float x, float m, float m_l2) {
     }
 }
 
+struct CtaBarrier {
+    __device__ __forceinline__ static void sync() { __syncthreads(); }
+};
+struct ConsumerBarrier {
+    __device__ __forceinline__ static void sync() {
+        asm volatile("bar.sync 1, %0;" ::"n"(kSplitThreads) : "memory");
+    }
+};
+
 // Block-wide online (max, sum) merge; every thread returns the result. Ends
 // with a barrier, so `red` may be reused at once.
+template <typename Bar = CtaBarrier>
 __device__ __forceinline__ void block_merge(float& m, float& s, float2* red) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -148,12 +157,12 @@ __device__ __forceinline__ void block_merge(float& m, float& s, float2* red) {
         merge_ms(m, s, m2, s2);
     }
     if (lane == 0) red[warp] = make_float2(m, s);
-    __syncthreads();
+    Bar::sync();
     m = red[0].x;
     s = red[0].y;
 #pragma unroll
     for (int w = 1; w < kSplitNW; ++w) merge_ms(m, s, red[w].x, red[w].y);
-    __syncthreads();
+    Bar::sync();
 }
 
 // The units one thread holds in one step of a sweep: kSplitUnroll 16-byte
@@ -283,6 +292,7 @@ struct Exchange {
     // merging (after waiting, bounded, for them) pairs tid, tid + threads, ...;
     // false in every thread when a wait expired (the timeout bit is then set).
     // Block-wide.
+    template <typename Bar = CtaBarrier>
     __device__ __forceinline__ bool merge_row(int64_t q, float& M, float& S, float2* red,
                                               int* s_fail, unsigned int* err,
                                               unsigned long long timeout_ns) {
@@ -313,9 +323,9 @@ struct Exchange {
             *s_fail = 1;
             atomicOr(err, kErrTimeout);
         }
-        __syncthreads();
+        Bar::sync();
         if (*s_fail) return false;
-        block_merge(m, s, red);
+        block_merge<Bar>(m, s, red);
         M = m;
         S = s;
         return true;
@@ -351,13 +361,6 @@ __global__ void __launch_bounds__(kSplitThreads, SR_SPLIT_MIN_BLOCKS)
 #pragma unroll 1
     for (int64_t t = 0; t < steps + kLag; ++t) {
         const bool stats = t < steps, apply = t >= kLag;
-        if (VEC > 1 && SR_SPLIT_AHEAD > 0 && tid == 0 && u1 > u0) {
-            for (int64_t k = (t == 0 ? 1 : SR_SPLIT_AHEAD); k <= SR_SPLIT_AHEAD; ++k) {
-                if (t + k < steps)
-                    bulk_prefetch_l2(in + (g + (t + k) * lanes) * ld_in + u0 * VEC,
-                                     (uint32_t)((u1 - u0) * 16));
-            }
-        }
         if (!stats && !apply) continue;  // a group with fewer rows than kLag (block-uniform)
         float rm = neg_inf(), rsum = 0.0f;  // the row's (M, S) for pass 2
         if (apply && !x.merge_row(t - kLag, rm, rsum, red, &s_fail, err, timeout_ns)) return;
@@ -376,6 +379,221 @@ __global__ void __launch_bounds__(kSplitThreads, SR_SPLIT_MIN_BLOCKS)
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Aligned rows: the same schedule with the loads done by the bulk-copy
+// engine. A producer warp (lane 0) walks the block's chunk sequence -- for
+// every step t and every kBulkChunk-byte chunk c of the part: c of row t for
+// pass 1, then c of row t - kLag for pass 2 -- and issues each chunk as a
+// 1-D bulk copy (cp.async.bulk, L2 policy as in the sweep) into a ring of
+// kBulkSlots slots of shared memory as soon as the slot is free; slot i
+// completes on full[i] (transaction bytes). The kSplitThreads consumer
+// threads take the chunks in the same order, move their units into
+// registers, release the slot on empty[i] (one arrival per consumer warp)
+// and then reduce or normalise them. Consumers synchronise on named barrier 1
+// (the producer warp takes no part). Failure: a consumer whose wait expires
+// takes no further chunk and all consumers leave together after the next
+// consumer barrier; the producer stops issuing when a wait of its own expires
+// or a consumer failed, and before it exits waits (bounded) for every copy it
+// issued, so that no copy lands in the shared memory of a finished block.
+// ---------------------------------------------------------------------------
+// Chunk bytes and ring slots per block, and resident blocks per SM. Measured
+// on GB300 (cold L2, µs; f32 32 x 4194304 / bf16 128 x 524288 / bf16
+// 512 x 400008): 32 KiB x 3 slots, 2 blocks/SM 229 / 72 / 197; 16 KiB x 6
+// 243 / 78 / 204; 8 KiB x 12 294 / 91 / 255; 48 KiB x 2 253 / 77 / 190;
+// 64 KiB x 2, 1 block/SM 248 / 82 / 229; the register sweep (the kernel
+// unaligned rows take) 272 / 83 / 252. A bulk L2 prefetch of the next row's
+// part by the producer: 248 / 81 / 219 with 16 KiB chunks (against 243).
+#ifndef SR_SPLIT_BULK_SLOTS
+#define SR_SPLIT_BULK_SLOTS 3
+#endif
+#ifndef SR_SPLIT_BULK_CHUNK
+#define SR_SPLIT_BULK_CHUNK 32768
+#endif
+#ifndef SR_SPLIT_BULK_MIN_BLOCKS
+#define SR_SPLIT_BULK_MIN_BLOCKS 2
+#endif
+constexpr int kBulkSlots = SR_SPLIT_BULK_SLOTS;
+constexpr int kBulkChunk = SR_SPLIT_BULK_CHUNK;
+constexpr int kBulkUnits = kBulkChunk / 16;
+constexpr int kBulkThreads = kSplitThreads + 32;
+constexpr int kBulkPer = kBulkUnits / kSplitThreads;  // units per consumer thread and chunk
+static_assert(kBulkChunk % (16 * kSplitThreads) == 0, "whole units per consumer thread");
+constexpr size_t kBulkBarOffset = (size_t)kBulkSlots * kBulkChunk;
+constexpr size_t kBulkSmem = kBulkBarOffset + 16 * kBulkSlots;
+
+__device__ __forceinline__ void bulk_g2s_pol(uint32_t dst, const void* src, uint32_t bytes,
+                                             uint32_t bar, uint64_t pol) {
+    if (!SR_READ_OK(src, bytes)) return;  // never completes: the bounded wait expires
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive1(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kBulkThreads, SR_SPLIT_BULK_MIN_BLOCKS)
+    split_bulk_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                      int64_t ld_in, int64_t ld_out, int lanes, int parts, int64_t part_units,
+                      void* ws, unsigned int* err, unsigned long long timeout_ns, int flags) {
+    SR_GRID_DEPENDENCY();
+    constexpr int VEC = 16 / sizeof(T);
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N),
+                    SR_SPAN_OUT(ws, kSplitWorkspaceBytes));
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ float2 red[kSplitNW];
+    __shared__ int s_fail;
+    const int tid = threadIdx.x;
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t full0 = sbase + (uint32_t)kBulkBarOffset;
+    const uint32_t empty0 = full0 + 8u * kBulkSlots;
+    if (tid == 0) {
+        s_fail = 0;
+        for (int i = 0; i < kBulkSlots; ++i) {
+            mbar_init(full0 + 8u * i, 1);
+            mbar_init(empty0 + 8u * i, kSplitNW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int b_idx = blockIdx.x;
+    const int g = b_idx / parts, p = b_idx - g * parts;
+    const int64_t units = N / VEC;
+    const int64_t u0 = (p * part_units < units) ? p * part_units : units;
+    const int64_t u1 = (u0 + part_units < units) ? u0 + part_units : units;
+    const int64_t steps = (M > g) ? (M - g + lanes - 1) / lanes : 0;
+    const int nch = (int)((u1 - u0 + kBulkUnits - 1) / kBulkUnits);
+
+    if (tid >= kSplitThreads) {
+        // Producer warp: lane 0 issues the copies, in the consumers' order.
+        if (tid != kSplitThreads) return;
+        const uint64_t keep = l2_keep(), drop = l2_drop();
+        int64_t j = 0;
+        bool ok = true;
+        for (int64_t t = 0; t < steps + kLag && ok; ++t) {
+            for (int c = 0; c < nch && ok; ++c) {
+                const int64_t cu = u0 + (int64_t)c * kBulkUnits;
+                const uint32_t bytes = (uint32_t)((u1 - cu < kBulkUnits ? u1 - cu : kBulkUnits) * 16);
+                for (int kind = 0; kind < 2 && ok; ++kind) {
+                    if (kind == 0 ? t >= steps : t < kLag) continue;
+                    const int64_t r = g + (kind == 0 ? t : t - kLag) * lanes;
+                    const int slot = (int)(j % kBulkSlots);
+                    if (j >= kBulkSlots) {
+                        ok = mbar_wait_bounded(empty0 + 8u * slot,
+                                               (uint32_t)((j / kBulkSlots - 1) & 1), timeout_ns);
+                        if (!ok) break;
+                    }
+                    if (*(volatile int*)&s_fail) { ok = false; break; }
+                    mbar_expect_tx(full0 + 8u * slot, bytes);
+                    bulk_g2s_pol(sbase + (uint32_t)slot * kBulkChunk, in + r * ld_in + cu * VEC,
+                                 bytes, full0 + 8u * slot, kind == 0 ? keep : drop);
+                    ++j;
+                }
+            }
+        }
+        if (!ok) atomicOr(err, kErrTimeout);
+        // Before the block may exit, every issued copy must have landed.
+        for (int64_t i = (j > kBulkSlots ? j - kBulkSlots : 0); i < j; ++i)
+            mbar_wait_bounded(full0 + 8u * (uint32_t)(i % kBulkSlots),
+                              (uint32_t)((i / kBulkSlots) & 1), timeout_ns);
+        return;
+    }
+
+    // Consumers.
+    Exchange x(ws, (int)gridDim.x, parts, g, b_idx);
+    const int lane = tid & 31;
+    bool failed = false;
+    int64_t j = 0;
+#pragma unroll 1
+    for (int64_t t = 0; t < steps + kLag; ++t) {
+        const bool stats = t < steps, apply = t >= kLag;
+        if (!stats && !apply) continue;
+        float rm = neg_inf(), rsum = 0.0f;
+        if (apply && !x.merge_row<ConsumerBarrier>(t - kLag, rm, rsum, red, &s_fail, err, timeout_ns))
+            return;  // every consumer, after the same barrier
+        const float rs = final_rcp(rm, rsum);
+        const float rm_l2 = rm * kLog2e;
+        T* orow = apply ? out + (g + (t - kLag) * lanes) * ld_out : nullptr;
+        float m = neg_inf(), s = 0.0f;
+#pragma unroll 1
+        for (int c = 0; c < nch; ++c) {
+            const int64_t cu = u0 + (int64_t)c * kBulkUnits;
+            const int cnt = (int)(u1 - cu < kBulkUnits ? u1 - cu : kBulkUnits);
+#pragma unroll 1
+            for (int kind = 0; kind < 2; ++kind) {
+                if (kind == 0 ? !stats : !apply) continue;
+                const int slot = (int)(j % kBulkSlots);
+                const uint32_t parity = (uint32_t)((j / kBulkSlots) & 1);
+                ++j;
+                if (failed) continue;
+                if (!mbar_wait_bounded(full0 + 8u * slot, parity, timeout_ns)) {
+                    failed = true;
+                    s_fail = 1;
+                    atomicOr(err, kErrTimeout);
+                    continue;
+                }
+                const uint32_t chunk = sbase + (uint32_t)slot * kBulkChunk;
+                uint4 v[kBulkPer];
+#pragma unroll
+                for (int k = 0; k < kBulkPer; ++k)
+                    if (tid + k * kSplitThreads < cnt) v[k] = lds128(chunk + 16u * (tid + k * kSplitThreads));
+                __syncwarp();
+                if (lane == 0) mbar_arrive1(empty0 + 8u * slot);  // the slot's data is in registers
+                if (kind == 0) {
+                    float cm = neg_inf();
+#pragma unroll
+                    for (int k = 0; k < kBulkPer; ++k) {
+                        if (tid + k * kSplitThreads < cnt) {
+                            float f[VEC];
+                            Elem<T>::unpack(v[k], f);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) cm = fmaxf(cm, f[e]);
+                        }
+                    }
+                    const float mn = fmaxf(m, cm);
+                    const float shift = (mn == neg_inf()) ? 0.0f : mn;
+                    const float shift_l2 = shift * kLog2e;
+                    float cs = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kBulkPer; ++k) {
+                        if (tid + k * kSplitThreads < cnt) {
+                            float f[VEC];
+                            Elem<T>::unpack(v[k], f);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) cs += split_exp<T>(f[e], shift, shift_l2);
+                        }
+                    }
+                    s = s * merge_scale(m, mn) + cs;
+                    m = mn;
+                } else {
+#pragma unroll
+                    for (int k = 0; k < kBulkPer; ++k) {
+                        const int vi = tid + k * kSplitThreads;
+                        if (vi < cnt) {
+                            float f[VEC];
+                            Elem<T>::unpack(v[k], f);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) f[e] = split_exp<T>(f[e], rm, rm_l2) * rs;
+                            stg_stream(orow + (cu + vi) * VEC, Elem<T>::pack(f));
+                        }
+                    }
+                }
+            }
+        }
+        ConsumerBarrier::sync();
+        if (s_fail) return;  // every consumer, after the same barrier
+        if (stats) {
+            block_merge<ConsumerBarrier>(m, s, red);
+            x.publish(t, m, s, flags);
+        }
+    }
+}
+
 template <typename T, int VEC>
 cudaError_t launch_vec(const Problem& p, const SplitShape& sh, void* ws) {
     // Zero the slots the launch uses (slots[kRing][B], 16 bytes each).
@@ -384,9 +602,20 @@ cudaError_t launch_vec(const Problem& p, const SplitShape& sh, void* ws) {
     if (e != cudaSuccess) return e;
     LaunchShape ls{dim3((unsigned)B), dim3(kSplitThreads)};
     ls.cooperative = true;
-    return launch_kernel(split_grid_kernel<T, VEC>, ls, p.stream, static_cast<const T*>(p.in),
-                         static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, sh.lanes, sh.parts,
-                         sh.part_units, ws, p.dev->err, p.timeout_ns, p.flags);
+    if constexpr (VEC > 1) {
+        ls.block = dim3(kBulkThreads);
+        ls.smem = kBulkSmem;
+        e = ensure_smem_limit(reinterpret_cast<const void*>(split_bulk_kernel<T>), ls.smem, false);
+        if (e != cudaSuccess) return e;
+        return launch_kernel(split_bulk_kernel<T>, ls, p.stream, static_cast<const T*>(p.in),
+                             static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, sh.lanes,
+                             sh.parts, sh.part_units, ws, p.dev->err, p.timeout_ns, p.flags);
+    } else {
+        return launch_kernel(split_grid_kernel<T, VEC>, ls, p.stream,
+                             static_cast<const T*>(p.in), static_cast<T*>(p.out), p.M, p.N,
+                             p.ld_in, p.ld_out, sh.lanes, sh.parts, sh.part_units, ws, p.dev->err,
+                             p.timeout_ns, p.flags);
+    }
 }
 
 template <typename T>
@@ -397,11 +626,14 @@ cudaError_t launch_typed(const Problem& p, const SplitShape& sh, void* ws) {
 
 template <typename T>
 const void* typed_kernel(int vec) {
-    return vec > 1 ? reinterpret_cast<const void*>(split_grid_kernel<T, 16 / sizeof(T)>)
+    return vec > 1 ? reinterpret_cast<const void*>(split_bulk_kernel<T>)
                    : reinterpret_cast<const void*>(split_grid_kernel<T, 1>);
 }
 
 }  // namespace
+
+size_t split_smem(int vec) { return vec > 1 ? kBulkSmem : 0; }
+int split_threads(int vec) { return vec > 1 ? kBulkThreads : kSplitThreads; }
 
 const void* split_kernel(int dtype, int vec) {
     switch (dtype) {

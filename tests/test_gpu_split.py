@@ -93,8 +93,8 @@ def test_split_launch_shape_matches_host_query():
     sr.softmax_rows_split(x, y, M, N, N, N, dtype, ws, ws.numel())
     torch.cuda.synchronize()
     info = sr.softmax_rows_last_launch()
-    assert "split_grid_kernel" in info["name"]
-    assert info["grid"] == sh["lanes"] * sh["parts"] and info["block"] == 256
+    assert "split_bulk_kernel" in info["name"]  # aligned rows: the bulk-copy kernel
+    assert info["grid"] == sh["lanes"] * sh["parts"] and info["block"] == 288
     if sr.load().softmax_rows_build_flags() == 0:  # the product build spills nothing
         assert info["local_bytes"] == 0
     assert torch.allclose(y.float(), torch.full_like(y.float(), 1.0 / N))
