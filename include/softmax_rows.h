@@ -102,7 +102,9 @@ enum sr_status {
  *           cluster, the exponential recomputed for the output; rows up to
  *           512 KiB, and aligned rows of exactly 1 MiB with half of each
  *           slice in shared memory. Other wider aligned rows are streamed:
- *           each block reads its slice twice, the second time mostly from L2.
+ *           each block reads its slice twice, the second time mostly from L2
+ *           (on 8-block clusters through a ring of shared memory that a
+ *           producer warp fills by bulk copies).
  * All plans but ROW and WIDE run a persistent grid sized to the device's SM
  * count.
  */

@@ -18,7 +18,9 @@
 // a new cluster as soon as one finishes.
 //
 // Aligned rows too wide for the cluster's registers (over 512 KiB) take a
-// streamed variant (wide_stream_kernel) that reads each slice twice instead.
+// streamed variant that reads each slice twice instead (wide_bulk_kernel on
+// 8-block clusters, its loads by the bulk-copy engine; wide_stream_kernel on
+// 16-block clusters).
 //
 // Failure: a wait that expires marks the block failed; it writes nothing
 // more, records the failure in the error word and, before leaving, waits once
@@ -611,6 +613,270 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
     }
 }
 
+// Streamed rows with the loads done by the bulk-copy engine (streamed rows on
+// 8-block clusters; SR_WIDE_BULK = 0 keeps wide_stream_kernel for all). A producer warp
+// (lane 0) walks the block's chunk sequence -- for each of its rows, the
+// slice's kWBUnits-vector chunks for pass 1, then the same chunks again for
+// pass 2 -- and issues each as a 1-D bulk copy (L2 policy: keep for pass 1,
+// drop for pass 2) into a ring of kWBSlots shared-memory slots as soon as the
+// slot is free; slot i completes on full[i] (transaction bytes). The eight
+// consumer warps take the chunks in the same order, move their units into
+// registers, release the slot on empty[i] (one arrival per warp) and compute
+// exactly as wide_stream_kernel does; the exchange is the same. Failure: a
+// consumer warp whose wait for a chunk or for the exchange expires stops
+// taking chunks and writing, keeps sending its pairs, and waits once more
+// before it leaves, as in wide_stream_kernel; the producer stops issuing when
+// a wait of its own expires or a consumer failed, and waits (bounded) for
+// every copy it issued before it leaves.
+#ifndef SR_WIDE_BULK
+#define SR_WIDE_BULK 1
+#endif
+#ifndef SR_WIDE_BULK_CHUNK
+#define SR_WIDE_BULK_CHUNK 16384
+#endif
+#ifndef SR_WIDE_BULK_SLOTS
+#define SR_WIDE_BULK_SLOTS 3
+#endif
+#ifndef SR_WIDE_BULK_MIN_BLOCKS
+#define SR_WIDE_BULK_MIN_BLOCKS 3
+#endif
+constexpr int kWBChunk = SR_WIDE_BULK_CHUNK;        // bytes
+constexpr int kWBUnits = kWBChunk / 16;             // vectors per chunk
+constexpr int kWBSlots = SR_WIDE_BULK_SLOTS;
+constexpr int kWBThreads = kWideThreads + 32;       // consumers + the producer warp
+constexpr int kWBPer = kWBUnits / kWideThreads;     // vectors per consumer thread and chunk
+static_assert(kWBChunk % (16 * kWideThreads) == 0, "whole vectors per consumer thread");
+constexpr size_t kWBBarOff = (size_t)kWBSlots * kWBChunk;
+constexpr size_t kWBSmem = kWBBarOff + 16 * kWBSlots;
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_policy(uint32_t dst, const void* src, uint32_t bytes,
+                                                uint32_t bar, uint64_t pol) {
+    if (!SR_READ_OK(src, bytes)) return;  // never completes: the bounded wait expires
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWBThreads, SR_WIDE_BULK_MIN_BLOCKS)
+    wide_bulk_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
+                     int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
+                     unsigned long long timeout_ns, int flags, int64_t /* ahead: unused */) {
+    SR_GRID_DEPENDENCY();
+    SR_BOUNDS_BEGIN(SR_MAT_IN(in, M, ld_in, N), SR_MAT_OUT(out, M, ld_out, N));
+    constexpr int VEC = Elem<T>::kVec;
+    constexpr int NT = kWideThreads;
+    constexpr int NW = kWideWarps;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ float2 pairs[2][kMaxCluster * NW];
+    __shared__ __align__(8) unsigned long long xbar[2];
+    __shared__ int s_fail;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rank = (int)cluster_ctarank();
+    const int64_t nclusters = gridDim.x / csize;
+    const int64_t nvec = N / VEC;
+    const int64_t u0 = (int64_t)rank * slice;
+    const int64_t u1 = (u0 + slice < nvec) ? u0 + slice : nvec;
+    const int64_t nch = u1 > u0 ? (u1 - u0 + kWBUnits - 1) / kWBUnits : 0;
+    const int npairs = csize * NW;
+    const bool send = !(flags & kFlagNoCopy);  // test hook: send nothing, every wait expires
+    const uint32_t sbase = smem_addr(ring);
+    const uint32_t full0 = sbase + (uint32_t)kWBBarOff;  // full[i] at full0 + 8 i
+    const uint32_t empty0 = full0 + 8u * kWBSlots;       // empty[i] at empty0 + 8 i
+
+    if (tid == 0) {
+        s_fail = 0;
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        for (int i = 0; i < kWBSlots; ++i) {
+            mbar_init(full0 + 8u * i, 1);
+            mbar_init(empty0 + 8u * i, NW);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    cluster_arrive_relaxed();
+
+    if (warp == NW) {
+        // Producer warp: the whole warp passes the cluster barrier, then lane 0
+        // issues the copies in the consumers' order.
+        cluster_wait();
+        if (lane != 0) return;
+        const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
+        int64_t j = 0;
+        bool ok = true;
+        for (int64_t r = blockIdx.x / csize; r < M && ok; r += nclusters) {
+            const T* rin = in + r * ld_in;
+            for (int pass = 0; pass < 2 && ok; ++pass) {
+                for (int64_t c = 0; c < nch && ok; ++c) {
+                    const int64_t cu = u0 + c * kWBUnits;
+                    const uint32_t bytes = (uint32_t)((u1 - cu < kWBUnits ? u1 - cu : kWBUnits) * 16);
+                    const int slot = (int)(j % kWBSlots);
+                    if (j >= kWBSlots) {
+                        // Wait for the consumers to release the slot, watching for their failure.
+                        const uint32_t bar = empty0 + 8u * slot;
+                        const uint32_t par = (uint32_t)((j / kWBSlots - 1) & 1);
+                        const uint64_t t0 = global_timer_ns();
+                        while (!mbar_try_wait(bar, par)) {
+                            if (*(volatile int*)&s_fail || global_timer_ns() - t0 > timeout_ns) {
+                                ok = false;
+                                break;
+                            }
+                        }
+                        if (!ok) break;
+                    }
+                    if (*(volatile int*)&s_fail) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(full0 + 8u * slot, bytes);
+                    bulk_g2s_policy(sbase + (uint32_t)slot * kWBChunk, rin + cu * VEC, bytes,
+                                    full0 + 8u * slot, pass == 0 ? keep : drop);
+                    ++j;
+                }
+            }
+        }
+        if (!ok) atomicOr(err, 1u);
+        // Before the block may exit, every issued copy must have landed.
+        for (int64_t i = (j > kWBSlots ? j - kWBSlots : 0); i < j; ++i)
+            mbar_wait_bounded(full0 + 8u * (uint32_t)(i % kWBSlots),
+                              (uint32_t)((i / kWBSlots) & 1), timeout_ns);
+        return;
+    }
+
+    // Consumer warps.
+    bool started = false, failed = false;
+    uint32_t fail_bar = 0, fail_phase = 0, last_bar = 0, last_phase = 0;
+    int64_t it = 0, j = 0;
+    auto take = [&](int64_t c, uint4 (&v)[kWBPer], int& cnt) -> bool {
+        // Chunk c of the slice into registers; false once this warp has failed.
+        const int slot = (int)(j % kWBSlots);
+        const uint32_t par = (uint32_t)((j / kWBSlots) & 1);
+        ++j;
+        if (failed) return false;
+        if (!mbar_wait_bounded(full0 + 8u * slot, par, timeout_ns)) {
+            failed = true;
+            s_fail = 1;
+            fail_bar = 0;
+            return false;
+        }
+        const int64_t cu = u0 + c * kWBUnits;
+        cnt = (int)(u1 - cu < kWBUnits ? u1 - cu : kWBUnits);
+        const uint32_t chunk = sbase + (uint32_t)slot * kWBChunk;
+#pragma unroll
+        for (int k = 0; k < kWBPer; ++k)
+            if (tid + k * NT < cnt) v[k] = lds128(chunk + 16u * (tid + k * NT));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+        return true;
+    };
+    for (int64_t r = blockIdx.x / csize; r < M; r += nclusters, ++it) {
+        const int p = (int)(it & 1);
+        const uint32_t phase = (uint32_t)((it >> 1) & 1);
+        // Pass 1: per-thread online (m, s).
+        float m = neg_inf(), s = 0.0f;
+        for (int64_t c = 0; c < nch; ++c) {
+            uint4 v[kWBPer];
+            int cnt = 0;
+            if (!take(c, v, cnt)) break;
+            VecMax<T> vm;
+#pragma unroll
+            for (int k = 0; k < kWBPer; ++k)
+                if (tid + k * NT < cnt) vm.add(v[k]);
+            const float mn = fmaxf(m, vm.get());
+            const float shift = (mn == neg_inf()) ? 0.0f : mn;
+            const float shift_l2 = shift * kLog2e;
+            float sa = 0.0f, sb = 0.0f;
+#pragma unroll
+            for (int k = 0; k < kWBPer; ++k) {
+                if (tid + k * NT < cnt) {
+                    float f[VEC];
+                    Elem<T>::unpack(v[k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        const float x = wide_exp<T>(f[e], shift, shift_l2);
+                        if (e & 1) sb += x; else sa += x;
+                    }
+                }
+            }
+            s = s * merge_scale(m, mn) + (sa + sb);
+            m = mn;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+            const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+            merge_ms(m, s, m2, s2);
+        }
+        if (!started) {
+            cluster_wait();
+            started = true;
+        }
+        const uint32_t xb = smem_addr(&xbar[p]);
+        last_bar = xb;
+        last_phase = phase;
+        if (tid == 0) mbar_expect_tx(xb, (uint32_t)npairs * 8u);
+        if (send && lane < csize)
+            st_async_f2(map_to_rank(smem_addr(&pairs[p][rank * NW + warp]), (uint32_t)lane), m, s,
+                        map_to_rank(xb, (uint32_t)lane));
+        if (!failed && !mbar_wait_bounded(xb, phase, timeout_ns)) {
+            failed = true;
+            s_fail = 1;
+            fail_bar = xb;
+            fail_phase = phase;
+        }
+        if (failed) continue;  // no output; keep sending, so peers do not wait in vain
+        float mloc = neg_inf();
+        for (int i = lane; i < npairs; i += 32) mloc = fmaxf(mloc, pairs[p][i].x);
+        const float Mr = warp_max(mloc);
+        float sloc = 0.0f;
+        for (int i = lane; i < npairs; i += 32) {
+            const float2 q = pairs[p][i];
+            sloc += q.y * merge_scale(q.x, Mr);
+        }
+        const float Sr = warp_sum(sloc);
+        // Pass 2: the output, as in wide_stream_kernel.
+        T* rout = out + r * ld_out;
+        const float rs = Elem<T>::kAccurateExp ? final_rcp(Mr, Sr) : 0.0f;
+        const float cexp = Elem<T>::kAccurateExp ? 0.0f : fmaf(Mr, kLog2e, lg2_approx(Sr));
+        for (int64_t c = 0; c < nch; ++c) {
+            uint4 v[kWBPer];
+            int cnt = 0;
+            if (!take(c, v, cnt)) break;
+            const int64_t cu = u0 + c * kWBUnits;
+#pragma unroll
+            for (int k = 0; k < kWBPer; ++k) {
+                if (tid + k * NT < cnt) {
+                    float f[VEC];
+                    Elem<T>::unpack(v[k], f);
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) {
+                        if constexpr (Elem<T>::kAccurateExp)
+                            f[e] = wide_exp<T>(f[e], Mr, 0.0f) * rs;
+                        else
+                            f[e] = ex2_approx(fmaf(f[e], kLog2e, -cexp));
+                    }
+                    stg_stream(rout + (cu + tid + k * NT) * VEC, Elem<T>::pack(f));
+                }
+            }
+        }
+    }
+    if (!started) cluster_wait();
+    if (failed) {
+        // Once more (bounded): the exchange that failed, or else the last one,
+        // so that a late peer's pair does not land after this block exits.
+        if (tid == 0) atomicOr(err, 1u);
+        if (fail_bar != 0) mbar_wait_bounded(fail_bar, fail_phase, timeout_ns);
+        else if (last_bar != 0) mbar_wait_bounded(last_bar, last_phase, timeout_ns);
+    }
+}
+
 template <typename T>
 using WideKernel = void (*)(const T*, T*, int64_t, int64_t, int64_t, int64_t, int, int64_t,
                             unsigned int*, unsigned long long, int, int64_t);
@@ -677,6 +943,27 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     }
     if (sh.streamed) {
         if (!aligned) return cudaErrorInvalidValue;
+        // The bulk-copy ring on 8-block clusters; 16-block clusters (few rows) stay on
+        // register loads. Measured on GB300 (cold L2, µs, bulk against register
+        // loads): 8-block clusters: bf16 512 x 400008 150.5 / 156.7, bf16
+        // 256 x 1048576 209.6 / 245.8, f32 256 x 524288 209.2 / 247.3, f16
+        // 96 x 1500000 125.1 / 161.8; 16-block clusters: f32 32 x 4194304 272.2 /
+        // 268.8, bf16 64 x 600008 40.1 / 36.5.
+        if (SR_WIDE_BULK && sh.csize <= 8) {
+            auto kern = wide_bulk_kernel<T>;
+            const void* fn = reinterpret_cast<const void*>(kern);
+            const int c = sh.csize;
+            cudaError_t e = ensure_smem_limit(fn, kWBSmem, c > 8);
+            if (e != cudaSuccess) return e;
+            if (max_active_clusters(fn, kWBThreads, kWBSmem, c) <= 0)
+                return cudaErrorInvalidConfiguration;
+            const int64_t cap = 0x7fffffff / c;
+            const LaunchShape ls{dim3((unsigned)((p.M < cap ? p.M : cap) * c)), dim3(kWBThreads),
+                                 kWBSmem, c, SR_WIDE_POLICY};
+            return launch_kernel(kern, ls, p.stream, static_cast<const T*>(p.in),
+                                 static_cast<T*>(p.out), p.M, p.N, p.ld_in, p.ld_out, c, sh.slice,
+                                 p.dev->err, p.timeout_ns, p.flags, (int64_t)0);
+        }
         return launch_clusters<T>(wide_stream_kernel<T>, p, sh.csize, sh.slice);
     }
     int mode = kShifted;
