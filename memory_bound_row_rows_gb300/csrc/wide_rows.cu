@@ -635,10 +635,7 @@ __global__ void __launch_bounds__(kWideThreads, SR_WIDE_STREAM_MIN_BLOCKS)
 #define SR_WIDE_BULK_CHUNK 16384
 #endif
 #ifndef SR_WIDE_BULK_SLOTS
-#define SR_WIDE_BULK_SLOTS 3
-#endif
-#ifndef SR_WIDE_BULK_MIN_BLOCKS
-#define SR_WIDE_BULK_MIN_BLOCKS 3
+#define SR_WIDE_BULK_SLOTS 4
 #endif
 constexpr int kWBChunk = SR_WIDE_BULK_CHUNK;        // bytes
 constexpr int kWBUnits = kWBChunk / 16;             // vectors per chunk
@@ -663,8 +660,11 @@ __device__ __forceinline__ void bulk_g2s_policy(uint32_t dst, const void* src, u
         : "memory");
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kWBThreads, SR_WIDE_BULK_MIN_BLOCKS)
+// MINB: resident blocks per SM it is compiled for (3, or 2 when the rows of
+// the clusters resident at 3 blocks/SM would not fit in half the L2 between a
+// slice's two reads).
+template <typename T, int MINB>
+__global__ void __launch_bounds__(kWBThreads, MINB)
     wide_bulk_kernel(const T* __restrict__ in, T* __restrict__ out, int64_t M, int64_t N,
                      int64_t ld_in, int64_t ld_out, int csize, int64_t slice, unsigned int* err,
                      unsigned long long timeout_ns, int flags, int64_t /* ahead: unused */) {
@@ -944,13 +944,19 @@ cudaError_t launch_typed(const Problem& p, const WideShape& sh) {
     if (sh.streamed) {
         if (!aligned) return cudaErrorInvalidValue;
         // The bulk-copy ring on 8-block clusters; 16-block clusters (few rows) stay on
-        // register loads. Measured on GB300 (cold L2, µs, bulk against register
-        // loads): 8-block clusters: bf16 512 x 400008 150.5 / 156.7, bf16
-        // 256 x 1048576 209.6 / 245.8, f32 256 x 524288 209.2 / 247.3, f16
-        // 96 x 1500000 125.1 / 161.8; 16-block clusters: f32 32 x 4194304 272.2 /
-        // 268.8, bf16 64 x 600008 40.1 / 36.5.
+        // register loads. Measured on GB300 (cold L2, µs, bulk with 16 KiB x 3
+        // slots at 3 blocks/SM against register loads): 8-block clusters: bf16
+        // 512 x 400008 150.5 / 156.7, bf16 256 x 1048576 209.6 / 245.8, f32
+        // 256 x 524288 209.2 / 247.3, f16 96 x 1500000 125.1 / 161.8; 16-block
+        // clusters: f32 32 x 4194304 272.2 / 268.8, bf16 64 x 600008 40.1 / 36.5.
+        // With 4 slots, at 3 / 2 blocks per SM: bf16 512 x 400008 145.5 / 162.5,
+        // bf16 256 x 1048576 209.2 / 192.3, f16 96 x 1500000 128.0 / 115.7, f32
+        // 128 x 600000 130.8 / 121.1 (32 KiB x 2 slots 169-279, 8 KiB x 6 127-218):
+        // 3 blocks per SM while the resident clusters' rows fit in half the L2.
         if (SR_WIDE_BULK && sh.csize <= 8) {
-            auto kern = wide_bulk_kernel<T>;
+            const int64_t row_bytes = p.N * (int64_t)sizeof(T);
+            const bool three = (int64_t)3 * p.dev->sm_count / sh.csize * row_bytes <= p.dev->l2_bytes / 2;
+            auto kern = three ? wide_bulk_kernel<T, 3> : wide_bulk_kernel<T, 2>;
             const void* fn = reinterpret_cast<const void*>(kern);
             const int c = sh.csize;
             cudaError_t e = ensure_smem_limit(fn, kWBSmem, c > 8);

@@ -303,6 +303,54 @@ def test_streamed_wide_wait_expiry():
     assert sr.softmax_rows_last_device_error() == sr.SR_OK
 
 
+
+# Streamed rows with enough rows for 8-block clusters take the bulk-copy ring
+# kernel: 800 KB rows at 3 blocks/SM, 1.2 MB rows at 2 (their resident rows
+# would not fit in half the L2 at 3), ragged chunks at the end of each slice.
+@pytest.mark.parametrize("dtype,M,N", [(synth.F16, 96, 400000), (synth.BF16, 80, 600008),
+                                       (synth.F32, 80, 300000), (synth.F32, 77, 262148)],
+                         ids=lambda v: str(v))
+def test_streamed_bulk_rows(dtype, M, N):
+    from tests import pins
+    x = synth.generate(M, N, dtype=dtype, seed=N + 3 * M, p1=3.0)
+    sp = pins.encode_exact(special_rows(N, dtype), dtype)
+    x[M - sp.shape[0]:] = sp  # special rows at the end, on the last clusters
+    xd = gu.to_device(x, dtype)
+    st, y = run_plan(xd, M, N, N, N, dtype, sr.SR_PLAN_AUTO)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    assert "wide_bulk_kernel" in sr.softmax_rows_last_launch()["name"]
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "bulk streamed %dx%d" % (M, N))
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
+
+def test_streamed_bulk_in_place():
+    M, N, dtype = 96, 400008, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=93, p1=3.0)
+    buf = gu.to_device(x, dtype)
+    st = sr.load().softmax_rows_ex(buf.data_ptr(), buf.data_ptr(), M, N, N, N, dtype,
+                                   sr.SR_PLAN_WIDE, torch.cuda.current_stream().cuda_stream)
+    assert st == sr.SR_OK
+    torch.cuda.synchronize()
+    assert "wide_bulk_kernel" in sr.softmax_rows_last_launch()["name"]
+    gu.check_rows(gu.to_host(buf, dtype), x, N, N, dtype, "bulk streamed in place")
+
+
+def test_streamed_bulk_wait_expiry():
+    M, N, dtype = 80, 600008, synth.BF16
+    x = synth.generate(M, N, dtype=dtype, seed=79, p1=2.0)
+    xd = gu.to_device(x, dtype)
+    y = nan_filled(M, N, dtype)
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+    sr.softmax_rows_test_expiry(xd, y, M, N, N, N, dtype, sr.SR_PLAN_WIDE, 2_000_000)
+    assert sr.softmax_rows_last_device_error() == sr.SR_EDEVICE_TIMEOUT
+    assert "wide_bulk_kernel" in sr.softmax_rows_last_launch()["name"]
+    assert torch.isnan(y).all(), "an expired kernel wrote output"
+    sr.softmax_rows_ex(xd, y, M, N, N, N, dtype, sr.SR_PLAN_WIDE)
+    torch.cuda.synchronize()
+    gu.check_rows(gu.to_host(y, dtype), x, N, N, dtype, "bulk streamed after expiry")
+    assert sr.softmax_rows_last_device_error() == sr.SR_OK
+
 # ---- many short rows: the WARP plan's shared-lane layouts ----
 
 # Rows of at most 64 vectors with rows enough for 4 blocks per SM are taken by
