@@ -311,6 +311,7 @@ RMSNORM = {
     w.name: w
     for w in [
         RmsNormWorkload("f16_16384x4096", F16, 16384, 4096, 4096, 30),
+        RmsNormWorkload("bf16_16384x4096", BF16, 16384, 4096, 4096, 42),
         RmsNormWorkload("f16_1024x1024", F16, 1024, 1024, 1024, 31),
         RmsNormWorkload("f16_512x4097", F16, 512, 4097, 4097, 32),
         RmsNormWorkload("f16_32x127", F16, 32, 127, 127, 33),

@@ -140,7 +140,7 @@ def test_empty_and_rejected():
                                    16, 16, 16, 1e-6, 0, s) == sr.SR_EINVAL
 
 
-@pytest.mark.parametrize("name", ["f16_16384x4096", "f16_64x131072"])
+@pytest.mark.parametrize("name", ["f16_16384x4096", "bf16_16384x4096", "f16_64x131072"])
 def test_full_size_sampled_rows(name):
     w = synth.RMSNORM[name]
     x, r, wt = w.x_rows(0, w.M), w.residual_rows(0, w.M), w.weight()
