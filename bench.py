@@ -417,6 +417,40 @@ def kernel_record(sr) -> dict:
             "block": info["block"], "cluster": info["cluster"]}
 
 
+def parse_cpulist(text: str) -> set:
+    """A Linux cpulist ("0-3,8,10-11") as a set of CPU numbers."""
+    cpus = set()
+    for part in text.strip().split(","):
+        if not part:
+            continue
+        if "-" in part:
+            lo, hi = part.split("-")
+            cpus.update(range(int(lo), int(hi) + 1))
+        else:
+            cpus.add(int(part))
+    return cpus
+
+
+def gpu_numa_cpus(dev):
+    """The CPUs (of those this process may use) on the NUMA node the GPU's PCI device
+    reports in sysfs, and a note saying where they came from; (None, note) when the
+    node or its CPUs cannot be found. Host buffers pinned by a thread running there are
+    placed in that node's memory, next to the GPU's host link."""
+    try:
+        import torch
+        p = torch.cuda.get_device_properties(dev)
+        bus = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        with open("/sys/bus/pci/devices/%s/numa_node" % bus) as f:
+            node = int(f.read())
+        if node < 0:
+            return None, {"gpu_pci": bus, "numa_node": node}
+        with open("/sys/devices/system/node/node%d/cpulist" % node) as f:
+            cpus = parse_cpulist(f.read()) & os.sched_getaffinity(0)
+        return (cpus or None), {"gpu_pci": bus, "numa_node": node, "cpus": len(cpus)}
+    except (OSError, ValueError, AttributeError) as e:
+        return None, {"numa": "not found (%s)" % type(e).__name__}
+
+
 def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
     """Same metric through the C ABI with host buffers, timed around whole calls with the
     input in pinned host memory and the result landing back in pinned host memory. Two
@@ -426,8 +460,18 @@ def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
     The line reports the faster, and both figures."""
     import torch
     import memory_bound_row_rows_gb300 as sr
-    x_pin = host_tensor(x).pin_memory()
-    y_pin = torch.empty((w.M, w.ld_out), dtype=tdt).pin_memory()
+    # Pin the host buffers from a thread on the GPU's NUMA node, so that their pages
+    # sit next to its host link; the process's CPU set is restored afterwards.
+    cpus, numa = gpu_numa_cpus(dev)
+    saved = os.sched_getaffinity(0)
+    try:
+        if cpus:
+            os.sched_setaffinity(0, cpus)
+        x_pin = host_tensor(x).pin_memory()
+        y_pin = torch.empty((w.M, w.ld_out), dtype=tdt).pin_memory()
+        y_pin.zero_()
+    finally:
+        os.sched_setaffinity(0, saved)
     need = sr.softmax_rows_host_workspace_bytes(w.M, w.N, w.dtype)
     ws = torch.empty(need, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -471,7 +515,8 @@ def run_e2e(args, w, x, dev, lib, host_tensor, tdt):
                     ("softmax_rows_host: pinned host -> device workspace -> pinned host, "
                      "chunks overlapped on three streams"),
             "mapped_gbs": round(w.fused_bytes / sec_m / 1e9, 2),
-            "staged_gbs": round(w.fused_bytes / sec_s / 1e9, 2)}
+            "staged_gbs": round(w.fused_bytes / sec_s / 1e9, 2),
+            "host_buffers": numa}
 
 
 
@@ -952,10 +997,19 @@ def bench_pair(args, lane):
                         "torch_copy_* is torch.add of the same matrices")
     e2e = None
     if not args.no_e2e:
-        # Host buffers: the pinned inputs copied in, the call, the output copied back.
-        pins = [to_device(m, w.dtype, "cpu").pin_memory() for m in lane.mats + lane.vecs]
+        # Host buffers: the pinned inputs copied in, the call, the output copied back,
+        # pinned from a thread on the GPU's NUMA node (as in run_e2e).
+        cpus, numa = gpu_numa_cpus(dev)
+        saved = os.sched_getaffinity(0)
+        try:
+            if cpus:
+                os.sched_setaffinity(0, cpus)
+            pins = [to_device(m, w.dtype, "cpu").pin_memory() for m in lane.mats + lane.vecs]
+            out_pin = torch.empty((w.M, w.ld), dtype=tdt).pin_memory()
+            out_pin.zero_()
+        finally:
+            os.sched_setaffinity(0, saved)
         mats0, out = sets[0]
-        out_pin = torch.empty((w.M, w.ld), dtype=tdt).pin_memory()
         targets = mats0 + vecs
 
         def e2e_step():
@@ -980,7 +1034,8 @@ def bench_pair(args, lane):
                "d2h_bytes_per_step": w.M * w.ld * w.elem_bytes,
                "ms_per_step": round(sec * 1e3, 4), "steps": k,
                "path": "pinned host inputs -> device (copies), %s call, output -> pinned host, "
-                       "in order on one stream" % lane.api}
+                       "in order on one stream" % lane.api,
+               "host_buffers": numa}
     if rank != 0:
         return None
     steps = bounds[-1][1]

@@ -99,3 +99,9 @@ def test_compare_rows_counts_planted_errors():
     assert r["outside_tolerance"] == 2
     ref[1, 0] = got[1, 0] = 0x7FC0  # NaN on both sides passes
     assert bench.compare_rows(w, got, ref, rows)["outside_tolerance"] == 2
+
+
+def test_cpulist_parsing():
+    assert bench.parse_cpulist("0-3,8,10-11\n") == {0, 1, 2, 3, 8, 10, 11}
+    assert bench.parse_cpulist("5") == {5}
+    assert bench.parse_cpulist("") == set()
