@@ -73,11 +73,12 @@ constexpr int kLag = kSplitLag;  // pass 2 of step t runs kLag steps after its p
 #endif
 constexpr int kSplitUnroll = SR_SPLIT_UNROLL;
 
-// Resident blocks per SM the kernel is compiled for (bounds its registers).
-// Measured on GB300 (cold L2, µs, 2 / 3 / 4 blocks per SM with 4 / 4 / 2
-// units per step): f32 32 x 4194304 272 / 327 / 300, bf16 128 x 524288
-// 83 / 86 / 85, bf16 512 x 400008 251 / 249 / 236, f16 64 x 131072
-// 38 / 46 / 48; 2 blocks per SM with 8 units per step 367 / 101 / 332 / 50.
+// Resident blocks per SM the register sweep is compiled for (bounds its
+// registers). Measured on GB300 while the sweep also took aligned rows (cold
+// L2, µs, 2 / 3 / 4 blocks per SM with 4 / 4 / 2 units per step): f32
+// 32 x 4194304 272 / 327 / 300, bf16 128 x 524288 83 / 86 / 85, bf16
+// 512 x 400008 251 / 249 / 236, f16 64 x 131072 38 / 46 / 48; 2 blocks per SM
+// with 8 units per step 367 / 101 / 332 / 50.
 #ifndef SR_SPLIT_MIN_BLOCKS
 #define SR_SPLIT_MIN_BLOCKS 2
 #endif
