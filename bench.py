@@ -23,8 +23,14 @@ Protocol (cold lane, the default):
      value = algorithmic bytes / that median (2*M*N*elem_bytes per step);
      the mean step is reported beside it.
   4. The output of the last timed call is checked against the oracle again.
-  5. copy_baseline: a device copy of the same M x N elements (torch copy_,
-     same sets, same batches), the practical ceiling at this size.
+  5. copy_baseline: softmax_rows_copy_ceiling, a copy of exactly the bytes the
+     softmax moves at the same pitches with the same 16-byte streaming accesses,
+     on the same sets and batches (torch's copy_ beside it); the row-pair lanes
+     (--api backward / rmsnorm) use softmax_rows_copy_ceiling2 (two inputs read,
+     one written) and torch's add.
+  6. e2e: the same metric through the C ABI with pinned host buffers (pinned
+     from a thread on the GPU's NUMA node), copies or host-link traffic inside
+     the timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME|all|wide]
                   [--lane cold|warm] [--impl ours|reference] [--api ...]
