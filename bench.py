@@ -453,7 +453,7 @@ def gpu_numa_cpus(dev):
         with open("/sys/devices/system/node/node%d/cpulist" % node) as f:
             cpus = parse_cpulist(f.read()) & os.sched_getaffinity(0)
         return (cpus or None), {"gpu_pci": bus, "numa_node": node, "cpus": len(cpus)}
-    except (OSError, ValueError, AttributeError) as e:
+    except (OSError, ValueError, AttributeError, RuntimeError, AssertionError) as e:
         return None, {"numa": "not found (%s)" % type(e).__name__}
 
 
