@@ -119,6 +119,15 @@ def measured_peaks() -> dict:
         return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
 
 
+def dram_rate(traffic, median_step_us: float, peak_gbs: float) -> dict:
+    """DRAM GB/s implied by the recorded bytes per launch (ncu, steady state) over the
+    measured median step, beside the algorithmic GB/s: {} when no traffic is recorded."""
+    if not traffic or median_step_us <= 0:
+        return {}
+    gbs = traffic / (median_step_us / 1e6) / 1e9
+    return {"dram_gbs": round(gbs, 2), "dram_frac": round(gbs / peak_gbs, 4)}
+
+
 def recorded_traffic(workload: str, plan: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current sources of the kernel this plan runs (else None)."""
@@ -752,6 +761,7 @@ def bench_ours(args, w):
                      "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic,
+                     **dram_rate(traffic, stats["median_step_us"], peaks["hbm_gbs"]),
                      "traffic_note": (rec or {}).get("note") if traffic else
                      "null: no ncu capture recorded for the current kernel sources"},
         "source_hash": src_hash,
@@ -1072,6 +1082,7 @@ def bench_pair(args, lane):
                      "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic,
+                     **dram_rate(traffic, stats["median_step_us"], peaks["hbm_gbs"]),
                      "traffic_note": (rec or {}).get("note") if traffic else
                      "null: no ncu capture recorded for the current kernel sources"},
         "source_hash": _build.source_hash(_build.PLAN_SOURCES[lane.api]),

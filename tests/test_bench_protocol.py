@@ -113,3 +113,10 @@ def test_numa_lookup_never_raises():
     cpus, note = bench.gpu_numa_cpus(0)
     assert cpus is None or (isinstance(cpus, set) and cpus)
     assert isinstance(note, dict) and note
+
+
+def test_dram_rate_from_recorded_traffic():
+    r = bench.dram_rate(4281244331, 603.92, 6787.6)
+    assert abs(r["dram_gbs"] - 4281244331 / 603.92e-6 / 1e9) < 0.01
+    assert abs(r["dram_frac"] - r["dram_gbs"] / 6787.6) < 1e-4
+    assert bench.dram_rate(None, 603.92, 6787.6) == {}
